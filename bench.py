@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on one GB300 (or N replicas under torchrun).
+
+One step = one pass of the whole hot path on synthetic K3-shaped inputs:
+  prefill leg:  gate + chunked prefill, B=1, T=4096, H=96, d=128 (the headline
+                tokens/s workload);
+  decode leg:   gate + recurrent decode, 256 sequences x 96 heads, fp32 states
+                [256, 96, 128, 128] (1.61 GB) updated in place.
+`value` is prefill sequence tokens/s over all ranks; the decode leg reports
+state GB/s against the measured HBM peak.  Inputs are larger than L2 (129 MB):
+the prefill leg reads ~0.6 GB and the decode leg streams 3.2 GB per step.
+
+`--impl reference` times the CPU oracle (fp64 recurrence + fp32 gate spec) on
+the host cores, on a bounded sample of the same prefill workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+T_PREFILL = 4096
+H = 96
+D = 128
+CHUNK = 64
+B_DECODE = 256
+WORKLOAD = (f"KDA gate+chunked prefill B=1 T={T_PREFILL} H={H} d={D} (chunk {CHUNK}); "
+            f"gate+recurrent decode B={B_DECODE} H={H} d={D} fp32 state in place")
+METRIC = "KDA prefill tokens/s (H=96,d=128,T=4096); decode state GB/s vs HBM peak"
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# --- algorithmic work --------------------------------------------------------------------
+
+def prefill_flops_per_head(lengths, K=D, V=D, C=CHUNK):
+    """Algorithmic flops of the chunked form for one head (triangular products
+    counted as triangular): per chunk of L tokens, A_kk (strict lower) and A_qk
+    (lower) inner products over K, the UT inverse (L^3/3), W = T beta Kbar and
+    Ut = T beta V, U = Ut - W S, O = Qbar S + A_qk U, S update."""
+    total = 0
+    for n in lengths:
+        for c0 in range(0, n, C):
+            L = min(C, n - c0)
+            tri_lo, tri = L * (L - 1) // 2, L * (L + 1) // 2
+            total += 2 * K * tri_lo + 2 * K * tri          # A_kk, A_qk
+            total += L ** 3 // 3                           # UT inverse
+            total += 2 * K * tri + 2 * V * tri             # W, Ut
+            total += 2 * L * K * V * 3                     # U, Qbar S, S update
+            total += 2 * V * tri                           # A_qk U
+    return total
+
+
+def prefill_io_bytes(T, Hh=H, K=D, V=D, o_bytes=2):
+    """Minimal HBM bytes of gate+prefill: f (bf16) read by the gate, g (fp32)
+    written by the gate and read by prefill, b/beta, q/k/v (bf16) read, o written."""
+    per_token_head = 2 * K + 4 * K * 2 + 4 * 2 + 2 * K * 2 + 2 * V + o_bytes * V
+    return T * Hh * per_token_head
+
+
+def prefill_kernel_bytes(T, Hh=H, K=D, V=D, o_bytes=2):
+    """Minimal HBM bytes of the prefill kernel alone: q, k, v (bf16), g (fp32),
+    beta (fp32) read, o written (zero initial state, final state written)."""
+    return T * Hh * (2 * K * 2 + 2 * V + 4 * K + 4 + o_bytes * V) + Hh * K * V * 4
+
+
+def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D):
+    """Decode kernel: every fp32 state read once and written once, plus the token
+    (q, k, v bf16; g fp32; beta fp32) and the output (bf16)."""
+    return B * Hh * (2 * K * V * 4 + 2 * K * 2 + 2 * V + 4 * K + 4 + 2 * V)
+
+
+# --- clocks ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "samples": len(sms), "reasons": sorted(reasons)}
+
+
+# --- distributed helpers -----------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --- reference arm (the CPU oracle) --------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from gated_delta_rule_33_gb300 import synth
+
+    oracle.build()
+    cores = oracle.default_threads()
+    heads = args.ref_heads
+    x = synth.make_inputs(T_PREFILL, H=H, D=D, seed=0)
+    sel = list(range(heads))
+    f = x.f[:, sel].float().numpy()
+    b = x.b[:, sel].numpy()
+    dt = x.dt_bias[sel].numpy()
+    q, k, v = (t[:, sel].double().numpy() for t in (x.q, x.k, x.v))
+
+    def step():
+        g, beta = oracle.gate(f, b, x.A_log.numpy(), dt, x.alog_mode)
+        oracle.recurrent(q, k, v, g, beta, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt_s = (time.perf_counter() - t0) / args.steps
+    # tokens/s of the full 96-head workload = sampled token-heads/s / 96
+    value = T_PREFILL * heads / H / dt_s
+    sample = (f"gate + fp64 recurrence on {heads} of {H} heads, T={T_PREFILL}, d={D}; "
+              f"tokens/s scaled to all {H} heads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def cpu_baseline(heads: int):
+    """The oracle, as it stands, on the host cores: gate + fp64 recurrence on a
+    sample of heads of the T=4096 workload."""
+    import oracle
+    from gated_delta_rule_33_gb300 import synth
+
+    oracle.build()
+    cores = oracle.default_threads()
+    x = synth.make_inputs(T_PREFILL, H=H, D=D, seed=0)
+    sel = list(range(heads))
+    f, b, dt = x.f[:, sel].float().numpy(), x.b[:, sel].numpy(), x.dt_bias[sel].numpy()
+    q, k, v = (t[:, sel].double().numpy() for t in (x.q, x.k, x.v))
+    t0 = time.perf_counter()
+    g, beta = oracle.gate(f, b, x.A_log.numpy(), dt, x.alog_mode)
+    oracle.recurrent(q, k, v, g, beta, nthreads=cores)
+    elapsed = time.perf_counter() - t0
+    return {"value": T_PREFILL * heads / H / elapsed, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"gate + fp64 recurrence on {heads} of {H} heads, T={T_PREFILL}, d={D} "
+                      f"({elapsed:.1f} s); tokens/s scaled to all {H} heads"}
+
+
+# --- our arm -------------------------------------------------------------------------------
+
+def run_ours(args):
+    import gated_delta_rule_33_gb300 as kda
+    from gated_delta_rule_33_gb300 import synth
+
+    rank, world, local_rank = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    kda.load()
+    stream = torch.cuda.current_stream(dev)
+
+    # prefill leg inputs (resident in HBM before timing)
+    x = synth.make_inputs(T_PREFILL, H=H, D=D, seed=rank)
+    q, k, v, f = (t.to(dev) for t in (x.q, x.k, x.v, x.f))
+    b, A_log, dt_bias = x.b.to(dev), x.A_log.to(dev), x.dt_bias.to(dev)
+    g = torch.empty(T_PREFILL, H, D, device=dev)
+    beta = torch.empty(T_PREFILL, H, device=dev)
+    o = torch.empty(T_PREFILL, H, D, dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty(1, H, D, D, device=dev)
+    ws = torch.empty(max(kda.kda_chunk_prefill_workspace_size(T_PREFILL, 1, H), 16),
+                     dtype=torch.uint8, device=dev)
+    # decode leg inputs
+    d = synth.make_decode_inputs(B_DECODE, H=H, D=D, seed=rank, state_device=dev)
+    dq, dk, dv, df = (t.to(dev) for t in (d.q, d.k, d.v, d.f))
+    db, dA, ddt = d.b.to(dev), d.A_log.to(dev), d.dt_bias.to(dev)
+    dg = torch.empty(B_DECODE, H, D, device=dev)
+    dbeta = torch.empty(B_DECODE, H, device=dev)
+    dout = torch.empty(B_DECODE, H, D, dtype=torch.bfloat16, device=dev)
+    state = d.state
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    launches_per_step = 4
+
+    def step(record=None):
+        if record is not None:
+            record[0].record(stream)
+        kda.kda_gate_fused(f, b, A_log, x.alog_mode, dt_bias, g, beta, stream)
+        if record is not None:
+            record[1].record(stream)
+        kda.kda_chunk_prefill(q, k, v, g, beta, None, 1.0, None, Sf, o, ws, stream)
+        if record is not None:
+            record[2].record(stream)
+        kda.kda_gate_fused(df, db, dA, d.alog_mode, ddt, dg, dbeta, stream)
+        if record is not None:
+            record[3].record(stream)
+        kda.kda_recurrent_decode(dq, dk, dv, dg, dbeta, state, 1.0, dout, stream)
+        if record is not None:
+            record[4].record(stream)
+
+    for _ in range(max(args.warmup, 3) if args.warmup >= 3 else args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if kda.kda_get_last_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    per_step = []
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    step_events = []
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        step(evs)
+        step_events.append(evs)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    for evs in step_events:
+        per_step.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
+    gate_ms = statistics.mean(p[0] for p in per_step)
+    prefill_ms = statistics.mean(p[1] for p in per_step)
+    dgate_ms = statistics.mean(p[2] for p in per_step)
+    decode_ms = statistics.mean(p[3] for p in per_step)
+    step_ms = total_ms / args.steps
+
+    prefill_leg_ms = max_over_ranks(gate_ms + prefill_ms, world, dev)
+    step_ms_max = max_over_ranks(step_ms, world, dev)
+    decode_ms_max = max_over_ranks(decode_ms, world, dev)
+    value = world * T_PREFILL / (prefill_leg_ms * 1e-3)
+
+    # e2e: through the same C ABI, inputs from pinned host memory every step,
+    # outputs (o and the final state) read back every step.
+    host_in = [t.pin_memory() for t in (x.q, x.k, x.v, x.f, x.b)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    host_S = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_o.numel() * host_o.element_size() + host_S.numel() * host_S.element_size()
+
+    def e2e_step():
+        for hsrc, ddst in zip(host_in, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        eq, ek, evv, ef, eb = dev_in
+        kda.kda_gate_fused(ef, eb, A_log, x.alog_mode, dt_bias, g, beta, stream)
+        kda.kda_chunk_prefill(eq, ek, evv, g, beta, None, 1.0, None, Sf, o, ws, stream)
+        host_o.copy_(o, non_blocking=True)
+        host_S.copy_(Sf, non_blocking=True)
+
+    for _ in range(max(args.warmup, 1)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_value = world * T_PREFILL / (e2e_ms * 1e-3)
+
+    if kda.kda_get_last_device_error(stream) != 0:
+        raise RuntimeError("device error during the timed region")
+
+    if rank != 0:
+        return 0
+    peaks = measured_peaks()
+    hbm = peaks["hbm_gbs"]
+    # dominant kernel: the chunked prefill.  Its algorithm runs on CUDA cores in
+    # fp32 in this build, so its roof is the fp32 FMA issue rate: 152 SMs x 128
+    # lanes x 2 flop x SM clock.
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    rec_flops = T_PREFILL * H * (7 * D * D + 4 * D)
+    achieved = rec_flops / (prefill_ms * 1e-3) / 1e12
+    roofline = {"kernel": "kda prefill (token-recurrent, CUDA cores)", "bound": "alu",
+                "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": None,
+                "peak_note": "fp32 FMA issue rate 152 SMs x 128 lanes x 2 x max SM clock",
+                "algorithmic_flops_per_launch": rec_flops}
+    dec_gbs = decode_bytes() / (decode_ms_max * 1e-3) / 1e9
+    roofline_decode = {"kernel": "kda recurrent decode", "bound": "hbm", "achieved": dec_gbs,
+                       "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm, "traffic": None,
+                       "peak_source": peaks["source"],
+                       "algorithmic_bytes_per_launch": decode_bytes()}
+    cpu = cpu_baseline(args.cpu_heads) if not args.no_cpu_baseline else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "inputs_exceed_l2": True, "l2_flush": False,
+                   "prefill_T": T_PREFILL, "heads": H, "d": D, "decode_batch": B_DECODE,
+                   "parallelism": f"replicas x{world}"},
+        "prefill_ms": prefill_ms, "gate_ms": gate_ms, "decode_gate_ms": dgate_ms,
+        "decode_ms": decode_ms_max,
+        "decode_state_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / hbm,
+        "roofline": roofline, "roofline_decode": roofline_decode,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "peaks": peaks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-heads", type=int, default=8,
+                    help="heads of the T=4096 workload per reference-arm step")
+    ap.add_argument("--cpu-heads", type=int, default=24,
+                    help="heads of the T=4096 workload timed for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

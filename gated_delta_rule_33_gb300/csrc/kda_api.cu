@@ -1,0 +1,191 @@
+// kda_api.cu -- the extern "C" entry points of libkda (declared in include/kda.h).
+//
+// Host-side argument checks, the per-device error word, and the launches.  No
+// CUDA allocation happens here; every buffer is the caller's.
+#include <mutex>
+
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+// One error word per device: kernels record the first error they meet, the
+// host reads and clears it in kda_get_last_device_error().
+__device__ unsigned int g_device_error_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned int *error_word = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+// Looks up (once per device) the SM count, whether the device is an sm_103
+// part this library was built for, and the device address of the error word.
+kda_status current_device(DeviceInfo **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return KDA_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
+    DeviceInfo &info = g_devices[dev];
+    if (!info.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_NO_DEVICE;
+        }
+        info.supported = (prop.major == 10 && prop.minor == 3);
+        info.num_sms = prop.multiProcessorCount;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_error_word) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        info.error_word = static_cast<unsigned int *>(addr);
+        info.ready = true;
+    }
+    if (!info.supported) return KDA_ERR_NO_DEVICE;
+    *out = &info;
+    return KDA_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool valid_dtype(kda_dtype d) { return d == KDA_BF16 || d == KDA_FP32; }
+
+kda_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return KDA_OK;
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return KDA_VERSION; }
+
+const char *kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED_SHAPE: return "KDA_ERR_UNSUPPORTED_SHAPE";
+        case KDA_ERR_UNSUPPORTED_DTYPE: return "KDA_ERR_UNSUPPORTED_DTYPE";
+        case KDA_ERR_MISALIGNED: return "KDA_ERR_MISALIGNED";
+        case KDA_ERR_WORKSPACE_TOO_SMALL: return "KDA_ERR_WORKSPACE_TOO_SMALL";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT";
+        case KDA_ERR_NONFINITE: return "KDA_ERR_NONFINITE";
+        case KDA_ERR_NOT_IMPLEMENTED: return "KDA_ERR_NOT_IMPLEMENTED";
+        case KDA_ERR_NO_DEVICE: return "KDA_ERR_NO_DEVICE";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+kda_status kda_gate_fused(const void *f, kda_dtype f_dtype, const void *b, kda_dtype b_dtype,
+                          const float *A_log, kda_alog_mode alog_mode, const float *dt_bias,
+                          float *g_out, float *beta_out, int64_t N, int H, int K, void *stream) {
+    if (N < 0 || H < 1 || K < 1) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (alog_mode != KDA_ALOG_PER_HEAD && alog_mode != KDA_ALOG_PER_CHANNEL &&
+        alog_mode != KDA_ALOG_PER_HEAD_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    if ((b == nullptr) != (beta_out == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (f == nullptr || g_out == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (A_log == nullptr || dt_bias == nullptr) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(f) || !aligned16(b) || !aligned16(A_log) || !aligned16(dt_bias) ||
+        !aligned16(g_out) || !aligned16(beta_out))
+        return KDA_ERR_MISALIGNED;
+    if (N == 0) return KDA_OK;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_gate(f, f_dtype == KDA_BF16, b, b_dtype == KDA_BF16, A_log,
+                                      static_cast<int>(alog_mode), dt_bias, g_out, beta_out, N, H,
+                                      K, dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V) {
+    if (N < 0 || B < 1 || H < 1 || K != 128 || V != 128) return 0;
+    return kda::prefill_workspace_bytes(N, B, H);
+}
+
+kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const int32_t *cu_seqlens, int B, int64_t N, int H,
+                             int K, int V, float scale, const float *initial_state,
+                             float *final_state, void *o, kda_dtype o_dtype, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(o_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (cu_seqlens == nullptr && B != 1) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr ||
+                  beta == nullptr || o == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
+        !aligned16(workspace) || !aligned16(cu_seqlens))
+        return KDA_ERR_MISALIGNED;
+    const size_t need = kda::prefill_workspace_bytes(N, B, H);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr))
+        return KDA_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_prefill(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), g, beta, cu_seqlens, B, N, H, scale, initial_state,
+        final_state, o, o_dtype == KDA_BF16, workspace, dev->error_word, dev->num_sms,
+        static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_recurrent_decode(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float *state, int B, int H, int K, int V,
+                                float scale, void *o, kda_dtype o_dtype, void *stream) {
+    if (B < 0 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(o_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (B > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr ||
+                  beta == nullptr || state == nullptr || o == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(state) || !aligned16(o))
+        return KDA_ERR_MISALIGNED;
+    if (B == 0) return KDA_OK;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_decode(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), g, beta, state, B, H, scale, o,
+        o_dtype == KDA_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_get_last_device_error(void *stream) {
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_error_word, sizeof(word)) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero)) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+    }
+    return static_cast<kda_status>(word);
+}
+
+}  // extern "C"

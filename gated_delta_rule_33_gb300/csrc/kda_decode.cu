@@ -1,0 +1,122 @@
+// kda_decode.cu -- fused recurrent KDA for one-token cached decoding.
+//
+// The Kimi-K3 code audit (data/code-audit.json, finding
+// "dual-kda-execution-regimes") names this regime: one new token per sequence
+// against a cached state.  For each (sequence, head), with the 128 x 128 fp32
+// state S (d_k rows, d_v columns):
+//
+//   S' = Diag(exp(g)) S
+//   w  = S'^T k,   z = S'^T (scale q)
+//   u  = beta (v - w)
+//   S  = S' + k u^T                   (written back in place)
+//   o  = S^T (scale q) = z + (scale k.q) u
+//
+// Data path: the step is HBM-bound (0.9 flop/byte); every state is read once
+// and written once.  One 256-thread CTA per (sequence, head): warp w owns rows
+// w, w+8, ..., w+120 and lane l owns columns 4l..4l+3, so each warp-wide 16-byte
+// load or store moves one contiguous 512-byte state row.  The 64 KB state stays
+// in registers (16 float4 per thread) between the column reductions and the
+// write, so HBM sees exactly one read and one write of it.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kThreads = 256;
+constexpr int kRowsPerThread = kD / (kThreads / 32);  // 16
+
+template <bool kOutBf16>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(
+    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+    const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
+    const float *__restrict__ beta, float *__restrict__ state, float scale,
+    void *__restrict__ o) {
+    __shared__ float s_k[kD], s_q[kD], s_decay[kD], s_u[kD];
+    __shared__ float s_red[2][kThreads / 32][kD];
+    __shared__ float s_kq;
+
+    const int64_t bh = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float *S = state + bh * (kD * kD);
+
+    // Issue the whole state read first: 64 KB in flight per CTA.
+    float4 s[kRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i)
+        s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (warp + 8 * i) * kD) + lane);
+
+    if (tid < kD) {
+        const int64_t idx = bh * kD + tid;
+        s_k[tid] = __bfloat162float(k[idx]);
+        s_q[tid] = scale * __bfloat162float(q[idx]);
+        s_decay[tid] = expf(g[idx]);
+    }
+    __syncthreads();
+
+    if (warp == 0) {  // scale * k.q
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc += s_k[lane + 32 * j] * s_q[lane + 32 * j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) s_kq = acc;
+    }
+
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f), z = w;
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const int r = warp + 8 * i;
+        const float d = s_decay[r], kr = s_k[r], qr = s_q[r];
+        s[i].x *= d; s[i].y *= d; s[i].z *= d; s[i].w *= d;
+        w.x += s[i].x * kr; w.y += s[i].y * kr; w.z += s[i].z * kr; w.w += s[i].w * kr;
+        z.x += s[i].x * qr; z.y += s[i].y * qr; z.z += s[i].z * qr; z.w += s[i].w * qr;
+    }
+    reinterpret_cast<float4 *>(s_red[0][warp])[lane] = w;
+    reinterpret_cast<float4 *>(s_red[1][warp])[lane] = z;
+    __syncthreads();
+
+    if (tid < kD) {
+        float ws = 0.f, zs = 0.f;
+#pragma unroll
+        for (int j = 0; j < kThreads / 32; ++j) {
+            ws += s_red[0][j][tid];
+            zs += s_red[1][j][tid];
+        }
+        const float u = beta[bh] * (__bfloat162float(v[bh * kD + tid]) - ws);
+        s_u[tid] = u;
+        const float out = zs + s_kq * u;
+        if (kOutBf16)
+            static_cast<__nv_bfloat16 *>(o)[bh * kD + tid] = __float2bfloat16_rn(out);
+        else
+            static_cast<float *>(o)[bh * kD + tid] = out;
+    }
+    __syncthreads();
+
+    const float4 u4 = reinterpret_cast<const float4 *>(s_u)[lane];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const float kr = s_k[warp + 8 * i];
+        s[i].x += kr * u4.x; s[i].y += kr * u4.y; s[i].z += kr * u4.z; s[i].w += kr * u4.w;
+        __stcs(reinterpret_cast<float4 *>(S + (warp + 8 * i) * kD) + lane, s[i]);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, const float *g, const float *beta,
+                          float *state, int B, int H, float scale, void *o, bool o_bf16,
+                          cudaStream_t s) {
+    const int64_t units = static_cast<int64_t>(B) * H;
+    if (units == 0) return cudaSuccess;
+    if (o_bf16)
+        decode_kernel<true><<<static_cast<unsigned>(units), kThreads, 0, s>>>(q, k, v, g, beta,
+                                                                              state, scale, o);
+    else
+        decode_kernel<false><<<static_cast<unsigned>(units), kThreads, 0, s>>>(q, k, v, g, beta,
+                                                                               state, scale, o);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

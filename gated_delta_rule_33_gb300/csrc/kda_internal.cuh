@@ -1,0 +1,44 @@
+// kda_internal.cuh -- declarations shared by libkda's CUDA translation units.
+// Not part of the public ABI (include/kda.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Device error codes written to the device error word (first error wins).
+// Values match kda_status so the host can return them directly.
+enum : unsigned int {
+    kDevOk = 0,
+    kDevInvalidArg = 1,      // KDA_ERR_INVALID_ARG: a bad cu_seqlens entry
+    kDevTimeout = 7,         // KDA_ERR_DEVICE_TIMEOUT: a bounded wait ran out
+};
+
+__device__ __forceinline__ void record_device_error(unsigned int *err, unsigned int code) {
+    if (err != nullptr) atomicCAS(err, 0u, code);
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Launchers (defined next to their kernels).  All are asynchronous on `s`.
+cudaError_t launch_gate(const void *f, bool f_bf16, const void *b, bool b_bf16,
+                        const float *A_log, int alog_mode, const float *dt_bias, float *g,
+                        float *beta, int64_t N, int H, int K, int num_sms, cudaStream_t s);
+
+cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, const float *g, const float *beta,
+                          float *state, int B, int H, float scale, void *o, bool o_bf16,
+                          cudaStream_t s);
+
+// Prefill workspace layout is private to kda_prefill.cu.
+size_t prefill_workspace_bytes(int64_t N, int B, int H);
+
+cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                           const __nv_bfloat16 *v, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+                           const float *initial_state, float *final_state, void *o, bool o_bf16,
+                           void *workspace, unsigned int *err, int num_sms, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,187 @@
+"""ctypes binding for libkda (include/kda.h): argument marshalling only.
+
+Each ``kda_*`` function takes torch tensors that already live on the GPU,
+passes their device pointers and sizes to the C entry point of the same name
+on the current torch stream, and raises ``KDAError`` on a non-OK status.
+``gate``/``prefill``/``decode`` are conveniences that allocate the outputs
+with torch and call the same entry points.  Nothing here computes any part of
+KDA; if libkda.so is missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import _build
+
+KDA_BF16 = 0
+KDA_FP32 = 1
+KDA_ALOG_PER_HEAD = 0
+KDA_ALOG_PER_CHANNEL = 1
+KDA_ALOG_PER_HEAD_CHANNEL = 2
+
+_STATUS_NAMES = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
+    3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE_TOO_SMALL",
+    6: "KDA_ERR_CUDA", 7: "KDA_ERR_DEVICE_TIMEOUT", 8: "KDA_ERR_NONFINITE",
+    9: "KDA_ERR_NOT_IMPLEMENTED", 10: "KDA_ERR_NO_DEVICE",
+}
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {_STATUS_NAMES.get(self.status, self.status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libkda.so for sm_103a (in-tree)."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def load():
+    """Load libkda.so (it must have been built); declares every entry point."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkda.so is not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.kda_version.argtypes = []
+        lib.kda_version.restype = I
+        lib.kda_status_string.argtypes = [I]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_gate_fused.argtypes = [P, I, P, I, P, I, P, P, P, I64, I, I, P]
+        lib.kda_gate_fused.restype = I
+        lib.kda_chunk_prefill_workspace_size.argtypes = [I64, I, I, I, I]
+        lib.kda_chunk_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_prefill.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, P, I, P,
+                                          ctypes.c_size_t, P]
+        lib.kda_chunk_prefill.restype = I
+        lib.kda_recurrent_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, I, P]
+        lib.kda_recurrent_decode.restype = I
+        lib.kda_get_last_device_error.argtypes = [P]
+        lib.kda_get_last_device_error.restype = I
+        _lib = lib
+        return lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("libkda needs contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device=None) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise KDAError(status, where)
+
+
+def kda_version() -> int:
+    return load().kda_version()
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def kda_gate_fused(f, b, A_log, alog_mode, dt_bias, g_out, beta_out, stream=None):
+    N, H, K = f.shape
+    st = load().kda_gate_fused(_p(f), _dtype_code(f), _p(b), _dtype_code(b) if b is not None else 0,
+                               _p(A_log), int(alog_mode), _p(dt_bias), _p(g_out), _p(beta_out),
+                               N, H, K, _stream(stream, f.device))
+    _check(st, "kda_gate_fused")
+
+
+def kda_chunk_prefill_workspace_size(N: int, B: int, H: int, K: int = 128, V: int = 128) -> int:
+    return int(load().kda_chunk_prefill_workspace_size(N, B, H, K, V))
+
+
+def kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, scale, initial_state, final_state, o,
+                      workspace, stream=None):
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kda_chunk_prefill(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), B, N, H,
+                                  K, V, float(scale), _p(initial_state), _p(final_state), _p(o),
+                                  _dtype_code(o), _p(workspace), ws_bytes,
+                                  _stream(stream, q.device))
+    _check(st, "kda_chunk_prefill")
+
+
+def kda_recurrent_decode(q, k, v, g, beta, state, scale, o, stream=None):
+    B, H, K = q.shape
+    V = v.shape[-1]
+    st = load().kda_recurrent_decode(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state), B, H, K, V,
+                                     float(scale), _p(o), _dtype_code(o), _stream(stream, q.device))
+    _check(st, "kda_recurrent_decode")
+
+
+def kda_get_last_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    return int(load().kda_get_last_device_error(_stream(stream)))
+
+
+# --- conveniences (allocate outputs with torch, then call the entry points) -----
+
+def gate(f, b, A_log, dt_bias, alog_mode=KDA_ALOG_PER_CHANNEL, stream=None
+         ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    N, H, K = f.shape
+    g = torch.empty(N, H, K, dtype=torch.float32, device=f.device)
+    beta = None if b is None else torch.empty(N, H, dtype=torch.float32, device=f.device)
+    kda_gate_fused(f, b, A_log, alog_mode, dt_bias, g, beta, stream)
+    return g, beta
+
+
+def prefill(q, k, v, g, beta, cu_seqlens=None, scale=1.0, initial_state=None,
+            o_dtype=torch.bfloat16, output_final_state=True, stream=None):
+    N, H, K = q.shape
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    o = torch.empty(N, H, v.shape[-1], dtype=o_dtype, device=q.device)
+    final = (torch.empty(B, H, K, v.shape[-1], dtype=torch.float32, device=q.device)
+             if output_final_state else None)
+    ws = torch.empty(max(kda_chunk_prefill_workspace_size(N, B, H, K, v.shape[-1]), 16),
+                     dtype=torch.uint8, device=q.device)
+    kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, scale, initial_state, final, o, ws, stream)
+    return o, final
+
+
+def decode(q, k, v, g, beta, state, scale=1.0, o_dtype=torch.bfloat16, stream=None):
+    B, H, K = q.shape
+    o = torch.empty(B, H, v.shape[-1], dtype=o_dtype, device=q.device)
+    kda_recurrent_decode(q, k, v, g, beta, state, scale, o, stream)
+    return o

@@ -1,0 +1,183 @@
+/*
+ * kda.h -- C ABI of libkda, Kimi Delta Attention (KDA) on NVIDIA GB300 (sm_103a).
+ *
+ * KDA is the gated delta rule with a per-channel decay.  For one sequence and
+ * one head the state S is a K x V fp32 matrix (K = d_k rows, V = d_v columns)
+ * and each token t updates it and produces an output:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T (scale * q_t)
+ *
+ * with the gate g = -exp(A_log) * softplus(f + dt_bias) and beta = sigmoid(b).
+ * The Kimi-K3 code audit (data/code-audit.json, finding
+ * "dual-kda-execution-regimes") names the two regimes this library serves: a
+ * chunked form for prefill and a fused recurrent form for one-token cached
+ * decoding.  K3_ARTIFACT_AUDIT.md section 7.1 lists the interface facts of the
+ * FlashKDA kernel library that this ABI also follows: K = V = 128, bf16 q/k/v,
+ * fp32 A_log/dt_bias, fixed and variable length, initial and final recurrent
+ * state.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer to row-major contiguous memory
+ *   owned by the caller.  libkda allocates nothing except where an entry
+ *   point says otherwise; scratch memory is passed in as `workspace`.
+ * - Token tensors are laid out [N, H, D] (token, head, channel); states are
+ *   [B, H, K, V] with the d_k row index first; beta is [N, H].
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls are asynchronous on it: the returned status covers host
+ *   argument checks and launch errors only.
+ * - Errors found on the device (an out-of-range cu_seqlens entry, a bounded
+ *   wait that ran out) are recorded in a device error word and returned by
+ *   kda_get_last_device_error().  No kernel traps or asserts.
+ * - Pointers must be 16-byte aligned (KDA_ERR_MISALIGNED otherwise).
+ * - No C++ exception crosses this ABI.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_VERSION 10000 /* 1.0.0 */
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED_SHAPE = 2,  /* e.g. K or V != 128 for prefill/decode */
+    KDA_ERR_UNSUPPORTED_DTYPE = 3,
+    KDA_ERR_MISALIGNED = 4,         /* a pointer is not 16-byte aligned */
+    KDA_ERR_WORKSPACE_TOO_SMALL = 5,
+    KDA_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+    KDA_ERR_DEVICE_TIMEOUT = 7,     /* a bounded device-side wait ran out */
+    KDA_ERR_NONFINITE = 8,          /* reserved for debug checks */
+    KDA_ERR_NOT_IMPLEMENTED = 9,
+    KDA_ERR_NO_DEVICE = 10          /* no usable sm_103 device / driver */
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_BF16 = 0,
+    KDA_FP32 = 1
+} kda_dtype;
+
+/*
+ * Shape of A_log.  K3_ARTIFACT_AUDIT.md section 5.2 records that the public
+ * configuration, the HF code and FlashKDA's check expect A_log of shape [H]
+ * while the checkpoint header holds [128]; all three readings are accepted.
+ */
+typedef enum kda_alog_mode {
+    KDA_ALOG_PER_HEAD = 0,          /* A_log [H] */
+    KDA_ALOG_PER_CHANNEL = 1,       /* A_log [K] */
+    KDA_ALOG_PER_HEAD_CHANNEL = 2   /* A_log [H, K] */
+} kda_alog_mode;
+
+/*
+ * kda_gate_fused -- the KDA gate in one pass (parameters: K3_ARTIFACT_AUDIT.md
+ * section 4.1 tensor table and section 5.1 statistics; beta as an fp32 sigmoid
+ * of the raw gate: finding 1 of the "[OMNIML-6079] [20/21] Add the Kimi-K3
+ * expert-parallel adapter" review).
+ *
+ *   g[n,h,c]  = -(exp(A_log[.]) * softplus(f[n,h,c] + dt_bias[h,c]))
+ *   beta[n,h] = 1 / (1 + exp(-b[n,h]))
+ *
+ * with softplus(x) = max(x, 0) + log1p(exp(-|x|)).  The result is bit-exact
+ * with respect to a fixed binary32 specification (libkda's own exp and log1p,
+ * every operation rounded to nearest, no contraction).
+ *
+ *   f        [N, H, K] of f_dtype (bf16 or fp32)
+ *   b        [N, H] of b_dtype (bf16 or fp32) beta logits; may be NULL, in
+ *            which case beta_out must be NULL and no beta is written
+ *   A_log    fp32, shape selected by alog_mode
+ *   dt_bias  fp32 [H, K]
+ *   g_out    fp32 [N, H, K] (written)
+ *   beta_out fp32 [N, H] (written) or NULL
+ *
+ * Shape-generic in K.  N == 0 is a no-op.
+ */
+kda_status kda_gate_fused(const void *f, kda_dtype f_dtype,
+                          const void *b, kda_dtype b_dtype,
+                          const float *A_log, kda_alog_mode alog_mode,
+                          const float *dt_bias,
+                          float *g_out, float *beta_out,
+                          int64_t N, int H, int K, void *stream);
+
+/*
+ * Bytes of device workspace kda_chunk_prefill needs for these sizes.
+ * The value never exceeds a few kilobytes; it is 0 only when nothing runs.
+ */
+size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V);
+
+/*
+ * kda_chunk_prefill -- the chunked KDA regime for prefill (code-audit.json,
+ * finding "dual-kda-execution-regimes"; varlen and initial/final state as in
+ * K3_ARTIFACT_AUDIT.md section 7.1).  Computes o and the final state exactly
+ * as the token recurrence above would, chunk by chunk.
+ *
+ *   q, k, v       bf16 [N, H, 128]; q and k are used as given (no normalisation)
+ *   g             fp32 [N, H, 128] log-decay (g <= 0 for a decay)
+ *   beta          fp32 [N, H], already passed through the sigmoid
+ *   cu_seqlens    int32 [B+1] device offsets of B packed sequences
+ *                 (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = N); NULL
+ *                 means one sequence of N tokens (B must be 1).  Entries that
+ *                 break these rules are caught on the device: the sequence is
+ *                 skipped and the device error word is set to INVALID_ARG.
+ *                 Zero-length sequences are allowed (final = initial).
+ *   scale         multiplies q
+ *   initial_state fp32 [B, H, 128, 128] or NULL (zero state)
+ *   final_state   fp32 [B, H, 128, 128] (written) or NULL; may alias
+ *                 initial_state (each state is read before it is written)
+ *   o             [N, H, 128] of o_dtype (bf16 or fp32), written
+ *   workspace     device scratch of at least
+ *                 kda_chunk_prefill_workspace_size(N, B, H, 128, 128) bytes,
+ *                 16-byte aligned; its contents need not be initialised and
+ *                 it must not be used by another call running concurrently.
+ *
+ * K and V must be 128 (KDA_ERR_UNSUPPORTED_SHAPE otherwise).
+ */
+kda_status kda_chunk_prefill(const void *q, const void *k, const void *v,
+                             const float *g, const float *beta,
+                             const int32_t *cu_seqlens, int B,
+                             int64_t N, int H, int K, int V, float scale,
+                             const float *initial_state, float *final_state,
+                             void *o, kda_dtype o_dtype,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kda_recurrent_decode -- the fused recurrent KDA regime for one-token cached
+ * decoding (code-audit.json, finding "dual-kda-execution-regimes"): one new
+ * token for each of B sequences, the state updated in place.
+ *
+ *   q, k, v   bf16 [B, H, 128]
+ *   g         fp32 [B, H, 128];  beta fp32 [B, H] (post-sigmoid)
+ *   state     fp32 [B, H, 128, 128], read and overwritten with S_t
+ *   o         [B, H, 128] of o_dtype, written
+ *
+ * K and V must be 128.  B == 0 is a no-op.
+ */
+kda_status kda_recurrent_decode(const void *q, const void *k, const void *v,
+                                const float *g, const float *beta,
+                                float *state, int B, int H, int K, int V, float scale,
+                                void *o, kda_dtype o_dtype, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device error word of the
+ * current device (KDA_OK when no kernel recorded an error).  Returns
+ * KDA_ERR_CUDA if the synchronisation itself fails.
+ */
+kda_status kda_get_last_device_error(void *stream);
+
+/* A static, human-readable name for a status code. */
+const char *kda_status_string(kda_status status);
+
+/* KDA_VERSION of the built library. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,110 @@
+"""Host-side checks of the libkda C ABI that need no GPU.
+
+The library must load and export every function include/kda.h declares, and
+its argument checks (which run before any CUDA call) must reject bad input
+with the documented status codes.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    import gated_delta_rule_33_gb300 as kda
+    kda.build()
+    return kda.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("kda_gate_fused", "kda_chunk_prefill", "kda_chunk_prefill_workspace_size",
+                     "kda_recurrent_decode", "kda_get_last_device_error", "kda_status_string",
+                     "kda_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for name in declared_functions():
+        assert hasattr(clib, name), f"libkda.so does not export {name}"
+
+
+def test_version_and_status_strings(clib):
+    import gated_delta_rule_33_gb300 as kda
+    assert kda.kda_version() == 10000
+    assert kda.kda_status_string(0) == "KDA_OK"
+    assert kda.kda_status_string(5) == "KDA_ERR_WORKSPACE_TOO_SMALL"
+    assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
+
+
+def test_workspace_size_rules(clib):
+    import gated_delta_rule_33_gb300 as kda
+    assert kda.kda_chunk_prefill_workspace_size(4096, 1, 96) > 0
+    assert kda.kda_chunk_prefill_workspace_size(4096, 1, 96) < 64 * 1024
+    assert kda.kda_chunk_prefill_workspace_size(4096, 1, 96, 64, 128) == 0
+    assert kda.kda_chunk_prefill_workspace_size(-1, 1, 96) == 0
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_prefill_argument_checks(clib):
+    P = _fake()
+    ws = _fake()
+    args = dict(q=P, k=P, v=P, g=P, beta=P, cu=None, B=1, N=64, H=2, K=128, V=128, scale=1.0,
+                s0=None, sf=None, o=P, odt=0, ws=ws, wsb=4096, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return clib.kda_chunk_prefill(a["q"], a["k"], a["v"], a["g"], a["beta"], a["cu"], a["B"],
+                                      a["N"], a["H"], a["K"], a["V"], a["scale"], a["s0"], a["sf"],
+                                      a["o"], a["odt"], a["ws"], a["wsb"], a["stream"])
+    assert call(K=64) == 2                       # KDA_ERR_UNSUPPORTED_SHAPE
+    assert call(V=256) == 2
+    assert call(odt=7) == 3                      # KDA_ERR_UNSUPPORTED_DTYPE
+    assert call(N=-1) == 1                       # KDA_ERR_INVALID_ARG
+    assert call(B=2) == 1                        # B > 1 needs cu_seqlens
+    assert call(q=None) == 1
+    assert call(q=_fake(0x10008)) == 4           # KDA_ERR_MISALIGNED
+    assert call(wsb=0) == 5                      # KDA_ERR_WORKSPACE_TOO_SMALL
+    assert call(ws=None) == 5
+
+
+def test_decode_and_gate_argument_checks(clib):
+    P = _fake()
+    assert clib.kda_recurrent_decode(P, P, P, P, P, P, 4, 2, 128, 64, 1.0, P, 0, None) == 2
+    assert clib.kda_recurrent_decode(P, P, P, P, P, None, 4, 2, 128, 128, 1.0, P, 0, None) == 1
+    assert clib.kda_recurrent_decode(P, P, P, P, P, P, -1, 2, 128, 128, 1.0, P, 0, None) == 1
+    assert clib.kda_recurrent_decode(P, _fake(0x10004), P, P, P, P, 4, 2, 128, 128, 1.0, P, 0,
+                                     None) == 4
+    # a beta output without b (or b without a beta output) is rejected
+    assert clib.kda_gate_fused(P, 0, None, 0, P, 1, P, P, P, 16, 2, 128, None) == 1
+    assert clib.kda_gate_fused(P, 0, P, 0, P, 5, P, P, P, 16, 2, 128, None) == 1
+    assert clib.kda_gate_fused(P, 2, P, 0, P, 1, P, P, P, 16, 2, 128, None) == 3
+    # empty work is a no-op that never touches a device
+    assert clib.kda_gate_fused(None, 0, None, 0, P, 1, P, None, None, 0, 2, 128, None) == 0
+    assert clib.kda_recurrent_decode(None, None, None, None, None, None, 0, 2, 128, 128, 1.0,
+                                     None, 0, None) == 0
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "gated_delta_rule_33_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "kdaref" not in text, fn
