@@ -215,8 +215,9 @@ def test_prefill_then_decode_continuation(lib):
                         x.initial_state.to(DEV), o_dtype=torch.float32)
     outs = [o1]
     for t in range(T1, T1 + T2):
-        ot = lib.decode(q[t:t + 1].contiguous(), k[t:t + 1].contiguous(), v[t:t + 1].contiguous(),
-                        g[t:t + 1].contiguous(), beta[t:t + 1].contiguous(), S, 1.0,
+        # clone(): fresh 16-byte-aligned buffers (a one-token slice of beta is not)
+        ot = lib.decode(q[t:t + 1].clone(), k[t:t + 1].clone(), v[t:t + 1].clone(),
+                        g[t:t + 1].clone(), beta[t:t + 1].clone(), S, 1.0,
                         o_dtype=torch.float32)
         outs.append(ot)
     o = torch.cat(outs)
