@@ -360,28 +360,35 @@ def run_ours(args):
         return 0
     peaks = measured_peaks()
     hbm = peaks["hbm_gbs"]
-    # dominant kernel: the chunked prefill.  Its algorithm runs on CUDA cores in
-    # fp32 in this build, so its roof is the fp32 FMA issue rate: 152 SMs x 128
-    # lanes x 2 flop x SM clock.
-    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
-    alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
-    rec_flops = T_PREFILL * H * (7 * D * D + 4 * D)
-    achieved = rec_flops / (prefill_ms * 1e-3) / 1e12
-    roofline = {"kernel": "kda prefill (token-recurrent, CUDA cores)", "bound": "alu",
-                "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                "frac": achieved / alu_peak, "traffic": None,
-                "peak_note": "fp32 FMA issue rate 152 SMs x 128 lanes x 2 x max SM clock",
-                "algorithmic_flops_per_launch": rec_flops}
+    # tf32 dense peak = measured bf16 peak x the nominal tf32/bf16 ratio (1.1/2.25)
+    tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
+    pf_flops = H * prefill_flops_per_head([T_PREFILL])
+    pf_tflops = pf_flops / (prefill_ms * 1e-3) / 1e12
+    pf_bytes = prefill_kernel_bytes(T_PREFILL)
+    rl_prefill = {"kernel": "kda chunked prefill (tcgen05 kind::tf32)", "bound": "tensor",
+                  "achieved": pf_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
+                  "frac": pf_tflops / tf32_peak, "traffic": None,
+                  "peak_source": f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio 1.1/2.25",
+                  "algorithmic_flops_per_launch": pf_flops,
+                  "hbm_achieved_gbs": pf_bytes / (prefill_ms * 1e-3) / 1e9,
+                  "hbm_frac": pf_bytes / (prefill_ms * 1e-3) / 1e9 / hbm,
+                  "algorithmic_bytes_per_launch": pf_bytes}
     dec_gbs = decode_bytes() / (decode_ms_max * 1e-3) / 1e9
-    roofline_decode = {"kernel": "kda recurrent decode", "bound": "hbm", "achieved": dec_gbs,
-                       "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm, "traffic": None,
-                       "peak_source": peaks["source"],
-                       "algorithmic_bytes_per_launch": decode_bytes()}
+    rl_decode = {"kernel": "kda recurrent decode", "bound": "hbm", "achieved": dec_gbs,
+                 "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm, "traffic": None,
+                 "peak_source": peaks["source"], "algorithmic_bytes_per_launch": decode_bytes()}
+    gate_bytes = T_PREFILL * H * (2 * D + 4 * D + 8)
+    gate_gbs = gate_bytes / (gate_ms * 1e-3) / 1e9
+    rl_gate = {"kernel": "kda gate", "bound": "hbm", "achieved": gate_gbs, "peak": hbm,
+               "unit": "GB/s", "frac": gate_gbs / hbm, "traffic": None,
+               "peak_source": peaks["source"], "algorithmic_bytes_per_launch": gate_bytes}
+    # the dominant kernel is the one with the largest share of the step
+    roofline = rl_prefill if prefill_ms >= decode_ms_max else rl_decode
     cpu = cpu_baseline(args.cpu_heads) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "inputs_exceed_l2": True, "l2_flush": False,
                    "prefill_T": T_PREFILL, "heads": H, "d": D, "decode_batch": B_DECODE,
@@ -389,7 +396,8 @@ def run_ours(args):
         "prefill_ms": prefill_ms, "gate_ms": gate_ms, "decode_gate_ms": dgate_ms,
         "decode_ms": decode_ms_max,
         "decode_state_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / hbm,
-        "roofline": roofline, "roofline_decode": roofline_decode,
+        "roofline": roofline,
+        "rooflines": {"gate": rl_gate, "prefill": rl_prefill, "decode": rl_decode},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -82,6 +82,7 @@ const char *kda_status_string(kda_status status) {
         case KDA_ERR_NONFINITE: return "KDA_ERR_NONFINITE";
         case KDA_ERR_NOT_IMPLEMENTED: return "KDA_ERR_NOT_IMPLEMENTED";
         case KDA_ERR_NO_DEVICE: return "KDA_ERR_NO_DEVICE";
+        case KDA_ERR_DECAY_RANGE: return "KDA_ERR_DECAY_RANGE";
     }
     return "KDA_ERR_UNKNOWN";
 }

@@ -1,0 +1,640 @@
+// kda_chunk.cu -- chunked KDA prefill on tcgen05 tensor cores (sm_103a).
+//
+// The chunked regime of Kimi Delta Attention (data/code-audit.json, finding
+// "dual-kda-execution-regimes"), over packed variable-length sequences with
+// initial and final state (K3_ARTIFACT_AUDIT.md section 7.1).  For a chunk of
+// L <= 64 tokens starting from state S (rows r, s are tokens of the chunk):
+//
+//   Gam_r     = sum_{i<=r} g_i                                 (per channel)
+//   A_kk[r,s] = beta_r <k_r exp(Gam_r - Gam_s), k_s>   (s < r)
+//   A_qk[r,s] = scale <q_r exp(Gam_r - Gam_s), k_s>    (s <= r)
+//   T         = (I + A_kk)^{-1}
+//   W         = T diag(beta) (k exp(Gam)),   Ut = T diag(beta) V
+//   U         = Ut - W S
+//   O         = scale (q exp(Gam)) S + A_qk U
+//   S        <- Diag(exp(Gam_L)) S + (k exp(Gam_L - Gam))^T U
+//
+// Numerics.  Every per-channel exponential is split around a per-channel
+// reference m = Gam_L / 2 so that each factor lies in [e^{-D/2}, e^{D/2}] with
+// D = -Gam_L the chunk's total decay (D <= 160 is representable; larger
+// decays are reported as KDA_ERR_DECAY_RANGE).  A_qk and A_kk come from one
+// product [Qt; Kr] Ks^T with Qt = scale q e^{Gam-m}, Kr = k e^{Gam-m} and
+// Ks = k e^{m-Gam}.  The same Qt and Kr serve the state products because the
+// state operand is stored pre-scaled, S_op = Diag(e^m) S, and
+// W' = T diag(beta) Kr = W Diag(e^{-m}).  All products run as tcgen05
+// kind::tf32 MMAs (operands rounded to tf32, to nearest) with fp32
+// accumulation in tensor memory; Ut = T beta V uses kind::f16 with the bf16 V
+// tile as loaded and T beta split into a bf16 high and low part.  The state S
+// stays in tensor memory in fp32 for the whole sequence.
+//
+// Work decomposition: one CTA of 128 threads per (sequence, head) chain at a
+// time, chains taken from a counter in the workspace; thread t owns channel t
+// when building operands and tensor-memory lane t for the state (the d_v index
+// of S^T) and for the products whose M dimension is a channel.
+#include <cuda.h>
+
+#include "kda_internal.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int kC = 64;          // chunk length
+constexpr int kD = 128;         // d_k = d_v
+constexpr int kThreads = 128;
+constexpr float kMaxDecay = 160.f;  // largest per-channel chunk decay represented
+constexpr uint32_t kMaxPolls = 1u << 20;
+
+// Shared memory map (bytes from a 1024-aligned base).  Operand tiles are
+// K-major with the 128-byte swizzle; "rows" is the M or N extent.
+constexpr uint32_t OFF_Q = 0;            // raw q bf16 [64][128] (TMA, no swizzle)
+constexpr uint32_t OFF_K = 16384;        // raw k bf16 [64][128] (TMA, no swizzle)
+constexpr uint32_t OFF_V = 32768;        // raw v bf16 [64 s][128 v] (TMA, 2 swizzled boxes)
+constexpr uint32_t OFF_QK = 49152;       // [Qt ; Kr] tf32, 128 rows (r) x 128 (channel)
+constexpr uint32_t OFF_KS = 114688;      // Ks tf32 64 x 128 -> A_kk | T fp32 -> W' tf32 64 x 128
+constexpr uint32_t OFF_KH = 147456;      // Khat^T tf32, 128 rows (channel) x 64 (r)
+constexpr uint32_t OFF_TB = 180224;      // T beta tf32 64 x 64 -> A_qk tf32 64 x 64
+constexpr uint32_t OFF_TB16 = 196608;    // T beta bf16 hi 64 x 64 | lo 64 x 64
+constexpr uint32_t OFF_MISC = 212992;
+constexpr uint32_t MISC_BETA = 0;        // float[64]
+constexpr uint32_t MISC_EM = 256;        // float[128] e^{m}
+constexpr uint32_t MISC_DEC = 768;       // float[128] e^{Gam_L}
+constexpr uint32_t MISC_P = 1280;        // float[3][256] T-inverse scratch
+constexpr uint32_t MISC_BAR = 4352;      // 3 mbarriers
+constexpr uint32_t MISC_CTRL = 4384;     // int[8]: tmem base, chain, abort, decay flag
+constexpr uint32_t kSmemBytes = OFF_MISC + 4416;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+
+// Tensor memory columns (lane = M row).
+//   S_acc: S^T fp32 (lane v, column k)      S_op: tf32(e^{m_k} S[k][v])
+//   U: U^T (lane v, column r)               O: O^T; before that Kr^T (lane k, column s)
+//   A: [Qt; Kr] Ks^T (lane = row of [Qt; Kr], column s)   W: W'^T (lane k, column r)
+constexpr uint32_t T_SACC = 0, T_SOP = 128, T_U = 256, T_O = 320, T_A = 384, T_W = 448;
+
+struct Params {
+    const float *g;
+    const float *beta;
+    const int32_t *cu_seqlens;
+    int B;
+    int64_t N;
+    int H;
+    float scale;
+    const float *S0;
+    float *Sf;
+    void *o;
+    unsigned int *err;
+    unsigned int *counter;
+};
+
+__device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
+}
+
+__device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
+    *reinterpret_cast<float *>(base + off) = x;
+}
+
+// A_kk is stored row-major with its column index XOR-ed by (row % 32), so that
+// one thread per row can write it without shared-memory bank conflicts.
+__device__ __forceinline__ int akk_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
+
+// Waits (bounded) on an mbarrier phase; on time-out raises the CTA abort flag.
+__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, int *abort_flag,
+                                              unsigned int *err) {
+    if (!mbar_wait_bounded(bar, parity, kMaxPolls)) {
+        *abort_flag = 1;
+        record_device_error(err, kDevTimeout);
+    }
+}
+
+// T = (I + A)^{-1} for a 64x64 strictly lower-triangular A (fp32, akk_idx
+// layout), by 16x16 blocks: diagonal blocks by forward substitution, then
+// T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj along the block sub-diagonals.
+// T is row-major with stride 64.
+__device__ void ut_inverse(const float *A, float *T, float *P, int tid) {
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        if ((c >> 4) > (r >> 4)) T[e] = 0.f;
+    }
+    if (tid < 64) {
+        const int bb = tid >> 4, j = tid & 15, base = bb * 16;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int s = 0; s < r; ++s) acc -= A[akk_idx(base + r, base + s)] * x[s];
+            x[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T[(base + r) * 64 + base + j] = x[r];
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+        const int ntgt = 4 - d;
+        // P_t = sum_{m=j}^{i-1} A_im T_mj for the targets (i, j) = (t + d, t)
+        for (int e = tid; e < ntgt * 256; e += kThreads) {
+            const int t = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int j = t, i = t + d;
+            float acc = 0.f;
+            for (int m = j; m < i; ++m) {
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    acc += A[akk_idx(16 * i + r, 16 * m + s)] * T[(16 * m + s) * 64 + 16 * j + cc];
+            }
+            P[e] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < ntgt * 256; e += kThreads) {
+            const int t = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int j = t, i = t + d;
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                acc += T[(16 * i + r) * 64 + 16 * i + s] * P[(t << 8) + (s << 4) + cc];
+            T[(16 * i + r) * 64 + 16 * j + cc] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+template <bool kOutBf16>
+__global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                            const __grid_constant__ CUtensorMap tm_k,
+                                                            const __grid_constant__ CUtensorMap tm_v,
+                                                            const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *misc = smem + OFF_MISC;
+    float *s_beta = reinterpret_cast<float *>(misc + MISC_BETA);
+    float *s_em = reinterpret_cast<float *>(misc + MISC_EM);
+    float *s_dec = reinterpret_cast<float *>(misc + MISC_DEC);
+    float *s_P = reinterpret_cast<float *>(misc + MISC_P);
+    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(misc + MISC_BAR);
+    uint64_t *bar_v = bar_qk + 1;
+    uint64_t *bar_mma = bar_qk + 2;
+    int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [3] decay
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int H = p.H;
+    const int num_chains = p.B * H;
+
+    if (warp == 0) tmem_alloc(reinterpret_cast<uint32_t *>(&ctrl[0]), 512);
+    if (tid == 0) {
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        ctrl[2] = 0;
+        ctrl[3] = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = static_cast<uint32_t>(ctrl[0]);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    // Phases consumed so far (identical in every thread) and, in thread 0,
+    // whether a TMA batch is in flight.
+    uint32_t ph_qk = 0, ph_v = 0, ph_mma = 0;
+    bool pend_qk = false, pend_v = false;
+
+    const uint32_t a_qk = smem_addr(smem + OFF_QK);
+    const uint32_t a_ks = smem_addr(smem + OFF_KS);
+    const uint32_t a_kh = smem_addr(smem + OFF_KH);
+    const uint32_t a_tb = smem_addr(smem + OFF_TB);
+    const uint32_t a_tb16 = smem_addr(smem + OFF_TB16);
+    const uint32_t a_v = smem_addr(smem + OFF_V);
+    float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
+    float *Tm = Akk + 64 * 64;
+
+    while (true) {
+        __syncthreads();
+        if (tid == 0) ctrl[1] = static_cast<int>(atomicAdd(p.counter, 1u));
+        __syncthreads();
+        const int chain = ctrl[1];
+        if (chain >= num_chains || ctrl[2] != 0) break;
+        const int b = chain / H, h = chain % H;
+        int64_t t0 = 0, t1 = p.N;
+        if (p.cu_seqlens != nullptr) {
+            t0 = p.cu_seqlens[b];
+            t1 = p.cu_seqlens[b + 1];
+            if (t0 < 0 || t1 < t0 || t1 > p.N) {
+                if (tid == 0) record_device_error(p.err, kDevInvalidArg);
+                continue;
+            }
+        }
+        const int64_t state_off = (static_cast<int64_t>(b) * H + h) * kD * kD;
+
+        // ---- initial state into S_acc (lane v, column k holds S[k][v]) ----
+        {
+            float r[32];
+            for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    r[j] = (p.S0 != nullptr) ? p.S0[state_off + (32 * cb + j) * kD + tid] : 0.f;
+                tmem_st32(tmem + lane_base + T_SACC + 32 * cb, r);
+            }
+            tmem_wait_st();
+        }
+
+        auto issue_qk = [&](int64_t tc) {
+            mbar_arrive_expect_tx(bar_qk, 2 * 16384);
+            tma_load_3d(smem + OFF_Q, &tm_q, bar_qk, 0, h, static_cast<int32_t>(tc));
+            tma_load_3d(smem + OFF_K, &tm_k, bar_qk, 0, h, static_cast<int32_t>(tc));
+            pend_qk = true;
+        };
+        auto issue_v = [&](int64_t tc) {
+            mbar_arrive_expect_tx(bar_v, 16384);
+            tma_load_3d(smem + OFF_V, &tm_v, bar_v, 0, h, static_cast<int32_t>(tc));
+            tma_load_3d(smem + OFF_V + 8192, &tm_v, bar_v, 64, h, static_cast<int32_t>(tc));
+            pend_v = true;
+        };
+        // g of the chunk (one channel per thread) and beta (one row per thread)
+        // in registers, loaded one chunk ahead; g becomes the cumulative sum.
+        float gam[kC];
+        float breg = 0.f;
+        auto load_g = [&](int64_t tc, int L) {
+#pragma unroll
+            for (int r = 0; r < kC; ++r)
+                gam[r] = (r < L) ? p.g[((tc + r) * H + h) * kD + tid] : 0.f;
+            breg = (tid < L) ? p.beta[(tc + tid) * H + h] : 0.f;
+        };
+        if (t1 > t0) {
+            if (tid == 0) {
+                issue_qk(t0);
+                issue_v(t0);
+            }
+            load_g(t0, static_cast<int>((t1 - t0) < kC ? (t1 - t0) : kC));
+        }
+
+        for (int64_t tc = t0; tc < t1; tc += kC) {
+            const int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
+            const int64_t tn = tc + kC;
+            const int Ln = static_cast<int>(tn >= t1 ? 0 : ((t1 - tn) < kC ? (t1 - tn) : kC));
+
+            // ---- S1: cumulative decay, references, operands ----
+            {
+                float acc = 0.f;
+#pragma unroll
+                for (int r = 0; r < kC; ++r) {  // rows >= L carry g = 0
+                    acc += gam[r];
+                    gam[r] = acc;
+                }
+            }
+            const float gam_l = gam[kC - 1];
+            if (-gam_l > kMaxDecay) ctrl[3] = 1;
+            const float m = 0.5f * gam_l;
+            s_em[tid] = __expf(m);
+            s_dec[tid] = __expf(gam_l);
+            const float ekh = __expf(gam_l - m);
+            if (tid < kC) s_beta[tid] = breg;
+            const float qscale = p.scale;
+            wait_or_abort(bar_qk, ph_qk & 1, &ctrl[2], p.err);
+            ph_qk++;
+            pend_qk = false;
+            float krt[32];
+#pragma unroll
+            for (int r = 0; r < kC; ++r) {
+                float qt = 0.f, kr = 0.f, ks = 0.f, kh = 0.f;
+                if (r < L) {
+                    const float e_up = __expf(gam[r] - m);   // e^{Gam_r - m}
+                    const float e_dn = __expf(m - gam[r]);   // e^{m - Gam_r}
+                    const float qv = bf(smem + OFF_Q, (r * kD + tid) * 2);
+                    const float kv = bf(smem + OFF_K, (r * kD + tid) * 2);
+                    qt = to_tf32(qscale * qv * e_up);
+                    kr = to_tf32(kv * e_up);
+                    ks = to_tf32(kv * e_dn);
+                    kh = to_tf32(kv * (e_dn * ekh));
+                }
+                st_f32(smem + OFF_QK, sw128_offset(r, tid, 128, 4), qt);
+                st_f32(smem + OFF_QK, sw128_offset(r + 64, tid, 128, 4), kr);
+                st_f32(smem + OFF_KS, sw128_offset(r, tid, 64, 4), ks);
+                st_f32(smem + OFF_KH, sw128_offset(tid, r, 128, 4), kh);
+                krt[r & 31] = kr;
+                if ((r & 31) == 31) tmem_st32(tmem + lane_base + T_O + (r & 32), krt);
+            }
+            tmem_wait_st();
+            if (Ln > 0) load_g(tn, Ln);  // next chunk, consumed next iteration
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (ctrl[2] != 0) break;
+
+            // ---- S2: D_A = [Qt; Kr] Ks^T ; next q/k loads ; state pass ----
+            if (tid == 0) {
+                if (Ln > 0) issue_qk(tn);
+                const uint32_t id = instr_desc(128, 64, kFmtTF32, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t ad = smem_desc(a_qk + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bd = smem_desc(a_ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_tf32_ss(tmem + T_A, ad, bd, id, kk > 0);
+                }
+                mma_commit(bar_mma);
+            }
+            {   // S_op = tf32(e^{m_k} S[k][v]);  S_acc = e^{Gam_L,k} S[k][v]
+                float r[32], o32[32];
+                for (int cb = 0; cb < 4; ++cb) {
+                    tmem_ld32(tmem + lane_base + T_SACC + 32 * cb, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        o32[j] = to_tf32(r[j] * s_em[32 * cb + j]);
+                        r[j] = r[j] * s_dec[32 * cb + j];
+                    }
+                    tmem_st32(tmem + lane_base + T_SOP + 32 * cb, o32);
+                    tmem_st32(tmem + lane_base + T_SACC + 32 * cb, r);
+                }
+                tmem_wait_st();
+            }
+
+            // ---- S3: A_kk from the k-side rows of D_A ----
+            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            ph_mma++;
+            tc_fence_after();
+            if (warp >= 2) {
+                const int r = tid - 64;
+                const float br = s_beta[r];
+                float d32[32];
+                for (int cb = 0; cb < 2; ++cb) {
+                    tmem_ld32(tmem + lane_base + T_A + 32 * cb, d32);
+                    tmem_wait_ld();
+                    // Ks is dead once D_A is complete; A_kk overwrites it
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int s = 32 * cb + j;
+                        Akk[akk_idx(r, s)] = (s < r) ? br * d32[j] : 0.f;
+                    }
+                }
+            }
+            __syncthreads();
+
+            // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
+            ut_inverse(Akk, Tm, s_P, tid);
+            for (int e = tid; e < 64 * 64; e += kThreads) {
+                const int r = e >> 6, s = e & 63;
+                const float x = Tm[e] * s_beta[s];
+                st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), to_tf32(x));
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+                *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + sw128_offset(r, s, 64, 2)) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + 8192 + sw128_offset(r, s, 64, 2)) = lo;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+
+            // ---- S5: W'^T = Kr^T (T beta)^T ;  Ut^T = V^T (T beta)^T ----
+            if (tid == 0) {
+                const uint32_t idw = instr_desc(128, 64, kFmtTF32, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bd = smem_desc(a_tb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_tf32_ts(tmem + T_W, tmem + T_O + kk * 8, bd, idw, kk > 0);
+                }
+                if (!mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
+                    ctrl[2] = 1;
+                    record_device_error(p.err, kDevTimeout);
+                } else {
+                    pend_v = false;
+                    const uint32_t idu = instr_desc(128, 64, kFmtBF16, 1, 0);
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = smem_desc(a_v + kk * 2048, 8192, 1024, kSwizzle128B);
+                            const uint64_t bd = smem_desc(a_tb16 + part * 8192 + kk * 32, 16, 1024, kSwizzle128B);
+                            mma_f16_ss(tmem + T_U, ad, bd, idu, (part | kk) != 0);
+                        }
+                    }
+                }
+                mma_commit(bar_mma);
+            }
+            ph_v++;
+            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            ph_mma++;
+            tc_fence_after();
+            __syncthreads();
+            if (ctrl[2] != 0) break;
+            if (tid == 0 && Ln > 0) issue_v(tn);
+
+            // ---- S6: W' to shared memory (K-major [r][k]); A_qk (K-major [r][s]) ----
+            {
+                float w32[32];
+                for (int cb = 0; cb < 2; ++cb) {
+                    tmem_ld32(tmem + lane_base + T_W + 32 * cb, w32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        st_f32(smem + OFF_KS, sw128_offset(32 * cb + j, tid, 64, 4), to_tf32(w32[j]));
+                }
+                if (warp < 2) {
+                    const int r = tid;
+                    for (int cb = 0; cb < 2; ++cb) {
+                        tmem_ld32(tmem + lane_base + T_A + 32 * cb, w32);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int s = 32 * cb + j;
+                            st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), (s <= r) ? to_tf32(w32[j]) : 0.f);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+
+            // ---- S7: U^T -= S_op W'^T ;  O^T = S_op Qt^T ----
+            if (tid == 0) {
+                const uint32_t idn = instr_desc(128, 64, kFmtTF32, 0, 0, 1);
+                const uint32_t ido = instr_desc(128, 64, kFmtTF32, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t bw = smem_desc(a_ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_tf32_ts(tmem + T_U, tmem + T_SOP + kk * 8, bw, idn, 1);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    const uint64_t bq = smem_desc(a_qk + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_tf32_ts(tmem + T_O, tmem + T_SOP + kk * 8, bq, ido, kk > 0);
+                }
+                mma_commit(bar_mma);
+            }
+            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            ph_mma++;
+            tc_fence_after();
+
+            // ---- S8: U rounded to tf32 in place (A operand of the next MMAs) ----
+            {
+                float u32[32];
+                for (int cb = 0; cb < 2; ++cb) {
+                    tmem_ld32(tmem + lane_base + T_U + 32 * cb, u32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) u32[j] = to_tf32(u32[j]);
+                    tmem_st32(tmem + lane_base + T_U + 32 * cb, u32);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (ctrl[2] != 0) break;
+
+            // ---- S9: S_acc^T += U^T Khat ;  O^T += U^T A_qk^T ----
+            if (tid == 0) {
+                const uint32_t ids = instr_desc(128, 128, kFmtTF32, 0, 0);
+                const uint32_t ido = instr_desc(128, 64, kFmtTF32, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bk = smem_desc(a_kh + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_tf32_ts(tmem + T_SACC, tmem + T_U + kk * 8, bk, ids, 1);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ba = smem_desc(a_tb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    mma_tf32_ts(tmem + T_O, tmem + T_U + kk * 8, ba, ido, 1);
+                }
+                mma_commit(bar_mma);
+            }
+            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            ph_mma++;
+            tc_fence_after();
+
+            // ---- S10: outputs ----
+            {
+                float o32[32];
+                for (int cb = 0; cb < 2; ++cb) {
+                    tmem_ld32(tmem + lane_base + T_O + 32 * cb, o32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int r = 32 * cb + j;
+                        if (r < L) {
+                            const int64_t idx = ((tc + r) * H + h) * kD + tid;
+                            if (kOutBf16)
+                                static_cast<__nv_bfloat16 *>(p.o)[idx] = __float2bfloat16_rn(o32[j]);
+                            else
+                                static_cast<float *>(p.o)[idx] = o32[j];
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+        if (ctrl[2] != 0) break;
+
+        // ---- final state ----
+        if (p.Sf != nullptr) {
+            float r[32];
+            for (int cb = 0; cb < 4; ++cb) {
+                tmem_ld32(tmem + lane_base + T_SACC + 32 * cb, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) p.Sf[state_off + (32 * cb + j) * kD + tid] = r[j];
+            }
+        }
+    }
+
+    // Drain: after an abort, wait (bounded) for TMA batches still in flight so
+    // that no copy lands in shared memory after this CTA has exited.
+    if (tid == 0) {
+        if (pend_qk) mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls);
+        if (pend_v) mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls);
+        if (ctrl[3] != 0) record_device_error(p.err, kDevDecayRange);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// Tensor map of a [N, H, 128] bf16 tensor with a (box_x, 1, 64) box.
+bool make_map(CUtensorMap *map, const void *base, int64_t N, int H, uint32_t box_x, bool swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                   static_cast<cuuint64_t>(H) * kD * 2};
+    const cuuint32_t box[3] = {box_x, 1, static_cast<cuuint32_t>(kC)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int64_t N, int B, int H) {
+    (void)N;
+    return (B > 0 && H > 0) ? 256 : 0;
+}
+
+cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                           const __nv_bfloat16 *v, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+                           const float *initial_state, float *final_state, void *o, bool o_bf16,
+                           void *workspace, unsigned int *err, int num_sms, cudaStream_t s) {
+    if (B == 0 || H == 0) return cudaSuccess;
+    static bool attr_done[2] = {false, false};
+    if (!attr_done[o_bf16 ? 1 : 0]) {
+        cudaError_t e = o_bf16 ? cudaFuncSetAttribute(chunk_kernel<true>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      kSmemAlloc)
+                               : cudaFuncSetAttribute(chunk_kernel<false>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        attr_done[o_bf16 ? 1 : 0] = true;
+    }
+    CUtensorMap mq, mk, mv;
+    const int64_t Nmap = N > 0 ? N : 1;
+    if (!make_map(&mq, q, Nmap, H, 128, false) || !make_map(&mk, k, Nmap, H, 128, false) ||
+        !make_map(&mv, v, Nmap, H, 64, true))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    const Params p{g, beta, cu_seqlens, B, N, H, scale, initial_state, final_state, o, err,
+                   static_cast<unsigned int *>(workspace)};
+    const int chains = B * H;
+    const int grid = chains < num_sms ? chains : num_sms;
+    if (o_bf16)
+        chunk_kernel<true><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, p);
+    else
+        chunk_kernel<false><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -14,6 +14,7 @@ enum : unsigned int {
     kDevOk = 0,
     kDevInvalidArg = 1,      // KDA_ERR_INVALID_ARG: a bad cu_seqlens entry
     kDevTimeout = 7,         // KDA_ERR_DEVICE_TIMEOUT: a bounded wait ran out
+    kDevDecayRange = 11,     // KDA_ERR_DECAY_RANGE: a chunk's decay is out of range
 };
 
 __device__ __forceinline__ void record_device_error(unsigned int *err, unsigned int code) {

@@ -28,7 +28,7 @@ _STATUS_NAMES = {
     0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED_SHAPE",
     3: "KDA_ERR_UNSUPPORTED_DTYPE", 4: "KDA_ERR_MISALIGNED", 5: "KDA_ERR_WORKSPACE_TOO_SMALL",
     6: "KDA_ERR_CUDA", 7: "KDA_ERR_DEVICE_TIMEOUT", 8: "KDA_ERR_NONFINITE",
-    9: "KDA_ERR_NOT_IMPLEMENTED", 10: "KDA_ERR_NO_DEVICE",
+    9: "KDA_ERR_NOT_IMPLEMENTED", 10: "KDA_ERR_NO_DEVICE", 11: "KDA_ERR_DECAY_RANGE",
 }
 
 

@@ -56,7 +56,9 @@ typedef enum kda_status {
     KDA_ERR_DEVICE_TIMEOUT = 7,     /* a bounded device-side wait ran out */
     KDA_ERR_NONFINITE = 8,          /* reserved for debug checks */
     KDA_ERR_NOT_IMPLEMENTED = 9,
-    KDA_ERR_NO_DEVICE = 10          /* no usable sm_103 device / driver */
+    KDA_ERR_NO_DEVICE = 10,         /* no usable sm_103 device / driver */
+    KDA_ERR_DECAY_RANGE = 11        /* prefill: in some channel the decay summed over one
+                                       64-token chunk is below -160 (device-side check) */
 } kda_status;
 
 typedef enum kda_dtype {
