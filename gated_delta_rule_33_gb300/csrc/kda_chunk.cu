@@ -27,10 +27,11 @@
 // tile as loaded and T beta split into a bf16 high and low part.  The state S
 // stays in tensor memory in fp32 for the whole sequence.
 //
-// Work decomposition: one CTA of 128 threads per (sequence, head) chain at a
-// time, chains taken from a counter in the workspace; thread t owns channel t
-// when building operands and tensor-memory lane t for the state (the d_v index
-// of S^T) and for the products whose M dimension is a channel.
+// Work decomposition: one CTA of 512 threads per (sequence, head) chain at a
+// time, chains taken from a counter in the workspace.  Warp w serves lane
+// quarter w % 4 (channels / tensor-memory lanes 32 (w % 4) ... + 31) and group
+// w / 4, which selects its 16 chunk rows when building operands and its slice
+// of columns in every tensor-memory epilogue.
 #include <cuda.h>
 
 #include "kda_internal.cuh"
@@ -43,7 +44,7 @@ using namespace sm100;
 
 constexpr int kC = 64;          // chunk length
 constexpr int kD = 128;         // d_k = d_v
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;  // 16 warps: 4 lane quarters x 4 column/row groups
 constexpr float kMaxDecay = 160.f;  // largest per-channel chunk decay represented
 constexpr uint32_t kMaxPolls = 1u << 20;
 
@@ -62,9 +63,10 @@ constexpr uint32_t MISC_BETA = 0;        // float[64]
 constexpr uint32_t MISC_EM = 256;        // float[128] e^{m}
 constexpr uint32_t MISC_DEC = 768;       // float[128] e^{Gam_L}
 constexpr uint32_t MISC_P = 1280;        // float[3][256] T-inverse scratch
-constexpr uint32_t MISC_BAR = 4352;      // 3 mbarriers
-constexpr uint32_t MISC_CTRL = 4384;     // int[8]: tmem base, chain, abort, decay flag
-constexpr uint32_t kSmemBytes = OFF_MISC + 4416;
+constexpr uint32_t MISC_PART = 4352;     // float[4][128] partial decay sums per row group
+constexpr uint32_t MISC_BAR = 6400;      // 3 mbarriers
+constexpr uint32_t MISC_CTRL = 6432;     // int[8]: tmem base, chain, abort, decay flag
+constexpr uint32_t kSmemBytes = OFF_MISC + 6464;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 // Tensor memory columns (lane = M row).
@@ -179,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [3] decay
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int quarter = warp & 3, grp = warp >> 2;
+    const int ch = quarter * 32 + (tid & 31);  // channel / tensor-memory lane
     const int H = p.H;
     const int num_chains = p.B * H;
 
@@ -198,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = static_cast<uint32_t>(ctrl[0]);
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    float *s_part = reinterpret_cast<float *>(misc + MISC_PART);
 
     // Phases consumed so far (identical in every thread) and, in thread 0,
     // whether a TMA batch is in flight.
@@ -235,12 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         // ---- initial state into S_acc (lane v, column k holds S[k][v]) ----
         {
             float r[32];
-            for (int cb = 0; cb < 4; ++cb) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    r[j] = (p.S0 != nullptr) ? p.S0[state_off + (32 * cb + j) * kD + tid] : 0.f;
-                tmem_st32(tmem + lane_base + T_SACC + 32 * cb, r);
-            }
+            for (int j = 0; j < 32; ++j)
+                r[j] = (p.S0 != nullptr) ? p.S0[state_off + (32 * grp + j) * kD + ch] : 0.f;
+            tmem_st32(tmem + lane_base + T_SACC + 32 * grp, r);
             tmem_wait_st();
         }
 
@@ -256,14 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tma_load_3d(smem + OFF_V + 8192, &tm_v, bar_v, 64, h, static_cast<int32_t>(tc));
             pend_v = true;
         };
-        // g of the chunk (one channel per thread) and beta (one row per thread)
-        // in registers, loaded one chunk ahead; g becomes the cumulative sum.
-        float gam[kC];
+        // g of the thread's 16 chunk rows (one channel) and beta (one row per
+        // thread of the first 64) in registers, loaded one chunk ahead.
+        float gam[16];
         float breg = 0.f;
         auto load_g = [&](int64_t tc, int L) {
 #pragma unroll
-            for (int r = 0; r < kC; ++r)
-                gam[r] = (r < L) ? p.g[((tc + r) * H + h) * kD + tid] : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * grp + i;
+                gam[i] = (r < L) ? p.g[((tc + r) * H + h) * kD + ch] : 0.f;
+            }
             breg = (tid < L) ? p.beta[(tc + tid) * H + h] : 0.f;
         };
         if (t1 > t0) {
@@ -283,43 +288,55 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             {
                 float acc = 0.f;
 #pragma unroll
-                for (int r = 0; r < kC; ++r) {  // rows >= L carry g = 0
-                    acc += gam[r];
-                    gam[r] = acc;
+                for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
+                    acc += gam[i];
+                    gam[i] = acc;
                 }
+                s_part[grp * kD + ch] = acc;
             }
-            const float gam_l = gam[kC - 1];
+            if (tid < kC) s_beta[tid] = breg;
+            __syncthreads();
+            float prefix = 0.f, gam_l = 0.f;
+#pragma unroll
+            for (int g2 = 0; g2 < 4; ++g2) {
+                const float pg = s_part[g2 * kD + ch];
+                if (g2 < grp) prefix += pg;
+                gam_l += pg;
+            }
             if (-gam_l > kMaxDecay) ctrl[3] = 1;
             const float m = 0.5f * gam_l;
-            s_em[tid] = __expf(m);
-            s_dec[tid] = __expf(gam_l);
+            if (grp == 0) {
+                s_em[ch] = __expf(m);
+                s_dec[ch] = __expf(gam_l);
+            }
             const float ekh = __expf(gam_l - m);
-            if (tid < kC) s_beta[tid] = breg;
             const float qscale = p.scale;
             wait_or_abort(bar_qk, ph_qk & 1, &ctrl[2], p.err);
             ph_qk++;
             pend_qk = false;
-            float krt[32];
+            float krt[16];
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * grp + i;
                 float qt = 0.f, kr = 0.f, ks = 0.f, kh = 0.f;
                 if (r < L) {
-                    const float e_up = __expf(gam[r] - m);   // e^{Gam_r - m}
-                    const float e_dn = __expf(m - gam[r]);   // e^{m - Gam_r}
-                    const float qv = bf(smem + OFF_Q, (r * kD + tid) * 2);
-                    const float kv = bf(smem + OFF_K, (r * kD + tid) * 2);
+                    const float gr = prefix + gam[i];
+                    const float e_up = __expf(gr - m);   // e^{Gam_r - m}
+                    const float e_dn = __expf(m - gr);   // e^{m - Gam_r}
+                    const float qv = bf(smem + OFF_Q, (r * kD + ch) * 2);
+                    const float kv = bf(smem + OFF_K, (r * kD + ch) * 2);
                     qt = to_tf32(qscale * qv * e_up);
                     kr = to_tf32(kv * e_up);
                     ks = to_tf32(kv * e_dn);
                     kh = to_tf32(kv * (e_dn * ekh));
                 }
-                st_f32(smem + OFF_QK, sw128_offset(r, tid, 128, 4), qt);
-                st_f32(smem + OFF_QK, sw128_offset(r + 64, tid, 128, 4), kr);
-                st_f32(smem + OFF_KS, sw128_offset(r, tid, 64, 4), ks);
-                st_f32(smem + OFF_KH, sw128_offset(tid, r, 128, 4), kh);
-                krt[r & 31] = kr;
-                if ((r & 31) == 31) tmem_st32(tmem + lane_base + T_O + (r & 32), krt);
+                st_f32(smem + OFF_QK, sw128_offset(r, ch, 128, 4), qt);
+                st_f32(smem + OFF_QK, sw128_offset(r + 64, ch, 128, 4), kr);
+                st_f32(smem + OFF_KS, sw128_offset(r, ch, 64, 4), ks);
+                st_f32(smem + OFF_KH, sw128_offset(ch, r, 128, 4), kh);
+                krt[i] = kr;
             }
+            tmem_st16(tmem + lane_base + T_O + 16 * grp, krt);
             tmem_wait_st();
             if (Ln > 0) load_g(tn, Ln);  // next chunk, consumed next iteration
             fence_proxy_async_smem();
@@ -341,17 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 mma_commit(bar_mma);
             }
             {   // S_op = tf32(e^{m_k} S[k][v]);  S_acc = e^{Gam_L,k} S[k][v]
-                float r[32], o32[32];
-                for (int cb = 0; cb < 4; ++cb) {
-                    tmem_ld32(tmem + lane_base + T_SACC + 32 * cb, r);
+                float r[16], o16[16];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c0 = 32 * grp + 16 * half;
+                    tmem_ld16(tmem + lane_base + T_SACC + c0, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        o32[j] = to_tf32(r[j] * s_em[32 * cb + j]);
-                        r[j] = r[j] * s_dec[32 * cb + j];
+                    for (int j = 0; j < 16; ++j) {
+                        o16[j] = to_tf32(r[j] * s_em[c0 + j]);
+                        r[j] = r[j] * s_dec[c0 + j];
                     }
-                    tmem_st32(tmem + lane_base + T_SOP + 32 * cb, o32);
-                    tmem_st32(tmem + lane_base + T_SACC + 32 * cb, r);
+                    tmem_st16(tmem + lane_base + T_SOP + c0, o16);
+                    tmem_st16(tmem + lane_base + T_SACC + c0, r);
                 }
                 tmem_wait_st();
             }
@@ -360,19 +379,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
             ph_mma++;
             tc_fence_after();
-            if (warp >= 2) {
-                const int r = tid - 64;
+            if (quarter >= 2) {
+                const int r = ch - 64;
                 const float br = s_beta[r];
-                float d32[32];
-                for (int cb = 0; cb < 2; ++cb) {
-                    tmem_ld32(tmem + lane_base + T_A + 32 * cb, d32);
-                    tmem_wait_ld();
-                    // Ks is dead once D_A is complete; A_kk overwrites it
+                float d16[16];
+                tmem_ld16(tmem + lane_base + T_A + 16 * grp, d16);
+                tmem_wait_ld();
+                // Ks is dead once D_A is complete; A_kk overwrites it
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int s = 32 * cb + j;
-                        Akk[akk_idx(r, s)] = (s < r) ? br * d32[j] : 0.f;
-                    }
+                for (int j = 0; j < 16; ++j) {
+                    const int s = 16 * grp + j;
+                    Akk[akk_idx(r, s)] = (s < r) ? br * d16[j] : 0.f;
                 }
             }
             __syncthreads();
@@ -428,24 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
             // ---- S6: W' to shared memory (K-major [r][k]); A_qk (K-major [r][s]) ----
             {
-                float w32[32];
-                for (int cb = 0; cb < 2; ++cb) {
-                    tmem_ld32(tmem + lane_base + T_W + 32 * cb, w32);
+                float w16[16];
+                tmem_ld16(tmem + lane_base + T_W + 16 * grp, w16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    st_f32(smem + OFF_KS, sw128_offset(16 * grp + j, ch, 64, 4), to_tf32(w16[j]));
+                if (quarter < 2) {
+                    const int r = ch;
+                    tmem_ld16(tmem + lane_base + T_A + 16 * grp, w16);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        st_f32(smem + OFF_KS, sw128_offset(32 * cb + j, tid, 64, 4), to_tf32(w32[j]));
-                }
-                if (warp < 2) {
-                    const int r = tid;
-                    for (int cb = 0; cb < 2; ++cb) {
-                        tmem_ld32(tmem + lane_base + T_A + 32 * cb, w32);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int s = 32 * cb + j;
-                            st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), (s <= r) ? to_tf32(w32[j]) : 0.f);
-                        }
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = 16 * grp + j;
+                        st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), (s <= r) ? to_tf32(w16[j]) : 0.f);
                     }
                 }
             }
@@ -476,14 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
             // ---- S8: U rounded to tf32 in place (A operand of the next MMAs) ----
             {
-                float u32[32];
-                for (int cb = 0; cb < 2; ++cb) {
-                    tmem_ld32(tmem + lane_base + T_U + 32 * cb, u32);
-                    tmem_wait_ld();
+                float u16[16];
+                tmem_ld16(tmem + lane_base + T_U + 16 * grp, u16);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) u32[j] = to_tf32(u32[j]);
-                    tmem_st32(tmem + lane_base + T_U + 32 * cb, u32);
-                }
+                for (int j = 0; j < 16; ++j) u16[j] = to_tf32(u16[j]);
+                tmem_st16(tmem + lane_base + T_U + 16 * grp, u16);
                 tmem_wait_st();
             }
             tc_fence_before();
@@ -513,20 +524,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
             // ---- S10: outputs ----
             {
-                float o32[32];
-                for (int cb = 0; cb < 2; ++cb) {
-                    tmem_ld32(tmem + lane_base + T_O + 32 * cb, o32);
-                    tmem_wait_ld();
+                float o16[16];
+                tmem_ld16(tmem + lane_base + T_O + 16 * grp, o16);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int r = 32 * cb + j;
-                        if (r < L) {
-                            const int64_t idx = ((tc + r) * H + h) * kD + tid;
-                            if (kOutBf16)
-                                static_cast<__nv_bfloat16 *>(p.o)[idx] = __float2bfloat16_rn(o32[j]);
-                            else
-                                static_cast<float *>(p.o)[idx] = o32[j];
-                        }
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * grp + j;
+                    if (r < L) {
+                        const int64_t idx = ((tc + r) * H + h) * kD + ch;
+                        if (kOutBf16)
+                            static_cast<__nv_bfloat16 *>(p.o)[idx] = __float2bfloat16_rn(o16[j]);
+                        else
+                            static_cast<float *>(p.o)[idx] = o16[j];
                     }
                 }
             }
@@ -539,12 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         // ---- final state ----
         if (p.Sf != nullptr) {
             float r[32];
-            for (int cb = 0; cb < 4; ++cb) {
-                tmem_ld32(tmem + lane_base + T_SACC + 32 * cb, r);
-                tmem_wait_ld();
+            tmem_ld32(tmem + lane_base + T_SACC + 32 * grp, r);
+            tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) p.Sf[state_off + (32 * cb + j) * kD + tid] = r[j];
-            }
+            for (int j = 0; j < 32; ++j) p.Sf[state_off + (32 * grp + j) * kD + ch] = r[j];
         }
     }
 
