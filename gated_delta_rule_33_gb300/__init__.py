@@ -17,6 +17,7 @@ from .kda import (  # noqa: F401
     decode,
     gate,
     kda_chunk_prefill,
+    kda_chunk_prefill_noalloc,
     kda_chunk_prefill_workspace_size,
     kda_gate_fused,
     kda_get_last_device_error,

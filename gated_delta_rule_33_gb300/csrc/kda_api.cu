@@ -144,6 +144,24 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, const int32_t *cu_seqlens, int B,
+                                     int64_t N, int H, int K, int V, float scale,
+                                     const float *initial_state, float *final_state, void *o,
+                                     kda_dtype o_dtype, void *stream) {
+    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    void *scratch = nullptr;
+    size_t scratch_bytes = 0;
+    if (kda::builtin_prefill_scratch(&scratch, &scratch_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    if (kda::prefill_workspace_bytes(N, B, H) > scratch_bytes) return KDA_ERR_WORKSPACE_TOO_SMALL;
+    return kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, B, N, H, K, V, scale, initial_state,
+                             final_state, o, o_dtype, scratch, scratch_bytes, stream);
+}
+
 kda_status kda_recurrent_decode(const void *q, const void *k, const void *v, const float *g,
                                 const float *beta, float *state, int B, int H, int K, int V,
                                 float scale, void *o, kda_dtype o_dtype, void *stream) {

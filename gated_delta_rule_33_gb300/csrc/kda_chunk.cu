@@ -34,6 +34,8 @@
 // of columns in every tensor-memory epilogue.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -644,4 +646,41 @@ cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     return cudaGetLastError();
 }
 
+// ---- built-in scratch for callers that cannot allocate ---------------------------------
+//
+// kda_chunk_prefill_noalloc() (include/kda.h) runs the same launch as
+// kda_chunk_prefill() but takes its scratch from this file-scope device array
+// instead of a caller-provided workspace.  Every GPU that loads the library
+// holds the array until the process exits, and every call on a device shares
+// it, so calls whose kernels overlap on the GPU race on it.
+namespace {
+constexpr size_t kBuiltinScratchBytes = 4096;
+static __device__ __align__(256) unsigned char g_builtin_scratch[kBuiltinScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+void *g_builtin_scratch_ptr[kMaxScratchDevices];
+std::mutex g_builtin_scratch_mutex;
+}  // namespace
+
+// The device address of the built-in scratch on the current device.  The
+// first call on a device looks it up with cudaGetSymbolAddress (the array's
+// name is a host-side stand-in, not a device address); later calls reuse it.
+cudaError_t builtin_prefill_scratch(void **ptr, size_t *bytes) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_builtin_scratch_mutex);
+    if (g_builtin_scratch_ptr[dev] == nullptr) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_builtin_scratch);
+        if (e != cudaSuccess) return e;
+        g_builtin_scratch_ptr[dev] = addr;
+    }
+    *ptr = g_builtin_scratch_ptr[dev];
+    *bytes = kBuiltinScratchBytes;
+    return cudaSuccess;
+}
+
 }  // namespace kda
+

@@ -73,6 +73,9 @@ def load():
         lib.kda_chunk_prefill.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, P, I, P,
                                           ctypes.c_size_t, P]
         lib.kda_chunk_prefill.restype = I
+        lib.kda_chunk_prefill_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, P,
+                                                  I, P]
+        lib.kda_chunk_prefill_noalloc.restype = I
         lib.kda_recurrent_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, I, P]
         lib.kda_recurrent_decode.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
@@ -141,6 +144,19 @@ def kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, scale, initial_state, final_
                                   _dtype_code(o), _p(workspace), ws_bytes,
                                   _stream(stream, q.device))
     _check(st, "kda_chunk_prefill")
+
+
+def kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, scale, initial_state, final_state, o,
+                              stream=None):
+    """kda_chunk_prefill with the library's built-in scratch instead of a workspace."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_chunk_prefill_noalloc(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), B,
+                                          N, H, K, V, float(scale), _p(initial_state),
+                                          _p(final_state), _p(o), _dtype_code(o),
+                                          _stream(stream, q.device))
+    _check(st, "kda_chunk_prefill_noalloc")
 
 
 def kda_recurrent_decode(q, k, v, g, beta, state, scale, o, stream=None):

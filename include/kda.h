@@ -149,6 +149,32 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v,
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_chunk_prefill_noalloc -- kda_chunk_prefill without a workspace argument,
+ * for callers that cannot allocate device memory: a host plugin interface that
+ * hands the library only its input and output buffers and offers no way to ask
+ * for scratch, or a serving process that reserved all device memory at start-up
+ * and must not call cudaMalloc afterwards (it can fail, and it can synchronise
+ * the device).  The pages this library follows have no counterpart to it.
+ *
+ * Arguments, layouts and results are those of kda_chunk_prefill.  The scratch
+ * comes from a device array built into the library (4096 bytes; every GPU that
+ * loads the library holds it until the process exits).  Sizes whose
+ * kda_chunk_prefill_workspace_size() exceeds it are rejected with
+ * KDA_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing: it never calls
+ * cudaMalloc, cudaFree or any allocating library routine.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current, so make that first call before any stream capture.  All
+ * calls on a device share the array: calls whose kernels overlap on the GPU
+ * (on different streams) race on it; calls in stream order do not.
+ */
+kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
+                                     const float *g, const float *beta,
+                                     const int32_t *cu_seqlens, int B,
+                                     int64_t N, int H, int K, int V, float scale,
+                                     const float *initial_state, float *final_state,
+                                     void *o, kda_dtype o_dtype, void *stream);
+
+/*
  * kda_recurrent_decode -- the fused recurrent KDA regime for one-token cached
  * decoding (code-audit.json, finding "dual-kda-execution-regimes"): one new
  * token for each of B sequences, the state updated in place.
