@@ -56,7 +56,7 @@ constexpr uint32_t OFF_Q = 0;            // raw q bf16 [64][128] (TMA, no swizzl
 constexpr uint32_t OFF_K = 16384;        // raw k bf16 [64][128] (TMA, no swizzle)
 constexpr uint32_t OFF_V = 32768;        // raw v bf16 [64 s][128 v] (TMA, 2 swizzled boxes)
 constexpr uint32_t OFF_QK = 49152;       // [Qt ; Kr] tf32, 128 rows (r) x 128 (channel)
-constexpr uint32_t OFF_KS = 114688;      // Ks tf32 64 x 128 -> A_kk | T fp32 -> W' tf32 64 x 128
+constexpr uint32_t OFF_KS = 114688;      // g fp32 64 x 128 (TMA) -> Ks tf32 -> A_kk | T fp32 -> W' tf32
 constexpr uint32_t OFF_KH = 147456;      // Khat^T tf32, 128 rows (channel) x 64 (r)
 constexpr uint32_t OFF_TB = 180224;      // T beta tf32 64 x 64 -> A_qk tf32 64 x 64
 constexpr uint32_t OFF_TB16 = 196608;    // T beta bf16 hi 64 x 64 | lo 64 x 64
@@ -66,9 +66,10 @@ constexpr uint32_t MISC_EM = 256;        // float[128] e^{m}
 constexpr uint32_t MISC_DEC = 768;       // float[128] e^{Gam_L}
 constexpr uint32_t MISC_P = 1280;        // float[3][256] T-inverse scratch
 constexpr uint32_t MISC_PART = 4352;     // float[4][128] partial decay sums per row group
-constexpr uint32_t MISC_BAR = 6400;      // 3 mbarriers
-constexpr uint32_t MISC_CTRL = 6432;     // int[8]: tmem base, chain, abort, decay flag
-constexpr uint32_t kSmemBytes = OFF_MISC + 6464;
+constexpr uint32_t MISC_BNEXT = 6400;    // float[64] beta of the next chunk (cp.async)
+constexpr uint32_t MISC_BAR = 6656;      // 4 mbarriers
+constexpr uint32_t MISC_CTRL = 6688;     // int[8]: tmem base, chain, abort, decay flag
+constexpr uint32_t kSmemBytes = OFF_MISC + 6720;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 // Tensor memory columns (lane = M row).
@@ -104,20 +105,29 @@ __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
 // one thread per row can write it without shared-memory bank conflicts.
 __device__ __forceinline__ int akk_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
 
-// Waits (bounded) on an mbarrier phase; on time-out raises the CTA abort flag.
-__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity, int *abort_flag,
-                                              unsigned int *err) {
-    if (!mbar_wait_bounded(bar, parity, kMaxPolls)) {
+// Thread 0 waits (bounded) on an mbarrier phase, then the whole CTA meets at a
+// barrier; a time-out raises the CTA abort flag, which every thread reads
+// after the barrier.  Only one thread polls, so the other warps do not compete
+// with the tensor core for shared-memory bandwidth while they wait.
+__device__ __forceinline__ void cta_wait(uint64_t *bar, uint32_t parity, int *abort_flag,
+                                         unsigned int *err, int tid) {
+    if (tid == 0 && !mbar_wait_bounded(bar, parity, kMaxPolls)) {
         *abort_flag = 1;
         record_device_error(err, kDevTimeout);
     }
+    __syncthreads();
+    tc_fence_after();
 }
 
 // T = (I + A)^{-1} for a 64x64 strictly lower-triangular A (fp32, akk_idx
-// layout), by 16x16 blocks: diagonal blocks by forward substitution, then
-// T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj along the block sub-diagonals.
-// T is row-major with stride 64.
-__device__ void ut_inverse(const float *A, float *T, float *P, int tid) {
+// layout), by 16x16 blocks.  Diagonal blocks by forward substitution in its
+// right-looking form (once x_s is final, subtract A[r][s] x_s from every later
+// row), whose dependency depth is 15 steps of independent FMAs.  Then the
+// off-diagonal blocks along the block sub-diagonals d = 1, 2, 3:
+//   P_ij = sum_{m=j}^{i-1} A_im T_mj,   T_ij = -T_ii P_ij,   i = j + d.
+// Each thread computes four adjacent columns of a block row (one broadcast A
+// load and one 16-byte T load per four FMAs).  T is row-major, stride 64.
+__device__ __noinline__ void ut_inverse(const float *A, float *T, float *P, int tid) {
     for (int e = tid; e < 64 * 64; e += kThreads) {
         const int r = e >> 6, c = e & 63;
         if ((c >> 4) > (r >> 4)) T[e] = 0.f;
@@ -126,39 +136,48 @@ __device__ void ut_inverse(const float *A, float *T, float *P, int tid) {
         const int bb = tid >> 4, j = tid & 15, base = bb * 16;
         float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == j) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc -= A[akk_idx(base + r, base + s)] * x[s];
-            x[r] = acc;
+        for (int s = 0; s < 15; ++s) {
+            const float xs = x[s];
+#pragma unroll
+            for (int r = s + 1; r < 16; ++r) x[r] -= A[akk_idx(base + r, base + s)] * xs;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(base + r) * 64 + base + j] = x[r];
     }
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
-        const int ntgt = 4 - d;
-        // P_t = sum_{m=j}^{i-1} A_im T_mj for the targets (i, j) = (t + d, t)
-        for (int e = tid; e < ntgt * 256; e += kThreads) {
-            const int t = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int ntasks = (4 - d) * 64;  // (target, row, column quad)
+        if (tid < ntasks) {
+            const int t = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
             const int j = t, i = t + d;
-            float acc = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int m = j; m < i; ++m) {
 #pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    acc += A[akk_idx(16 * i + r, 16 * m + s)] * T[(16 * m + s) * 64 + 16 * j + cc];
+                for (int s = 0; s < 16; ++s) {
+                    const float a = A[akk_idx(16 * i + r, 16 * m + s)];
+                    const float4 tv = *reinterpret_cast<const float4 *>(&T[(16 * m + s) * 64 + 16 * j + c4]);
+                    acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
+                }
             }
-            P[e] = acc;
+            *reinterpret_cast<float4 *>(&P[(t << 8) + (r << 4) + c4]) = acc;
         }
         __syncthreads();
-        for (int e = tid; e < ntgt * 256; e += kThreads) {
-            const int t = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        if (tid < ntasks) {
+            const int t = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
             const int j = t, i = t + d;
-            float acc = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int s = 0; s < 16; ++s)
-                acc += T[(16 * i + r) * 64 + 16 * i + s] * P[(t << 8) + (s << 4) + cc];
-            T[(16 * i + r) * 64 + 16 * j + cc] = -acc;
+            for (int s = 0; s < 16; ++s) {
+                if (s <= r) {
+                    const float a = T[(16 * i + r) * 64 + 16 * i + s];
+                    const float4 pv = *reinterpret_cast<const float4 *>(&P[(t << 8) + (s << 4) + c4]);
+                    acc.x += a * pv.x; acc.y += a * pv.y; acc.z += a * pv.z; acc.w += a * pv.w;
+                }
+            }
+            *reinterpret_cast<float4 *>(&T[(16 * i + r) * 64 + 16 * j + c4]) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
@@ -168,6 +187,7 @@ template <bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                             const __grid_constant__ CUtensorMap tm_k,
                                                             const __grid_constant__ CUtensorMap tm_v,
+                                                            const __grid_constant__ CUtensorMap tm_g,
                                                             const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -180,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     uint64_t *bar_qk = reinterpret_cast<uint64_t *>(misc + MISC_BAR);
     uint64_t *bar_v = bar_qk + 1;
     uint64_t *bar_mma = bar_qk + 2;
+    uint64_t *bar_g = bar_qk + 3;
+    float *s_bnext = reinterpret_cast<float *>(misc + MISC_BNEXT);
     int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [3] decay
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -193,10 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         mbar_init(bar_qk, 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_g, 1);
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_g);
         ctrl[2] = 0;
         ctrl[3] = 0;
     }
@@ -209,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
     // Phases consumed so far (identical in every thread) and, in thread 0,
     // whether a TMA batch is in flight.
-    uint32_t ph_qk = 0, ph_v = 0, ph_mma = 0;
-    bool pend_qk = false, pend_v = false;
+    uint32_t ph_qk = 0, ph_v = 0, ph_mma = 0, ph_g = 0;
+    bool pend_qk = false, pend_v = false, pend_g = false;
 
     const uint32_t a_qk = smem_addr(smem + OFF_QK);
     const uint32_t a_ks = smem_addr(smem + OFF_KS);
@@ -261,24 +285,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tma_load_3d(smem + OFF_V + 8192, &tm_v, bar_v, 64, h, static_cast<int32_t>(tc));
             pend_v = true;
         };
-        // g of the thread's 16 chunk rows (one channel) and beta (one row per
-        // thread of the first 64) in registers, loaded one chunk ahead.
-        float gam[16];
-        float breg = 0.f;
-        auto load_g = [&](int64_t tc, int L) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = 16 * grp + i;
-                gam[i] = (r < L) ? p.g[((tc + r) * H + h) * kD + ch] : 0.f;
-            }
-            breg = (tid < L) ? p.beta[(tc + tid) * H + h] : 0.f;
+        // g of the chunk: one TMA tile into the OFF_KS region; beta: one
+        // zero-filled 4-byte cp.async per row into s_bnext (threads 0..63).
+        auto issue_g = [&](int64_t tc) {
+            mbar_arrive_expect_tx(bar_g, 32768);
+            tma_load_3d(smem + OFF_KS, &tm_g, bar_g, 0, h, static_cast<int32_t>(tc));
+            pend_g = true;
+        };
+        auto load_beta = [&](int64_t tc, int L) {
+            if (tid < kC)
+                cp_async_4(&s_bnext[tid], p.beta + ((tid < L) ? (tc + tid) * H + h : 0), tid < L);
         };
         if (t1 > t0) {
             if (tid == 0) {
+                issue_g(t0);
                 issue_qk(t0);
                 issue_v(t0);
             }
-            load_g(t0, static_cast<int>((t1 - t0) < kC ? (t1 - t0) : kC));
+            load_beta(t0, static_cast<int>((t1 - t0) < kC ? (t1 - t0) : kC));
         }
 
         for (int64_t tc = t0; tc < t1; tc += kC) {
@@ -287,17 +311,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             const int Ln = static_cast<int>(tn >= t1 ? 0 : ((t1 - tn) < kC ? (t1 - tn) : kC));
 
             // ---- S1: cumulative decay, references, operands ----
+            cp_async_wait_all();
+            cta_wait(bar_g, ph_g & 1, &ctrl[2], p.err, tid);
+            ph_g++;
+            pend_g = false;
+            float gam[16];
             {
+                const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
-                    acc += gam[i];
+                    const int r = 16 * grp + i;
+                    acc += (r < L) ? gt[r * kD + ch] : 0.f;
                     gam[i] = acc;
                 }
                 s_part[grp * kD + ch] = acc;
             }
-            if (tid < kC) s_beta[tid] = breg;
-            __syncthreads();
+            if (tid < kC) s_beta[tid] = s_bnext[tid];
+            __syncthreads();  // every g read is done before Ks overwrites the tile
             float prefix = 0.f, gam_l = 0.f;
 #pragma unroll
             for (int g2 = 0; g2 < 4; ++g2) {
@@ -313,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
             const float ekh = __expf(gam_l - m);
             const float qscale = p.scale;
-            wait_or_abort(bar_qk, ph_qk & 1, &ctrl[2], p.err);
+            cta_wait(bar_qk, ph_qk & 1, &ctrl[2], p.err, tid);
             ph_qk++;
             pend_qk = false;
-            float krt[16];
+            float krt[16], khv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = 16 * grp + i;
@@ -335,12 +366,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 st_f32(smem + OFF_QK, sw128_offset(r, ch, 128, 4), qt);
                 st_f32(smem + OFF_QK, sw128_offset(r + 64, ch, 128, 4), kr);
                 st_f32(smem + OFF_KS, sw128_offset(r, ch, 64, 4), ks);
-                st_f32(smem + OFF_KH, sw128_offset(ch, r, 128, 4), kh);
+                khv[i] = kh;
                 krt[i] = kr;
             }
+            // Khat^T row ch, columns r = 16 grp .. +15: four 16-byte stores
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<float4 *>(smem + OFF_KH + sw128_offset(ch, 16 * grp + 4 * q4, 128, 4)) =
+                    make_float4(khv[4 * q4], khv[4 * q4 + 1], khv[4 * q4 + 2], khv[4 * q4 + 3]);
             tmem_st16(tmem + lane_base + T_O + 16 * grp, krt);
             tmem_wait_st();
-            if (Ln > 0) load_g(tn, Ln);  // next chunk, consumed next iteration
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -378,9 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
 
             // ---- S3: A_kk from the k-side rows of D_A ----
-            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
-            tc_fence_after();
             if (quarter >= 2) {
                 const int r = ch - 64;
                 const float br = s_beta[r];
@@ -438,10 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 mma_commit(bar_mma);
             }
             ph_v++;
-            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
-            tc_fence_after();
-            __syncthreads();
             if (ctrl[2] != 0) break;
             if (tid == 0 && Ln > 0) issue_v(tn);
 
@@ -485,9 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
-            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
-            tc_fence_after();
+            // W' (in OFF_KS) is consumed: stage the next chunk's g and beta
+            if (Ln > 0) {
+                if (tid == 0) issue_g(tn);
+                load_beta(tn, Ln);
+            }
 
             // ---- S8: U rounded to tf32 in place (A operand of the next MMAs) ----
             {
@@ -520,9 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
-            wait_or_abort(bar_mma, ph_mma & 1, &ctrl[2], p.err);
+            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
-            tc_fence_after();
 
             // ---- S10: outputs ----
             {
@@ -559,9 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
     // Drain: after an abort, wait (bounded) for TMA batches still in flight so
     // that no copy lands in shared memory after this CTA has exited.
+    cp_async_wait_all();
     if (tid == 0) {
         if (pend_qk) mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls);
         if (pend_v) mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls);
+        if (pend_g) mbar_wait_bounded(bar_g, ph_g & 1, kMaxPolls);
         if (ctrl[3] != 0) record_device_error(p.err, kDevDecayRange);
     }
     tc_fence_before();
@@ -588,17 +625,21 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Tensor map of a [N, H, 128] bf16 tensor with a (box_x, 1, 64) box.
-bool make_map(CUtensorMap *map, const void *base, int64_t N, int H, uint32_t box_x, bool swizzle) {
+// Tensor map of a [N, H, 128] tensor (bf16, or fp32 when `f32`) with a
+// (box_x, 1, 64) box.
+bool make_map(CUtensorMap *map, const void *base, int64_t N, int H, uint32_t box_x, bool swizzle,
+              bool f32 = false) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(N)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                                   static_cast<cuuint64_t>(H) * kD * 2};
+    const cuuint64_t esize = f32 ? 4 : 2;
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * esize,
+                                   static_cast<cuuint64_t>(H) * kD * esize};
     const cuuint32_t box[3] = {box_x, 1, static_cast<cuuint32_t>(kC)};
     const cuuint32_t es[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+    return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides,
               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -628,10 +669,10 @@ cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
         if (e != cudaSuccess) return e;
         attr_done[o_bf16 ? 1 : 0] = true;
     }
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mg;
     const int64_t Nmap = N > 0 ? N : 1;
     if (!make_map(&mq, q, Nmap, H, 128, false) || !make_map(&mk, k, Nmap, H, 128, false) ||
-        !make_map(&mv, v, Nmap, H, 64, true))
+        !make_map(&mv, v, Nmap, H, 64, true) || !make_map(&mg, g, Nmap, H, 128, false, true))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
@@ -640,9 +681,9 @@ cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     const int chains = B * H;
     const int grid = chains < num_sms ? chains : num_sms;
     if (o_bf16)
-        chunk_kernel<true><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, p);
+        chunk_kernel<true><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
     else
-        chunk_kernel<false><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, p);
+        chunk_kernel<false><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
     return cudaGetLastError();
 }
 

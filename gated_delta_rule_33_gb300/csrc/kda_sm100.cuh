@@ -80,6 +80,19 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---- cp.async (small asynchronous global -> shared copies) -------------------------------
+
+// Copies 4 bytes, or writes 4 zero bytes when `valid` is false (src is not read).
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(smem_dst)),
+                 "l"(gmem_src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---- tcgen05: tensor memory ------------------------------------------------------------
 
 // Allocates `ncols` TMEM columns (power of two >= 32); the base address is
@@ -242,10 +255,10 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 
 // Rounds an fp32 value to tf32 (10 explicit mantissa bits), to nearest, ties
 // away from zero; the result is an fp32 bit pattern with the low 13 bits zero.
+// Adding half a tf32 unit to the magnitude bits and clearing the 13 low bits
+// is that rounding for every finite input (sign and magnitude are separate).
 __device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 // Byte offset of element (row, col) of a K-major operand tile stored with the
