@@ -64,12 +64,14 @@ constexpr uint32_t OFF_MISC = 212992;
 constexpr uint32_t MISC_BETA = 0;        // float[64]
 constexpr uint32_t MISC_EM = 256;        // float[128] e^{m}
 constexpr uint32_t MISC_DEC = 768;       // float[128] e^{Gam_L}
-constexpr uint32_t MISC_P = 1280;        // float[3][256] T-inverse scratch
-constexpr uint32_t MISC_PART = 4352;     // float[4][128] partial decay sums per row group
-constexpr uint32_t MISC_BNEXT = 6400;    // float[64] beta of the next chunk (cp.async)
-constexpr uint32_t MISC_BAR = 6656;      // 4 mbarriers
-constexpr uint32_t MISC_CTRL = 6688;     // int[8]: tmem base, chain, abort, decay flag
-constexpr uint32_t kSmemBytes = OFF_MISC + 6720;
+constexpr uint32_t MISC_P = 1280;        // float[4][256] T-inverse partial products
+constexpr uint32_t MISC_PART = 5376;     // float[4][128] partial decay sums per row group
+constexpr uint32_t MISC_BNEXT = 7424;    // float[64] beta of the next chunk (cp.async)
+constexpr uint32_t MISC_DIAG = 7680;     // float[4][16][16] diagonal blocks of A_kk, column-major
+constexpr uint32_t MISC_TDIAG = 11776;   // float[4][16][16] diagonal blocks of T, column-major
+constexpr uint32_t MISC_BAR = 15872;     // 4 mbarriers
+constexpr uint32_t MISC_CTRL = 15904;    // int[8]: tmem base, chain, abort, decay flag
+constexpr uint32_t kSmemBytes = OFF_MISC + 15936;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 // Tensor memory columns (lane = M row).
@@ -119,68 +121,132 @@ __device__ __forceinline__ void cta_wait(uint64_t *bar, uint32_t parity, int *ab
     tc_fence_after();
 }
 
-// T = (I + A)^{-1} for a 64x64 strictly lower-triangular A (fp32, akk_idx
-// layout), by 16x16 blocks.  Diagonal blocks by forward substitution in its
-// right-looking form (once x_s is final, subtract A[r][s] x_s from every later
-// row), whose dependency depth is 15 steps of independent FMAs.  Then the
-// off-diagonal blocks along the block sub-diagonals d = 1, 2, 3:
-//   P_ij = sum_{m=j}^{i-1} A_im T_mj,   T_ij = -T_ii P_ij,   i = j + d.
-// Each thread computes four adjacent columns of a block row (one broadcast A
-// load and one 16-byte T load per four FMAs).  T is row-major, stride 64.
-__device__ __noinline__ void ut_inverse(const float *A, float *T, float *P, int tid) {
-    for (int e = tid; e < 64 * 64; e += kThreads) {
-        const int r = e >> 6, c = e & 63;
-        if ((c >> 4) > (r >> 4)) T[e] = 0.f;
+// T beta[r][s] = T[r][s] beta_s as a tf32 operand tile and as bf16 high + low
+// tiles (all K-major [r][s], 128-byte swizzle), four adjacent s at a time.
+__device__ __forceinline__ void store_tbeta4(uint8_t *smem, int r, int s4, float4 t,
+                                             const float *beta) {
+    const float x0 = t.x * beta[s4], x1 = t.y * beta[s4 + 1];
+    const float x2 = t.z * beta[s4 + 2], x3 = t.w * beta[s4 + 3];
+    *reinterpret_cast<float4 *>(smem + OFF_TB + sw128_offset(r, s4, 64, 4)) =
+        make_float4(to_tf32(x0), to_tf32(x1), to_tf32(x2), to_tf32(x3));
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(x0, x1), h23 = __floats2bfloat162_rn(x2, x3);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(x0 - f01.x, x1 - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(x2 - f23.x, x3 - f23.y);
+    uint2 hv, lv;
+    hv.x = *reinterpret_cast<const uint32_t *>(&h01); hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+    lv.x = *reinterpret_cast<const uint32_t *>(&l01); lv.y = *reinterpret_cast<const uint32_t *>(&l23);
+    *reinterpret_cast<uint2 *>(smem + OFF_TB16 + sw128_offset(r, s4, 64, 2)) = hv;
+    *reinterpret_cast<uint2 *>(smem + OFF_TB16 + 8192 + sw128_offset(r, s4, 64, 2)) = lv;
+}
+
+// One block sub-diagonal d of T = (I + A)^{-1}:  T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj
+// for i = j + d.  Each term A_im T_mj is computed by its own 64 threads (16 rows
+// x 4 column quads); the -T_ii (sum of terms) step reads T_ii column-major.
+template <int D>
+__device__ __forceinline__ void ut_round(const float *A, const float *Tdiag, float *T, float *P,
+                                         uint8_t *smem, const float *beta, int tid) {
+    constexpr int kTargets = 4 - D;
+    if (tid < kTargets * D * 64) {
+        const int t = tid / (D * 64), rem = tid % (D * 64);
+        const int mp = rem >> 6, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
+        const int j = t, i = t + D, m = j + mp;
+        const int arow = 16 * i + r;
+        const float *Ar = A + arow * 64;
+        const int sw = arow & 31, acol = 16 * m;
+        const float *Tb = T + (16 * m) * 64 + 16 * j + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const float a = Ar[(acol + s) ^ sw];
+            const float4 tv = *reinterpret_cast<const float4 *>(Tb + s * 64);
+            acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
+        }
+        *reinterpret_cast<float4 *>(&P[((t * D + mp) << 8) + (r << 4) + c4]) = acc;
     }
+    __syncthreads();
+    if (tid < kTargets * 64) {
+        const int t = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const int j = t, i = t + D;
+        const float *Ti = Tdiag + i * 256 + r;        // T_ii[r][s] at Ti[16 s]
+        const float *Pb = P + ((t * D) << 8) + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            float4 pv = *reinterpret_cast<const float4 *>(Pb + s * 16);
+#pragma unroll
+            for (int mp = 1; mp < D; ++mp) {
+                const float4 p2 = *reinterpret_cast<const float4 *>(Pb + (mp << 8) + s * 16);
+                pv.x += p2.x; pv.y += p2.y; pv.z += p2.z; pv.w += p2.w;
+            }
+            const float a = Ti[16 * s];   // zero above the diagonal
+            acc.x += a * pv.x; acc.y += a * pv.y; acc.z += a * pv.z; acc.w += a * pv.w;
+        }
+        const float4 tij = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        *reinterpret_cast<float4 *>(&T[(16 * i + r) * 64 + 16 * j + c4]) = tij;
+        store_tbeta4(smem, 16 * i + r, 16 * j + c4, tij, beta);
+    }
+    __syncthreads();
+}
+
+// T = (I + A)^{-1} for a 64x64 strictly lower-triangular A (fp32, akk_idx
+// layout; `Adiag` holds its four 16x16 diagonal blocks column-major), by 16x16
+// blocks.  Diagonal blocks by forward substitution in its right-looking form
+// (once x_s is final, subtract A[r][s] x_s from every later row): 15 steps of
+// independent FMAs, each step reading one block column as four broadcast
+// 16-byte loads.  Then the off-diagonal blocks along the block sub-diagonals
+// d = 1, 2, 3 (ut_round).  T is row-major with stride 64; its strictly upper
+// blocks are left unwritten; Tdiag receives the diagonal blocks column-major.
+// Every lower block of T beta is written as soon as its block of T is final
+// (the strictly upper blocks of the T beta tiles hold zeros written once).
+// While warps 0-1 solve the diagonal blocks, warps 4-15 run `side_work`.
+template <typename SideWork>
+__device__ __forceinline__ void ut_inverse(const float *A, const float *Adiag, float *T,
+                                           float *Tdiag, float *P, uint8_t *smem,
+                                           const float *beta, int tid, SideWork side_work) {
     if (tid < 64) {
         const int bb = tid >> 4, j = tid & 15, base = bb * 16;
+        const float *Ab = Adiag + bb * 256;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
         for (int s = 0; s < 15; ++s) {
+            float col[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 v = *reinterpret_cast<const float4 *>(Ab + s * 16 + 4 * q4);
+                col[4 * q4] = v.x; col[4 * q4 + 1] = v.y; col[4 * q4 + 2] = v.z; col[4 * q4 + 3] = v.w;
+            }
             const float xs = x[s];
 #pragma unroll
-            for (int r = s + 1; r < 16; ++r) x[r] -= A[akk_idx(base + r, base + s)] * xs;
+            for (int r = s + 1; r < 16; ++r) x[r] -= col[r] * xs;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(base + r) * 64 + base + j] = x[r];
+        float *Td = Tdiag + bb * 256 + j * 16;  // column j of T_bb
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<float4 *>(Td + 4 * q4) =
+                make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+        // T beta of the diagonal block, column j (16 rows)
+        const float bj = beta[base + j];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float xb = x[r] * bj;
+            st_f32(smem, OFF_TB + sw128_offset(base + r, base + j, 64, 4), to_tf32(xb));
+            const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
+            *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + sw128_offset(base + r, base + j, 64, 2)) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + 8192 + sw128_offset(base + r, base + j, 64, 2)) = lo;
+        }
+    } else if (tid >= 128) {
+        side_work();
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-        const int ntasks = (4 - d) * 64;  // (target, row, column quad)
-        if (tid < ntasks) {
-            const int t = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-            const int j = t, i = t + d;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m = j; m < i; ++m) {
-#pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float a = A[akk_idx(16 * i + r, 16 * m + s)];
-                    const float4 tv = *reinterpret_cast<const float4 *>(&T[(16 * m + s) * 64 + 16 * j + c4]);
-                    acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
-                }
-            }
-            *reinterpret_cast<float4 *>(&P[(t << 8) + (r << 4) + c4]) = acc;
-        }
-        __syncthreads();
-        if (tid < ntasks) {
-            const int t = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-            const int j = t, i = t + d;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                if (s <= r) {
-                    const float a = T[(16 * i + r) * 64 + 16 * i + s];
-                    const float4 pv = *reinterpret_cast<const float4 *>(&P[(t << 8) + (s << 4) + c4]);
-                    acc.x += a * pv.x; acc.y += a * pv.y; acc.z += a * pv.z; acc.w += a * pv.w;
-                }
-            }
-            *reinterpret_cast<float4 *>(&T[(16 * i + r) * 64 + 16 * j + c4]) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        }
-        __syncthreads();
-    }
+    ut_round<1>(A, Tdiag, T, P, smem, beta, tid);
+    ut_round<2>(A, Tdiag, T, P, smem, beta, tid);
+    ut_round<3>(A, Tdiag, T, P, smem, beta, tid);
 }
 
 template <bool kOutBf16>
@@ -224,6 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         ctrl[2] = 0;
         ctrl[3] = 0;
     }
+    // The strictly upper blocks of the T beta tiles are zero for every chunk and
+    // are never written again (A_qk, which reuses the tf32 tile, is zero there too).
+    for (int e = tid; e < 16384 / 16; e += kThreads)
+        reinterpret_cast<float4 *>(smem + OFF_TB)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = tid; e < 16384 / 16; e += kThreads)
+        reinterpret_cast<float4 *>(smem + OFF_TB16)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -242,8 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint32_t a_tb = smem_addr(smem + OFF_TB);
     const uint32_t a_tb16 = smem_addr(smem + OFF_TB16);
     const uint32_t a_v = smem_addr(smem + OFF_V);
+    // Shared-memory descriptors of every operand tile (128-byte swizzle), built
+    // once; a k-step adds its constant byte offset / 16 to the start address.
+    const uint64_t d_qk = smem_desc(a_qk, 16, 1024, kSwizzle128B);
+    const uint64_t d_ks = smem_desc(a_ks, 16, 1024, kSwizzle128B);
+    const uint64_t d_kh = smem_desc(a_kh, 16, 1024, kSwizzle128B);
+    const uint64_t d_tb = smem_desc(a_tb, 16, 1024, kSwizzle128B);
+    const uint64_t d_tb16 = smem_desc(a_tb16, 16, 1024, kSwizzle128B);
+    const uint64_t d_v = smem_desc(a_v, 8192, 1024, kSwizzle128B);  // MN-major, 64-wide M blocks
     float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
     float *Tm = Akk + 64 * 64;
+    float *s_diag = reinterpret_cast<float *>(misc + MISC_DIAG);
+    float *s_tdiag = reinterpret_cast<float *>(misc + MISC_TDIAG);
 
     while (true) {
         __syncthreads();
@@ -312,9 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
             // ---- S1: cumulative decay, references, operands ----
             cp_async_wait_all();
+            if (tid == 0 && !mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls)) {
+                ctrl[2] = 1;
+                record_device_error(p.err, kDevTimeout);
+            }
             cta_wait(bar_g, ph_g & 1, &ctrl[2], p.err, tid);
             ph_g++;
+            ph_qk++;
             pend_g = false;
+            pend_qk = false;
             float gam[16];
             {
                 const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
@@ -344,9 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
             const float ekh = __expf(gam_l - m);
             const float qscale = p.scale;
-            cta_wait(bar_qk, ph_qk & 1, &ctrl[2], p.err, tid);
-            ph_qk++;
-            pend_qk = false;
             float krt[16], khv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -388,28 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 const uint32_t id = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t ad = smem_desc(a_qk + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(a_ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t ad = (d_qk + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
+                    const uint64_t bd = (d_ks + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
                     mma_tf32_ss(tmem + T_A, ad, bd, id, kk > 0);
                 }
                 mma_commit(bar_mma);
-            }
-            {   // S_op = tf32(e^{m_k} S[k][v]);  S_acc = e^{Gam_L,k} S[k][v]
-                float r[16], o16[16];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int c0 = 32 * grp + 16 * half;
-                    tmem_ld16(tmem + lane_base + T_SACC + c0, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        o16[j] = to_tf32(r[j] * s_em[c0 + j]);
-                        r[j] = r[j] * s_dec[c0 + j];
-                    }
-                    tmem_st16(tmem + lane_base + T_SOP + c0, o16);
-                    tmem_st16(tmem + lane_base + T_SACC + c0, r);
-                }
-                tmem_wait_st();
             }
 
             // ---- S3: A_kk from the k-side rows of D_A ----
@@ -425,22 +494,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int s = 16 * grp + j;
-                    Akk[akk_idx(r, s)] = (s < r) ? br * d16[j] : 0.f;
+                    const float a = (s < r) ? br * d16[j] : 0.f;
+                    Akk[akk_idx(r, s)] = a;
+                    if ((r >> 4) == grp) s_diag[grp * 256 + j * 16 + (r & 15)] = a;
                 }
             }
             __syncthreads();
 
             // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
-            ut_inverse(Akk, Tm, s_P, tid);
-            for (int e = tid; e < 64 * 64; e += kThreads) {
-                const int r = e >> 6, s = e & 63;
-                const float x = Tm[e] * s_beta[s];
-                st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), to_tf32(x));
-                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-                *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + sw128_offset(r, s, 64, 2)) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + 8192 + sw128_offset(r, s, 64, 2)) = lo;
-            }
+            // The state pass runs on warps 4-15 while warps 0-1 solve the
+            // diagonal blocks: S_op = tf32(e^{m_k} S[k][v]); S_acc = e^{Gam_L,k} S[k][v].
+            // Warp w serves lane quarter w % 4 and 16-column slices
+            // (w / 4 - 1) + 3 n of the 128 state columns.
+            auto state_pass = [&]() {
+                float r16[16], o16[16];
+                for (int cs = (warp >> 2) - 1; cs < 8; cs += 3) {
+                    const int c0 = 16 * cs;
+                    tmem_ld16(tmem + lane_base + T_SACC + c0, r16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        o16[j] = to_tf32(r16[j] * s_em[c0 + j]);
+                        r16[j] = r16[j] * s_dec[c0 + j];
+                    }
+                    tmem_st16(tmem + lane_base + T_SOP + c0, o16);
+                    tmem_st16(tmem + lane_base + T_SACC + c0, r16);
+                }
+                tmem_wait_st();
+            };
+            ut_inverse(Akk, s_diag, Tm, s_tdiag, s_P, smem, s_beta, tid, state_pass);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -451,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 const uint32_t idw = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = smem_desc(a_tb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bd = (d_tb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
                     mma_tf32_ts(tmem + T_W, tmem + T_O + kk * 8, bd, idw, kk > 0);
                 }
                 if (!mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
@@ -463,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = smem_desc(a_v + kk * 2048, 8192, 1024, kSwizzle128B);
-                            const uint64_t bd = smem_desc(a_tb16 + part * 8192 + kk * 32, 16, 1024, kSwizzle128B);
+                            const uint64_t ad = (d_v + static_cast<uint64_t>((kk * 2048) >> 4));
+                            const uint64_t bd = (d_tb16 + static_cast<uint64_t>((part * 8192 + kk * 32) >> 4));
                             mma_f16_ss(tmem + T_U, ad, bd, idu, (part | kk) != 0);
                         }
                     }
@@ -507,12 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 const uint32_t ido = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bw = smem_desc(a_ks + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bw = (d_ks + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
                     mma_tf32_ts(tmem + T_U, tmem + T_SOP + kk * 8, bw, idn, 1);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bq = smem_desc(a_qk + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bq = (d_qk + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
                     mma_tf32_ts(tmem + T_O, tmem + T_SOP + kk * 8, bq, ido, kk > 0);
                 }
                 mma_commit(bar_mma);
@@ -546,12 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 const uint32_t ido = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bk = smem_desc(a_kh + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bk = (d_kh + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
                     mma_tf32_ts(tmem + T_SACC, tmem + T_U + kk * 8, bk, ids, 1);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ba = smem_desc(a_tb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t ba = (d_tb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
                     mma_tf32_ts(tmem + T_O, tmem + T_U + kk * 8, ba, ido, 1);
                 }
                 mma_commit(bar_mma);
