@@ -16,6 +16,7 @@ the host cores, on a bounded sample of the same prefill workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -93,20 +94,30 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D):
 # --- clocks ----------------------------------------------------------------------------
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms.  start()
+    returns once the first sample has arrived; stop() keeps only the samples
+    whose timestamps fall inside the marked window."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.gpu_index = gpu_index
+        self.lines = []
+        self.window = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline()  # the sampler is running
+            if first:
+                self.lines.append(first)
         except (FileNotFoundError, OSError):
             self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -117,22 +128,30 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sms, maxes, reasons = [], [], set()
+        sms, maxes, reasons, all_sms = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in (self.lines + out.strip().splitlines()):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sms.append(float(parts[1]))
-                maxes.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
+            all_sms.append(sm)
+            if self.window is not None and not (self.window[0] - 0.03 <= ts <= self.window[1] + 0.03):
+                continue
+            sms.append(sm)
+            maxes.append(mx)
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sms:
-            return None
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": [],
+                    "note": f"timed region shorter than the 20 ms sampling interval; "
+                            f"{len(all_sms)} samples around it, median "
+                            f"{statistics.median(all_sms) if all_sms else None} MHz"}
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
                 "samples": len(sms), "reasons": sorted(reasons)}
 
@@ -295,6 +314,7 @@ def run_ours(args):
     per_step = []
     barrier(world)
     torch.cuda.synchronize(dev)
+    wall0 = time.time()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -305,6 +325,7 @@ def run_ours(args):
         step_events.append(evs)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    sampler.mark(wall0, time.time())
     barrier(world)
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
@@ -409,6 +430,34 @@ def run_ours(args):
     return 0
 
 
+def run_profile_case(args):
+    """A few launches of one kernel at a chosen size, for ncu captures
+    (`ncu -k regex:<kernel> -s <warm-up launches> -c 1 python bench.py --profile ...`).
+    Prints one line; its timings are not bench values."""
+    import gated_delta_rule_33_gb300 as kda
+    from gated_delta_rule_33_gb300 import synth
+    dev = torch.device("cuda", 0)
+    kda.load()
+    if args.profile in ("gate", "prefill"):
+        x = synth.make_inputs(args.size, H=H, D=D, seed=0, device=dev)
+        g, beta = kda.gate(x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
+        for _ in range(args.warmup + 1):
+            if args.profile == "gate":
+                kda.gate(x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
+            else:
+                kda.prefill(x.q, x.k, x.v, g, beta)
+    else:
+        d = synth.make_decode_inputs(args.size, H=H, D=D, seed=0, state_device=dev)
+        q, k, v, f, b = (t.to(dev) for t in (d.q, d.k, d.v, d.f, d.b))
+        g, beta = kda.gate(f, b, d.A_log.to(dev), d.dt_bias.to(dev), d.alog_mode)
+        for _ in range(args.warmup + 1):
+            kda.decode(q, k, v, g, beta, d.state)
+    torch.cuda.synchronize()
+    st = kda.kda_get_last_device_error()
+    print(json.dumps({"profile": args.profile, "size": args.size, "device_error": st}))
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,10 +466,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-heads", type=int, default=8,
                     help="heads of the T=4096 workload per reference-arm step")
-    ap.add_argument("--cpu-heads", type=int, default=24,
+    ap.add_argument("--cpu-heads", type=int, default=96,
                     help="heads of the T=4096 workload timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["gate", "prefill", "decode"], default=None,
+                    help="run only this kernel (warm-up + 1 launch) for an ncu capture")
+    ap.add_argument("--size", type=int, default=1024,
+                    help="--profile size: tokens (gate, prefill) or sequences (decode)")
     args = ap.parse_args()
+    if args.profile is not None:
+        return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

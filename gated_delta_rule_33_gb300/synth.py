@@ -66,31 +66,35 @@ def varlen_lengths(num_seqs: int, lo: int, hi: int, seed: int = 0) -> List[int]:
 def make_inputs(N: Optional[int] = None, H: int = 96, D: int = 128, *, seed: int = 0,
                 lengths: Optional[List[int]] = None, s0_std: float = 0.0,
                 dtype: torch.dtype = torch.bfloat16, f_dtype: Optional[torch.dtype] = None,
-                alog_mode: int = ALOG_PER_CHANNEL, varlen: bool = False) -> KDAInputs:
-    """Draw one KDA problem on the CPU.
+                alog_mode: int = ALOG_PER_CHANNEL, varlen: bool = False,
+                device=None) -> KDAInputs:
+    """Draw one KDA problem (on the CPU unless ``device`` is given, in which
+    case the same draws come from a generator on that device).
 
     ``lengths`` (or ``varlen=True`` with N tokens in one sequence) makes a
     packed batch with int32 cu_seqlens.  ``s0_std`` > 0 draws an initial state
     N(0, s0_std) per (sequence, head)."""
-    gen = torch.Generator().manual_seed(seed)
+    dev = torch.device("cpu") if device is None else torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    kw = {"generator": gen, "device": dev}
     if lengths is not None:
         lengths = [int(x) for x in lengths]
         N = sum(lengths)
     if N is None:
         raise ValueError("N or lengths is required")
     f_dtype = dtype if f_dtype is None else f_dtype
-    q = _unit_rows(torch.randn(N, H, D, generator=gen)).to(dtype)
-    k = _unit_rows(torch.randn(N, H, D, generator=gen)).to(dtype)
-    v = torch.randn(N, H, D, generator=gen).to(dtype)
-    f = torch.randn(N, H, D, generator=gen).to(f_dtype)
-    b = torch.randn(N, H, generator=gen)
+    q = _unit_rows(torch.randn(N, H, D, **kw)).to(dtype)
+    k = _unit_rows(torch.randn(N, H, D, **kw)).to(dtype)
+    v = torch.randn(N, H, D, **kw).to(dtype)
+    f = torch.randn(N, H, D, **kw).to(f_dtype)
+    b = torch.randn(N, H, **kw)
     if alog_mode == ALOG_PER_HEAD:
-        A_log = torch.normal(-0.15, 0.3, (H,), generator=gen)
+        A_log = torch.normal(-0.15, 0.3, (H,), **kw)
     elif alog_mode == ALOG_PER_CHANNEL:
-        A_log = torch.normal(-0.15, 0.3, (D,), generator=gen)
+        A_log = torch.normal(-0.15, 0.3, (D,), **kw)
     else:
-        A_log = torch.normal(-0.15, 0.3, (H, D), generator=gen)
-    dt_bias = torch.normal(-4.6, 1.2, (H, D), generator=gen)
+        A_log = torch.normal(-0.15, 0.3, (H, D), **kw)
+    dt_bias = torch.normal(-4.6, 1.2, (H, D), **kw)
     cu = None
     B = 1
     if lengths is not None or varlen:
@@ -98,9 +102,10 @@ def make_inputs(N: Optional[int] = None, H: int = 96, D: int = 128, *, seed: int
         B = len(lens)
         cu = torch.zeros(B + 1, dtype=torch.int32)
         cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+        cu = cu.to(dev)
     S0 = None
     if s0_std > 0:
-        S0 = torch.normal(0.0, s0_std, (B, H, D, D), generator=gen)
+        S0 = torch.normal(0.0, s0_std, (B, H, D, D), **kw)
     return KDAInputs(q, k, v, f, b, A_log.float(), dt_bias.float(), alog_mode, cu, S0)
 
 
