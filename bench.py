@@ -91,6 +91,32 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D):
     return B * Hh * (2 * K * V * 4 + 2 * K * 2 + 2 * V + 4 * K + 4 + 2 * V)
 
 
+# DRAM read+write bytes per benchmark launch, from the ncu captures summarised
+# in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
+# of the kernel source they were taken on: a changed source reports null.
+NCU_TRAFFIC = {
+    "kda_chunk.cu": {"sha256": "572b1d17dc522819e6f0ed3f231fe0e278b98f3b828fe8ee1ab75fea4b8e4ed1", "bytes": 4 * 139.11e6,
+                     "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
+    "kda_decode.cu": {"sha256": "23fa09c312ad130bff268601ce628625ab6f908a0902f15ac5d86404f0f54c64", "bytes": 4 * 754.49e6,
+                      "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
+    "kda_gate.cu": {"sha256": "c571ed29aa63aa23447ebb39f20cf362297d7d0e0342dce221f132091a056852", "bytes": 246.78e6,
+                    "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
+}
+
+
+def measured_traffic(src_name):
+    import hashlib
+    ent = NCU_TRAFFIC.get(src_name)
+    path = os.path.join(ROOT, "gated_delta_rule_33_gb300", "csrc", src_name)
+    if ent is None or not os.path.exists(path):
+        return None, None
+    with open(path, "rb") as fh:
+        digest = hashlib.sha256(fh.read()).hexdigest()
+    if digest != ent["sha256"]:
+        return None, "kernel changed since the ncu capture"
+    return ent["bytes"], ent["note"]
+
+
 # --- clocks ----------------------------------------------------------------------------
 
 class ClockSampler:
@@ -403,6 +429,9 @@ def run_ours(args):
     rl_gate = {"kernel": "kda gate", "bound": "hbm", "achieved": gate_gbs, "peak": hbm,
                "unit": "GB/s", "frac": gate_gbs / hbm, "traffic": None,
                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": gate_bytes}
+    for rl, src in ((rl_prefill, "kda_chunk.cu"), (rl_decode, "kda_decode.cu"),
+                    (rl_gate, "kda_gate.cu")):
+        rl["traffic"], rl["traffic_note"] = measured_traffic(src)
     # the dominant kernel is the one with the largest share of the step
     roofline = rl_prefill if prefill_ms >= decode_ms_max else rl_decode
     cpu = cpu_baseline(args.cpu_heads) if not args.no_cpu_baseline else None
