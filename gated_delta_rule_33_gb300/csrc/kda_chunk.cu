@@ -76,8 +76,9 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 // Tensor memory columns (lane = M row).
 //   S_acc: S^T fp32 (lane v, column k)      S_op: tf32(e^{m_k} S[k][v])
-//   U: U^T (lane v, column r)               O: O^T; before that Kr^T (lane k, column s)
-//   A: [Qt; Kr] Ks^T (lane = row of [Qt; Kr], column s)   W: W'^T (lane k, column r)
+//   U: U^T (lane v, column r)               O: W'^T (lane k, column r), then O^T
+//   A: [Qt; Kr] Ks^T (lane = row of [Qt; Kr], column s)   W: Kr^T (lane k, column s)
+// O^T of a chunk is read out while the next chunk's first MMA runs.
 constexpr uint32_t T_SACC = 0, T_SOP = 128, T_U = 256, T_O = 320, T_A = 384, T_W = 448;
 
 struct Params {
@@ -106,6 +107,13 @@ __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
 // A_kk is stored row-major with its column index XOR-ed by (row % 32), so that
 // one thread per row can write it without shared-memory bank conflicts.
 __device__ __forceinline__ int akk_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
+
+// 2^x with the special-function unit (inputs here lie within +-116).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Thread 0 waits (bounded) on an mbarrier phase, then the whole CTA meets at a
 // barrier; a time-out raises the CTA abort flag, which every thread reads
@@ -140,51 +148,94 @@ __device__ __forceinline__ void store_tbeta4(uint8_t *smem, int r, int s4, float
     *reinterpret_cast<uint2 *>(smem + OFF_TB16 + 8192 + sw128_offset(r, s4, 64, 2)) = lv;
 }
 
-// One block sub-diagonal d of T = (I + A)^{-1}:  T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj
-// for i = j + d.  Each term A_im T_mj is computed by its own 64 threads (16 rows
-// x 4 column quads); the -T_ii (sum of terms) step reads T_ii column-major.
-template <int D>
-__device__ __forceinline__ void ut_round(const float *A, const float *Tdiag, float *T, float *P,
-                                         uint8_t *smem, const float *beta, int tid) {
-    constexpr int kTargets = 4 - D;
-    if (tid < kTargets * D * 64) {
-        const int t = tid / (D * 64), rem = tid % (D * 64);
-        const int mp = rem >> 6, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
-        const int j = t, i = t + D, m = j + mp;
-        const int arow = 16 * i + r;
+// Level 1 of the off-diagonal blocks: T_10 and T_32 (the block sub-diagonal
+// inside each 32x32 half), T_{t+1,t} = -T_{t+1,t+1} A_{t+1,t} T_tt, t = 0, 2.
+// 64 threads per target: 16 rows x 4 column quads.
+__device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, float *T, float *P,
+                                          uint8_t *smem, const float *beta, int tid) {
+    if (tid < 128) {
+        const int t = 2 * (tid >> 6), r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const int arow = 16 * (t + 1) + r;
         const float *Ar = A + arow * 64;
-        const int sw = arow & 31, acol = 16 * m;
-        const float *Tb = T + (16 * m) * 64 + 16 * j + c4;
+        const int sw = arow & 31;
+        const float *Tb = T + (16 * t) * 64 + 16 * t + c4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            const float a = Ar[(acol + s) ^ sw];
+            const float a = Ar[(16 * t + s) ^ sw];
             const float4 tv = *reinterpret_cast<const float4 *>(Tb + s * 64);
             acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
         }
-        *reinterpret_cast<float4 *>(&P[((t * D + mp) << 8) + (r << 4) + c4]) = acc;
+        *reinterpret_cast<float4 *>(&P[((tid >> 6) << 8) + (r << 4) + c4]) = acc;
     }
     __syncthreads();
-    if (tid < kTargets * 64) {
-        const int t = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        const int j = t, i = t + D;
-        const float *Ti = Tdiag + i * 256 + r;        // T_ii[r][s] at Ti[16 s]
-        const float *Pb = P + ((t * D) << 8) + c4;
+    if (tid < 128) {
+        const int t = 2 * (tid >> 6), r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        const float *Ti = Tdiag + (t + 1) * 256 + r;   // T_{t+1,t+1}[r][s] at Ti[16 s]
+        const float *Pb = P + ((tid >> 6) << 8) + c4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-            float4 pv = *reinterpret_cast<const float4 *>(Pb + s * 16);
-#pragma unroll
-            for (int mp = 1; mp < D; ++mp) {
-                const float4 p2 = *reinterpret_cast<const float4 *>(Pb + (mp << 8) + s * 16);
-                pv.x += p2.x; pv.y += p2.y; pv.z += p2.z; pv.w += p2.w;
-            }
+            const float4 pv = *reinterpret_cast<const float4 *>(Pb + s * 16);
             const float a = Ti[16 * s];   // zero above the diagonal
             acc.x += a * pv.x; acc.y += a * pv.y; acc.z += a * pv.z; acc.w += a * pv.w;
         }
         const float4 tij = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        *reinterpret_cast<float4 *>(&T[(16 * i + r) * 64 + 16 * j + c4]) = tij;
-        store_tbeta4(smem, 16 * i + r, 16 * j + c4, tij, beta);
+        *reinterpret_cast<float4 *>(&T[(16 * (t + 1) + r) * 64 + 16 * t + c4]) = tij;
+        store_tbeta4(smem, 16 * (t + 1) + r, 16 * t + c4, tij, beta);
+    }
+    __syncthreads();
+}
+
+// Level 2: the lower-left 32x32 block X = T[32:64, 0:32] = -T_bot (A_bl T_top),
+// with T_top = T[0:32, 0:32], T_bot = T[32:64, 32:64] (both block lower
+// triangular, complete after level 1) and A_bl = A[32:64, 0:32].
+// 256 threads, 32 rows x 8 column quads; every warp's rows and columns fall in
+// one 16-block, so the triangular bounds are compile-time per branch.
+// Y = A_bl T_top goes through P.
+template <int S0>
+__device__ __forceinline__ float4 level2_y(const float *Ar, int sw, const float *T, int c) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = S0; s < 32; ++s) {
+        const float a = Ar[s ^ sw];
+        const float4 tv = *reinterpret_cast<const float4 *>(&T[s * 64 + c]);
+        acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
+    }
+    return acc;
+}
+
+template <int S1>
+__device__ __forceinline__ float4 level2_x(const float *Tr, const float *P, int c) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < S1; ++s) {
+        const float a = Tr[s];
+        const float4 yv = *reinterpret_cast<const float4 *>(&P[s * 32 + c]);
+        acc.x += a * yv.x; acc.y += a * yv.y; acc.z += a * yv.z; acc.w += a * yv.w;
+    }
+    return acc;
+}
+
+__device__ __forceinline__ void ut_level2(const float *A, float *T, float *P, uint8_t *smem,
+                                          const float *beta, int tid) {
+    // task: column block cb = tid / 128, row r = (tid / 4) % 32, quad q = tid % 4
+    const int cb = tid >> 7, r = (tid >> 2) & 31, c = 16 * cb + 4 * (tid & 3);
+    if (tid < 256) {
+        const int arow = 32 + r;
+        // T_top[s][c] is zero for s < 16 * block(c)
+        const float4 y = (cb == 0) ? level2_y<0>(A + arow * 64, arow & 31, T, c)
+                                   : level2_y<16>(A + arow * 64, arow & 31, T, c);
+        *reinterpret_cast<float4 *>(&P[r * 32 + c]) = y;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        const float *Tr = T + (32 + r) * 64 + 32;   // T_bot[r][s]
+        // T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
+        const float4 acc = (r < 16) ? level2_x<16>(Tr, P, c) : level2_x<32>(Tr, P, c);
+        const float4 x = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        *reinterpret_cast<float4 *>(&T[(32 + r) * 64 + c]) = x;
+        store_tbeta4(smem, 32 + r, c, x, beta);
     }
     __syncthreads();
 }
@@ -194,16 +245,20 @@ __device__ __forceinline__ void ut_round(const float *A, const float *Tdiag, flo
 // blocks.  Diagonal blocks by forward substitution in its right-looking form
 // (once x_s is final, subtract A[r][s] x_s from every later row): 15 steps of
 // independent FMAs, each step reading one block column as four broadcast
-// 16-byte loads.  Then the off-diagonal blocks along the block sub-diagonals
-// d = 1, 2, 3 (ut_round).  T is row-major with stride 64; its strictly upper
+// 16-byte loads.  Then the off-diagonal blocks in two levels: T_10 and T_32
+// (ut_level1), then the whole lower-left 32x32 block (ut_level2) -- the
+// 2x2-block inverse [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
+// applied at 16 and then at 32 rows.  T is row-major with stride 64; its strictly upper
 // blocks are left unwritten; Tdiag receives the diagonal blocks column-major.
 // Every lower block of T beta is written as soon as its block of T is final
 // (the strictly upper blocks of the T beta tiles hold zeros written once).
-// While warps 0-1 solve the diagonal blocks, warps 4-15 run `side_work`.
-template <typename SideWork>
-__device__ __forceinline__ void ut_inverse(const float *A, const float *Adiag, float *T,
-                                           float *Tdiag, float *P, uint8_t *smem,
-                                           const float *beta, int tid, SideWork side_work) {
+// While warps 0-1 solve the diagonal blocks, warps 4-15 run the state pass:
+// S_op = tf32(e^{m_k} S[k][v]) and S_acc = e^{Gam_L,k} S[k][v] in tensor memory
+// (warp w: lane quarter w % 4, 16-column slices (w / 4 - 1) + 3 n).
+__device__ __noinline__ void ut_inverse(const float *A, const float *Adiag, float *T,
+                                        float *Tdiag, float *P, uint8_t *smem,
+                                        const float *beta, int tid, uint32_t tmem_lane,
+                                        const float *em, const float *dec) {
     if (tid < 64) {
         const int bb = tid >> 4, j = tid & 15, base = bb * 16;
         const float *Ab = Adiag + bb * 256;
@@ -241,12 +296,24 @@ __device__ __forceinline__ void ut_inverse(const float *A, const float *Adiag, f
             *reinterpret_cast<__nv_bfloat16 *>(smem + OFF_TB16 + 8192 + sw128_offset(base + r, base + j, 64, 2)) = lo;
         }
     } else if (tid >= 128) {
-        side_work();
+        float r16[16], o16[16];
+        for (int cs = (tid >> 7) - 1; cs < 8; cs += 3) {
+            const int c0 = 16 * cs;
+            tmem_ld16(tmem_lane + T_SACC + c0, r16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                o16[j] = to_tf32(r16[j] * em[c0 + j]);
+                r16[j] = r16[j] * dec[c0 + j];
+            }
+            tmem_st16(tmem_lane + T_SOP + c0, o16);
+            tmem_st16(tmem_lane + T_SACC + c0, r16);
+        }
+        tmem_wait_st();
     }
     __syncthreads();
-    ut_round<1>(A, Tdiag, T, P, smem, beta, tid);
-    ut_round<2>(A, Tdiag, T, P, smem, beta, tid);
-    ut_round<3>(A, Tdiag, T, P, smem, beta, tid);
+    ut_level1(A, Tdiag, T, P, smem, beta, tid);
+    ut_level2(A, T, P, smem, beta, tid);
 }
 
 template <bool kOutBf16>
@@ -345,6 +412,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
         }
         const int64_t state_off = (static_cast<int64_t>(b) * H + h) * kD * kD;
+        // O^T of the chunk starting at token tc (L valid rows) from tensor memory to o
+        auto write_output = [&](int64_t tcw, int Lw) {
+            float o16[16];
+            tmem_ld16(tmem + lane_base + T_O + 16 * grp, o16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * grp + j;
+                if (r < Lw) {
+                    const int64_t idx = ((tcw + r) * H + h) * kD + ch;
+                    if (kOutBf16)
+                        static_cast<__nv_bfloat16 *>(p.o)[idx] = __float2bfloat16_rn(o16[j]);
+                    else
+                        static_cast<float *>(p.o)[idx] = o16[j];
+                }
+            }
+        };
 
         // ---- initial state into S_acc (lane v, column k holds S[k][v]) ----
         {
@@ -404,14 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             ph_qk++;
             pend_g = false;
             pend_qk = false;
+            // cumulative decay in log2 units: gam = log2(e) * sum g
             float gam[16];
             {
                 const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
+                const float kLog2e = 1.4426950408889634f;
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
                     const int r = 16 * grp + i;
-                    acc += (r < L) ? gt[r * kD + ch] : 0.f;
+                    acc += (r < L) ? kLog2e * gt[r * kD + ch] : 0.f;
                     gam[i] = acc;
                 }
                 s_part[grp * kD + ch] = acc;
@@ -425,13 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 if (g2 < grp) prefix += pg;
                 gam_l += pg;
             }
-            if (-gam_l > kMaxDecay) ctrl[3] = 1;
+            if (-gam_l > kMaxDecay * 1.4426950408889634f) ctrl[3] = 1;
             const float m = 0.5f * gam_l;
             if (grp == 0) {
-                s_em[ch] = __expf(m);
-                s_dec[ch] = __expf(gam_l);
+                s_em[ch] = fast_exp2(m);
+                s_dec[ch] = fast_exp2(gam_l);
             }
-            const float ekh = __expf(gam_l - m);
+            const float ekh = fast_exp2(gam_l - m);
             const float qscale = p.scale;
             float krt[16], khv[16];
 #pragma unroll
@@ -440,8 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 float qt = 0.f, kr = 0.f, ks = 0.f, kh = 0.f;
                 if (r < L) {
                     const float gr = prefix + gam[i];
-                    const float e_up = __expf(gr - m);   // e^{Gam_r - m}
-                    const float e_dn = __expf(m - gr);   // e^{m - Gam_r}
+                    const float e_up = fast_exp2(gr - m);   // e^{Gam_r - m}
+                    const float e_dn = fast_exp2(m - gr);   // e^{m - Gam_r}
                     const float qv = bf(smem + OFF_Q, (r * kD + ch) * 2);
                     const float kv = bf(smem + OFF_K, (r * kD + ch) * 2);
                     qt = to_tf32(qscale * qv * e_up);
@@ -460,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             for (int q4 = 0; q4 < 4; ++q4)
                 *reinterpret_cast<float4 *>(smem + OFF_KH + sw128_offset(ch, 16 * grp + 4 * q4, 128, 4)) =
                     make_float4(khv[4 * q4], khv[4 * q4 + 1], khv[4 * q4 + 2], khv[4 * q4 + 3]);
-            tmem_st16(tmem + lane_base + T_O + 16 * grp, krt);
+            tmem_st16(tmem + lane_base + T_W + 16 * grp, krt);
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -468,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_after();
             if (ctrl[2] != 0) break;
 
-            // ---- S2: D_A = [Qt; Kr] Ks^T ; next q/k loads ; state pass ----
+            // ---- S2: D_A = [Qt; Kr] Ks^T ; next q/k loads ; previous chunk's output ----
             if (tid == 0) {
                 if (Ln > 0) issue_qk(tn);
                 const uint32_t id = instr_desc(128, 64, kFmtTF32, 0, 0);
@@ -480,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
+            if (tc > t0) write_output(tc - kC, kC);
 
             // ---- S3: A_kk from the k-side rows of D_A ----
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
@@ -502,27 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             __syncthreads();
 
             // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
-            // The state pass runs on warps 4-15 while warps 0-1 solve the
-            // diagonal blocks: S_op = tf32(e^{m_k} S[k][v]); S_acc = e^{Gam_L,k} S[k][v].
-            // Warp w serves lane quarter w % 4 and 16-column slices
-            // (w / 4 - 1) + 3 n of the 128 state columns.
-            auto state_pass = [&]() {
-                float r16[16], o16[16];
-                for (int cs = (warp >> 2) - 1; cs < 8; cs += 3) {
-                    const int c0 = 16 * cs;
-                    tmem_ld16(tmem + lane_base + T_SACC + c0, r16);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        o16[j] = to_tf32(r16[j] * s_em[c0 + j]);
-                        r16[j] = r16[j] * s_dec[c0 + j];
-                    }
-                    tmem_st16(tmem + lane_base + T_SOP + c0, o16);
-                    tmem_st16(tmem + lane_base + T_SACC + c0, r16);
-                }
-                tmem_wait_st();
-            };
-            ut_inverse(Akk, s_diag, Tm, s_tdiag, s_P, smem, s_beta, tid, state_pass);
+            ut_inverse(Akk, s_diag, Tm, s_tdiag, s_P, smem, s_beta, tid, tmem + lane_base, s_em,
+                       s_dec);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -534,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bd = (d_tb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_W, tmem + T_O + kk * 8, bd, idw, kk > 0);
+                    mma_tf32_ts(tmem + T_O, tmem + T_W + kk * 8, bd, idw, kk > 0);
                 }
                 if (!mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
                     ctrl[2] = 1;
@@ -559,24 +627,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             if (ctrl[2] != 0) break;
             if (tid == 0 && Ln > 0) issue_v(tn);
 
-            // ---- S6: W' to shared memory (K-major [r][k]); A_qk (K-major [r][s]) ----
+            // ---- S6: W' to shared memory (K-major [r][k]) ----
             {
                 float w16[16];
-                tmem_ld16(tmem + lane_base + T_W + 16 * grp, w16);
+                tmem_ld16(tmem + lane_base + T_O + 16 * grp, w16);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     st_f32(smem + OFF_KS, sw128_offset(16 * grp + j, ch, 64, 4), to_tf32(w16[j]));
-                if (quarter < 2) {
-                    const int r = ch;
-                    tmem_ld16(tmem + lane_base + T_A + 16 * grp, w16);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s = 16 * grp + j;
-                        st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), (s <= r) ? to_tf32(w16[j]) : 0.f);
-                    }
-                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -599,6 +657,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
+            // A_qk (K-major [r][s], zero above the diagonal) while MMA1/MMA2 run;
+            // the T beta tile it overwrites was consumed by the W' product.
+            if (quarter < 2) {
+                const int r = ch;
+                float a16[16];
+                tmem_ld16(tmem + lane_base + T_A + 16 * grp, a16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s = 16 * grp + j;
+                    st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), (s <= r) ? to_tf32(a16[j]) : 0.f);
+                }
+            }
+            fence_proxy_async_smem();
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
             // W' (in OFF_KS) is consumed: stage the next chunk's g and beta
@@ -641,28 +713,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
 
-            // ---- S10: outputs ----
-            {
-                float o16[16];
-                tmem_ld16(tmem + lane_base + T_O + 16 * grp, o16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r = 16 * grp + j;
-                    if (r < L) {
-                        const int64_t idx = ((tc + r) * H + h) * kD + ch;
-                        if (kOutBf16)
-                            static_cast<__nv_bfloat16 *>(p.o)[idx] = __float2bfloat16_rn(o16[j]);
-                        else
-                            static_cast<float *>(p.o)[idx] = o16[j];
-                    }
-                }
-            }
+            // ---- S10: (the output of this chunk is read out under the next MMA) ----
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
         }
         if (ctrl[2] != 0) break;
+        if (t1 > t0) {  // output of the last chunk
+            const int64_t tl = t0 + ((t1 - t0 - 1) / kC) * kC;
+            write_output(tl, static_cast<int>(t1 - tl));
+        }
 
         // ---- final state ----
         if (p.Sf != nullptr) {
