@@ -3,11 +3,13 @@
 
 One step = one pass of the whole hot path on synthetic K3-shaped inputs:
   prefill leg:  gate + chunked prefill, B=1, T=4096, H=96, d=128 (the headline
-                tokens/s workload);
+                tokens/s workload), as one launch of the chunked kernel that
+                computes the gate itself (kda_chunk_prefill_gated);
   decode leg:   gate + recurrent decode, 256 sequences x 96 heads, fp32 states
                 [256, 96, 128, 128] (1.61 GB) updated in place.
 `value` is prefill sequence tokens/s over all ranks; the decode leg reports
-state GB/s against the measured HBM peak.  Inputs are larger than L2 (129 MB):
+state GB/s against the measured HBM peak.  The unfused pair (bit-exact gate
+kernel, then kda_chunk_prefill) is timed in a second loop and reported too.  Inputs are larger than L2 (129 MB):
 the prefill leg reads ~0.6 GB and the decode leg streams 3.2 GB per step.
 
 `--impl reference` times the CPU oracle (fp64 recurrence + fp32 gate spec) on
@@ -311,24 +313,29 @@ def run_ours(args):
     dout = torch.empty(B_DECODE, H, D, dtype=torch.bfloat16, device=dev)
     state = d.state
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    launches_per_step = 4
+
+    launches_per_step = 3
 
     def step(record=None):
         if record is not None:
             record[0].record(stream)
-        kda.kda_gate_fused(f, b, A_log, x.alog_mode, dt_bias, g, beta, stream)
+        kda.kda_chunk_prefill_gated(q, k, v, f, b, A_log, x.alog_mode, dt_bias, None, 1.0, None,
+                                    Sf, o, ws, stream)
         if record is not None:
             record[1].record(stream)
-        kda.kda_chunk_prefill(q, k, v, g, beta, None, 1.0, None, Sf, o, ws, stream)
-        if record is not None:
-            record[2].record(stream)
         kda.kda_gate_fused(df, db, dA, d.alog_mode, ddt, dg, dbeta, stream)
         if record is not None:
-            record[3].record(stream)
+            record[2].record(stream)
         kda.kda_recurrent_decode(dq, dk, dv, dg, dbeta, state, 1.0, dout, stream)
         if record is not None:
-            record[4].record(stream)
+            record[3].record(stream)
+
+    def unfused_step(record):
+        record[0].record(stream)
+        kda.kda_gate_fused(f, b, A_log, x.alog_mode, dt_bias, g, beta, stream)
+        record[1].record(stream)
+        kda.kda_chunk_prefill(q, k, v, g, beta, None, 1.0, None, Sf, o, ws, stream)
+        record[2].record(stream)
 
     for _ in range(max(args.warmup, 3) if args.warmup >= 3 else args.warmup):
         step()
@@ -346,7 +353,7 @@ def run_ours(args):
     t_start.record(stream)
     step_events = []
     for _ in range(args.steps):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         step(evs)
         step_events.append(evs)
     t_end.record(stream)
@@ -356,14 +363,26 @@ def run_ours(args):
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     for evs in step_events:
-        per_step.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
-    gate_ms = statistics.mean(p[0] for p in per_step)
-    prefill_ms = statistics.mean(p[1] for p in per_step)
-    dgate_ms = statistics.mean(p[2] for p in per_step)
-    decode_ms = statistics.mean(p[3] for p in per_step)
+        per_step.append([evs[i].elapsed_time(evs[i + 1]) for i in range(3)])
+    fused_ms = statistics.mean(p[0] for p in per_step)
+    dgate_ms = statistics.mean(p[1] for p in per_step)
+    decode_ms = statistics.mean(p[2] for p in per_step)
     step_ms = total_ms / args.steps
 
-    prefill_leg_ms = max_over_ranks(gate_ms + prefill_ms, world, dev)
+    # the unfused pair, same inputs, its own timed loop (not part of `value`)
+    for _ in range(max(args.warmup, 1)):
+        unfused_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize(dev)
+    uf = []
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        unfused_step(evs)
+        uf.append(evs)
+    torch.cuda.synchronize(dev)
+    gate_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in uf)
+    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in uf)
+
+    prefill_leg_ms = max_over_ranks(fused_ms, world, dev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
     decode_ms_max = max_over_ranks(decode_ms, world, dev)
     value = world * T_PREFILL / (prefill_leg_ms * 1e-3)
@@ -381,8 +400,8 @@ def run_ours(args):
         for hsrc, ddst in zip(host_in, dev_in):
             ddst.copy_(hsrc, non_blocking=True)
         eq, ek, evv, ef, eb = dev_in
-        kda.kda_gate_fused(ef, eb, A_log, x.alog_mode, dt_bias, g, beta, stream)
-        kda.kda_chunk_prefill(eq, ek, evv, g, beta, None, 1.0, None, Sf, o, ws, stream)
+        kda.kda_chunk_prefill_gated(eq, ek, evv, ef, eb, A_log, x.alog_mode, dt_bias, None, 1.0,
+                                    None, Sf, o, ws, stream)
         host_o.copy_(o, non_blocking=True)
         host_S.copy_(Sf, non_blocking=True)
 
@@ -410,16 +429,26 @@ def run_ours(args):
     # tf32 dense peak = measured bf16 peak x the nominal tf32/bf16 ratio (1.1/2.25)
     tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
     pf_flops = H * prefill_flops_per_head([T_PREFILL])
-    pf_tflops = pf_flops / (prefill_ms * 1e-3) / 1e12
-    pf_bytes = prefill_kernel_bytes(T_PREFILL)
-    rl_prefill = {"kernel": "kda chunked prefill (tcgen05 kind::tf32)", "bound": "tensor",
-                  "achieved": pf_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
+    pf_tflops = pf_flops / (fused_ms * 1e-3) / 1e12
+    # fused kernel bytes: q, k, v, f (bf16) and beta logits read, o written, final state
+    pf_bytes = T_PREFILL * H * (2 * D * 4 + 4 + 2 * D) + H * D * D * 4
+    rl_prefill = {"kernel": "kda chunked prefill with in-kernel gate (tcgen05 kind::tf32)",
+                  "bound": "tensor", "achieved": pf_tflops, "peak": tf32_peak, "unit": "TFLOP/s",
                   "frac": pf_tflops / tf32_peak, "traffic": None,
                   "peak_source": f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio 1.1/2.25",
                   "algorithmic_flops_per_launch": pf_flops,
-                  "hbm_achieved_gbs": pf_bytes / (prefill_ms * 1e-3) / 1e9,
-                  "hbm_frac": pf_bytes / (prefill_ms * 1e-3) / 1e9 / hbm,
+                  "hbm_achieved_gbs": pf_bytes / (fused_ms * 1e-3) / 1e9,
+                  "hbm_frac": pf_bytes / (fused_ms * 1e-3) / 1e9 / hbm,
                   "algorithmic_bytes_per_launch": pf_bytes}
+    up_bytes = prefill_kernel_bytes(T_PREFILL)
+    rl_prefill_unfused = {"kernel": "kda chunked prefill, precomputed g and beta",
+                          "bound": "tensor",
+                          "achieved": pf_flops / (prefill_ms * 1e-3) / 1e12, "peak": tf32_peak,
+                          "unit": "TFLOP/s",
+                          "frac": pf_flops / (prefill_ms * 1e-3) / 1e12 / tf32_peak,
+                          "traffic": None, "algorithmic_flops_per_launch": pf_flops,
+                          "hbm_frac": up_bytes / (prefill_ms * 1e-3) / 1e9 / hbm,
+                          "algorithmic_bytes_per_launch": up_bytes}
     dec_gbs = decode_bytes() / (decode_ms_max * 1e-3) / 1e9
     rl_decode = {"kernel": "kda recurrent decode", "bound": "hbm", "achieved": dec_gbs,
                  "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm, "traffic": None,
@@ -429,11 +458,12 @@ def run_ours(args):
     rl_gate = {"kernel": "kda gate", "bound": "hbm", "achieved": gate_gbs, "peak": hbm,
                "unit": "GB/s", "frac": gate_gbs / hbm, "traffic": None,
                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": gate_bytes}
-    for rl, src in ((rl_prefill, "kda_chunk.cu"), (rl_decode, "kda_decode.cu"),
+    rl_prefill["traffic"], rl_prefill["traffic_note"] = None, "no capture of the fused kernel yet"
+    for rl, src in ((rl_prefill_unfused, "kda_chunk.cu"), (rl_decode, "kda_decode.cu"),
                     (rl_gate, "kda_gate.cu")):
         rl["traffic"], rl["traffic_note"] = measured_traffic(src)
     # the dominant kernel is the one with the largest share of the step
-    roofline = rl_prefill if prefill_ms >= decode_ms_max else rl_decode
+    roofline = rl_prefill if fused_ms >= decode_ms_max else rl_decode
     cpu = cpu_baseline(args.cpu_heads) if not args.no_cpu_baseline else None
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -443,11 +473,13 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "inputs_exceed_l2": True, "l2_flush": False,
                    "prefill_T": T_PREFILL, "heads": H, "d": D, "decode_batch": B_DECODE,
                    "parallelism": f"replicas x{world}"},
-        "prefill_ms": prefill_ms, "gate_ms": gate_ms, "decode_gate_ms": dgate_ms,
-        "decode_ms": decode_ms_max,
+        "prefill_gated_ms": fused_ms, "decode_gate_ms": dgate_ms, "decode_ms": decode_ms_max,
+        "unfused": {"gate_ms": gate_ms, "prefill_ms": prefill_ms,
+                    "tokens_per_s": T_PREFILL / ((gate_ms + prefill_ms) * 1e-3)},
         "decode_state_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / hbm,
         "roofline": roofline,
-        "rooflines": {"gate": rl_gate, "prefill": rl_prefill, "decode": rl_decode},
+        "rooflines": {"gate": rl_gate, "prefill_gated": rl_prefill,
+                      "prefill_unfused": rl_prefill_unfused, "decode": rl_decode},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

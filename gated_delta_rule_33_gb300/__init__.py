@@ -17,6 +17,7 @@ from .kda import (  # noqa: F401
     decode,
     gate,
     kda_chunk_prefill,
+    kda_chunk_prefill_gated,
     kda_chunk_prefill_noalloc,
     kda_chunk_prefill_workspace_size,
     kda_gate_fused,
@@ -27,4 +28,5 @@ from .kda import (  # noqa: F401
     library_path,
     load,
     prefill,
+    prefill_gated,
 )

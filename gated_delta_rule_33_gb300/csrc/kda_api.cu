@@ -144,6 +144,44 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v, const void *f,
+                                   kda_dtype f_dtype, const void *b, kda_dtype b_dtype,
+                                   const float *A_log, kda_alog_mode alog_mode,
+                                   const float *dt_bias, const int32_t *cu_seqlens, int B,
+                                   int64_t N, int H, int K, int V, float scale,
+                                   const float *initial_state, float *final_state, void *o,
+                                   kda_dtype o_dtype, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(o_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (f_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (alog_mode != KDA_ALOG_PER_HEAD && alog_mode != KDA_ALOG_PER_CHANNEL &&
+        alog_mode != KDA_ALOG_PER_HEAD_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && B != 1) return KDA_ERR_INVALID_ARG;
+    if (A_log == nullptr || dt_bias == nullptr) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (q == nullptr || k == nullptr || v == nullptr || f == nullptr || b == nullptr ||
+                  o == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(f) || !aligned16(b) ||
+        !aligned16(A_log) || !aligned16(dt_bias) || !aligned16(o) || !aligned16(initial_state) ||
+        !aligned16(final_state) || !aligned16(workspace) || !aligned16(cu_seqlens))
+        return KDA_ERR_MISALIGNED;
+    const size_t need = kda::prefill_workspace_bytes(N, B, H);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr))
+        return KDA_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_prefill_gated(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(f), b,
+        b_dtype == KDA_BF16, A_log, static_cast<int>(alog_mode), dt_bias, cu_seqlens, B, N, H,
+        scale, initial_state, final_state, o, o_dtype == KDA_BF16, workspace, dev->error_word,
+        dev->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v, const float *g,
                                      const float *beta, const int32_t *cu_seqlens, int B,
                                      int64_t N, int H, int K, int V, float scale,

@@ -82,8 +82,14 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr uint32_t T_SACC = 0, T_SOP = 128, T_U = 256, T_O = 320, T_A = 384, T_W = 448;
 
 struct Params {
-    const float *g;
-    const float *beta;
+    const float *g;              // fp32 log-decay [N, H, 128]   (unfused)
+    const float *beta;           // fp32 beta [N, H]             (unfused)
+    const void *f;               // bf16 gate pre-activation     (fused gate)
+    const void *blog;            // beta logits, bf16 or fp32    (fused gate)
+    int blog_bf16;
+    const float *A_log;          // per alog_mode                (fused gate)
+    int alog_mode;
+    const float *dt_bias;        // [H, 128]                     (fused gate)
     const int32_t *cu_seqlens;
     int B;
     int64_t N;
@@ -316,7 +322,11 @@ __device__ __noinline__ void ut_inverse(const float *A, const float *Adiag, floa
     ut_level2(A, T, P, smem, beta, tid);
 }
 
-template <bool kOutBf16>
+// kGate: the gate is computed in this kernel from the bf16 pre-activation f,
+// A_log, dt_bias and the beta logits (g = -exp(A_log) softplus(f + dt_bias),
+// beta = sigmoid(logit)) with the special-function unit, instead of reading a
+// precomputed fp32 g and beta.
+template <bool kOutBf16, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                             const __grid_constant__ CUtensorMap tm_k,
                                                             const __grid_constant__ CUtensorMap tm_v,
@@ -455,13 +465,34 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         // g of the chunk: one TMA tile into the OFF_KS region; beta: one
         // zero-filled 4-byte cp.async per row into s_bnext (threads 0..63).
         auto issue_g = [&](int64_t tc) {
-            mbar_arrive_expect_tx(bar_g, 32768);
+            mbar_arrive_expect_tx(bar_g, kGate ? 16384 : 32768);
             tma_load_3d(smem + OFF_KS, &tm_g, bar_g, 0, h, static_cast<int32_t>(tc));
             pend_g = true;
         };
+        // fused gate: per-channel exp(A_log) and dt_bias of this head
+        float gate_a = 0.f, gate_dt = 0.f, blog_reg = 0.f;
+        if (kGate) {
+            const int ai = (p.alog_mode == 0) ? h : (p.alog_mode == 1 ? ch : h * kD + ch);
+            gate_a = expf(p.A_log[ai]);
+            gate_dt = p.dt_bias[h * kD + ch];
+        }
         auto load_beta = [&](int64_t tc, int L) {
-            if (tid < kC)
+            if (kGate) {
+                // the logit stays in a register until the chunk is processed;
+                // rows past the sequence get -inf, whose sigmoid is 0
+                if (tid < kC) {
+                    if (tid < L) {
+                        const int64_t bi = (tc + tid) * H + h;
+                        blog_reg = p.blog_bf16
+                                       ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.blog)[bi])
+                                       : static_cast<const float *>(p.blog)[bi];
+                    } else {
+                        blog_reg = -__int_as_float(0x7f800000);
+                    }
+                }
+            } else if (tid < kC) {
                 cp_async_4(&s_bnext[tid], p.beta + ((tid < L) ? (tc + tid) * H + h : 0), tid < L);
+            }
         };
         if (t1 > t0) {
             if (tid == 0) {
@@ -491,18 +522,41 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             // cumulative decay in log2 units: gam = log2(e) * sum g
             float gam[16];
             {
-                const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
                 const float kLog2e = 1.4426950408889634f;
                 float acc = 0.f;
+                if (kGate) {
+                    // log2(e) g = -exp(A_log) (log2(e) max(x, 0) + log2(1 + 2^{-log2(e)|x|})),
+                    // x = f + dt_bias
+                    const __nv_bfloat16 *ft = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_KS);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
-                    const int r = 16 * grp + i;
-                    acc += (r < L) ? kLog2e * gt[r * kD + ch] : 0.f;
-                    gam[i] = acc;
+                    for (int i = 0; i < 16; ++i) {
+                        const int r = 16 * grp + i;
+                        const float x = __bfloat162float(ft[r * kD + ch]) + gate_dt;
+                        const float e = fast_exp2(-kLog2e * fabsf(x));
+                        // log2(1 + e) as log2(u) e / (u - 1), u = 1 + e (D. Goldberg,
+                        // "What every computer scientist should know about
+                        // floating-point arithmetic", 1991): exact-ish even when
+                        // 1 + e rounds; u == 1 leaves log2(1 + e) = e log2(e).
+                        const float u = 1.f + e;
+                        float lg;
+                        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(u));
+                        lg = (u == 1.f) ? kLog2e * e : lg * __fdividef(e, u - 1.f);
+                        const float g2 = -gate_a * (kLog2e * fmaxf(x, 0.f) + lg);
+                        acc += (r < L) ? g2 : 0.f;
+                        gam[i] = acc;
+                    }
+                } else {
+                    const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
+                        const int r = 16 * grp + i;
+                        acc += (r < L) ? kLog2e * gt[r * kD + ch] : 0.f;
+                        gam[i] = acc;
+                    }
                 }
                 s_part[grp * kD + ch] = acc;
             }
-            if (tid < kC) s_beta[tid] = s_bnext[tid];
+            if (tid < kC) s_beta[tid] = kGate ? 1.f / (1.f + __expf(-blog_reg)) : s_bnext[tid];
             __syncthreads();  // every g read is done before Ks overwrites the tile
             float prefix = 0.f, gam_l = 0.f;
 #pragma unroll
@@ -794,39 +848,64 @@ size_t prefill_workspace_bytes(int64_t N, int B, int H) {
     return (B > 0 && H > 0) ? 256 : 0;
 }
 
-cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                           const __nv_bfloat16 *v, const float *g, const float *beta,
-                           const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
-                           const float *initial_state, float *final_state, void *o, bool o_bf16,
-                           void *workspace, unsigned int *err, int num_sms, cudaStream_t s) {
-    if (B == 0 || H == 0) return cudaSuccess;
+namespace {
+
+template <bool kGate>
+cudaError_t launch_chunk(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                         const void *g_or_f, const Params &p, bool o_bf16, int num_sms,
+                         cudaStream_t s) {
+    if (p.B == 0 || p.H == 0) return cudaSuccess;
     static bool attr_done[2] = {false, false};
     if (!attr_done[o_bf16 ? 1 : 0]) {
-        cudaError_t e = o_bf16 ? cudaFuncSetAttribute(chunk_kernel<true>,
+        cudaError_t e = o_bf16 ? cudaFuncSetAttribute(chunk_kernel<true, kGate>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                       kSmemAlloc)
-                               : cudaFuncSetAttribute(chunk_kernel<false>,
+                               : cudaFuncSetAttribute(chunk_kernel<false, kGate>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                       kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_done[o_bf16 ? 1 : 0] = true;
     }
     CUtensorMap mq, mk, mv, mg;
-    const int64_t Nmap = N > 0 ? N : 1;
-    if (!make_map(&mq, q, Nmap, H, 128, false) || !make_map(&mk, k, Nmap, H, 128, false) ||
-        !make_map(&mv, v, Nmap, H, 64, true) || !make_map(&mg, g, Nmap, H, 128, false, true))
+    const int64_t Nmap = p.N > 0 ? p.N : 1;
+    if (!make_map(&mq, q, Nmap, p.H, 128, false) || !make_map(&mk, k, Nmap, p.H, 128, false) ||
+        !make_map(&mv, v, Nmap, p.H, 64, true) ||
+        !make_map(&mg, g_or_f, Nmap, p.H, 128, false, !kGate))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s);
+    cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
-    const Params p{g, beta, cu_seqlens, B, N, H, scale, initial_state, final_state, o, err,
-                   static_cast<unsigned int *>(workspace)};
-    const int chains = B * H;
+    const int chains = p.B * p.H;
     const int grid = chains < num_sms ? chains : num_sms;
     if (o_bf16)
-        chunk_kernel<true><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
+        chunk_kernel<true, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
     else
-        chunk_kernel<false><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
+        chunk_kernel<false, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                           const __nv_bfloat16 *v, const float *g, const float *beta,
+                           const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+                           const float *initial_state, float *final_state, void *o, bool o_bf16,
+                           void *workspace, unsigned int *err, int num_sms, cudaStream_t s) {
+    const Params p{g, beta, nullptr, nullptr, 0, nullptr, 0, nullptr, cu_seqlens, B, N, H, scale,
+                   initial_state, final_state, o, err, static_cast<unsigned int *>(workspace)};
+    return launch_chunk<false>(q, k, v, g, p, o_bf16, num_sms, s);
+}
+
+cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                 const __nv_bfloat16 *v, const __nv_bfloat16 *f, const void *b,
+                                 bool b_bf16, const float *A_log, int alog_mode,
+                                 const float *dt_bias, const int32_t *cu_seqlens, int B, int64_t N,
+                                 int H, float scale, const float *initial_state,
+                                 float *final_state, void *o, bool o_bf16, void *workspace,
+                                 unsigned int *err, int num_sms, cudaStream_t s) {
+    const Params p{nullptr, nullptr, f, b, b_bf16 ? 1 : 0, A_log, alog_mode, dt_bias, cu_seqlens,
+                   B, N, H, scale, initial_state, final_state, o, err,
+                   static_cast<unsigned int *>(workspace)};
+    return launch_chunk<true>(q, k, v, f, p, o_bf16, num_sms, s);
 }
 
 // ---- built-in scratch for callers that cannot allocate ---------------------------------

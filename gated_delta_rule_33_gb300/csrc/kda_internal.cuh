@@ -42,6 +42,14 @@ cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const float *initial_state, float *final_state, void *o, bool o_bf16,
                            void *workspace, unsigned int *err, int num_sms, cudaStream_t s);
 
+cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                 const __nv_bfloat16 *v, const __nv_bfloat16 *f, const void *b,
+                                 bool b_bf16, const float *A_log, int alog_mode,
+                                 const float *dt_bias, const int32_t *cu_seqlens, int B, int64_t N,
+                                 int H, float scale, const float *initial_state,
+                                 float *final_state, void *o, bool o_bf16, void *workspace,
+                                 unsigned int *err, int num_sms, cudaStream_t s);
+
 // Device address and size of the built-in prefill scratch on the current device
 // (looked up once per device; see kda_chunk.cu).
 cudaError_t builtin_prefill_scratch(void **ptr, size_t *bytes);

@@ -73,6 +73,9 @@ def load():
         lib.kda_chunk_prefill.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, P, I, P,
                                           ctypes.c_size_t, P]
         lib.kda_chunk_prefill.restype = I
+        lib.kda_chunk_prefill_gated.argtypes = [P, P, P, P, I, P, I, P, I, P, P, I, I64, I, I, I, F,
+                                                P, P, P, I, P, ctypes.c_size_t, P]
+        lib.kda_chunk_prefill_gated.restype = I
         lib.kda_chunk_prefill_noalloc.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, P,
                                                   I, P]
         lib.kda_chunk_prefill_noalloc.restype = I
@@ -146,6 +149,21 @@ def kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, scale, initial_state, final_
     _check(st, "kda_chunk_prefill")
 
 
+def kda_chunk_prefill_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, cu_seqlens, scale,
+                            initial_state, final_state, o, workspace, stream=None):
+    """Chunked prefill with the gate computed in the kernel from f, b, A_log, dt_bias."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kda_chunk_prefill_gated(_p(q), _p(k), _p(v), _p(f), _dtype_code(f), _p(b),
+                                        _dtype_code(b), _p(A_log), int(alog_mode), _p(dt_bias),
+                                        _p(cu_seqlens), B, N, H, K, V, float(scale),
+                                        _p(initial_state), _p(final_state), _p(o), _dtype_code(o),
+                                        _p(workspace), ws_bytes, _stream(stream, q.device))
+    _check(st, "kda_chunk_prefill_gated")
+
+
 def kda_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, scale, initial_state, final_state, o,
                               stream=None):
     """kda_chunk_prefill with the library's built-in scratch instead of a workspace."""
@@ -193,6 +211,21 @@ def prefill(q, k, v, g, beta, cu_seqlens=None, scale=1.0, initial_state=None,
     ws = torch.empty(max(kda_chunk_prefill_workspace_size(N, B, H, K, v.shape[-1]), 16),
                      dtype=torch.uint8, device=q.device)
     kda_chunk_prefill(q, k, v, g, beta, cu_seqlens, scale, initial_state, final, o, ws, stream)
+    return o, final
+
+
+def prefill_gated(q, k, v, f, b, A_log, dt_bias, alog_mode=KDA_ALOG_PER_CHANNEL, cu_seqlens=None,
+                  scale=1.0, initial_state=None, o_dtype=torch.bfloat16, output_final_state=True,
+                  stream=None):
+    N, H, K = q.shape
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    o = torch.empty(N, H, v.shape[-1], dtype=o_dtype, device=q.device)
+    final = (torch.empty(B, H, K, v.shape[-1], dtype=torch.float32, device=q.device)
+             if output_final_state else None)
+    ws = torch.empty(max(kda_chunk_prefill_workspace_size(N, B, H, K, v.shape[-1]), 16),
+                     dtype=torch.uint8, device=q.device)
+    kda_chunk_prefill_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, cu_seqlens, scale,
+                            initial_state, final, o, ws, stream)
     return o, final
 
 

@@ -149,6 +149,37 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v,
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_chunk_prefill_gated -- kda_chunk_prefill with the gate computed inside
+ * the chunked kernel, the interface K3_ARTIFACT_AUDIT.md section 7.1 records for
+ * FlashKDA (gate pre-activation in bf16, A_log/dt_bias in fp32, beta logits):
+ *
+ *   g[n,h,c]  = -exp(A_log[.]) * softplus(f[n,h,c] + dt_bias[h,c])
+ *   beta[n,h] = sigmoid(b[n,h])
+ *
+ * evaluated with the special-function unit (relative error ~1e-6; it is not
+ * the bit-exact specification of kda_gate_fused).  The fp32 g and beta never
+ * reach global memory.
+ *
+ *   f        bf16 [N, H, 128] gate pre-activation (f_dtype must be KDA_BF16)
+ *   b        [N, H] beta logits, bf16 or fp32 (b_dtype); the sigmoid is applied
+ *            here, once (the EP-adapter review's finding 1: never pass raw
+ *            logits where post-sigmoid beta is expected, or vice versa)
+ *   A_log    fp32, shape by alog_mode;  dt_bias fp32 [H, 128]
+ * All other arguments, layouts and results are those of kda_chunk_prefill
+ * (same workspace size).
+ */
+kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v,
+                                   const void *f, kda_dtype f_dtype,
+                                   const void *b, kda_dtype b_dtype,
+                                   const float *A_log, kda_alog_mode alog_mode,
+                                   const float *dt_bias,
+                                   const int32_t *cu_seqlens, int B,
+                                   int64_t N, int H, int K, int V, float scale,
+                                   const float *initial_state, float *final_state,
+                                   void *o, kda_dtype o_dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * kda_chunk_prefill_noalloc -- kda_chunk_prefill without a workspace argument,
  * for callers that cannot allocate device memory: a host plugin interface that
  * hands the library only its input and output buffers and offers no way to ask
