@@ -13,6 +13,9 @@ The C source ``kdaref.c`` holds the oracle proper:
   decode) are named in the Kimi-K3 code audit, data/code-audit.json, finding
   "dual-kda-execution-regimes".
 * ``chunked``    -- the same result via the fp64 chunked (WY/UT) form.
+* ``recurrent_backward`` -- the reverse mode of the recurrence (gradients of
+  q, k, v, g, beta and the initial state): the training regime ("chunked KDA
+  for training", code-audit.json, finding "dual-kda-execution-regimes").
 * ``gate``       -- the fp32 gate specification g = -exp(A_log) softplus(f +
   dt_bias), beta = sigmoid(b), built on the oracle's own binary32 exp/log1p
   (parameters as in K3_ARTIFACT_AUDIT.md sections 4.1 and 5.1).
@@ -81,6 +84,10 @@ def _load():
         lib.kdaref_recurrent.restype = ctypes.c_int
         lib.kdaref_chunked.argtypes = common + [ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.kdaref_chunked.restype = ctypes.c_int
+        c_i, c_i64, c_d = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.kdaref_recurrent_backward.argtypes = [P, P, P, P, P, P, c_i, c_i64, c_i, c_i, c_i,
+                                                  c_d, P, P, P, P, P, P, P, P, P, c_i]
+        lib.kdaref_recurrent_backward.restype = c_i
         _lib = lib
         return lib
 
@@ -194,6 +201,37 @@ def chunked(q, k, v, g, beta, cu_seqlens=None, scale=1.0, initial_state=None, ch
     """fp64 chunked (WY/UT) KDA; frame < chunk uses the per-frame factorisation."""
     return _run("kdaref_chunked", q, k, v, g, beta, cu_seqlens, scale, initial_state,
                 (int(chunk), int(frame)), nthreads)
+
+
+def recurrent_backward(q, k, v, g, beta, dO, cu_seqlens=None, scale=1.0, initial_state=None,
+                       dS_final=None, nthreads=None):
+    """Reverse mode of ``recurrent``: given dO [N,H,V] and dS_final [B,H,K,V]
+    (None: zero), returns (dq, dk, dv, dg [N,H,K or V], dbeta [N,H],
+    dS0 [B,H,K,V]) in fp64."""
+    q, k, v, g, beta, dO = (_f64(a) for a in (q, k, v, g, beta, dO))
+    N, H, K = q.shape
+    V = v.shape[-1]
+    if cu_seqlens is None:
+        B, cu = 1, None
+    else:
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        B = cu.shape[0] - 1
+    S0, dSf = _f64(initial_state), _f64(dS_final)
+    for name, a in (("initial_state", S0), ("dS_final", dSf)):
+        if a is not None and a.shape != (B, H, K, V):
+            raise ValueError(f"{name} shape {a.shape} != {(B, H, K, V)}")
+    dq, dk, dg = (np.zeros((N, H, K)) for _ in range(3))
+    dv = np.zeros((N, H, V))
+    dbeta = np.zeros((N, H))
+    dS0 = np.zeros((B, H, K, V))
+    nt = default_threads() if nthreads is None else int(nthreads)
+    rc = _load().kdaref_recurrent_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu), B, N, H, K, V, float(scale),
+        _ptr(S0), _ptr(dO), _ptr(dSf), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+        _ptr(dS0), nt)
+    if rc != 0:
+        raise ValueError(f"kdaref_recurrent_backward rejected its arguments (code {rc})")
+    return dq, dk, dv, dg, dbeta, dS0
 
 
 def decode(q, k, v, g, beta, state, scale=1.0, nthreads=None):

@@ -40,6 +40,7 @@
  *   kdaref_exp_f32, kdaref_log1p_f32, kdaref_softplus_f32, kdaref_sigmoid_f32
  *   kdaref_gate_f32        -- the fp32 gate specification
  *   kdaref_recurrent       -- the fp64 token-by-token recurrence (the oracle)
+ *   kdaref_recurrent_backward -- its reverse mode: gradients of q, k, v, g, beta, S0
  *   kdaref_chunked         -- the fp64 chunked (WY/UT) form, used to show the
  *                             chunked algorithm reaches the recurrence's result
  */
@@ -492,6 +493,175 @@ int kdaref_chunked(const double *q, const double *k, const double *v, const doub
     job_t j = {q, k, v, g, beta, cu_seqlens, B, H, K, V, N, scale, initial_state, o,
                final_state, chunk, frame, nthreads, 0, 0};
     return run_jobs(&j);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Reverse mode of the recurrence (the training regime's gradients), fp64      */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    job_t f;                        /* the forward problem */
+    const double *dO, *dSf;         /* [N,H,V]; [B,H,K,V] or NULL (zero) */
+    double *dq, *dk, *dv, *dg, *dbeta, *dS0;
+} bjob_t;
+
+/*
+ * One (sequence, head).  The forward recurrence is rerun keeping every state
+ * S_t; then, from G = dL/dS_T, for t = T..1 with S' = Diag(exp g_t) S_{t-1},
+ * w = S'^T k_t, u = beta_t (v_t - w), S_t = S' + k_t u^T, o_t = S_t^T (scale q_t):
+ *   G   += (scale q_t) do_t^T           (o_t reads S_t)
+ *   dq_t = scale S_t do_t
+ *   du   = G^T k_t;   dk_t = G u;   dv_t = beta_t du;   dbeta_t = du . (v_t - w)
+ *   dw   = -beta_t du;   dS' = G + k_t dw^T;   dk_t += S' dw
+ *   dg_t = rowsum(dS' (.) S')           (S' = Diag(exp g_t) S_{t-1})
+ *   G    = Diag(exp g_t) dS'            (= dL/dS_{t-1})
+ * and dL/dS_0 = G.  Each line is the derivative of one forward line.
+ */
+static int backward_unit(const bjob_t *bj, int seq, int h)
+{
+    const job_t *j = &bj->f;
+    const int K = j->K, V = j->V, H = j->H;
+    const size_t KV = (size_t)K * V;
+    int64_t t0, t1;
+    seq_range(j, seq, &t0, &t1);
+    const int64_t L = t1 - t0;
+    double *Sall = malloc(sizeof(double) * KV * (size_t)(L + 1));
+    double *Sp = malloc(sizeof(double) * KV);
+    double *G = malloc(sizeof(double) * KV);
+    double *w = malloc(sizeof(double) * V);
+    double *u = malloc(sizeof(double) * V);
+    double *du = malloc(sizeof(double) * V);
+    double *dw = malloc(sizeof(double) * V);
+    double *d = malloc(sizeof(double) * K);
+    int ok = Sall && Sp && G && w && u && du && dw && d;
+    if (!ok) goto done;
+    load_state(j, seq, h, Sall);
+    for (int64_t i = 0; i < L; i++) {            /* forward, keeping S_t at Sall[i + 1] */
+        const int64_t t = t0 + i;
+        const double *kt = j->k + (t * H + h) * K, *vt = j->v + (t * H + h) * V;
+        const double *gt = j->g + (t * H + h) * K;
+        const double bt = j->beta[t * H + h];
+        const double *Sprev = Sall + (size_t)i * KV;
+        double *S = Sall + (size_t)(i + 1) * KV;
+        for (int a = 0; a < K; a++) {
+            const double e = exp(gt[a]);
+            for (int c = 0; c < V; c++) S[a * V + c] = e * Sprev[a * V + c];
+        }
+        for (int c = 0; c < V; c++) w[c] = 0.0;
+        for (int a = 0; a < K; a++)
+            for (int c = 0; c < V; c++) w[c] += S[a * V + c] * kt[a];
+        for (int c = 0; c < V; c++) u[c] = bt * (vt[c] - w[c]);
+        for (int a = 0; a < K; a++)
+            for (int c = 0; c < V; c++) S[a * V + c] += kt[a] * u[c];
+    }
+    if (bj->dSf) memcpy(G, bj->dSf + ((size_t)seq * H + h) * KV, KV * sizeof(double));
+    else memset(G, 0, KV * sizeof(double));
+    for (int64_t i = L - 1; i >= 0; i--) {
+        const int64_t t = t0 + i;
+        const double *qt = j->q + (t * H + h) * K, *kt = j->k + (t * H + h) * K;
+        const double *vt = j->v + (t * H + h) * V, *gt = j->g + (t * H + h) * K;
+        const double *dot = bj->dO + (t * H + h) * V;
+        const double bt = j->beta[t * H + h];
+        const double *Sprev = Sall + (size_t)i * KV, *St = Sall + (size_t)(i + 1) * KV;
+        double *dqt = bj->dq + (t * H + h) * K, *dkt = bj->dk + (t * H + h) * K;
+        double *dvt = bj->dv + (t * H + h) * V, *dgt = bj->dg + (t * H + h) * K;
+        for (int a = 0; a < K; a++) {                      /* S' and the step's u */
+            d[a] = exp(gt[a]);
+            for (int c = 0; c < V; c++) Sp[a * V + c] = d[a] * Sprev[a * V + c];
+        }
+        for (int c = 0; c < V; c++) w[c] = 0.0;
+        for (int a = 0; a < K; a++)
+            for (int c = 0; c < V; c++) w[c] += Sp[a * V + c] * kt[a];
+        for (int c = 0; c < V; c++) u[c] = bt * (vt[c] - w[c]);
+        for (int a = 0; a < K; a++)                        /* G += (scale q) do^T */
+            for (int c = 0; c < V; c++) G[a * V + c] += j->scale * qt[a] * dot[c];
+        for (int a = 0; a < K; a++) {                      /* dq = scale S_t do */
+            double acc = 0.0;
+            for (int c = 0; c < V; c++) acc += St[a * V + c] * dot[c];
+            dqt[a] = j->scale * acc;
+        }
+        for (int c = 0; c < V; c++) du[c] = 0.0;           /* du = G^T k */
+        for (int a = 0; a < K; a++)
+            for (int c = 0; c < V; c++) du[c] += G[a * V + c] * kt[a];
+        double db = 0.0;
+        for (int c = 0; c < V; c++) {
+            dvt[c] = bt * du[c];
+            db += du[c] * (vt[c] - w[c]);
+            dw[c] = -bt * du[c];
+        }
+        bj->dbeta[t * H + h] = db;
+        for (int a = 0; a < K; a++) {
+            double gu = 0.0, sdw = 0.0, dgs = 0.0;
+            for (int c = 0; c < V; c++) {
+                const double dsp = G[a * V + c] + kt[a] * dw[c];    /* dS' */
+                gu += G[a * V + c] * u[c];
+                sdw += Sp[a * V + c] * dw[c];
+                dgs += dsp * Sp[a * V + c];
+                G[a * V + c] = d[a] * dsp;                         /* dL/dS_{t-1} */
+            }
+            dkt[a] = gu + sdw;
+            dgt[a] = dgs;
+        }
+    }
+    if (bj->dS0) memcpy(bj->dS0 + ((size_t)seq * H + h) * KV, G, KV * sizeof(double));
+done:
+    free(Sall); free(Sp); free(G); free(w); free(u); free(du); free(dw); free(d);
+    return ok ? 0 : 1;
+}
+
+typedef struct {
+    bjob_t *bj;
+    int nthreads, thread_id, status;
+} bworker_t;
+
+static void *bworker(void *arg)
+{
+    bworker_t *w = (bworker_t *)arg;
+    const int units = w->bj->f.B * w->bj->f.H;
+    for (int u = w->thread_id; u < units; u += w->nthreads) {
+        int rc = backward_unit(w->bj, u / w->bj->f.H, u % w->bj->f.H);
+        if (rc) w->status = rc;
+    }
+    return NULL;
+}
+
+/*
+ * Gradients of the recurrence (kdaref_recurrent) with respect to q, k, v, g,
+ * beta and the initial state, given dO [N,H,V] and dS_final [B,H,K,V] (NULL:
+ * zero).  dS0 may be NULL.  Every output is written in full.  Returns 0 on
+ * success.
+ */
+int kdaref_recurrent_backward(const double *q, const double *k, const double *v,
+                              const double *g, const double *beta, const int32_t *cu_seqlens,
+                              int B, int64_t N, int H, int K, int V, double scale,
+                              const double *initial_state, const double *dO,
+                              const double *dS_final, double *dq, double *dk, double *dv,
+                              double *dg, double *dbeta, double *dS0, int nthreads)
+{
+    int rc = check_args(q, k, v, g, beta, cu_seqlens, B, N, H, K, V, dq);
+    if (rc) return rc;
+    if (!dO || !dk || !dv || !dg || !dbeta) return 3;
+    bjob_t bj;
+    memset(&bj, 0, sizeof bj);
+    bj.f = (job_t){q, k, v, g, beta, cu_seqlens, B, H, K, V, N, scale, initial_state, NULL,
+                   NULL, 0, 0, 1, 0, 0};
+    bj.dO = dO; bj.dSf = dS_final;
+    bj.dq = dq; bj.dk = dk; bj.dv = dv; bj.dg = dg; bj.dbeta = dbeta; bj.dS0 = dS0;
+    int nt = nthreads < 1 ? 1 : nthreads;
+    if (nt > B * H) nt = B * H;
+    bworker_t *ws = malloc(sizeof(bworker_t) * nt);
+    pthread_t *th = malloc(sizeof(pthread_t) * nt);
+    if (!ws || !th) { free(ws); free(th); return 1; }
+    for (int i = 0; i < nt; i++) ws[i] = (bworker_t){&bj, nt, i, 0};
+    for (int i = 1; i < nt; i++)
+        if (pthread_create(&th[i], NULL, bworker, &ws[i])) { ws[i].status = 2; th[i] = 0; }
+    bworker(&ws[0]);
+    int status = 0;
+    for (int i = 1; i < nt; i++)
+        if (ws[i].status != 2) pthread_join(th[i], NULL);
+    for (int i = 0; i < nt; i++) if (ws[i].status) status = ws[i].status;
+    free(ws); free(th);
+    return status;
 }
 
 /* Element-wise array forms of the scalar functions (used by the ulp sweeps). */
