@@ -15,6 +15,7 @@ from .kda import (  # noqa: F401
     KDAError,
     build,
     decode,
+    decode_indexed,
     gate,
     kda_chunk_prefill,
     kda_chunk_prefill_gated,
@@ -23,6 +24,7 @@ from .kda import (  # noqa: F401
     kda_gate_fused,
     kda_get_last_device_error,
     kda_recurrent_decode,
+    kda_recurrent_decode_indexed,
     kda_status_string,
     kda_version,
     library_path,

@@ -222,6 +222,32 @@ kda_status kda_recurrent_decode(const void *q, const void *k, const void *v, con
         o_dtype == KDA_BF16, static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta, void *state_pool,
+                                        kda_dtype state_dtype, const int32_t *state_indices,
+                                        int num_slots, int B, int H, int K, int V, float scale,
+                                        void *o, kda_dtype o_dtype, void *stream) {
+    if (B < 0 || H < 1 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(o_dtype) || !valid_dtype(state_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (B > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr ||
+                  beta == nullptr || state_pool == nullptr || state_indices == nullptr ||
+                  o == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(state_pool) || !aligned16(state_indices) || !aligned16(o))
+        return KDA_ERR_MISALIGNED;
+    if (B == 0) return KDA_OK;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_decode_indexed(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), g, beta, state_pool, state_dtype == KDA_BF16,
+        state_indices, num_slots, B, H, scale, o, o_dtype == KDA_BF16, dev->error_word,
+        static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_get_last_device_error(void *stream) {
     DeviceInfo *dev = nullptr;
     kda_status st = current_device(&dev);

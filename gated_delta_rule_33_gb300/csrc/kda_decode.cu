@@ -26,25 +26,69 @@ constexpr int kD = 128;
 constexpr int kThreads = 256;
 constexpr int kRowsPerThread = kD / (kThreads / 32);  // 16
 
-template <bool kOutBf16>
+// State element access for fp32 or bf16 state storage (four adjacent columns).
+template <bool kStateBf16>
+__device__ __forceinline__ float4 load_state4(const void *S, int64_t idx) {
+    if (kStateBf16) {
+        const uint2 raw = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(S) + idx));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    return __ldcs(reinterpret_cast<const float4 *>(static_cast<const float *>(S) + idx));
+}
+
+template <bool kStateBf16>
+__device__ __forceinline__ void store_state4(void *S, int64_t idx, float4 v) {
+    if (kStateBf16) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 raw;
+        raw.x = *reinterpret_cast<const uint32_t *>(&a);
+        raw.y = *reinterpret_cast<const uint32_t *>(&b);
+        __stcs(reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(S) + idx), raw);
+    } else {
+        __stcs(reinterpret_cast<float4 *>(static_cast<float *>(S) + idx), v);
+    }
+}
+
+// One CTA per (sequence, head).  With `slots` the state of sequence b lives in
+// pool slot slots[b] (negative: inactive sequence, nothing read or written,
+// o = 0; >= num_slots: a device error, skipped); without it, slot b.
+template <bool kOutBf16, bool kStateBf16>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(
     const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
-    const float *__restrict__ beta, float *__restrict__ state, float scale,
-    void *__restrict__ o) {
+    const float *__restrict__ beta, void *__restrict__ state, const int32_t *__restrict__ slots,
+    int num_slots, int H, float scale, void *__restrict__ o, unsigned int *err) {
     __shared__ float s_k[kD], s_q[kD], s_decay[kD], s_u[kD];
     __shared__ float s_red[2][kThreads / 32][kD];
     __shared__ float s_kq;
 
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float *S = state + bh * (kD * kD);
+    int64_t slot = bh / H;
+    if (slots != nullptr) {
+        const int sl = slots[bh / H];
+        if (sl < 0 || sl >= num_slots) {
+            if (sl >= num_slots && tid == 0) record_device_error(err, kDevInvalidArg);
+            if (tid < kD) {
+                if (kOutBf16)
+                    static_cast<__nv_bfloat16 *>(o)[bh * kD + tid] = __float2bfloat16_rn(0.f);
+                else
+                    static_cast<float *>(o)[bh * kD + tid] = 0.f;
+            }
+            return;
+        }
+        slot = sl;
+    }
+    const int64_t sbase = (slot * H + bh % H) * (kD * kD);
 
-    // Issue the whole state read first: 64 KB in flight per CTA.
+    // Issue the whole state read first: the full state in flight per CTA.
     float4 s[kRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i)
-        s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (warp + 8 * i) * kD) + lane);
+        s[i] = load_state4<kStateBf16>(state, sbase + (warp + 8 * i) * kD + 4 * lane);
 
     if (tid < kD) {
         const int64_t idx = bh * kD + tid;
@@ -98,11 +142,26 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(
     for (int i = 0; i < kRowsPerThread; ++i) {
         const float kr = s_k[warp + 8 * i];
         s[i].x += kr * u4.x; s[i].y += kr * u4.y; s[i].z += kr * u4.z; s[i].w += kr * u4.w;
-        __stcs(reinterpret_cast<float4 *>(S + (warp + 8 * i) * kD) + lane, s[i]);
+        store_state4<kStateBf16>(state, sbase + (warp + 8 * i) * kD + 4 * lane, s[i]);
     }
 }
 
 }  // namespace
+
+template <bool kOutBf16>
+static cudaError_t launch_decode_t(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                   const __nv_bfloat16 *v, const float *g, const float *beta,
+                                   void *state, bool state_bf16, const int32_t *slots,
+                                   int num_slots, int64_t units, int H, float scale, void *o,
+                                   unsigned int *err, cudaStream_t s) {
+    if (state_bf16)
+        decode_kernel<kOutBf16, true><<<static_cast<unsigned>(units), kThreads, 0, s>>>(
+            q, k, v, g, beta, state, slots, num_slots, H, scale, o, err);
+    else
+        decode_kernel<kOutBf16, false><<<static_cast<unsigned>(units), kThreads, 0, s>>>(
+            q, k, v, g, beta, state, slots, num_slots, H, scale, o, err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, const float *g, const float *beta,
@@ -110,13 +169,23 @@ cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                           cudaStream_t s) {
     const int64_t units = static_cast<int64_t>(B) * H;
     if (units == 0) return cudaSuccess;
-    if (o_bf16)
-        decode_kernel<true><<<static_cast<unsigned>(units), kThreads, 0, s>>>(q, k, v, g, beta,
-                                                                              state, scale, o);
-    else
-        decode_kernel<false><<<static_cast<unsigned>(units), kThreads, 0, s>>>(q, k, v, g, beta,
-                                                                               state, scale, o);
-    return cudaGetLastError();
+    return o_bf16 ? launch_decode_t<true>(q, k, v, g, beta, state, false, nullptr, B, units, H,
+                                          scale, o, nullptr, s)
+                  : launch_decode_t<false>(q, k, v, g, beta, state, false, nullptr, B, units, H,
+                                           scale, o, nullptr, s);
+}
+
+cudaError_t launch_decode_indexed(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                  const __nv_bfloat16 *v, const float *g, const float *beta,
+                                  void *state_pool, bool state_bf16, const int32_t *slots,
+                                  int num_slots, int B, int H, float scale, void *o, bool o_bf16,
+                                  unsigned int *err, cudaStream_t s) {
+    const int64_t units = static_cast<int64_t>(B) * H;
+    if (units == 0) return cudaSuccess;
+    return o_bf16 ? launch_decode_t<true>(q, k, v, g, beta, state_pool, state_bf16, slots,
+                                          num_slots, units, H, scale, o, err, s)
+                  : launch_decode_t<false>(q, k, v, g, beta, state_pool, state_bf16, slots,
+                                           num_slots, units, H, scale, o, err, s);
 }
 
 }  // namespace kda

@@ -33,7 +33,13 @@ cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                           float *state, int B, int H, float scale, void *o, bool o_bf16,
                           cudaStream_t s);
 
-// Prefill workspace layout is private to kda_prefill.cu.
+cudaError_t launch_decode_indexed(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                  const __nv_bfloat16 *v, const float *g, const float *beta,
+                                  void *state_pool, bool state_bf16, const int32_t *slots,
+                                  int num_slots, int B, int H, float scale, void *o, bool o_bf16,
+                                  unsigned int *err, cudaStream_t s);
+
+// Prefill workspace layout is private to kda_chunk.cu.
 size_t prefill_workspace_bytes(int64_t N, int B, int H);
 
 cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,

@@ -81,6 +81,9 @@ def load():
         lib.kda_chunk_prefill_noalloc.restype = I
         lib.kda_recurrent_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, I, P]
         lib.kda_recurrent_decode.restype = I
+        lib.kda_recurrent_decode_indexed.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, F, P,
+                                                     I, P]
+        lib.kda_recurrent_decode_indexed.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
         lib.kda_get_last_device_error.restype = I
         _lib = lib
@@ -185,6 +188,17 @@ def kda_recurrent_decode(q, k, v, g, beta, state, scale, o, stream=None):
     _check(st, "kda_recurrent_decode")
 
 
+def kda_recurrent_decode_indexed(q, k, v, g, beta, state_pool, state_indices, scale, o,
+                                 stream=None):
+    B, H, K = q.shape
+    V = v.shape[-1]
+    st = load().kda_recurrent_decode_indexed(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool),
+                                             _dtype_code(state_pool), _p(state_indices),
+                                             state_pool.shape[0], B, H, K, V, float(scale), _p(o),
+                                             _dtype_code(o), _stream(stream, q.device))
+    _check(st, "kda_recurrent_decode_indexed")
+
+
 def kda_get_last_device_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word."""
     return int(load().kda_get_last_device_error(_stream(stream)))
@@ -227,6 +241,14 @@ def prefill_gated(q, k, v, f, b, A_log, dt_bias, alog_mode=KDA_ALOG_PER_CHANNEL,
     kda_chunk_prefill_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, cu_seqlens, scale,
                             initial_state, final, o, ws, stream)
     return o, final
+
+
+def decode_indexed(q, k, v, g, beta, state_pool, state_indices, scale=1.0, o_dtype=torch.bfloat16,
+                   stream=None):
+    B, H, K = q.shape
+    o = torch.empty(B, H, v.shape[-1], dtype=o_dtype, device=q.device)
+    kda_recurrent_decode_indexed(q, k, v, g, beta, state_pool, state_indices, scale, o, stream)
+    return o
 
 
 def decode(q, k, v, g, beta, state, scale=1.0, o_dtype=torch.bfloat16, stream=None):

@@ -223,6 +223,33 @@ kda_status kda_recurrent_decode(const void *q, const void *k, const void *v,
                                 void *o, kda_dtype o_dtype, void *stream);
 
 /*
+ * kda_recurrent_decode_indexed -- kda_recurrent_decode over a pool of cached
+ * states addressed by slot, with fp32 or bf16 state storage: the decode side
+ * of continuous batching, where sequences come and go and their states live in
+ * preallocated slots that are updated in place (indexed writes rather than
+ * concatenation: the Kimi-K3 code audit's "repeated-mla-cache-concatenation"
+ * recommendation; FlashKDA's bf16 / fp32 state modes, K3_ARTIFACT_AUDIT.md
+ * section 7.4).
+ *
+ *   q, k, v        bf16 [B, H, 128];  g fp32 [B, H, 128];  beta fp32 [B, H]
+ *   state_pool     [num_slots, H, 128, 128] of state_dtype (fp32 or bf16),
+ *                  read and written in place; a bf16 state is computed in fp32
+ *                  and rounded to nearest on the way back
+ *   state_indices  int32 [B] device: the slot of each sequence.  A negative
+ *                  index marks an inactive sequence (its state is untouched and
+ *                  its output row is zero); an index >= num_slots is skipped the
+ *                  same way and sets the device error word to INVALID_ARG.  Two
+ *                  sequences must not share a slot.
+ *   o              [B, H, 128] of o_dtype
+ */
+kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta,
+                                        void *state_pool, kda_dtype state_dtype,
+                                        const int32_t *state_indices, int num_slots,
+                                        int B, int H, int K, int V, float scale,
+                                        void *o, kda_dtype o_dtype, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word of the
  * current device (KDA_OK when no kernel recorded an error).  Returns
  * KDA_ERR_CUDA if the synchronisation itself fails.

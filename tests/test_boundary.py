@@ -100,6 +100,29 @@ def test_decode_and_gate_argument_checks(clib):
                                      None, 0, None) == 0
 
 
+def test_indexed_decode_and_gated_prefill_argument_checks(clib):
+    P = _fake()
+    # kda_recurrent_decode_indexed(q,k,v,g,beta,pool,state_dtype,idx,slots,B,H,K,V,scale,o,odt,s)
+    assert clib.kda_recurrent_decode_indexed(P, P, P, P, P, P, 0, P, 4, 2, 2, 64, 128, 1.0, P, 0,
+                                             None) == 2
+    assert clib.kda_recurrent_decode_indexed(P, P, P, P, P, P, 5, P, 4, 2, 2, 128, 128, 1.0, P, 0,
+                                             None) == 3
+    assert clib.kda_recurrent_decode_indexed(P, P, P, P, P, P, 0, None, 4, 2, 2, 128, 128, 1.0, P,
+                                             0, None) == 1
+    assert clib.kda_recurrent_decode_indexed(P, P, P, P, P, P, 0, P, -1, 2, 2, 128, 128, 1.0, P,
+                                             0, None) == 1
+    assert clib.kda_recurrent_decode_indexed(None, None, None, None, None, None, 0, None, 0, 0, 2,
+                                             128, 128, 1.0, None, 0, None) == 0
+    # kda_chunk_prefill_gated: f must be bf16; alog_mode must be one of the three
+    ws = _fake()
+    assert clib.kda_chunk_prefill_gated(P, P, P, P, 1, P, 1, P, 1, P, None, 1, 64, 2, 128, 128,
+                                        1.0, None, None, P, 0, ws, 4096, None) == 3
+    assert clib.kda_chunk_prefill_gated(P, P, P, P, 0, P, 1, P, 7, P, None, 1, 64, 2, 128, 128,
+                                        1.0, None, None, P, 0, ws, 4096, None) == 1
+    assert clib.kda_chunk_prefill_gated(P, P, P, P, 0, P, 1, None, 1, P, None, 1, 64, 2, 128, 128,
+                                        1.0, None, None, P, 0, ws, 4096, None) == 1
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "gated_delta_rule_33_gb300")
     for dirpath, _, files in os.walk(pkg):
