@@ -25,10 +25,14 @@ from .kda import (  # noqa: F401
     kda_get_last_device_error,
     kda_recurrent_decode,
     kda_recurrent_decode_indexed,
+    kda_short_conv_qkv,
+    kda_short_conv_qkv_step,
     kda_status_string,
     kda_version,
     library_path,
     load,
     prefill,
     prefill_gated,
+    short_conv,
+    short_conv_step,
 )

@@ -57,6 +57,12 @@ kda_status current_device(DeviceInfo **out) {
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool valid_dtype(kda_dtype d) { return d == KDA_BF16 || d == KDA_FP32; }
 
+// Whether two byte ranges share an address.
+inline bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return a != nullptr && b != nullptr && na > 0 && nb > 0 && pa < pb + nb && pb < pa + na;
+}
+
 kda_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return KDA_OK;
     cudaGetLastError();
@@ -246,6 +252,82 @@ kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void
         static_cast<const __nv_bfloat16 *>(v), g, beta, state_pool, state_dtype == KDA_BF16,
         state_indices, num_slots, B, H, scale, o, o_dtype == KDA_BF16, dev->error_word,
         static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_short_conv_qkv(const void *x_q, const void *x_k, const void *x_v,
+                              const float *w_q, const float *w_k, const float *w_v,
+                              const int32_t *cu_seqlens, int B, int64_t N, int C,
+                              const void *conv_state_in, void *conv_state_out,
+                              void *q, void *k, void *v, void *stream) {
+    if (N < 0 || B < 1 || (cu_seqlens == nullptr && B != 1)) return KDA_ERR_INVALID_ARG;
+    if (C < 128 || C % 128 != 0) return KDA_ERR_UNSUPPORTED_SHAPE;
+    const void *xs[3] = {x_q, x_k, x_v};
+    const float *ws[3] = {w_q, w_k, w_v};
+    void *ys[3] = {q, k, v};
+    const size_t tok_bytes = static_cast<size_t>(N) * C * 2;
+    const size_t st_bytes = static_cast<size_t>(B) * 9 * C * 2;
+    if (N > 0) {
+        for (int i = 0; i < 3; ++i)
+            if (xs[i] == nullptr || ws[i] == nullptr || ys[i] == nullptr) return KDA_ERR_INVALID_ARG;
+        for (int i = 0; i < 3; ++i)
+            for (int j = 0; j < 3; ++j) {
+                if (overlaps(ys[i], tok_bytes, xs[j], tok_bytes)) return KDA_ERR_INVALID_ARG;
+                if (i < j && overlaps(ys[i], tok_bytes, ys[j], tok_bytes)) return KDA_ERR_INVALID_ARG;
+            }
+    }
+    if (overlaps(conv_state_in, st_bytes, conv_state_out, st_bytes)) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (!aligned16(xs[i]) || !aligned16(ws[i]) || !aligned16(ys[i])) return KDA_ERR_MISALIGNED;
+    if (!aligned16(conv_state_in) || !aligned16(conv_state_out) || !aligned16(cu_seqlens))
+        return KDA_ERR_MISALIGNED;
+    if (N == 0 && conv_state_out == nullptr) return KDA_OK;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    const __nv_bfloat16 *xb[3];
+    __nv_bfloat16 *yb[3];
+    for (int i = 0; i < 3; ++i) {
+        xb[i] = static_cast<const __nv_bfloat16 *>(xs[i]);
+        yb[i] = static_cast<__nv_bfloat16 *>(ys[i]);
+    }
+    return from_cuda(kda::launch_short_conv(
+        xb, ws, yb, cu_seqlens, B, N, C, static_cast<const __nv_bfloat16 *>(conv_state_in),
+        static_cast<__nv_bfloat16 *>(conv_state_out), dev->error_word,
+        static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_short_conv_qkv_step(const void *x_q, const void *x_k, const void *x_v,
+                                   const float *w_q, const float *w_k, const float *w_v,
+                                   void *conv_state_pool, const int32_t *state_indices,
+                                   int num_slots, int B, int C,
+                                   void *q, void *k, void *v, void *stream) {
+    if (B < 0 || B > 65535 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (state_indices == nullptr && num_slots < B) return KDA_ERR_INVALID_ARG;
+    if (C < 128 || C % 128 != 0) return KDA_ERR_UNSUPPORTED_SHAPE;
+    const void *xs[3] = {x_q, x_k, x_v};
+    const float *ws[3] = {w_q, w_k, w_v};
+    void *ys[3] = {q, k, v};
+    if (B > 0) {
+        for (int i = 0; i < 3; ++i)
+            if (xs[i] == nullptr || ws[i] == nullptr || ys[i] == nullptr) return KDA_ERR_INVALID_ARG;
+        if (conv_state_pool == nullptr) return KDA_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < 3; ++i)
+        if (!aligned16(xs[i]) || !aligned16(ws[i]) || !aligned16(ys[i])) return KDA_ERR_MISALIGNED;
+    if (!aligned16(conv_state_pool) || !aligned16(state_indices)) return KDA_ERR_MISALIGNED;
+    if (B == 0) return KDA_OK;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    const __nv_bfloat16 *xb[3];
+    __nv_bfloat16 *yb[3];
+    for (int i = 0; i < 3; ++i) {
+        xb[i] = static_cast<const __nv_bfloat16 *>(xs[i]);
+        yb[i] = static_cast<__nv_bfloat16 *>(ys[i]);
+    }
+    return from_cuda(kda::launch_short_conv_step(
+        xb, ws, yb, static_cast<__nv_bfloat16 *>(conv_state_pool), state_indices, num_slots, B, C,
+        dev->error_word, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_get_last_device_error(void *stream) {

@@ -39,6 +39,16 @@ cudaError_t launch_decode_indexed(const __nv_bfloat16 *q, const __nv_bfloat16 *k
                                   int num_slots, int B, int H, float scale, void *o, bool o_bf16,
                                   unsigned int *err, cudaStream_t s);
 
+cudaError_t launch_short_conv(const __nv_bfloat16 *const x[3], const float *const w[3],
+                              __nv_bfloat16 *const y[3], const int32_t *cu_seqlens, int B,
+                              int64_t N, int C, const __nv_bfloat16 *state_in,
+                              __nv_bfloat16 *state_out, unsigned int *err, cudaStream_t s);
+
+cudaError_t launch_short_conv_step(const __nv_bfloat16 *const x[3], const float *const w[3],
+                                   __nv_bfloat16 *const y[3], __nv_bfloat16 *pool,
+                                   const int32_t *slots, int num_slots, int B, int C,
+                                   unsigned int *err, cudaStream_t s);
+
 // Prefill workspace layout is private to kda_chunk.cu.
 size_t prefill_workspace_bytes(int64_t N, int B, int H);
 

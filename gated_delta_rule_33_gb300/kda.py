@@ -84,6 +84,10 @@ def load():
         lib.kda_recurrent_decode_indexed.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, F, P,
                                                      I, P]
         lib.kda_recurrent_decode_indexed.restype = I
+        lib.kda_short_conv_qkv.argtypes = [P, P, P, P, P, P, P, I, I64, I, P, P, P, P, P, P]
+        lib.kda_short_conv_qkv.restype = I
+        lib.kda_short_conv_qkv_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, P, P, P, P]
+        lib.kda_short_conv_qkv_step.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
         lib.kda_get_last_device_error.restype = I
         _lib = lib
@@ -199,6 +203,32 @@ def kda_recurrent_decode_indexed(q, k, v, g, beta, state_pool, state_indices, sc
     _check(st, "kda_recurrent_decode_indexed")
 
 
+def kda_short_conv_qkv(x_q, x_k, x_v, w_q, w_k, w_v, cu_seqlens, conv_state_in, conv_state_out,
+                       q, k, v, stream=None):
+    """x_* bf16 [N, C] (or [N, H, 128]); w_* fp32 [C, 4]; states bf16 [B, 3, 3, C]."""
+    N = x_q.shape[0]
+    C = w_q.shape[0]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_short_conv_qkv(_p(x_q), _p(x_k), _p(x_v), _p(w_q), _p(w_k), _p(w_v),
+                                   _p(cu_seqlens), B, N, C, _p(conv_state_in),
+                                   _p(conv_state_out), _p(q), _p(k), _p(v),
+                                   _stream(stream, x_q.device))
+    _check(st, "kda_short_conv_qkv")
+
+
+def kda_short_conv_qkv_step(x_q, x_k, x_v, w_q, w_k, w_v, conv_state_pool, state_indices, q, k,
+                            v, stream=None):
+    """x_* bf16 [B, C]; conv_state_pool bf16 [num_slots, 3, 3, C]; state_indices int32 [B]
+    or None (slot b = sequence b)."""
+    B = x_q.shape[0]
+    C = w_q.shape[0]
+    st = load().kda_short_conv_qkv_step(_p(x_q), _p(x_k), _p(x_v), _p(w_q), _p(w_k), _p(w_v),
+                                        _p(conv_state_pool), _p(state_indices),
+                                        conv_state_pool.shape[0], B, C, _p(q), _p(k), _p(v),
+                                        _stream(stream, x_q.device))
+    _check(st, "kda_short_conv_qkv_step")
+
+
 def kda_get_last_device_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word."""
     return int(load().kda_get_last_device_error(_stream(stream)))
@@ -249,6 +279,28 @@ def decode_indexed(q, k, v, g, beta, state_pool, state_indices, scale=1.0, o_dty
     o = torch.empty(B, H, v.shape[-1], dtype=o_dtype, device=q.device)
     kda_recurrent_decode_indexed(q, k, v, g, beta, state_pool, state_indices, scale, o, stream)
     return o
+
+
+def short_conv(x_q, x_k, x_v, w_q, w_k, w_v, cu_seqlens=None, conv_state=None,
+               output_final_state=True, stream=None):
+    """The pre-step on the three streams; returns (q, k, v, final conv state or None)."""
+    C = w_q.shape[0]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    q, k, v = (torch.empty_like(x) for x in (x_q, x_k, x_v))
+    final = (torch.empty(B, 3, 3, C, dtype=torch.bfloat16, device=x_q.device)
+             if output_final_state else None)
+    kda_short_conv_qkv(x_q, x_k, x_v, w_q, w_k, w_v, cu_seqlens, conv_state, final, q, k, v,
+                       stream)
+    return q, k, v, final
+
+
+def short_conv_step(x_q, x_k, x_v, w_q, w_k, w_v, conv_state_pool, state_indices=None,
+                    stream=None):
+    """One token per sequence; the pool is updated in place.  Returns (q, k, v)."""
+    q, k, v = (torch.empty_like(x) for x in (x_q, x_k, x_v))
+    kda_short_conv_qkv_step(x_q, x_k, x_v, w_q, w_k, w_v, conv_state_pool, state_indices, q, k,
+                            v, stream)
+    return q, k, v
 
 
 def decode(q, k, v, g, beta, state, scale=1.0, o_dtype=torch.bfloat16, stream=None):

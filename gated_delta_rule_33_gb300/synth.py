@@ -156,3 +156,37 @@ def make_decode_inputs(B: int, H: int = 96, D: int = 128, *, seed: int = 0,
 def tiny_config(seed: int = 0) -> KDAInputs:
     """The oracle-scale case: B=1, T=64, H=2, d_k=d_v=16, all fp32, zero state."""
     return make_inputs(64, H=2, D=16, seed=seed, dtype=torch.float32, f_dtype=torch.float32)
+
+
+@dataclass
+class ShortConvInputs:
+    x: List[torch.Tensor]            # q, k, v projection outputs, bf16 [N, H*D] each
+    w: List[torch.Tensor]            # conv taps, fp32 [H*D, 4] each
+    cu_seqlens: Optional[torch.Tensor]
+    state: Optional[torch.Tensor]    # bf16 [B, 3, 3, H*D] carried conv state or None
+
+
+def make_shortconv_inputs(N: Optional[int] = None, H: int = 96, D: int = 128, *, seed: int = 0,
+                          lengths: Optional[List[int]] = None, with_state: bool = False,
+                          w_std: float = 0.5) -> ShortConvInputs:
+    """Inputs of the pre-step: three projection streams x ~ N(0, 1) in bf16,
+    taps w ~ N(0, w_std) fp32 per channel (the pages give only their shape,
+    [H*D, 1, 4]), optional carried states ~ N(0, 1) in bf16.  Draw order: x_q,
+    x_k, x_v, w_q, w_k, w_v, state, from one CPU generator."""
+    gen = torch.Generator().manual_seed(seed)
+    if lengths is not None:
+        lengths = [int(t) for t in lengths]
+        N = sum(lengths)
+    C = H * D
+    x = [torch.randn(N, C, generator=gen).to(torch.bfloat16) for _ in range(3)]
+    w = [torch.normal(0.0, w_std, (C, 4), generator=gen) for _ in range(3)]
+    cu = None
+    B = 1
+    if lengths is not None:
+        B = len(lengths)
+        cu = torch.zeros(B + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    state = None
+    if with_state:
+        state = torch.randn(B, 3, 3, C, generator=gen).to(torch.bfloat16)
+    return ShortConvInputs(x, w, cu, state)

@@ -250,6 +250,63 @@ kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void
                                         void *o, kda_dtype o_dtype, void *stream);
 
 /*
+ * kda_short_conv_qkv -- the KDA input pre-step over a packed batch, on the three
+ * projection streams at once: a depthwise causal convolution of kernel size 4
+ * per channel (the checkpoint's q/k/v_conv1d.weight, fp32 [H*128, 1, 4];
+ * K3_ARTIFACT_AUDIT.md section 4.1, KDA tensor table), then SiLU, then for q
+ * and k an L2 norm over each head's 128 channels:
+ *
+ *   a[p, c] = sum_{j=0..3} w[c, j] x[p - 3 + j, c]     (tap 3 on the current token)
+ *   y = a * sigmoid(a);   q, k: y / sqrt(sum_head y^2 + 1e-6);   v: y
+ *
+ * Positions before a sequence's first token read that sequence's carried
+ * state (the last three raw inputs of its previous segment, oldest first), or
+ * zeros when conv_state_in is NULL.  Sequences never see each other.
+ *
+ *   x_q, x_k, x_v     bf16 [N, C] each, C = H * 128 (the projection outputs)
+ *   w_q, w_k, w_v     fp32 [C, 4] each
+ *   cu_seqlens, B     as in kda_chunk_prefill (NULL: one sequence, B = 1)
+ *   conv_state_in     bf16 [B, 3 (q, k, v), 3 (oldest first), C] or NULL
+ *   conv_state_out    bf16 [B, 3, 3, C] or NULL: each sequence's last three
+ *                     inputs (state rows fill in for sequences shorter than 3;
+ *                     an empty sequence passes its state through).  Must not
+ *                     overlap conv_state_in.
+ *   q, k, v           bf16 [N, C] outputs, ready for kda_chunk_prefill as
+ *                     [N, H, 128]; must not overlap any input
+ *
+ * C must be a positive multiple of 128 (KDA_ERR_UNSUPPORTED_SHAPE).  A bad
+ * cu_seqlens array sets the device error word to INVALID_ARG.  N == 0 with
+ * conv_state_out copies the states through.
+ */
+kda_status kda_short_conv_qkv(const void *x_q, const void *x_k, const void *x_v,
+                              const float *w_q, const float *w_k, const float *w_v,
+                              const int32_t *cu_seqlens, int B, int64_t N, int C,
+                              const void *conv_state_in, void *conv_state_out,
+                              void *q, void *k, void *v, void *stream);
+
+/*
+ * kda_short_conv_qkv_step -- the same pre-step for one new token per sequence,
+ * the carried conv states kept in a pool addressed by slot and updated in
+ * place (the decode side of kda_short_conv_qkv).
+ *
+ *   x_q, x_k, x_v     bf16 [B, C];  w_q, w_k, w_v fp32 [C, 4]
+ *   conv_state_pool   bf16 [num_slots, 3, 3, C], read and shifted in place
+ *   state_indices     int32 [B] device, or NULL for slot b = sequence b
+ *                     (then num_slots >= B).  Negative: inactive sequence
+ *                     (outputs zero, state untouched); >= num_slots: skipped
+ *                     the same way and the device error word set to
+ *                     INVALID_ARG.  Two sequences must not share a slot.
+ *   q, k, v           bf16 [B, C] outputs (may be the inputs themselves)
+ *
+ * C must be a positive multiple of 128; B <= 65535.
+ */
+kda_status kda_short_conv_qkv_step(const void *x_q, const void *x_k, const void *x_v,
+                                   const float *w_q, const float *w_k, const float *w_v,
+                                   void *conv_state_pool, const int32_t *state_indices,
+                                   int num_slots, int B, int C,
+                                   void *q, void *k, void *v, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device error word of the
  * current device (KDA_OK when no kernel recorded an error).  Returns
  * KDA_ERR_CUDA if the synchronisation itself fails.

@@ -123,6 +123,34 @@ def test_indexed_decode_and_gated_prefill_argument_checks(clib):
                                         1.0, None, None, P, 0, ws, 4096, None) == 1
 
 
+def test_short_conv_argument_checks(clib):
+    P, Q, R = _fake(0x10000), _fake(0x900000), _fake(0x1900000)
+    # kda_short_conv_qkv(xq,xk,xv,wq,wk,wv,cu,B,N,C,st_in,st_out,q,k,v,stream)
+    def call(**kw):
+        a = dict(x=(P, P, P), w=(P, P, P), cu=None, B=1, N=16, C=256, si=None, so=None,
+                 y=(Q, R, _fake(0x2900000)))
+        a.update(kw)
+        return clib.kda_short_conv_qkv(*a["x"], *a["w"], a["cu"], a["B"], a["N"], a["C"], a["si"],
+                                       a["so"], *a["y"], None)
+    assert call(C=200) == 2                      # not a multiple of 128
+    assert call(C=0) == 2
+    assert call(N=-1) == 1
+    assert call(B=2) == 1                        # B > 1 needs cu_seqlens
+    assert call(x=(None, P, P)) == 1
+    assert call(y=(P, R, _fake(0x2900000))) == 1  # output overlaps an input
+    assert call(y=(Q, Q, _fake(0x2900000))) == 1  # two outputs overlap
+    assert call(si=P, so=P) == 1                 # state in and out overlap
+    assert call(x=(_fake(0x10008), P, P)) == 4
+    assert call(N=0) == 0                        # nothing to do, no device touched
+    # kda_short_conv_qkv_step(xq,xk,xv,wq,wk,wv,pool,idx,num_slots,B,C,q,k,v,stream)
+    assert clib.kda_short_conv_qkv_step(P, P, P, P, P, P, P, None, 1, 2, 256, P, P, P, None) == 1
+    assert clib.kda_short_conv_qkv_step(P, P, P, P, P, P, P, P, 4, 70000, 256, P, P, P,
+                                        None) == 1
+    assert clib.kda_short_conv_qkv_step(P, P, P, P, P, P, None, P, 4, 2, 256, P, P, P, None) == 1
+    assert clib.kda_short_conv_qkv_step(P, P, P, P, P, P, P, P, 4, 2, 100, P, P, P, None) == 2
+    assert clib.kda_short_conv_qkv_step(P, P, P, P, P, P, P, P, 4, 0, 256, P, P, P, None) == 0
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "gated_delta_rule_33_gb300")
     for dirpath, _, files in os.walk(pkg):
