@@ -13,6 +13,7 @@ from .kda import (  # noqa: F401
     KDA_BF16,
     KDA_FP32,
     KDAError,
+    backward,
     build,
     decode,
     decode_indexed,
@@ -23,6 +24,8 @@ from .kda import (  # noqa: F401
     kda_chunk_prefill_workspace_size,
     kda_gate_fused,
     kda_get_last_device_error,
+    kda_recurrent_backward,
+    kda_recurrent_backward_workspace_size,
     kda_recurrent_decode,
     kda_recurrent_decode_indexed,
     kda_short_conv_qkv,

@@ -49,6 +49,18 @@ cudaError_t launch_short_conv_step(const __nv_bfloat16 *const x[3], const float 
                                    const int32_t *slots, int num_slots, int B, int C,
                                    unsigned int *err, cudaStream_t s);
 
+// Backward (kda_backward.cu): workspace for `ctas` CTAs, and the launch.
+constexpr int kBackwardMaxCtas = 256;
+size_t backward_workspace_bytes(int64_t N, int B, int H, int ctas);
+int backward_ctas(int B, int H, int max_ctas);
+
+cudaError_t launch_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                            const __nv_bfloat16 *v, const float *g, const float *beta,
+                            const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+                            const float *S0, const void *dO, bool dO_bf16, const float *dSf,
+                            float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
+                            void *workspace, int ctas, unsigned int *err, cudaStream_t s);
+
 // Prefill workspace layout is private to kda_chunk.cu.
 size_t prefill_workspace_bytes(int64_t N, int B, int H);
 

@@ -88,6 +88,11 @@ def load():
         lib.kda_short_conv_qkv.restype = I
         lib.kda_short_conv_qkv_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, P, P, P, P]
         lib.kda_short_conv_qkv_step.restype = I
+        lib.kda_recurrent_backward_workspace_size.argtypes = [I64, I, I, I, I]
+        lib.kda_recurrent_backward_workspace_size.restype = ctypes.c_size_t
+        lib.kda_recurrent_backward.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, I, P,
+                                               P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.kda_recurrent_backward.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
         lib.kda_get_last_device_error.restype = I
         _lib = lib
@@ -229,6 +234,23 @@ def kda_short_conv_qkv_step(x_q, x_k, x_v, w_q, w_k, w_v, conv_state_pool, state
     _check(st, "kda_short_conv_qkv_step")
 
 
+def kda_recurrent_backward_workspace_size(N, B, H, K=128, V=128) -> int:
+    return int(load().kda_recurrent_backward_workspace_size(N, B, H, K, V))
+
+
+def kda_recurrent_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final,
+                           dq, dk, dv, dg, dbeta, dS0, workspace, stream=None):
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_recurrent_backward(
+        _p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), B, N, H, K, V, float(scale),
+        _p(initial_state), _p(dO), _dtype_code(dO), _p(dS_final), _p(dq), _p(dk), _p(dv), _p(dg),
+        _p(dbeta), _p(dS0), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, q.device))
+    _check(st, "kda_recurrent_backward")
+
+
 def kda_get_last_device_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word."""
     return int(load().kda_get_last_device_error(_stream(stream)))
@@ -301,6 +323,24 @@ def short_conv_step(x_q, x_k, x_v, w_q, w_k, w_v, conv_state_pool, state_indices
     kda_short_conv_qkv_step(x_q, x_k, x_v, w_q, w_k, w_v, conv_state_pool, state_indices, q, k,
                             v, stream)
     return q, k, v
+
+
+def backward(q, k, v, g, beta, dO, cu_seqlens=None, scale=1.0, initial_state=None,
+             dS_final=None, want_dS0=True, stream=None):
+    """Gradients of the recurrence; returns (dq, dk, dv, dg, dbeta, dS0 or None)."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.device
+    dq, dk, dg = (torch.empty(N, H, K, device=dev) for _ in range(3))
+    dv = torch.empty(N, H, V, device=dev)
+    dbeta = torch.empty(N, H, device=dev)
+    dS0 = torch.empty(B, H, K, V, device=dev) if want_dS0 else None
+    ws = torch.empty(kda_recurrent_backward_workspace_size(N, B, H, K, V), dtype=torch.uint8,
+                     device=dev)
+    kda_recurrent_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final, dq,
+                           dk, dv, dg, dbeta, dS0, ws, stream)
+    return dq, dk, dv, dg, dbeta, dS0
 
 
 def decode(q, k, v, g, beta, state, scale=1.0, o_dtype=torch.bfloat16, stream=None):

@@ -250,6 +250,49 @@ kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void
                                         void *o, kda_dtype o_dtype, void *stream);
 
 /*
+ * kda_recurrent_backward -- gradients of the KDA recurrence for training
+ * ("chunked KDA for training", code-audit.json, finding
+ * "dual-kda-execution-regimes"): given dL/do and dL/dS_final for the forward
+ * pass that kda_chunk_prefill computes on the same inputs, the gradients with
+ * respect to q, k, v, g, beta and the initial state.  With
+ * S' = Diag(exp g_t) S_{t-1}, w = S'^T k_t, u = beta_t (v_t - w),
+ * S_t = S' + k_t u^T, o_t = S_t^T (scale q_t), each reverse step from
+ * G = dL/dS_t is
+ *   G += (scale q_t) do_t^T;  du = G^T k_t;  dv_t = beta_t du;
+ *   dbeta_t = du . (v_t - w);  dw = -beta_t du;  dk_t = G u + S' dw;
+ *   dq_t = scale S_t do_t;  dg_t = rowsum((G + k_t dw^T) (.) S');
+ *   G = Diag(exp g_t) (G + k_t dw^T)
+ * (dL/dS_0 = G at the end).  Computed token by token in fp32 on CUDA cores:
+ * a forward pass keeps the state every 16 tokens in the workspace, and each
+ * 16-token segment is rerun from it in reverse order.
+ *
+ *   q, k, v        bf16 [N, H, 128];  g fp32 [N, H, 128];  beta fp32 [N, H]
+ *   cu_seqlens, B, initial_state, scale   as in kda_chunk_prefill
+ *   dO             [N, H, 128] of dO_dtype (bf16 or fp32)
+ *   dS_final       fp32 [B, H, 128, 128] or NULL (zero)
+ *   dq, dk, dv, dg fp32 [N, H, 128];  dbeta fp32 [N, H]   (all written)
+ *   dS0            fp32 [B, H, 128, 128] or NULL (not computed)
+ *   workspace      device, >= kda_recurrent_backward_workspace_size() bytes
+ *                  (states every 16 tokens plus 1 MB per CTA; 1.7 GB for
+ *                  N = 4096, H = 96); its contents are scratch
+ *
+ * The gate's own gradients (to f, A_log, dt_bias and the beta logits) are
+ * the caller's: g and beta enter here as given tensors.  A bad cu_seqlens
+ * entry sets the device error word to INVALID_ARG.
+ */
+size_t kda_recurrent_backward_workspace_size(int64_t N, int B, int H, int K, int V);
+
+kda_status kda_recurrent_backward(const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta,
+                                  const int32_t *cu_seqlens, int B,
+                                  int64_t N, int H, int K, int V, float scale,
+                                  const float *initial_state,
+                                  const void *dO, kda_dtype dO_dtype, const float *dS_final,
+                                  float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                                  float *dS0, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
  * kda_short_conv_qkv -- the KDA input pre-step over a packed batch, on the three
  * projection streams at once: a depthwise causal convolution of kernel size 4
  * per channel (the checkpoint's q/k/v_conv1d.weight, fp32 [H*128, 1, 4];

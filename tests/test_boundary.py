@@ -151,6 +151,29 @@ def test_short_conv_argument_checks(clib):
     assert clib.kda_short_conv_qkv_step(P, P, P, P, P, P, P, P, 4, 0, 256, P, P, P, None) == 0
 
 
+def test_backward_argument_checks(clib):
+    import gated_delta_rule_33_gb300 as kda
+    P, ws = _fake(), _fake()
+    need = kda.kda_recurrent_backward_workspace_size(64, 1, 2)
+    assert need > 0 and kda.kda_recurrent_backward_workspace_size(64, 1, 2, 64, 128) == 0
+
+    def call(**kw):
+        a = dict(q=P, cu=None, B=1, N=64, K=128, dodt=0, ws=ws, wsb=need)
+        a.update(kw)
+        # (q,k,v,g,beta,cu,B,N,H,K,V,scale,S0,dO,dO_dtype,dSf,dq,dk,dv,dg,dbeta,dS0,ws,wsb,s)
+        return clib.kda_recurrent_backward(a["q"], P, P, P, P, a["cu"], a["B"], a["N"], 2, a["K"],
+                                           128, 1.0, None, P, a["dodt"], None, P, P, P, P, P,
+                                           None, a["ws"], a["wsb"], None)
+    assert call(K=64) == 2
+    assert call(dodt=9) == 3
+    assert call(N=-1) == 1
+    assert call(B=3) == 1
+    assert call(q=None) == 1
+    assert call(q=_fake(0x10004)) == 4
+    assert call(wsb=need - 1) == 5
+    assert call(ws=None) == 5
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "gated_delta_rule_33_gb300")
     for dirpath, _, files in os.walk(pkg):
