@@ -87,10 +87,11 @@ def prefill_kernel_bytes(T, Hh=H, K=D, V=D, o_bytes=2):
     return T * Hh * (2 * K * 2 + 2 * V + 4 * K + 4 + o_bytes * V) + Hh * K * V * 4
 
 
-def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D):
-    """Decode kernel: every fp32 state read once and written once, plus the token
-    (q, k, v bf16; g fp32; beta fp32) and the output (bf16)."""
-    return B * Hh * (2 * K * V * 4 + 2 * K * 2 + 2 * V + 4 * K + 4 + 2 * V)
+def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4):
+    """Decode kernel: every state (fp32, or bf16 with state_bytes=2) read once
+    and written once, plus the token (q, k, v bf16; g fp32; beta fp32) and the
+    output (bf16)."""
+    return B * Hh * (2 * K * V * state_bytes + 2 * K * 2 + 2 * V + 4 * K + 4 + 2 * V)
 
 
 # DRAM read+write bytes per benchmark launch, from the ncu captures summarised
@@ -382,6 +383,51 @@ def run_ours(args):
     gate_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in uf)
     prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in uf)
 
+    def timed(fn, steps):
+        """Mean CUDA-event time of fn() on the stream after one untimed call."""
+        fn()
+        torch.cuda.synchronize(dev)
+        evs = []
+        for _ in range(steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # decode from a bf16 state pool addressed by slot (reversed order); its own
+    # timed loop, not part of `value`
+    pool = state.to(torch.bfloat16)
+    slots = torch.arange(B_DECODE - 1, -1, -1, dtype=torch.int32, device=dev)
+    pool_ms = timed(lambda: kda.kda_recurrent_decode_indexed(dq, dk, dv, dg, dbeta, pool, slots,
+                                                             1.0, dout, stream), args.steps)
+    del pool
+
+    # the pre-step (ShortConv + SiLU + L2 norm on q, k, v) at the prefill size
+    sx = synth.make_shortconv_inputs(T_PREFILL, H=H, D=D, seed=rank)
+    sxs = [t.to(dev) for t in sx.x]
+    sws = [t.to(dev) for t in sx.w]
+    souts = [torch.empty_like(t) for t in sxs]
+    sfin = torch.empty(1, 3, 3, H * D, dtype=torch.bfloat16, device=dev)
+    conv_ms = timed(lambda: kda.kda_short_conv_qkv(*sxs, *sws, None, None, sfin, *souts, stream),
+                    args.steps)
+    del sx, sxs, souts
+
+    # the backward (training regime) of the prefill workload
+    kda.kda_gate_fused(f, b, A_log, x.alog_mode, dt_bias, g, beta, stream)
+    bgen = torch.Generator(device=dev).manual_seed(rank + 77)
+    bdO = torch.randn(T_PREFILL, H, D, device=dev, generator=bgen).to(torch.bfloat16)
+    bgrads = [torch.empty(T_PREFILL, H, D, device=dev) for _ in range(4)]
+    bdbeta = torch.empty(T_PREFILL, H, device=dev)
+    bws = torch.empty(kda.kda_recurrent_backward_workspace_size(T_PREFILL, 1, H),
+                      dtype=torch.uint8, device=dev)
+    bwd_ms = timed(lambda: kda.kda_recurrent_backward(q, k, v, g, beta, None, 1.0, None, bdO, None,
+                                                      *bgrads, bdbeta, None, bws, stream),
+                   max(args.steps // 3, 1))
+    del bgrads, bws, bdO
+
     prefill_leg_ms = max_over_ranks(fused_ms, world, dev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
     decode_ms_max = max_over_ranks(decode_ms, world, dev)
@@ -453,6 +499,33 @@ def run_ours(args):
     rl_decode = {"kernel": "kda recurrent decode", "bound": "hbm", "achieved": dec_gbs,
                  "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm, "traffic": None,
                  "peak_source": peaks["source"], "algorithmic_bytes_per_launch": decode_bytes()}
+    pool_bytes = decode_bytes(state_bytes=2) + B_DECODE * 4
+    pool_gbs = pool_bytes / (pool_ms * 1e-3) / 1e9
+    rl_pool = {"kernel": "kda recurrent decode, bf16 state pool by slot", "bound": "hbm",
+               "achieved": pool_gbs, "peak": hbm, "unit": "GB/s", "frac": pool_gbs / hbm,
+               "traffic": None, "traffic_note": "not captured", "ms": pool_ms,
+               "peak_source": peaks["source"], "algorithmic_bytes_per_launch": pool_bytes}
+    conv_bytes = 3 * (T_PREFILL * H * D * 4 + H * D * 16 + 3 * H * D * 2)
+    conv_gbs = conv_bytes / (conv_ms * 1e-3) / 1e9
+    rl_conv = {"kernel": "kda short conv + SiLU + L2 norm pre-step (q, k, v)", "bound": "hbm",
+               "achieved": conv_gbs, "peak": hbm, "unit": "GB/s", "frac": conv_gbs / hbm,
+               "traffic": None, "traffic_note": "not captured", "ms": conv_ms,
+               "peak_source": peaks["source"], "algorithmic_bytes_per_launch": conv_bytes}
+    # backward: per token-head one forward step (5 K V flops: decay, column sum,
+    # rank-1 update) and one reverse step (18 K V: G += q do^T, du, S', w, four
+    # row sums, G update), against the fp32 FMA rate of the CUDA cores (SMs x 128
+    # lanes x 2 flops x the median SM clock sampled in the timed region)
+    bwd_flops = T_PREFILL * H * 23 * D * D
+    sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    fp32_peak = (torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 *
+                 sm_mhz * 1e6 / 1e12)
+    bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    rl_bwd = {"kernel": "kda recurrent backward (token by token, CUDA cores)", "bound": "alu",
+              "achieved": bwd_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+              "frac": bwd_tflops / fp32_peak, "traffic": None, "traffic_note": "not captured",
+              "peak_source": "fp32 FMA lanes x median SM clock of the timed region",
+              "algorithmic_flops_per_launch": bwd_flops, "ms": bwd_ms,
+              "tokens_per_s": T_PREFILL / (bwd_ms * 1e-3)}
     gate_bytes = T_PREFILL * H * (2 * D + 4 * D + 8)
     gate_gbs = gate_bytes / (gate_ms * 1e-3) / 1e9
     rl_gate = {"kernel": "kda gate", "bound": "hbm", "achieved": gate_gbs, "peak": hbm,
@@ -479,7 +552,8 @@ def run_ours(args):
         "decode_state_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / hbm,
         "roofline": roofline,
         "rooflines": {"gate": rl_gate, "prefill_gated": rl_prefill,
-                      "prefill_unfused": rl_prefill_unfused, "decode": rl_decode},
+                      "prefill_unfused": rl_prefill_unfused, "decode": rl_decode,
+                      "decode_bf16_pool": rl_pool, "short_conv": rl_conv, "backward": rl_bwd},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -499,20 +573,38 @@ def run_profile_case(args):
     from gated_delta_rule_33_gb300 import synth
     dev = torch.device("cuda", 0)
     kda.load()
-    if args.profile in ("gate", "prefill"):
+    if args.profile == "short_conv":
+        sx = synth.make_shortconv_inputs(args.size, H=H, D=D, seed=0)
+        xs = [t.to(dev) for t in sx.x]
+        ws = [t.to(dev) for t in sx.w]
+        for _ in range(args.warmup + 1):
+            kda.short_conv(*xs, *ws)
+    elif args.profile in ("gate", "prefill", "prefill_gated", "backward"):
         x = synth.make_inputs(args.size, H=H, D=D, seed=0, device=dev)
         g, beta = kda.gate(x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
+        dO = torch.randn_like(x.q) if args.profile == "backward" else None
         for _ in range(args.warmup + 1):
             if args.profile == "gate":
                 kda.gate(x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
-            else:
+            elif args.profile == "prefill":
                 kda.prefill(x.q, x.k, x.v, g, beta)
+            elif args.profile == "prefill_gated":
+                kda.prefill_gated(x.q, x.k, x.v, x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
+            else:
+                kda.backward(x.q, x.k, x.v, g, beta, dO, want_dS0=False)
     else:
         d = synth.make_decode_inputs(args.size, H=H, D=D, seed=0, state_device=dev)
         q, k, v, f, b = (t.to(dev) for t in (d.q, d.k, d.v, d.f, d.b))
         g, beta = kda.gate(f, b, d.A_log.to(dev), d.dt_bias.to(dev), d.alog_mode)
+        if args.profile == "decode_pool":
+            pool = d.state.to(torch.bfloat16)
+            slots = torch.arange(args.size - 1, -1, -1, dtype=torch.int32, device=dev)
+            del d
         for _ in range(args.warmup + 1):
-            kda.decode(q, k, v, g, beta, d.state)
+            if args.profile == "decode":
+                kda.decode(q, k, v, g, beta, d.state)
+            else:
+                kda.decode_indexed(q, k, v, g, beta, pool, slots)
     torch.cuda.synchronize()
     st = kda.kda_get_last_device_error()
     print(json.dumps({"profile": args.profile, "size": args.size, "device_error": st}))
@@ -530,7 +622,8 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=96,
                     help="heads of the T=4096 workload timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["gate", "prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["gate", "prefill", "prefill_gated", "decode",
+                                                  "decode_pool", "short_conv", "backward"], default=None,
                     help="run only this kernel (warm-up + 1 launch) for an ncu capture")
     ap.add_argument("--size", type=int, default=1024,
                     help="--profile size: tokens (gate, prefill) or sequences (decode)")
