@@ -57,10 +57,13 @@ struct BwdParams {
     unsigned int *err;
 };
 
-struct TokenVecs {
+// 16-byte aligned (and so padded to a multiple of 16 bytes): the reverse
+// step reads dO as float4.
+struct __align__(16) TokenVecs {
     float q[kD], k[kD], v[kD], d[kD], dO[kD];
     float beta;
 };
+static_assert(sizeof(TokenVecs) % 16 == 0, "TokenVecs must keep float4 alignment in arrays");
 
 __device__ __forceinline__ float4 f4_scale(float4 a, float s) {
     return make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
@@ -104,9 +107,11 @@ __device__ __forceinline__ void load_token(const BwdParams &p, int64_t t, int h,
 }
 
 __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p) {
+    // float4 accesses below: every array 16-byte aligned
     __shared__ TokenVecs s_tok[2];
-    __shared__ float s_red[2][kThreads / 32][kD];
-    __shared__ float s_u[kD], s_dw[kD];
+    __shared__ __align__(16) float s_red[2][kThreads / 32][kD];
+    __shared__ __align__(16) float s_u[kD];
+    __shared__ __align__(16) float s_dw[kD];
     __shared__ float s_sc[2][4];
     __shared__ int s_chain;
 

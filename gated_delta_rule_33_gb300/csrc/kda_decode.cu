@@ -61,8 +61,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(
     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
     const float *__restrict__ beta, void *__restrict__ state, const int32_t *__restrict__ slots,
     int num_slots, int H, float scale, void *__restrict__ o, unsigned int *err) {
-    __shared__ float s_k[kD], s_q[kD], s_decay[kD], s_u[kD];
-    __shared__ float s_red[2][kThreads / 32][kD];
+    __shared__ float s_k[kD], s_q[kD], s_decay[kD];
+    __shared__ __align__(16) float s_u[kD];                   // read as float4
+    __shared__ __align__(16) float s_red[2][kThreads / 32][kD];   // written as float4
     __shared__ float s_kq;
 
     const int64_t bh = blockIdx.x;
