@@ -98,21 +98,37 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4):
 # in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
-    "kda_chunk.cu": {"sha256": "572b1d17dc522819e6f0ed3f231fe0e278b98f3b828fe8ee1ab75fea4b8e4ed1", "bytes": 4 * 139.11e6,
-                     "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
-    "kda_decode.cu": {"sha256": "23fa09c312ad130bff268601ce628625ab6f908a0902f15ac5d86404f0f54c64", "bytes": 4 * 754.49e6,
-                      "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
-    "kda_gate.cu": {"sha256": "c571ed29aa63aa23447ebb39f20cf362297d7d0e0342dce221f132091a056852", "bytes": 246.78e6,
-                    "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
+    "chunk_unfused": {"src": "kda_chunk.cu", "bytes": 4 * 140.25e6,
+                      "sha256": "5c62c77f05ef9cbda2911d9a5fe98de933524af116787b4df45c90e843eede6a",
+                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
+    "chunk_gated": {"src": "kda_chunk.cu", "bytes": 4 * 111.29e6,
+                    "sha256": "5c62c77f05ef9cbda2911d9a5fe98de933524af116787b4df45c90e843eede6a",
+                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
+    "decode": {"src": "kda_decode.cu", "bytes": 4 * 753.98e6,
+               "sha256": "cbce038541a155e0f5cd0b0a11e0ac8fc159311b6c620be5864600bb99740081",
+               "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
+    "decode_pool": {"src": "kda_decode.cu", "bytes": 4 * 350.65e6,
+                    "sha256": "cbce038541a155e0f5cd0b0a11e0ac8fc159311b6c620be5864600bb99740081",
+                    "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
+    "gate": {"src": "kda_gate.cu", "bytes": 246.78e6,
+             "sha256": "c571ed29aa63aa23447ebb39f20cf362297d7d0e0342dce221f132091a056852",
+             "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
+    "short_conv": {"src": "kda_shortconv.cu", "bytes": 557.47e6,
+                   "sha256": "63417a724d638dbee09d5b86b350fdc5bcaac7a7864b46ccf38e853228e0c920",
+                   "note": "T=4096 capture (profiles/short_conv_T4096_H96.md)"},
 }
 
 
-def measured_traffic(src_name):
+def measured_traffic(kernel_id):
+    """(bytes, note) of the ncu capture of one kernel, or (None, why) when the
+    kernel's source has changed since the capture."""
     import hashlib
-    ent = NCU_TRAFFIC.get(src_name)
-    path = os.path.join(ROOT, "gated_delta_rule_33_gb300", "csrc", src_name)
-    if ent is None or not os.path.exists(path):
-        return None, None
+    ent = NCU_TRAFFIC.get(kernel_id)
+    if ent is None:
+        return None, "not captured"
+    path = os.path.join(ROOT, "gated_delta_rule_33_gb300", "csrc", ent["src"])
+    if not os.path.exists(path):
+        return None, "source missing"
     with open(path, "rb") as fh:
         digest = hashlib.sha256(fh.read()).hexdigest()
     if digest != ent["sha256"]:
@@ -531,10 +547,10 @@ def run_ours(args):
     rl_gate = {"kernel": "kda gate", "bound": "hbm", "achieved": gate_gbs, "peak": hbm,
                "unit": "GB/s", "frac": gate_gbs / hbm, "traffic": None,
                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": gate_bytes}
-    rl_prefill["traffic"], rl_prefill["traffic_note"] = None, "no capture of the fused kernel yet"
-    for rl, src in ((rl_prefill_unfused, "kda_chunk.cu"), (rl_decode, "kda_decode.cu"),
-                    (rl_gate, "kda_gate.cu")):
-        rl["traffic"], rl["traffic_note"] = measured_traffic(src)
+    for rl, kid in ((rl_prefill, "chunk_gated"), (rl_prefill_unfused, "chunk_unfused"),
+                    (rl_decode, "decode"), (rl_pool, "decode_pool"), (rl_gate, "gate"),
+                    (rl_conv, "short_conv"), (rl_bwd, "backward")):
+        rl["traffic"], rl["traffic_note"] = measured_traffic(kid)
     # the dominant kernel is the one with the largest share of the step
     roofline = rl_prefill if fused_ms >= decode_ms_max else rl_decode
     cpu = cpu_baseline(args.cpu_heads) if not args.no_cpu_baseline else None
