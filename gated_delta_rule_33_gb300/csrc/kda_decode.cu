@@ -26,37 +26,51 @@ constexpr int kD = 128;
 constexpr int kThreads = 256;
 constexpr int kRowsPerThread = kD / (kThreads / 32);  // 16
 
-// State element access for fp32 or bf16 state storage (four adjacent columns).
+// The thread's 16 x 4 state elements between the two passes of a step: fp32
+// values, or the raw bf16 pairs as loaded (half the registers, so twice the
+// CTAs per SM and twice the state bytes in flight; the values are widened
+// again where used).
 template <bool kStateBf16>
-__device__ __forceinline__ float4 load_state4(const void *S, int64_t idx) {
-    if (kStateBf16) {
-        const uint2 raw = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(S) + idx));
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+struct StateRegs;
+
+template <>
+struct StateRegs<false> {
+    float4 v[kRowsPerThread];
+    __device__ __forceinline__ void load(int i, const void *S, int64_t idx) {
+        v[i] = __ldcs(reinterpret_cast<const float4 *>(static_cast<const float *>(S) + idx));
+    }
+    __device__ __forceinline__ float4 get(int i) const { return v[i]; }
+    __device__ __forceinline__ void store(void *S, int64_t idx, float4 x) const {
+        __stcs(reinterpret_cast<float4 *>(static_cast<float *>(S) + idx), x);
+    }
+};
+
+template <>
+struct StateRegs<true> {
+    uint2 v[kRowsPerThread];
+    __device__ __forceinline__ void load(int i, const void *S, int64_t idx) {
+        v[i] = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(S) + idx));
+    }
+    __device__ __forceinline__ float4 get(int i) const {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i].x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i].y));
         return make_float4(a.x, a.y, b.x, b.y);
     }
-    return __ldcs(reinterpret_cast<const float4 *>(static_cast<const float *>(S) + idx));
-}
-
-template <bool kStateBf16>
-__device__ __forceinline__ void store_state4(void *S, int64_t idx, float4 v) {
-    if (kStateBf16) {
-        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    __device__ __forceinline__ void store(void *S, int64_t idx, float4 x) const {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
         uint2 raw;
         raw.x = *reinterpret_cast<const uint32_t *>(&a);
         raw.y = *reinterpret_cast<const uint32_t *>(&b);
         __stcs(reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(S) + idx), raw);
-    } else {
-        __stcs(reinterpret_cast<float4 *>(static_cast<float *>(S) + idx), v);
     }
-}
+};
 
 // One CTA per (sequence, head).  With `slots` the state of sequence b lives in
 // pool slot slots[b] (negative: inactive sequence, nothing read or written,
 // o = 0; >= num_slots: a device error, skipped); without it, slot b.
 template <bool kOutBf16, bool kStateBf16>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(
+__global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
     const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
     const float *__restrict__ beta, void *__restrict__ state, const int32_t *__restrict__ slots,
@@ -86,10 +100,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(
     const int64_t sbase = (slot * H + bh % H) * (kD * kD);
 
     // Issue the whole state read first: the full state in flight per CTA.
-    float4 s[kRowsPerThread];
+    StateRegs<kStateBf16> s;
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i)
-        s[i] = load_state4<kStateBf16>(state, sbase + (warp + 8 * i) * kD + 4 * lane);
+    for (int i = 0; i < kRowsPerThread; ++i) s.load(i, state, sbase + (warp + 8 * i) * kD + 4 * lane);
 
     if (tid < kD) {
         const int64_t idx = bh * kD + tid;
@@ -113,9 +126,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(
     for (int i = 0; i < kRowsPerThread; ++i) {
         const int r = warp + 8 * i;
         const float d = s_decay[r], kr = s_k[r], qr = s_q[r];
-        s[i].x *= d; s[i].y *= d; s[i].z *= d; s[i].w *= d;
-        w.x += s[i].x * kr; w.y += s[i].y * kr; w.z += s[i].z * kr; w.w += s[i].w * kr;
-        z.x += s[i].x * qr; z.y += s[i].y * qr; z.z += s[i].z * qr; z.w += s[i].w * qr;
+        float4 x = s.get(i);
+        x.x *= d; x.y *= d; x.z *= d; x.w *= d;
+        if constexpr (!kStateBf16) s.v[i] = x;   // fp32: keep S'; bf16: formed again below
+        w.x += x.x * kr; w.y += x.y * kr; w.z += x.z * kr; w.w += x.w * kr;
+        z.x += x.x * qr; z.y += x.y * qr; z.z += x.z * qr; z.w += x.w * qr;
     }
     reinterpret_cast<float4 *>(s_red[0][warp])[lane] = w;
     reinterpret_cast<float4 *>(s_red[1][warp])[lane] = z;
@@ -141,9 +156,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(
     const float4 u4 = reinterpret_cast<const float4 *>(s_u)[lane];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
-        const float kr = s_k[warp + 8 * i];
-        s[i].x += kr * u4.x; s[i].y += kr * u4.y; s[i].z += kr * u4.z; s[i].w += kr * u4.w;
-        store_state4<kStateBf16>(state, sbase + (warp + 8 * i) * kD + 4 * lane, s[i]);
+        const int r = warp + 8 * i;
+        const float kr = s_k[r];
+        float4 x = s.get(i);
+        if constexpr (kStateBf16) {
+            const float d = s_decay[r];
+            x.x *= d; x.y *= d; x.z *= d; x.w *= d;
+        }
+        x.x += kr * u4.x; x.y += kr * u4.y; x.z += kr * u4.z; x.w += kr * u4.w;
+        s.store(state, sbase + r * kD + 4 * lane, x);
     }
 }
 

@@ -17,9 +17,10 @@
 // streams, ~12 instructions of arithmetic).  Lane l of a warp owns 8
 // consecutive channels (one 16-byte load or store of bf16), so a warp covers
 // two heads of 128 channels and the per-head norm is a reduction over 16 lanes
-// by shuffles.  A warp walks 16 consecutive tokens; the three tokens before
-// them (the halo) are re-read from L2 rather than HBM because the neighbouring
-// warp of the same block reads them as its last rows.
+// by shuffles.  A warp walks 16 consecutive tokens, requesting 8 rows at a
+// time; the three tokens before them (the halo) are re-read from L2 rather
+// than HBM because the neighbouring warp of the same block reads them as its
+// last rows.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -32,6 +33,7 @@ constexpr int kLaneCh = 8;                 // channels per lane
 constexpr int kWarpCh = 32 * kLaneCh;      // 256 channels per warp
 constexpr int kWarps = 8;
 constexpr int kTT = 16;                    // tokens per warp
+constexpr int kBatch = 8;                  // rows requested together
 constexpr float kNormEps = 1e-6f;
 
 static_assert(kWarpCh == 2 * kHeadDim, "a warp covers two heads; the norm reduces 16 lanes");
@@ -49,8 +51,7 @@ __device__ __forceinline__ T pick(const T (&a)[3], int z) {
     return z == 0 ? a[0] : (z == 1 ? a[1] : a[2]);
 }
 
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&r)[kLaneCh]) {
-    const uint4 raw = __ldcs(reinterpret_cast<const uint4 *>(p));
+__device__ __forceinline__ void unpack_row(uint4 raw, float (&r)[kLaneCh]) {
     const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -58,6 +59,10 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&r)[kLan
         r[2 * i] = f.x;
         r[2 * i + 1] = f.y;
     }
+}
+
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&r)[kLaneCh]) {
+    unpack_row(__ldcs(reinterpret_cast<const uint4 *>(p)), r);
 }
 
 __device__ __forceinline__ void store_row(__nv_bfloat16 *p, const float (&r)[kLaneCh]) {
@@ -200,29 +205,41 @@ __global__ void __launch_bounds__(kWarps * 32) short_conv_kernel(
     load_window(t_begin, s);
     int64_t next = seq_end(s);
 
-#pragma unroll 4
-    for (int64_t t = t_begin; t < t_end; ++t) {
-        if (t >= next) {   // a new sequence starts at t
-            while (s < B - 1 && seq_end(s) <= t) ++s;
-            next = seq_end(s);
-            load_window(t, s);
-        }
-        float xt[kLaneCh], out[kLaneCh];
-        if (active) load_row(x + t * C + c, xt); else zero_row(xt);
-        conv_row(w, win, xt, norm, out);
-        if (active) store_row(y + t * C + c, out);
+    // Tokens in batches of kBatch: every row of a batch is requested before the
+    // first is used, so a warp keeps kBatch 16-byte loads in flight.
+    for (int64_t tb = t_begin; tb < t_end; tb += kBatch) {
+        uint4 raw[kBatch];
 #pragma unroll
-        for (int i = 0; i < kLaneCh; ++i) {
-            win[0][i] = win[1][i];
-            win[1][i] = win[2][i];
-            win[2][i] = xt[i];
-        }
-        if (t == next - 1) {   // the last token of sequence s: its carried state
-            if (state_out != nullptr && active) {
+        for (int j = 0; j < kBatch; ++j)
+            raw[j] = (active && tb + j < t_end)
+                         ? __ldcs(reinterpret_cast<const uint4 *>(x + (tb + j) * C + c))
+                         : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int r = 0; r < kHalo; ++r) store_row(state_out + state_index(s, z, r, C, c), win[r]);
+        for (int j = 0; j < kBatch; ++j) {
+            const int64_t t = tb + j;
+            if (t >= t_end) break;
+            if (t >= next) {   // a new sequence starts at t
+                while (s < B - 1 && seq_end(s) <= t) ++s;
+                next = seq_end(s);
+                load_window(t, s);
             }
-            for (int s2 = s + 1; s2 < B && seq_end(s2) <= next; ++s2) pass_state(s2);
+            float xt[kLaneCh], out[kLaneCh];
+            unpack_row(raw[j], xt);
+            conv_row(w, win, xt, norm, out);
+            if (active) store_row(y + t * C + c, out);
+#pragma unroll
+            for (int i = 0; i < kLaneCh; ++i) {
+                win[0][i] = win[1][i];
+                win[1][i] = win[2][i];
+                win[2][i] = xt[i];
+            }
+            if (t == next - 1) {   // the last token of sequence s: its carried state
+                if (state_out != nullptr && active) {
+#pragma unroll
+                    for (int r = 0; r < kHalo; ++r) store_row(state_out + state_index(s, z, r, C, c), win[r]);
+                }
+                for (int s2 = s + 1; s2 < B && seq_end(s2) <= next; ++s2) pass_state(s2);
+            }
         }
     }
 }
