@@ -57,11 +57,11 @@ constexpr uint32_t A_MISC = 98304;
 constexpr uint32_t AM_BETA = 0;       // float[64]
 constexpr uint32_t AM_EM = 256;       // float[128]
 constexpr uint32_t AM_DEC = 768;      // float[128]
-constexpr uint32_t AM_PART = 1280;    // float[2][128] decay sums of the two row halves
-constexpr uint32_t AM_DIAG = 2304;    // float[4][256] diagonal blocks of A_kk, column-major
-constexpr uint32_t AM_BAR = 6400;     // mbarriers: MMA, V
-constexpr uint32_t AM_CTRL = 6416;    // int[4]: tmem base, unit, abort, decay flag
-constexpr uint32_t kASmem = A_MISC + 6432;
+constexpr uint32_t AM_PART = 1280;    // float[4][128] decay sums of the 16-row blocks
+constexpr uint32_t AM_DIAG = 3328;    // float[4][256] diagonal blocks of A_kk, column-major
+constexpr uint32_t AM_BAR = 7424;     // mbarriers: MMA, V
+constexpr uint32_t AM_CTRL = 7440;    // int[4]: tmem base, unit, abort, decay flag
+constexpr uint32_t kASmem = A_MISC + 7456;
 constexpr uint32_t kASmemAlloc = kASmem + 1024;
 // tensor memory (256 columns): D_A = [Qt; Kr] Ks^T, Kr^T, W'^T, Ut^T
 constexpr uint32_t AT_A = 0, AT_W = 64, AT_O = 128, AT_U = 192;
@@ -191,10 +191,16 @@ __global__ void __launch_bounds__(kAThreads, 2) intra_kernel(const __grid_consta
                 gate_a = expf(p.A_log[ai]);
                 gate_dt = p.dt_bias[h * kD + ch];
             }
+            // summed per 16-row block, the blocks then combined in order: the
+            // same additions, in the same order, as the one-kernel path
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int r = 32 * half + i;
+                if (i == 16) {
+                    s_part[(2 * half) * kD + ch] = acc;
+                    acc = 0.f;
+                }
                 float g2 = 0.f;
                 if (r < L) {
                     const int64_t idx = ((tc + r) * H + h) * kD + ch;
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kAThreads, 2) intra_kernel(const __grid_consta
                 acc += g2;
                 gam[i] = acc;
             }
-            s_part[half * kD + ch] = acc;
+            s_part[(2 * half + 1) * kD + ch] = acc;
             if (tid < kC) {
                 float bt = 0.f;
                 if (tid < L) {
@@ -235,8 +241,15 @@ __global__ void __launch_bounds__(kAThreads, 2) intra_kernel(const __grid_consta
             }
         }
         __syncthreads();
-        const float prefix = (half == 1) ? s_part[ch] : 0.f;
-        const float gam_l = s_part[ch] + s_part[kD + ch];
+        // prefix of each 16-row block and the chunk total, summed in block order
+        float pre[2] = {0.f, 0.f}, gam_l = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < 4; ++g2) {
+            const float pg = s_part[g2 * kD + ch];
+            if (g2 < 2 * half) pre[0] += pg;
+            if (g2 < 2 * half + 1) pre[1] += pg;
+            gam_l += pg;
+        }
         if (-gam_l > kMaxDecay * kLog2e) ctrl[3] = 1;
         const float m = 0.5f * gam_l;
         if (half == 0) {
@@ -259,7 +272,7 @@ __global__ void __launch_bounds__(kAThreads, 2) intra_kernel(const __grid_consta
                     float qt = 0.f, kr = 0.f, ks = 0.f, kh = 0.f;
                     if (r < L) {
                         const int64_t idx = ((tc + r) * H + h) * kD + ch;
-                        const float gr = prefix + gam[i];
+                        const float gr = pre[i >> 4] + gam[i];
                         const float e_up = fast_exp2(gr - m);   // e^{Gam_r - m}
                         const float e_dn = fast_exp2(m - gr);   // e^{m - Gam_r}
                         const float qv = __bfloat162float(p.q[idx]);
