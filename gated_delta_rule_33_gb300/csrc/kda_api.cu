@@ -118,7 +118,7 @@ kda_status kda_gate_fused(const void *f, kda_dtype f_dtype, const void *b, kda_d
 
 size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V) {
     if (N < 0 || B < 1 || H < 1 || K != 128 || V != 128) return 0;
-    return kda::prefill_split_workspace_bytes(N, B, H);
+    return kda::prefill_workspace_bytes(N, B, H);
 }
 
 kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
@@ -143,13 +143,6 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
     DeviceInfo *dev = nullptr;
     kda_status st = current_device(&dev);
     if (st != KDA_OK) return st;
-    if (workspace_bytes >= kda::prefill_split_workspace_bytes(N, B, H))
-        return from_cuda(kda::launch_prefill_split(
-            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-            static_cast<const __nv_bfloat16 *>(v), g, beta, nullptr, nullptr, false, nullptr, 0,
-            nullptr, cu_seqlens, B, N, H, scale, initial_state, final_state, o,
-            o_dtype == KDA_BF16, workspace, dev->error_word, dev->num_sms,
-            static_cast<cudaStream_t>(stream)));
     return from_cuda(kda::launch_prefill(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
         static_cast<const __nv_bfloat16 *>(v), g, beta, cu_seqlens, B, N, H, scale, initial_state,
@@ -187,14 +180,6 @@ kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v, 
     DeviceInfo *dev = nullptr;
     kda_status st = current_device(&dev);
     if (st != KDA_OK) return st;
-    if (workspace_bytes >= kda::prefill_split_workspace_bytes(N, B, H))
-        return from_cuda(kda::launch_prefill_split(
-            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-            static_cast<const __nv_bfloat16 *>(v), nullptr, nullptr,
-            static_cast<const __nv_bfloat16 *>(f), b, b_dtype == KDA_BF16, A_log,
-            static_cast<int>(alog_mode), dt_bias, cu_seqlens, B, N, H, scale, initial_state,
-            final_state, o, o_dtype == KDA_BF16, workspace, dev->error_word, dev->num_sms,
-            static_cast<cudaStream_t>(stream)));
     return from_cuda(kda::launch_prefill_gated(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
         static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(f), b,

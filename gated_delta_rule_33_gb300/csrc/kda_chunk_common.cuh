@@ -1,6 +1,7 @@
-// kda_chunk_common.cuh -- device helpers shared by the chunked prefill kernels
-// (kda_chunk.cu: one kernel per head chain; kda_chunk_split.cu: the
-// chunk-parallel and state-pass kernels).  Not part of the public ABI.
+// kda_chunk_common.cuh -- device and host helpers of the chunked prefill
+// kernel (kda_chunk.cu): chunk constants, the UT-inverse building blocks, the
+// T beta operand stores, bounded CTA waits and TMA tensor maps.  Not part of
+// the public ABI.
 #pragma once
 
 #include <cuda.h>

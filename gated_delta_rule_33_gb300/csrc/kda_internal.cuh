@@ -78,19 +78,6 @@ cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                  float *final_state, void *o, bool o_bf16, void *workspace,
                                  unsigned int *err, int num_sms, cudaStream_t s);
 
-// Two-phase prefill (kda_chunk_split.cu): workspace bytes and the launch
-// (g/beta given, or f/blog for the in-kernel gate when f is not null).
-size_t prefill_split_workspace_bytes(int64_t N, int B, int H);
-
-cudaError_t launch_prefill_split(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                                 const __nv_bfloat16 *v, const float *g, const float *beta,
-                                 const __nv_bfloat16 *f, const void *blog, bool blog_bf16,
-                                 const float *A_log, int alog_mode, const float *dt_bias,
-                                 const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
-                                 const float *initial_state, float *final_state, void *o,
-                                 bool o_bf16, void *workspace, unsigned int *err, int num_sms,
-                                 cudaStream_t s);
-
 // Device address and size of the built-in prefill scratch on the current device
 // (looked up once per device; see kda_chunk.cu).
 cudaError_t builtin_prefill_scratch(void **ptr, size_t *bytes);

@@ -108,19 +108,9 @@ kda_status kda_gate_fused(const void *f, kda_dtype f_dtype,
                           int64_t N, int H, int K, void *stream);
 
 /*
- * Bytes of device workspace for kda_chunk_prefill's two-phase path at these
- * sizes: one 145 KB chunk record per (64-token chunk, head), i.e. about
- * (N / 64 + B) * H * 148480 bytes (0.91 GB for N = 4096, H = 96).  It is 0
- * only when nothing runs.
- *
- * Two algorithms compute the same result.  Given at least this much
- * workspace, kda_chunk_prefill runs the two-phase path: the state-independent
- * work of every chunk of every head in parallel on all SMs, written to the
- * workspace, then one short serial pass per head over its chunks.  Given less
- * (but at least KDA_PREFILL_MIN_WORKSPACE bytes) it runs the one-kernel path:
- * one CTA per (sequence, head) chain doing all of each chunk's work in turn.
+ * Bytes of device workspace kda_chunk_prefill needs for these sizes.
+ * The value never exceeds a few kilobytes; it is 0 only when nothing runs.
  */
-#define KDA_PREFILL_MIN_WORKSPACE 256
 size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V);
 
 /*
@@ -143,12 +133,10 @@ size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V);
  *   final_state   fp32 [B, H, 128, 128] (written) or NULL; may alias
  *                 initial_state (each state is read before it is written)
  *   o             [N, H, 128] of o_dtype (bf16 or fp32), written
- *   workspace     device scratch, 16-byte aligned, of at least
- *                 KDA_PREFILL_MIN_WORKSPACE bytes (the one-kernel path), or of
- *                 kda_chunk_prefill_workspace_size(N, B, H, 128, 128) bytes
- *                 or more (the faster two-phase path); its contents need not
- *                 be initialised and it must not be used by another call
- *                 running concurrently.
+ *   workspace     device scratch of at least
+ *                 kda_chunk_prefill_workspace_size(N, B, H, 128, 128) bytes,
+ *                 16-byte aligned; its contents need not be initialised and
+ *                 it must not be used by another call running concurrently.
  *
  * K and V must be 128 (KDA_ERR_UNSUPPORTED_SHAPE otherwise).
  */
@@ -201,9 +189,8 @@ kda_status kda_chunk_prefill_gated(const void *q, const void *k, const void *v,
  *
  * Arguments, layouts and results are those of kda_chunk_prefill.  The scratch
  * comes from a device array built into the library (4096 bytes; every GPU that
- * loads the library holds it until the process exits), enough for the
- * one-kernel path at every size, which is the path it takes; a size whose
- * one-kernel scratch exceeded it would be rejected with
+ * loads the library holds it until the process exits).  Sizes whose
+ * kda_chunk_prefill_workspace_size() exceeds it are rejected with
  * KDA_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing: it never calls
  * cudaMalloc, cudaFree or any allocating library routine.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that
