@@ -98,40 +98,39 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4):
 # in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
-    "chunk_unfused": {"src": "kda_chunk.cu", "bytes": 4 * 140.25e6,
-                      "sha256": "5c62c77f05ef9cbda2911d9a5fe98de933524af116787b4df45c90e843eede6a",
-                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
-    "chunk_gated": {"src": "kda_chunk.cu", "bytes": 4 * 111.29e6,
-                    "sha256": "5c62c77f05ef9cbda2911d9a5fe98de933524af116787b4df45c90e843eede6a",
-                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
-    "decode": {"src": "kda_decode.cu", "bytes": 4 * 753.98e6,
-               "sha256": "cbce038541a155e0f5cd0b0a11e0ac8fc159311b6c620be5864600bb99740081",
-               "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
-    "decode_pool": {"src": "kda_decode.cu", "bytes": 4 * 350.65e6,
-                    "sha256": "cbce038541a155e0f5cd0b0a11e0ac8fc159311b6c620be5864600bb99740081",
+    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": None,
+                      "sha256": [], "note": "profiles/chunk_prefill_T1024_H96.md"},
+    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": None,
+                    "sha256": [], "note": "profiles/chunk_prefill_gated_T1024_H96.md"},
+    "decode": {"src": ["kda_decode.cu"], "bytes": None, "sha256": [],
+               "note": "profiles/decode_B64_H96.md"},
+    "decode_pool": {"src": ["kda_decode.cu"], "bytes": 4 * 353.94e6,
+                    "sha256": ["3ece8e3a0bcba9a9f37ec97513c5b4c422fef3cbcd67c50b9f3705c759c82d9a"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
-    "gate": {"src": "kda_gate.cu", "bytes": 246.78e6,
-             "sha256": "c571ed29aa63aa23447ebb39f20cf362297d7d0e0342dce221f132091a056852",
+    "gate": {"src": ["kda_gate.cu"], "bytes": 246.78e6,
+             "sha256": ["c571ed29aa63aa23447ebb39f20cf362297d7d0e0342dce221f132091a056852"],
              "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
-    "short_conv": {"src": "kda_shortconv.cu", "bytes": 557.47e6,
-                   "sha256": "63417a724d638dbee09d5b86b350fdc5bcaac7a7864b46ccf38e853228e0c920",
+    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 555.46e6,
+                   "sha256": ["1dda087737165eabb4bbda6c8ac279ddb646ca5a75868dec2cb52353227ea41e"],
                    "note": "T=4096 capture (profiles/short_conv_T4096_H96.md)"},
 }
 
 
 def measured_traffic(kernel_id):
-    """(bytes, note) of the ncu capture of one kernel, or (None, why) when the
-    kernel's source has changed since the capture."""
+    """(bytes, note) of the ncu capture of one kernel, or (None, why) when a
+    source file of the kernel has changed since the capture."""
     import hashlib
     ent = NCU_TRAFFIC.get(kernel_id)
-    if ent is None:
+    if ent is None or ent["bytes"] is None:
         return None, "not captured"
-    path = os.path.join(ROOT, "gated_delta_rule_33_gb300", "csrc", ent["src"])
-    if not os.path.exists(path):
-        return None, "source missing"
-    with open(path, "rb") as fh:
-        digest = hashlib.sha256(fh.read()).hexdigest()
-    if digest != ent["sha256"]:
+    digests = []
+    for name in ent["src"]:
+        path = os.path.join(ROOT, "gated_delta_rule_33_gb300", "csrc", name)
+        if not os.path.exists(path):
+            return None, "source missing"
+        with open(path, "rb") as fh:
+            digests.append(hashlib.sha256(fh.read()).hexdigest())
+    if digests != ent["sha256"]:
         return None, "kernel changed since the ncu capture"
     return ent["bytes"], ent["note"]
 
