@@ -98,12 +98,17 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4):
 # in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
-    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": None,
-                      "sha256": [], "note": "profiles/chunk_prefill_T1024_H96.md"},
-    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": None,
-                    "sha256": [], "note": "profiles/chunk_prefill_gated_T1024_H96.md"},
-    "decode": {"src": ["kda_decode.cu"], "bytes": None, "sha256": [],
-               "note": "profiles/decode_B64_H96.md"},
+    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": 4 * 139.84e6,
+                      "sha256": ["0249a1d5c7d96af693a0ac274572e8e542305369099093f792305e80d5a7c953",
+                                 "1b42adeb58c6dbf45e946f4ab4b77d0169d66fd292fdb92c54d4c387190d085a"],
+                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
+    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": 4 * 110.46e6,
+                    "sha256": ["0249a1d5c7d96af693a0ac274572e8e542305369099093f792305e80d5a7c953",
+                               "1b42adeb58c6dbf45e946f4ab4b77d0169d66fd292fdb92c54d4c387190d085a"],
+                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
+    "decode": {"src": ["kda_decode.cu"], "bytes": 4 * 753.89e6,
+               "sha256": ["3ece8e3a0bcba9a9f37ec97513c5b4c422fef3cbcd67c50b9f3705c759c82d9a"],
+               "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
     "decode_pool": {"src": ["kda_decode.cu"], "bytes": 4 * 353.94e6,
                     "sha256": ["3ece8e3a0bcba9a9f37ec97513c5b4c422fef3cbcd67c50b9f3705c759c82d9a"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
@@ -448,37 +453,69 @@ def run_ours(args):
     decode_ms_max = max_over_ranks(decode_ms, world, dev)
     value = world * T_PREFILL / (prefill_leg_ms * 1e-3)
 
-    # e2e: through the same C ABI, inputs from pinned host memory every step,
-    # outputs (o and the final state) read back every step.
+    # e2e: through the same C ABI, every step copies its inputs from pinned host
+    # memory and reads its outputs (o and the final state) back to pinned host
+    # memory.  Steps are pipelined as a serving loop would run them: two device
+    # buffer sets, host-to-device copies on one stream, the prefill on the
+    # compute stream, device-to-host copies on a third, so that step i+1's
+    # inputs and step i-1's outputs move while step i computes.  Events order
+    # each buffer set's reuse; every step still moves all of its bytes.
     host_in = [t.pin_memory() for t in (x.q, x.k, x.v, x.f, x.b)]
-    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
-    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    host_S = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_o.numel() * host_o.element_size() + host_S.numel() * host_S.element_size()
+    slots = []
+    for _ in range(2):
+        slots.append({
+            "in": [torch.empty_like(t, device=dev) for t in host_in],
+            "o": torch.empty_like(o), "S": torch.empty_like(Sf),
+            "host_o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+            "host_S": torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory(),
+            "h2d_done": torch.cuda.Event(), "compute_done": torch.cuda.Event(),
+            "d2h_done": torch.cuda.Event(), "used": False,
+        })
+    d2h = o.numel() * o.element_size() + Sf.numel() * Sf.element_size()
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
 
-    def e2e_step():
-        for hsrc, ddst in zip(host_in, dev_in):
-            ddst.copy_(hsrc, non_blocking=True)
-        eq, ek, evv, ef, eb = dev_in
+    def e2e_step(i):
+        sl = slots[i % 2]
+        with torch.cuda.stream(h2d_stream):
+            if sl["used"]:
+                h2d_stream.wait_event(sl["compute_done"])   # step i-2 has read this set
+            for hsrc, ddst in zip(host_in, sl["in"]):
+                ddst.copy_(hsrc, non_blocking=True)
+            sl["h2d_done"].record(h2d_stream)
+        stream.wait_event(sl["h2d_done"])
+        if sl["used"]:
+            stream.wait_event(sl["d2h_done"])              # step i-2's outputs are out
+        eq, ek, evv, ef, eb = sl["in"]
         kda.kda_chunk_prefill_gated(eq, ek, evv, ef, eb, A_log, x.alog_mode, dt_bias, None, 1.0,
-                                    None, Sf, o, ws, stream)
-        host_o.copy_(o, non_blocking=True)
-        host_S.copy_(Sf, non_blocking=True)
+                                    None, sl["S"], sl["o"], ws, stream)
+        sl["compute_done"].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(sl["compute_done"])
+            sl["host_o"].copy_(sl["o"], non_blocking=True)
+            sl["host_S"].copy_(sl["S"], non_blocking=True)
+            sl["d2h_done"].record(d2h_stream)
+        sl["used"] = True
 
-    for _ in range(max(args.warmup, 1)):
-        e2e_step()
+    for i in range(max(args.warmup, 1)):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(h2d_stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    d2h_stream.wait_event(slots[(args.steps - 1) % 2]["compute_done"])
+    e1.record(d2h_stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     e2e_value = world * T_PREFILL / (e2e_ms * 1e-3)
+    # the last step's read-back equals a direct read of its outputs
+    last = slots[(args.steps - 1) % 2]
+    if not (torch.equal(last["host_o"], last["o"].cpu()) and torch.equal(last["host_S"], last["S"].cpu())):
+        raise RuntimeError("e2e read-back does not match the device outputs")
 
     if kda.kda_get_last_device_error(stream) != 0:
         raise RuntimeError("device error during the timed region")
@@ -570,7 +607,9 @@ def run_ours(args):
                       "prefill_unfused": rl_prefill_unfused, "decode": rl_decode,
                       "decode_bf16_pool": rl_pool, "short_conv": rl_conv, "backward": rl_bwd},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "schedule": "steps pipelined over two buffer sets: H2D, prefill and D2H "
+                            "on three streams"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "peaks": peaks,
