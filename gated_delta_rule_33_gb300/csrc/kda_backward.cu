@@ -18,23 +18,25 @@
 // chain: a forward pass stores a checkpoint of the state every kCk tokens;
 // then, segment by segment from the last, the forward steps of the segment are
 // rerun from its checkpoint writing each S_{t-1} to a per-CTA scratch, and the
-// reverse steps read them back.  Every thread reads back only the elements it
+// reverse steps read them back (each step's token vectors and S_{t-1} are
+// requested one step ahead, so no step waits a full memory latency).  Every thread reads back only the elements it
 // wrote, so checkpoints and scratch are kept in a thread-interleaved order
 // (for a fixed row slot, the 256 threads' float4 are contiguous).
 //
-// Element ownership (as in the decode kernel): warp w owns rows w, w+8, ...,
-// w+120 and lane l owns columns 4l..4l+3.  Column sums (w, du) reduce over a
-// thread's 16 rows, then over the 8 warps in shared memory; row sums (for dk,
-// dq, dg) reduce over the 32 lanes with a halving exchange that leaves lane l
-// holding one of 32 (row, quantity) sums, twice per step.
+// Element ownership: 16 warps, warp w owns rows w, w+16, ..., w+112 and lane l
+// owns columns 4l..4l+3 (8 rows x 4 columns per thread).  Column sums (w, du)
+// reduce over a thread's 8 rows, then over the 16 warps in shared memory; row
+// sums (for dk, dq, dg) reduce over the 32 lanes with a halving exchange that
+// leaves lane l holding one of the 32 (row, quantity) sums of the step.
 #include "kda_internal.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 256;
-constexpr int kRows = 16;        // rows per thread
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = kD / kWarps;   // rows per thread (8)
 constexpr int kCk = 16;          // tokens per checkpoint segment
 constexpr int kStateF4 = kD * kD / 4;   // float4 per state
 
@@ -91,23 +93,61 @@ __device__ __forceinline__ void lane_transpose_sum32(float (&v)[32], int lane) {
     }
 }
 
-// Token t of head h into shared memory (threads 0..127).
-__device__ __forceinline__ void load_token(const BwdParams &p, int64_t t, int h, TokenVecs &tv,
-                                           int tid) {
+// A token's vectors as loaded by threads 0..127 (raw, so that nothing waits
+// on the loads until commit_token), one step before they are used.
+struct TokenRegs {
+    __nv_bfloat16 q, k, v;
+    float g, beta;
+    uint32_t dO;     // bf16 or fp32 bits
+};
+
+template <bool kDoBf16>
+__device__ __forceinline__ void fetch_token(const BwdParams &p, int64_t t, int h, int tid,
+                                            TokenRegs &r) {
     if (tid < kD) {
         const int64_t idx = (t * p.H + h) * kD + tid;
-        tv.q[tid] = p.scale * __bfloat162float(p.q[idx]);
-        tv.k[tid] = __bfloat162float(p.k[idx]);
-        tv.v[tid] = __bfloat162float(p.v[idx]);
-        tv.d[tid] = expf(p.g[idx]);
-        tv.dO[tid] = p.dO_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.dO)[idx])
-                               : static_cast<const float *>(p.dO)[idx];
-        if (tid == 0) tv.beta = p.beta[t * p.H + h];
+        r.q = p.q[idx];
+        r.k = p.k[idx];
+        r.v = p.v[idx];
+        r.g = p.g[idx];
+        if (kDoBf16)
+            r.dO = static_cast<const unsigned short *>(p.dO)[idx];
+        else
+            r.dO = static_cast<const uint32_t *>(p.dO)[idx];
+        if (tid == 0) r.beta = p.beta[t * p.H + h];
     }
 }
 
+template <bool kDoBf16>
+__device__ __forceinline__ void commit_token(const BwdParams &p, const TokenRegs &r,
+                                             TokenVecs &tv, int tid) {
+    if (tid < kD) {
+        tv.q[tid] = p.scale * __bfloat162float(r.q);
+        tv.k[tid] = __bfloat162float(r.k);
+        tv.v[tid] = __bfloat162float(r.v);
+        tv.d[tid] = expf(r.g);
+        tv.dO[tid] = kDoBf16 ? __uint_as_float(r.dO << 16) : __uint_as_float(r.dO);
+        if (tid == 0) tv.beta = r.beta;
+    }
+}
+
+// 16-byte asynchronous global -> shared copy (own data: only the issuing
+// thread reads it back, after cp_async_wait<N>).
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <bool kDoBf16>
 __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p) {
     // float4 accesses below: every array 16-byte aligned
+    extern __shared__ float4 s_prev[];   // [2][kStateF4]: S_{t-1} of the next two steps
     __shared__ TokenVecs s_tok[2];
     __shared__ __align__(16) float s_red[2][kThreads / 32][kD];
     __shared__ __align__(16) float s_u[kD];
@@ -149,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
             s[i] = (p.S0 != nullptr)
-                       ? *reinterpret_cast<const float4 *>(p.S0 + state_off + (warp + 8 * i) * kD + c0)
+                       ? *reinterpret_cast<const float4 *>(p.S0 + state_off + (warp + kWarps * i) * kD + c0)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
 
         // One forward step on s (token vectors in tv, visible to all threads).
@@ -157,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
             float4 wp = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kRows; ++i) {
-                const int r = warp + 8 * i;
+                const int r = warp + kWarps * i;
                 s[i] = f4_scale(s[i], tv.d[r]);
                 wp = f4_fma(tv.k[r], s[i], wp);
             }
@@ -172,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
             __syncthreads();
             const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[c0]);
 #pragma unroll
-            for (int i = 0; i < kRows; ++i) s[i] = f4_fma(tv.k[warp + 8 * i], u4, s[i]);
+            for (int i = 0; i < kRows; ++i) s[i] = f4_fma(tv.k[warp + kWarps * i], u4, s[i]);
         };
 
         // ---- forward pass: checkpoints at the start of every segment ----
@@ -181,9 +221,12 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
             for (int i = 0; i < kRows; ++i) *ckpt_at(j, i) = s[i];
             if (j == nseg - 1) break;   // the last segment's steps are not needed here
             const int64_t ts = t0 + static_cast<int64_t>(j) * kCk;
+            TokenRegs tr;
+            fetch_token<kDoBf16>(p, ts, h, tid, tr);
             for (int64_t t = ts; t < ts + kCk; ++t) {
                 TokenVecs &tv = s_tok[t & 1];
-                load_token(p, t, h, tv, tid);
+                commit_token<kDoBf16>(p, tr, tv, tid);
+                if (t + 1 < ts + kCk) fetch_token<kDoBf16>(p, t + 1, h, tid, tr);
                 __syncthreads();
                 forward_step(tv);
             }
@@ -195,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
             G[i] = (p.dSf != nullptr)
-                       ? *reinterpret_cast<const float4 *>(p.dSf + state_off + (warp + 8 * i) * kD + c0)
+                       ? *reinterpret_cast<const float4 *>(p.dSf + state_off + (warp + kWarps * i) * kD + c0)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
 
         for (int j = nseg - 1; j >= 0; --j) {
@@ -205,30 +248,51 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < kRows; ++i) s[i] = *ckpt_at(j, i);
+            TokenRegs tr;
+            if (ts + 1 < te) fetch_token<kDoBf16>(p, ts, h, tid, tr);
             for (int64_t t = ts; t < te; ++t) {
                 float4 *sc = scratch + (t - ts) * kStateF4 + tid;
 #pragma unroll
                 for (int i = 0; i < kRows; ++i) sc[i * kThreads] = s[i];
                 if (t + 1 < te) {   // the last step's S_t is not needed
                     TokenVecs &tv = s_tok[t & 1];
-                    load_token(p, t, h, tv, tid);
+                    commit_token<kDoBf16>(p, tr, tv, tid);
+                    if (t + 2 < te) fetch_token<kDoBf16>(p, t + 1, h, tid, tr);
                     __syncthreads();
                     forward_step(tv);
                 }
             }
             __syncthreads();
+            // reverse steps; the next step's token and S_{t-1} are requested
+            // one step ahead (registers; cp.async into s_prev)
+            auto prefetch_prev = [&](int64_t t) {
+                const float4 *src = scratch + (t - ts) * kStateF4 + tid;
+                float4 *dst = s_prev + (t & 1) * kStateF4 + tid;
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) cp_async_16(dst + i * kThreads, src + i * kThreads);
+                cp_async_commit();
+            };
+            fetch_token<kDoBf16>(p, te - 1, h, tid, tr);
+            prefetch_prev(te - 1);
             for (int64_t t = te - 1; t >= ts; --t) {
                 TokenVecs &tv = s_tok[t & 1];
-                load_token(p, t, h, tv, tid);
-                const float4 *sc = scratch + (t - ts) * kStateF4 + tid;
+                commit_token<kDoBf16>(p, tr, tv, tid);
+                if (t - 1 >= ts) {
+                    fetch_token<kDoBf16>(p, t - 1, h, tid, tr);
+                    prefetch_prev(t - 1);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+                const float4 *sp = s_prev + (t & 1) * kStateF4 + tid;
 #pragma unroll
-                for (int i = 0; i < kRows; ++i) s[i] = sc[i * kThreads];   // S_{t-1}
+                for (int i = 0; i < kRows; ++i) s[i] = sp[i * kThreads];   // S_{t-1}
                 __syncthreads();
                 const float4 do4 = *reinterpret_cast<const float4 *>(&tv.dO[c0]);
                 float4 wp = make_float4(0.f, 0.f, 0.f, 0.f), dup = wp;
 #pragma unroll
                 for (int i = 0; i < kRows; ++i) {
-                    const int r = warp + 8 * i;
+                    const int r = warp + kWarps * i;
                     s[i] = f4_scale(s[i], tv.d[r]);          // S'
                     G[i] = f4_fma(tv.q[r], do4, G[i]);        // G += (scale q) do^T
                     wp = f4_fma(tv.k[r], s[i], wp);
@@ -265,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
                 if (tid == 0) p.dbeta[t * H + h] = s_sc[0][0] + s_sc[0][1] + s_sc[0][2] + s_sc[0][3];
                 const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[c0]);
                 const float4 dw4 = *reinterpret_cast<const float4 *>(&s_dw[c0]);
-                // per-row partial sums, two halves of 8 rows (32 slots: 8 rows x 4)
+                // per-row partial sums: 8 rows x 4 quantities = 32 slots
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < kRows / 8; ++half) {
                     float v32[32];
 #pragma unroll
                     for (int ii = 0; ii < 8; ++ii) {
@@ -281,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
                     // lane l: row slot ii = l / 4, quantity l % 4
                     const float x = v32[0];
                     const float sdw = __shfl_sync(0xffffffffu, x, (lane & ~3) | 1);
-                    const int r = warp + 8 * (8 * half + (lane >> 2));
+                    const int r = warp + kWarps * (8 * half + (lane >> 2));
                     const int64_t oi = (t * H + h) * kD + r;
                     const int qn = lane & 3;
                     if (qn == 0) p.dk[oi] = x + sdw;
@@ -290,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
                 }
 #pragma unroll
                 for (int i = 0; i < kRows; ++i) {
-                    const int r = warp + 8 * i;
+                    const int r = warp + kWarps * i;
                     G[i] = f4_scale(f4_fma(tv.k[r], dw4, G[i]), tv.d[r]);
                 }
             }
@@ -298,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const BwdParams p
         if (p.dS0 != nullptr) {
 #pragma unroll
             for (int i = 0; i < kRows; ++i)
-                *reinterpret_cast<float4 *>(p.dS0 + state_off + (warp + 8 * i) * kD + c0) = G[i];
+                *reinterpret_cast<float4 *>(p.dS0 + state_off + (warp + kWarps * i) * kD + c0) = G[i];
         }
     }
 }
@@ -336,9 +400,23 @@ cudaError_t launch_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     p.ckpt = reinterpret_cast<float4 *>(ws + 256);
     p.scratch = reinterpret_cast<float4 *>(ws + 256 + slots * H * state);
     p.err = err;
+    constexpr size_t kDynSmem = 2 * kStateF4 * sizeof(float4);   // 128 KB
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(backward_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(backward_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
     cudaError_t e = cudaMemsetAsync(ws, 0, 256, s);
     if (e != cudaSuccess) return e;
-    backward_kernel<<<ctas, kThreads, 0, s>>>(p);
+    if (dO_bf16)
+        backward_kernel<true><<<ctas, kThreads, kDynSmem, s>>>(p);
+    else
+        backward_kernel<false><<<ctas, kThreads, kDynSmem, s>>>(p);
     return cudaGetLastError();
 }
 
