@@ -6,10 +6,13 @@ One step = one pass of the whole hot path on synthetic K3-shaped inputs:
                 tokens/s workload), as one launch of the chunked kernel that
                 computes the gate itself (kda_chunk_prefill_gated);
   decode leg:   gate + recurrent decode, 256 sequences x 96 heads, fp32 states
-                [256, 96, 128, 128] (1.61 GB) updated in place.
+                [256, 96, 128, 128] (1.61 GB) updated in place (kda_gate_fused on
+                the new token, then kda_recurrent_decode: 3 % faster than the
+                one-launch kda_recurrent_decode_gated, which is timed too).
 `value` is prefill sequence tokens/s over all ranks; the decode leg reports
-state GB/s against the measured HBM peak.  The unfused pair (bit-exact gate
-kernel, then kda_chunk_prefill) is timed in a second loop and reported too.  Inputs are larger than L2 (129 MB):
+state GB/s against the measured HBM peak.  The unfused prefill pair (bit-exact
+gate kernel, then kda_chunk_prefill) and the gated decode are timed in a second
+loop and reported too.  Inputs are larger than L2 (129 MB):
 the prefill leg reads ~0.6 GB and the decode leg streams 3.2 GB per step.
 
 `--impl reference` times the CPU oracle (fp64 recurrence + fp32 gate spec) on
@@ -87,11 +90,13 @@ def prefill_kernel_bytes(T, Hh=H, K=D, V=D, o_bytes=2):
     return T * Hh * (2 * K * 2 + 2 * V + 4 * K + 4 + o_bytes * V) + Hh * K * V * 4
 
 
-def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4):
+def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
     """Decode kernel: every state (fp32, or bf16 with state_bytes=2) read once
-    and written once, plus the token (q, k, v bf16; g fp32; beta fp32) and the
+    and written once, plus the token (q, k, v bf16; g and beta fp32, or with
+    gated=True the bf16 gate pre-activation and fp32 beta logit) and the
     output (bf16)."""
-    return B * Hh * (2 * K * V * state_bytes + 2 * K * 2 + 2 * V + 4 * K + 4 + 2 * V)
+    gate = 2 * K + 4 if gated else 4 * K + 4
+    return B * Hh * (2 * K * V * state_bytes + 2 * K * 2 + 2 * V + gate + 2 * V)
 
 
 # DRAM read+write bytes per benchmark launch, from the ncu captures summarised
@@ -357,6 +362,9 @@ def run_ours(args):
         record[1].record(stream)
         kda.kda_chunk_prefill(q, k, v, g, beta, None, 1.0, None, Sf, o, ws, stream)
         record[2].record(stream)
+        kda.kda_recurrent_decode_gated(dq, dk, dv, df, db, dA, d.alog_mode, ddt, state, None, 1.0,
+                                       dout, stream)
+        record[3].record(stream)
 
     for _ in range(max(args.warmup, 3) if args.warmup >= 3 else args.warmup):
         step()
@@ -392,16 +400,17 @@ def run_ours(args):
 
     # the unfused pair, same inputs, its own timed loop (not part of `value`)
     for _ in range(max(args.warmup, 1)):
-        unfused_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        unfused_step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
     torch.cuda.synchronize(dev)
     uf = []
     for _ in range(args.steps):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         unfused_step(evs)
         uf.append(evs)
     torch.cuda.synchronize(dev)
     gate_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in uf)
     prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in uf)
+    gdecode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in uf)
 
     def timed(fn, steps):
         """Mean CUDA-event time of fn() on the stream after one untimed call."""
@@ -547,10 +556,12 @@ def run_ours(args):
                           "traffic": None, "algorithmic_flops_per_launch": pf_flops,
                           "hbm_frac": up_bytes / (prefill_ms * 1e-3) / 1e9 / hbm,
                           "algorithmic_bytes_per_launch": up_bytes}
-    dec_gbs = decode_bytes() / (decode_ms_max * 1e-3) / 1e9
-    rl_decode = {"kernel": "kda recurrent decode", "bound": "hbm", "achieved": dec_gbs,
-                 "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm, "traffic": None,
-                 "peak_source": peaks["source"], "algorithmic_bytes_per_launch": decode_bytes()}
+    dec_bytes = decode_bytes()
+    dec_gbs = dec_bytes / (decode_ms_max * 1e-3) / 1e9
+    rl_decode = {"kernel": "kda recurrent decode", "bound": "hbm",
+                 "achieved": dec_gbs, "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm,
+                 "traffic": None, "peak_source": peaks["source"],
+                 "algorithmic_bytes_per_launch": dec_bytes}
     pool_bytes = decode_bytes(state_bytes=2) + B_DECODE * 4
     pool_gbs = pool_bytes / (pool_ms * 1e-3) / 1e9
     rl_pool = {"kernel": "kda recurrent decode, bf16 state pool by slot", "bound": "hbm",
@@ -601,6 +612,7 @@ def run_ours(args):
         "prefill_gated_ms": fused_ms, "decode_gate_ms": dgate_ms, "decode_ms": decode_ms_max,
         "unfused": {"gate_ms": gate_ms, "prefill_ms": prefill_ms,
                     "tokens_per_s": T_PREFILL / ((gate_ms + prefill_ms) * 1e-3)},
+        "decode_gated_ms": gdecode_ms,
         "decode_state_gbs": dec_gbs, "decode_frac_of_hbm": dec_gbs / hbm,
         "roofline": roofline,
         "rooflines": {"gate": rl_gate, "prefill_gated": rl_prefill,

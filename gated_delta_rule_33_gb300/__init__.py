@@ -16,6 +16,7 @@ from .kda import (  # noqa: F401
     backward,
     build,
     decode,
+    decode_gated,
     decode_indexed,
     gate,
     kda_chunk_prefill,
@@ -27,6 +28,7 @@ from .kda import (  # noqa: F401
     kda_recurrent_backward,
     kda_recurrent_backward_workspace_size,
     kda_recurrent_decode,
+    kda_recurrent_decode_gated,
     kda_recurrent_decode_indexed,
     kda_short_conv_qkv,
     kda_short_conv_qkv_step,

@@ -254,6 +254,42 @@ kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void
         static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_recurrent_decode_gated(const void *q, const void *k, const void *v,
+                                      const void *f, kda_dtype f_dtype, const void *b,
+                                      kda_dtype b_dtype, const float *A_log,
+                                      kda_alog_mode alog_mode, const float *dt_bias,
+                                      void *state_pool, kda_dtype state_dtype,
+                                      const int32_t *state_indices, int num_slots, int B, int H,
+                                      int K, int V, float scale, void *o, kda_dtype o_dtype,
+                                      void *stream) {
+    if (B < 0 || H < 1 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if (state_indices == nullptr && num_slots < B) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(o_dtype) || !valid_dtype(state_dtype) || !valid_dtype(f_dtype) ||
+        !valid_dtype(b_dtype))
+        return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (alog_mode != KDA_ALOG_PER_HEAD && alog_mode != KDA_ALOG_PER_CHANNEL &&
+        alog_mode != KDA_ALOG_PER_HEAD_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    if (B > 0 && (q == nullptr || k == nullptr || v == nullptr || f == nullptr || b == nullptr ||
+                  A_log == nullptr || dt_bias == nullptr || state_pool == nullptr ||
+                  o == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(f) || !aligned16(b) ||
+        !aligned16(state_pool) || !aligned16(state_indices) || !aligned16(o))
+        return KDA_ERR_MISALIGNED;
+    if (B == 0) return KDA_OK;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_decode_gated(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), f, f_dtype == KDA_BF16, b, b_dtype == KDA_BF16,
+        A_log, static_cast<int>(alog_mode), dt_bias, state_pool, state_dtype == KDA_BF16,
+        state_indices, state_indices == nullptr ? B : num_slots, B, H, scale, o,
+        o_dtype == KDA_BF16, dev->error_word, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_short_conv_qkv(const void *x_q, const void *x_k, const void *x_v,
                               const float *w_q, const float *w_k, const float *w_v,
                               const int32_t *cu_seqlens, int B, int64_t N, int C,

@@ -17,7 +17,7 @@
 // load or store moves one contiguous 512-byte state row.  The 64 KB state stays
 // in registers (16 float4 per thread) between the column reductions and the
 // write, so HBM sees exactly one read and one write of it.
-#include "kda_internal.cuh"
+#include "kda_gate_spec.cuh"
 
 namespace kda {
 namespace {
@@ -66,19 +66,32 @@ struct StateRegs<true> {
     }
 };
 
+// The gate inputs of the gated decode (kGate): g and beta are computed here
+// from them with the same binary32 operations as the gate kernel.
+struct DecodeGate {
+    const void *f;          // [B, H, 128] pre-activation, bf16 or fp32
+    int f_bf16;
+    const void *b;          // [B, H] beta logits, bf16 or fp32
+    int b_bf16;
+    const float *A_log;
+    int alog_mode;
+    const float *dt_bias;   // [H, 128]
+};
+
 // One CTA per (sequence, head).  With `slots` the state of sequence b lives in
 // pool slot slots[b] (negative: inactive sequence, nothing read or written,
 // o = 0; >= num_slots: a device error, skipped); without it, slot b.
-template <bool kOutBf16, bool kStateBf16>
+template <bool kOutBf16, bool kStateBf16, bool kGate>
 __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
     const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
-    const float *__restrict__ beta, void *__restrict__ state, const int32_t *__restrict__ slots,
-    int num_slots, int H, float scale, void *__restrict__ o, unsigned int *err) {
+    const float *__restrict__ beta, const DecodeGate gt, void *__restrict__ state,
+    const int32_t *__restrict__ slots, int num_slots, int H, float scale,
+    void *__restrict__ o, unsigned int *err) {
     __shared__ float s_k[kD], s_q[kD], s_decay[kD];
     __shared__ __align__(16) float s_u[kD];                   // read as float4
     __shared__ __align__(16) float s_red[2][kThreads / 32][kD];   // written as float4
-    __shared__ float s_kq;
+    __shared__ float s_kq, s_beta;
 
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -108,7 +121,25 @@ __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
         const int64_t idx = bh * kD + tid;
         s_k[tid] = __bfloat162float(k[idx]);
         s_q[tid] = scale * __bfloat162float(q[idx]);
-        s_decay[tid] = expf(g[idx]);
+        if (!kGate) {
+            s_decay[tid] = expf(g[idx]);
+            if (tid == 0) s_beta = beta[bh];
+        }
+    } else if (kGate) {
+        // the gate on the other four warps, alongside the loads above
+        using namespace gate_spec;
+        const int c = tid - kD;
+        const int64_t idx = bh * kD + c;
+        const int h = static_cast<int>(bh % H);
+        const float fv = gt.f_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(gt.f)[idx])
+                                   : static_cast<const float *>(gt.f)[idx];
+        const float a = gate_exp(alog_at(gt.A_log, gt.alog_mode, h, c, kD));
+        s_decay[c] = expf(gate_g(fv, gt.dt_bias[h * kD + c], a));
+        if (c == 0) {
+            const float bl = gt.b_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(gt.b)[bh])
+                                       : static_cast<const float *>(gt.b)[bh];
+            s_beta = gate_sigmoid(bl);
+        }
     }
     __syncthreads();
 
@@ -143,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
             ws += s_red[0][j][tid];
             zs += s_red[1][j][tid];
         }
-        const float u = beta[bh] * (__bfloat162float(v[bh * kD + tid]) - ws);
+        const float u = s_beta * (__bfloat162float(v[bh * kD + tid]) - ws);
         s_u[tid] = u;
         const float out = zs + s_kq * u;
         if (kOutBf16)
@@ -170,18 +201,18 @@ __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
 
 }  // namespace
 
-template <bool kOutBf16>
+template <bool kOutBf16, bool kGate>
 static cudaError_t launch_decode_t(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                    const __nv_bfloat16 *v, const float *g, const float *beta,
-                                   void *state, bool state_bf16, const int32_t *slots,
-                                   int num_slots, int64_t units, int H, float scale, void *o,
-                                   unsigned int *err, cudaStream_t s) {
+                                   const DecodeGate &gt, void *state, bool state_bf16,
+                                   const int32_t *slots, int num_slots, int64_t units, int H,
+                                   float scale, void *o, unsigned int *err, cudaStream_t s) {
     if (state_bf16)
-        decode_kernel<kOutBf16, true><<<static_cast<unsigned>(units), kThreads, 0, s>>>(
-            q, k, v, g, beta, state, slots, num_slots, H, scale, o, err);
+        decode_kernel<kOutBf16, true, kGate><<<static_cast<unsigned>(units), kThreads, 0, s>>>(
+            q, k, v, g, beta, gt, state, slots, num_slots, H, scale, o, err);
     else
-        decode_kernel<kOutBf16, false><<<static_cast<unsigned>(units), kThreads, 0, s>>>(
-            q, k, v, g, beta, state, slots, num_slots, H, scale, o, err);
+        decode_kernel<kOutBf16, false, kGate><<<static_cast<unsigned>(units), kThreads, 0, s>>>(
+            q, k, v, g, beta, gt, state, slots, num_slots, H, scale, o, err);
     return cudaGetLastError();
 }
 
@@ -191,10 +222,11 @@ cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                           cudaStream_t s) {
     const int64_t units = static_cast<int64_t>(B) * H;
     if (units == 0) return cudaSuccess;
-    return o_bf16 ? launch_decode_t<true>(q, k, v, g, beta, state, false, nullptr, B, units, H,
-                                          scale, o, nullptr, s)
-                  : launch_decode_t<false>(q, k, v, g, beta, state, false, nullptr, B, units, H,
-                                           scale, o, nullptr, s);
+    const DecodeGate none{};
+    return o_bf16 ? launch_decode_t<true, false>(q, k, v, g, beta, none, state, false, nullptr, B,
+                                                 units, H, scale, o, nullptr, s)
+                  : launch_decode_t<false, false>(q, k, v, g, beta, none, state, false, nullptr, B,
+                                                  units, H, scale, o, nullptr, s);
 }
 
 cudaError_t launch_decode_indexed(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
@@ -204,10 +236,28 @@ cudaError_t launch_decode_indexed(const __nv_bfloat16 *q, const __nv_bfloat16 *k
                                   unsigned int *err, cudaStream_t s) {
     const int64_t units = static_cast<int64_t>(B) * H;
     if (units == 0) return cudaSuccess;
-    return o_bf16 ? launch_decode_t<true>(q, k, v, g, beta, state_pool, state_bf16, slots,
-                                          num_slots, units, H, scale, o, err, s)
-                  : launch_decode_t<false>(q, k, v, g, beta, state_pool, state_bf16, slots,
-                                           num_slots, units, H, scale, o, err, s);
+    const DecodeGate none{};
+    return o_bf16 ? launch_decode_t<true, false>(q, k, v, g, beta, none, state_pool, state_bf16,
+                                                 slots, num_slots, units, H, scale, o, err, s)
+                  : launch_decode_t<false, false>(q, k, v, g, beta, none, state_pool, state_bf16,
+                                                  slots, num_slots, units, H, scale, o, err, s);
+}
+
+cudaError_t launch_decode_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                const __nv_bfloat16 *v, const void *f, bool f_bf16, const void *b,
+                                bool b_bf16, const float *A_log, int alog_mode,
+                                const float *dt_bias, void *state_pool, bool state_bf16,
+                                const int32_t *slots, int num_slots, int B, int H, float scale,
+                                void *o, bool o_bf16, unsigned int *err, cudaStream_t s) {
+    const int64_t units = static_cast<int64_t>(B) * H;
+    if (units == 0) return cudaSuccess;
+    const DecodeGate gt{f, f_bf16 ? 1 : 0, b, b_bf16 ? 1 : 0, A_log, alog_mode, dt_bias};
+    return o_bf16 ? launch_decode_t<true, true>(q, k, v, nullptr, nullptr, gt, state_pool,
+                                                state_bf16, slots, num_slots, units, H, scale, o,
+                                                err, s)
+                  : launch_decode_t<false, true>(q, k, v, nullptr, nullptr, gt, state_pool,
+                                                 state_bf16, slots, num_slots, units, H, scale, o,
+                                                 err, s);
 }
 
 }  // namespace kda

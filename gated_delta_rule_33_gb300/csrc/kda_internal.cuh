@@ -61,6 +61,13 @@ cudaError_t launch_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                             float *dq, float *dk, float *dv, float *dg, float *dbeta, float *dS0,
                             void *workspace, int ctas, unsigned int *err, cudaStream_t s);
 
+cudaError_t launch_decode_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                const __nv_bfloat16 *v, const void *f, bool f_bf16, const void *b,
+                                bool b_bf16, const float *A_log, int alog_mode,
+                                const float *dt_bias, void *state_pool, bool state_bf16,
+                                const int32_t *slots, int num_slots, int B, int H, float scale,
+                                void *o, bool o_bf16, unsigned int *err, cudaStream_t s);
+
 // Prefill workspace layout is private to kda_chunk.cu.
 size_t prefill_workspace_bytes(int64_t N, int B, int H);
 

@@ -93,6 +93,9 @@ def load():
         lib.kda_recurrent_backward.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, I, P,
                                                P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.kda_recurrent_backward.restype = I
+        lib.kda_recurrent_decode_gated.argtypes = [P, P, P, P, I, P, I, P, I, P, P, I, P, I, I, I,
+                                                   I, I, F, P, I, P]
+        lib.kda_recurrent_decode_gated.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
         lib.kda_get_last_device_error.restype = I
         _lib = lib
@@ -251,6 +254,19 @@ def kda_recurrent_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, d
     _check(st, "kda_recurrent_backward")
 
 
+def kda_recurrent_decode_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, state_pool,
+                               state_indices, scale, o, stream=None):
+    """state_indices None: slot b for sequence b."""
+    B, H, K = q.shape
+    V = v.shape[-1]
+    st = load().kda_recurrent_decode_gated(
+        _p(q), _p(k), _p(v), _p(f), _dtype_code(f), _p(b), _dtype_code(b), _p(A_log),
+        int(alog_mode), _p(dt_bias), _p(state_pool), _dtype_code(state_pool), _p(state_indices),
+        state_pool.shape[0], B, H, K, V, float(scale), _p(o), _dtype_code(o),
+        _stream(stream, q.device))
+    _check(st, "kda_recurrent_decode_gated")
+
+
 def kda_get_last_device_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word."""
     return int(load().kda_get_last_device_error(_stream(stream)))
@@ -341,6 +357,15 @@ def backward(q, k, v, g, beta, dO, cu_seqlens=None, scale=1.0, initial_state=Non
     kda_recurrent_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final, dq,
                            dk, dv, dg, dbeta, dS0, ws, stream)
     return dq, dk, dv, dg, dbeta, dS0
+
+
+def decode_gated(q, k, v, f, b, A_log, dt_bias, state_pool, alog_mode=KDA_ALOG_PER_CHANNEL,
+                 state_indices=None, scale=1.0, o_dtype=torch.bfloat16, stream=None):
+    B, H, K = q.shape
+    o = torch.empty(B, H, v.shape[-1], dtype=o_dtype, device=q.device)
+    kda_recurrent_decode_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, state_pool,
+                               state_indices, scale, o, stream)
+    return o
 
 
 def decode(q, k, v, g, beta, state, scale=1.0, o_dtype=torch.bfloat16, stream=None):

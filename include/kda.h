@@ -250,6 +250,38 @@ kda_status kda_recurrent_decode_indexed(const void *q, const void *k, const void
                                         void *o, kda_dtype o_dtype, void *stream);
 
 /*
+ * kda_recurrent_decode_gated -- the fused recurrent decode with the gate
+ * computed in the same kernel, from the gate's own inputs (the interface
+ * K3_ARTIFACT_AUDIT.md section 7.1 records for FlashKDA's prefill, applied to
+ * the one-token regime of code-audit.json, finding "dual-kda-execution-
+ * regimes").  g and beta are formed with exactly the binary32 operations of
+ * kda_gate_fused, so the result equals kda_gate_fused followed by
+ * kda_recurrent_decode_indexed bit for bit, with one launch and no fp32 g
+ * buffer.  (Measured at B = 256, H = 96 on GB300 it is about 3 % slower than
+ * the two launches: the exact gate arithmetic adds latency to every CTA of the
+ * HBM-bound step.)
+ *
+ *   q, k, v        bf16 [B, H, 128]
+ *   f              [B, H, 128] gate pre-activation, bf16 or fp32 (f_dtype)
+ *   b              [B, H] beta logits, bf16 or fp32 (b_dtype); the sigmoid is
+ *                  applied here, once
+ *   A_log          fp32, shape by alog_mode;  dt_bias fp32 [H, 128]
+ *   state_pool, state_dtype, state_indices, num_slots
+ *                  as in kda_recurrent_decode_indexed; state_indices may be
+ *                  NULL, meaning slot b for sequence b (then num_slots >= B)
+ *   o              [B, H, 128] of o_dtype
+ */
+kda_status kda_recurrent_decode_gated(const void *q, const void *k, const void *v,
+                                      const void *f, kda_dtype f_dtype,
+                                      const void *b, kda_dtype b_dtype,
+                                      const float *A_log, kda_alog_mode alog_mode,
+                                      const float *dt_bias,
+                                      void *state_pool, kda_dtype state_dtype,
+                                      const int32_t *state_indices, int num_slots,
+                                      int B, int H, int K, int V, float scale,
+                                      void *o, kda_dtype o_dtype, void *stream);
+
+/*
  * kda_recurrent_backward -- gradients of the KDA recurrence for training
  * ("chunked KDA for training", code-audit.json, finding
  * "dual-kda-execution-regimes"): given dL/do and dL/dS_final for the forward

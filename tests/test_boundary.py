@@ -174,6 +174,21 @@ def test_backward_argument_checks(clib):
     assert call(ws=None) == 5
 
 
+def test_gated_decode_argument_checks(clib):
+    P = _fake()
+    # (q,k,v,f,fdt,b,bdt,A_log,mode,dt,pool,sdt,idx,slots,B,H,K,V,scale,o,odt,s)
+    def call(**kw):
+        a = dict(fdt=0, bdt=1, mode=1, idx=P, slots=4, B=2, K=128, pool=P)
+        a.update(kw)
+        return clib.kda_recurrent_decode_gated(P, P, P, P, a["fdt"], P, a["bdt"], P, a["mode"], P,
+                                               a["pool"], 0, a["idx"], a["slots"], a["B"], 2,
+                                               a["K"], 128, 1.0, P, 0, None)
+    assert call(K=64) == 2
+    assert call(fdt=4) == 3
+    assert call(mode=3) == 1
+    assert call(pool=None) == 1
+    assert call(idx=None, slots=1) == 1          # dense slots need num_slots >= B
+    assert call(B=0) == 0                        # no work, no device touched
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "gated_delta_rule_33_gb300")
     for dirpath, _, files in os.walk(pkg):
