@@ -17,10 +17,10 @@
 // streams, ~12 instructions of arithmetic).  Lane l of a warp owns 8
 // consecutive channels (one 16-byte load or store of bf16), so a warp covers
 // two heads of 128 channels and the per-head norm is a reduction over 16 lanes
-// by shuffles.  A warp walks 16 consecutive tokens, requesting 8 rows at a
-// time; the three tokens before them (the halo) are re-read from L2 rather
-// than HBM because the neighbouring warp of the same block reads them as its
-// last rows.
+// by shuffles.  A warp walks 32 consecutive tokens, requesting 8 rows at a
+// time (the taps and the three-token halo before the first row are loaded
+// once per 32 tokens; the halo comes from L2, as the neighbouring warp of the
+// same block reads those rows as its last ones).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -32,7 +32,7 @@ constexpr int kHeadDim = 128;
 constexpr int kLaneCh = 8;                 // channels per lane
 constexpr int kWarpCh = 32 * kLaneCh;      // 256 channels per warp
 constexpr int kWarps = 8;
-constexpr int kTT = 16;                    // tokens per warp
+constexpr int kTT = 32;                    // tokens per warp
 constexpr int kBatch = 8;                  // rows requested together
 constexpr float kNormEps = 1e-6f;
 
