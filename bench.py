@@ -111,17 +111,18 @@ NCU_TRAFFIC = {
                     "sha256": ["0249a1d5c7d96af693a0ac274572e8e542305369099093f792305e80d5a7c953",
                                "1b42adeb58c6dbf45e946f4ab4b77d0169d66fd292fdb92c54d4c387190d085a"],
                     "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
-    "decode": {"src": ["kda_decode.cu"], "bytes": 4 * 753.89e6,
-               "sha256": ["3ece8e3a0bcba9a9f37ec97513c5b4c422fef3cbcd67c50b9f3705c759c82d9a"],
+    "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,
+               "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
+                          "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
-    "decode_pool": {"src": ["kda_decode.cu"], "bytes": 4 * 353.94e6,
-                    "sha256": ["3ece8e3a0bcba9a9f37ec97513c5b4c422fef3cbcd67c50b9f3705c759c82d9a"],
+    "decode_pool": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 354.09e6,
+                    "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
+                               "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
-    "gate": {"src": ["kda_gate.cu"], "bytes": 246.78e6,
-             "sha256": ["c571ed29aa63aa23447ebb39f20cf362297d7d0e0342dce221f132091a056852"],
-             "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
-    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 555.46e6,
-                   "sha256": ["1dda087737165eabb4bbda6c8ac279ddb646ca5a75868dec2cb52353227ea41e"],
+    "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh"], "bytes": None, "sha256": [],
+             "note": "profiles/gate_T4096_H96.md"},
+    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 559.92e6,
+                   "sha256": ["af1058f9eb8c8df068075fb627961c0a26e972f1d2d7c6c2cb4b3f7e7208e6cc"],
                    "note": "T=4096 capture (profiles/short_conv_T4096_H96.md)"},
 }
 
