@@ -19,10 +19,13 @@ from .kda import (  # noqa: F401
     decode_gated,
     decode_indexed,
     gate,
+    gate_backward,
     kda_chunk_prefill,
     kda_chunk_prefill_gated,
     kda_chunk_prefill_noalloc,
     kda_chunk_prefill_workspace_size,
+    kda_gate_backward,
+    kda_gate_backward_workspace_size,
     kda_gate_fused,
     kda_get_last_device_error,
     kda_recurrent_backward,

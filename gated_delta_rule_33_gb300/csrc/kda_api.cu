@@ -290,6 +290,38 @@ kda_status kda_recurrent_decode_gated(const void *q, const void *k, const void *
         o_dtype == KDA_BF16, dev->error_word, static_cast<cudaStream_t>(stream)));
 }
 
+size_t kda_gate_backward_workspace_size(int64_t N, int H, int K) {
+    return kda::gate_bwd_workspace_bytes(N, H, K);
+}
+
+kda_status kda_gate_backward(const void *f, kda_dtype f_dtype, const void *b, kda_dtype b_dtype,
+                             const float *A_log, kda_alog_mode alog_mode, const float *dt_bias,
+                             const float *dg, const float *dbeta, float *df, float *db,
+                             float *dA_log, float *ddt_bias, int64_t N, int H, int K,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+    if (N < 0 || H < 1 || K < 1) return KDA_ERR_INVALID_ARG;
+    if (K % 8 != 0) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(f_dtype) || !valid_dtype(b_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (alog_mode != KDA_ALOG_PER_HEAD && alog_mode != KDA_ALOG_PER_CHANNEL &&
+        alog_mode != KDA_ALOG_PER_HEAD_CHANNEL)
+        return KDA_ERR_INVALID_ARG;
+    const bool with_beta = b != nullptr;
+    if (with_beta != (dbeta != nullptr) || with_beta != (db != nullptr)) return KDA_ERR_INVALID_ARG;
+    if (A_log == nullptr || dt_bias == nullptr) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (f == nullptr || dg == nullptr || df == nullptr)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(f) || !aligned16(dg) || !aligned16(df) || !aligned16(workspace))
+        return KDA_ERR_MISALIGNED;
+    if (workspace == nullptr || workspace_bytes < kda::gate_bwd_workspace_bytes(N, H, K))
+        return KDA_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    return from_cuda(kda::launch_gate_backward(
+        f, f_dtype == KDA_BF16, b, b_dtype == KDA_BF16, A_log, static_cast<int>(alog_mode),
+        dt_bias, dg, dbeta, df, db, dA_log, ddt_bias, N, H, K, workspace,
+        static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_short_conv_qkv(const void *x_q, const void *x_k, const void *x_v,
                               const float *w_q, const float *w_k, const float *w_v,
                               const int32_t *cu_seqlens, int B, int64_t N, int C,

@@ -68,6 +68,14 @@ cudaError_t launch_decode_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                 const int32_t *slots, int num_slots, int B, int H, float scale,
                                 void *o, bool o_bf16, unsigned int *err, cudaStream_t s);
 
+// Gate backward (kda_gate_bwd.cu).
+size_t gate_bwd_workspace_bytes(int64_t N, int H, int K);
+cudaError_t launch_gate_backward(const void *f, bool f_bf16, const void *b, bool b_bf16,
+                                 const float *A_log, int alog_mode, const float *dt_bias,
+                                 const float *dg, const float *dbeta, float *df, float *db,
+                                 float *dA_log, float *ddt_bias, int64_t N, int H, int K,
+                                 void *workspace, cudaStream_t s);
+
 // Prefill workspace layout is private to kda_chunk.cu.
 size_t prefill_workspace_bytes(int64_t N, int B, int H);
 

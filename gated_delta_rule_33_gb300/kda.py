@@ -96,6 +96,11 @@ def load():
         lib.kda_recurrent_decode_gated.argtypes = [P, P, P, P, I, P, I, P, I, P, P, I, P, I, I, I,
                                                    I, I, F, P, I, P]
         lib.kda_recurrent_decode_gated.restype = I
+        lib.kda_gate_backward_workspace_size.argtypes = [I64, I, I]
+        lib.kda_gate_backward_workspace_size.restype = ctypes.c_size_t
+        lib.kda_gate_backward.argtypes = [P, I, P, I, P, I, P, P, P, P, P, P, P, I64, I, I, P,
+                                          ctypes.c_size_t, P]
+        lib.kda_gate_backward.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
         lib.kda_get_last_device_error.restype = I
         _lib = lib
@@ -267,6 +272,21 @@ def kda_recurrent_decode_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, state_p
     _check(st, "kda_recurrent_decode_gated")
 
 
+def kda_gate_backward_workspace_size(N, H, K) -> int:
+    return int(load().kda_gate_backward_workspace_size(N, H, K))
+
+
+def kda_gate_backward(f, b, A_log, alog_mode, dt_bias, dg, dbeta, df, db, dA_log, ddt_bias,
+                      workspace, stream=None):
+    N, H, K = f.shape
+    st = load().kda_gate_backward(
+        _p(f), _dtype_code(f), _p(b), KDA_FP32 if b is None else _dtype_code(b), _p(A_log),
+        int(alog_mode), _p(dt_bias), _p(dg), _p(dbeta), _p(df), _p(db), _p(dA_log), _p(ddt_bias),
+        N, H, K, _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, f.device))
+    _check(st, "kda_gate_backward")
+
+
 def kda_get_last_device_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error word."""
     return int(load().kda_get_last_device_error(_stream(stream)))
@@ -366,6 +386,21 @@ def decode_gated(q, k, v, f, b, A_log, dt_bias, state_pool, alog_mode=KDA_ALOG_P
     kda_recurrent_decode_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, state_pool,
                                state_indices, scale, o, stream)
     return o
+
+
+def gate_backward(f, b, A_log, dt_bias, dg, dbeta, alog_mode=KDA_ALOG_PER_CHANNEL,
+                  stream=None):
+    """Returns (df, db or None, dA_log, ddt_bias)."""
+    N, H, K = f.shape
+    dev = f.device
+    df = torch.empty(N, H, K, device=dev)
+    db = None if b is None else torch.empty(N, H, device=dev)
+    dA = torch.empty_like(A_log)
+    ddt = torch.empty(H, K, device=dev)
+    ws = torch.empty(max(kda_gate_backward_workspace_size(N, H, K), 16), dtype=torch.uint8,
+                     device=dev)
+    kda_gate_backward(f, b, A_log, alog_mode, dt_bias, dg, dbeta, df, db, dA, ddt, ws, stream)
+    return df, db, dA, ddt
 
 
 def decode(q, k, v, g, beta, state, scale=1.0, o_dtype=torch.bfloat16, stream=None):

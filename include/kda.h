@@ -325,6 +325,39 @@ kda_status kda_recurrent_backward(const void *q, const void *k, const void *v,
                                   void *stream);
 
 /*
+ * kda_gate_backward -- gradients of the gate (the training regime, after
+ * kda_recurrent_backward): from dL/dg and dL/dbeta to the gate's inputs.
+ * With x = f + dt_bias, a = exp(A_log), g = -a softplus(x), beta = sigmoid(b)
+ * (K3_ARTIFACT_AUDIT.md sections 4.1 and 5.1):
+ *   df = dg (-a sigmoid(x));   d dt_bias = sum over tokens of df;
+ *   d A_log = sum of dg g over the axes A_log is broadcast along;
+ *   db = dbeta beta (1 - beta)
+ * x, a, g and beta are formed with kda_gate_fused's binary32 specification.
+ * The sums are added in a fixed order (the result does not depend on timing).
+ *
+ *   f            [N, H, K] of f_dtype (bf16 or fp32);  dg fp32 [N, H, K]
+ *   b, dbeta     [N, H] (b_dtype) and fp32 [N, H], with db fp32 [N, H]
+ *                written; all three NULL to skip beta
+ *   A_log        fp32 by alog_mode;  dt_bias fp32 [H, K]
+ *   df           fp32 [N, H, K] written
+ *   dA_log       fp32, shape of A_log, written (or NULL)
+ *   ddt_bias     fp32 [H, K] written (or NULL)
+ *   workspace    >= kda_gate_backward_workspace_size(N, H, K) bytes (about
+ *                (2 min(N, 256) + 1) H K 4 bytes), 16-byte aligned
+ * K must be a multiple of 8; f, dg, df 16-byte aligned.
+ */
+size_t kda_gate_backward_workspace_size(int64_t N, int H, int K);
+
+kda_status kda_gate_backward(const void *f, kda_dtype f_dtype,
+                             const void *b, kda_dtype b_dtype,
+                             const float *A_log, kda_alog_mode alog_mode,
+                             const float *dt_bias,
+                             const float *dg, const float *dbeta,
+                             float *df, float *db, float *dA_log, float *ddt_bias,
+                             int64_t N, int H, int K,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * kda_short_conv_qkv -- the KDA input pre-step over a packed batch, on the three
  * projection streams at once: a depthwise causal convolution of kernel size 4
  * per channel (the checkpoint's q/k/v_conv1d.weight, fp32 [H*128, 1, 4];

@@ -189,6 +189,27 @@ def test_gated_decode_argument_checks(clib):
     assert call(pool=None) == 1
     assert call(idx=None, slots=1) == 1          # dense slots need num_slots >= B
     assert call(B=0) == 0                        # no work, no device touched
+def test_gate_backward_argument_checks(clib):
+    import gated_delta_rule_33_gb300 as kda
+    P, ws = _fake(), _fake()
+    need = kda.kda_gate_backward_workspace_size(64, 2, 128)
+    assert need == (2 * 64 + 1) * 2 * 128 * 4
+
+    def call(**kw):
+        a = dict(f=P, b=P, dbeta=P, db=P, mode=1, K=128, wsb=need, fdt=0)
+        a.update(kw)
+        # (f,fdt,b,bdt,A_log,mode,dt,dg,dbeta,df,db,dA,ddt,N,H,K,ws,wsb,s)
+        return clib.kda_gate_backward(a["f"], a["fdt"], a["b"], 1, P, a["mode"], P, P, a["dbeta"],
+                                      P, a["db"], P, P, 64, 2, a["K"], ws, a["wsb"], None)
+    assert call(K=12) == 2
+    assert call(fdt=3) == 3
+    assert call(mode=5) == 1
+    assert call(b=None) == 1                     # beta inputs all or none
+    assert call(b=None, dbeta=None, db=None) != 1
+    assert call(f=_fake(0x10004)) == 4
+    assert call(wsb=need - 4) == 5
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "gated_delta_rule_33_gb300")
     for dirpath, _, files in os.walk(pkg):

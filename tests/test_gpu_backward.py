@@ -91,3 +91,47 @@ def test_bad_cu_seqlens_reports(lib):
     lib.backward(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g, beta, dO.to(DEV),
                  cu_seqlens=x.cu_seqlens.to(DEV))
     assert lib.kda_get_last_device_error() == 1
+
+
+# --- gate backward -------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,H,mode,f_fp32,b_bf16,with_beta", [
+    (4096, 96, synth.ALOG_PER_CHANNEL, False, False, True),
+    (300, 3, synth.ALOG_PER_HEAD, True, True, True),
+    (77, 2, synth.ALOG_PER_HEAD_CHANNEL, False, False, False),
+    (1, 1, synth.ALOG_PER_CHANNEL, False, False, True)])
+def test_gate_backward(lib, N, H, mode, f_fp32, b_bf16, with_beta):
+    """kda_gate_backward against the fp64 chain rule of the gate
+    (oracle/gate_backward.py): every output within 1e-5 relative L2."""
+    from oracle import gate_backward as gb
+    x = synth.make_inputs(N, H=H, D=128, seed=N + mode, alog_mode=mode)
+    f = x.f.float() if f_fp32 else x.f
+    b = (x.b.to(torch.bfloat16) if b_bf16 else x.b) if with_beta else None
+    gen = torch.Generator().manual_seed(N)
+    dg = torch.randn(N, H, 128, generator=gen)
+    dbeta = torch.randn(N, H, generator=gen) if with_beta else None
+    df, db, dA, ddt = lib.gate_backward(f.to(DEV), None if b is None else b.to(DEV),
+                                        x.A_log.to(DEV), x.dt_bias.to(DEV), dg.to(DEV),
+                                        None if dbeta is None else dbeta.to(DEV), alog_mode=mode)
+    assert lib.kda_get_last_device_error() == 0
+    ref = gb.gate_backward(f.double().numpy(), None if b is None else b.double().numpy(),
+                           x.A_log.double().numpy(), x.dt_bias.double().numpy(),
+                           dg.double().numpy(), None if dbeta is None else dbeta.double().numpy(),
+                           mode)
+    for name, a, r in zip(("df", "db", "dA_log", "ddt_bias"), (df, db, dA, ddt), ref):
+        if r is None:
+            assert a is None
+            continue
+        err = rel_l2(f64(a), r)
+        assert err <= 1e-5, f"{name}: rel L2 {err:.2e}"
+
+
+def test_gate_backward_is_deterministic(lib):
+    x = synth.make_inputs(2000, H=4, D=128, seed=5)
+    dg = torch.randn(2000, 4, 128, device=DEV)
+    dbeta = torch.randn(2000, 4, device=DEV)
+    args = (x.f.to(DEV), x.b.to(DEV), x.A_log.to(DEV), x.dt_bias.to(DEV), dg, dbeta)
+    r1 = lib.gate_backward(*args)
+    r2 = lib.gate_backward(*args)
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
