@@ -119,8 +119,10 @@ NCU_TRAFFIC = {
                     "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
                                "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
-    "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh"], "bytes": None, "sha256": [],
-             "note": "profiles/gate_T4096_H96.md"},
+    "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh"], "bytes": 246.81e6,
+             "sha256": ["4740ee00bfb7b6772d91a0e0309468ee3f2fb421f9ea1fae2c4ad50bdfa4bf80",
+                        "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
+             "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
     "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 559.92e6,
                    "sha256": ["af1058f9eb8c8df068075fb627961c0a26e972f1d2d7c6c2cb4b3f7e7208e6cc"],
                    "note": "T=4096 capture (profiles/short_conv_T4096_H96.md)"},

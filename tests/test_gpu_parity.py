@@ -223,3 +223,31 @@ def test_prefill_then_decode_continuation(lib):
     o = torch.cat(outs)
     assert rel_l2(f64(o), o_ref) <= O_TOL
     assert rel_l2(f64(S), S_ref) <= STATE_TOL
+
+
+def test_prefill_many_short_sequences(lib):
+    """200 sequences of 1..40 tokens x 2 heads: more chains than SMs, every
+    chunk a partial one."""
+    lens = synth.varlen_lengths(200, 1, 40, seed=5)
+    x = synth.make_inputs(lengths=lens, H=2, D=128, seed=23, s0_std=0.05)
+    check_prefill(lib, x, o_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_prefill_decay_out_of_range_is_reported(lib, gated):
+    """A chunk whose per-channel decay exceeds the represented range (sum of g
+    below -160 within 64 tokens) sets KDA_ERR_DECAY_RANGE instead of
+    returning wrong numbers silently."""
+    x = synth.make_inputs(128, H=2, D=128, seed=8)
+    q, k, v = x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
+    if gated:
+        # A_log = 2, f = 30: g = -e^2 softplus(30 + dt_bias) ~ -190 per token
+        f = torch.full_like(x.f, 30.0).to(DEV)
+        A_log = torch.full_like(x.A_log, 2.0).to(DEV)
+        lib.prefill_gated(q, k, v, f, x.b.to(DEV), A_log, x.dt_bias.to(DEV), x.alog_mode)
+    else:
+        g = torch.full((128, 2, 128), -5.0, device=DEV)      # -320 per 64-token chunk
+        beta = torch.full((128, 2), 0.5, device=DEV)
+        lib.prefill(q, k, v, g, beta)
+    assert lib.kda_get_last_device_error() == 11   # KDA_ERR_DECAY_RANGE
+    assert lib.kda_get_last_device_error() == 0
