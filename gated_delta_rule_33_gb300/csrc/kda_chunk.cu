@@ -54,9 +54,9 @@ constexpr uint32_t OFF_Q = 0;            // raw q bf16 [64][128] (TMA, no swizzl
 constexpr uint32_t OFF_K = 16384;        // raw k bf16 [64][128] (TMA, no swizzle)
 constexpr uint32_t OFF_V = 32768;        // raw v bf16 [64 s][128 v] (TMA, 2 swizzled boxes)
 constexpr uint32_t OFF_QK = 49152;       // [Qt ; Kr] tf32, 128 rows (r) x 128 (channel)
-constexpr uint32_t OFF_KS = 114688;      // g fp32 64 x 128 (TMA) -> Ks tf32 -> A_kk | T fp32 -> W' tf32
-constexpr uint32_t OFF_KH = 147456;      // Khat^T tf32, 128 rows (channel) x 64 (r)
-constexpr uint32_t OFF_TB = 180224;      // T beta tf32 64 x 64 -> A_qk tf32 64 x 64
+constexpr uint32_t OFF_KS = 114688;      // g fp32 64 x 128 (TMA) -> Ks tf32 -> A_kk | T fp32
+constexpr uint32_t OFF_KH = 147456;      // one tf32 tile, 192 rows x 64 (r), k-block stride 24576:
+                                         // rows 0..127 Khat^T (channel), 128..191 T beta -> A_qk
 constexpr uint32_t OFF_TB16 = 196608;    // T beta bf16 hi 64 x 64 | lo 64 x 64
 constexpr uint32_t OFF_MISC = 212992;
 constexpr uint32_t MISC_BETA = 0;        // float[64]
@@ -76,8 +76,9 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 //   S_acc: S^T fp32 (lane v, column k)      S_op: tf32(e^{m_k} S[k][v])
 //   U: U^T (lane v, column r)               O: W'^T (lane k, column r), then O^T
 //   A: [Qt; Kr] Ks^T (lane = row of [Qt; Kr], column s)   W: Kr^T (lane k, column s)
-// O^T of a chunk is read out while the next chunk's first MMA runs.
-constexpr uint32_t T_SACC = 0, T_SOP = 128, T_U = 256, T_O = 320, T_A = 384, T_W = 448;
+// O^T of a chunk is read out while the next chunk's first MMA runs.  O sits
+// between S_acc and U so that one MMA updates [O | U] and one [S_acc | O].
+constexpr uint32_t T_SACC = 0, T_O = 128, T_U = 192, T_SOP = 256, T_A = 384, T_W = 448;
 
 struct Params {
     const float *g;              // fp32 log-decay [N, H, 128]   (unfused)
@@ -120,7 +121,7 @@ __device__ __noinline__ void ut_inverse(const float *A, const float *Adiag, floa
                                         const float *beta, int tid, uint32_t tmem_lane,
                                         const float *em, const float *dec) {
     if (tid < 64) {
-        ut_diag_solve(Adiag, T, Tdiag, smem + OFF_TB, smem + OFF_TB16, beta, tid);
+        ut_diag_solve(Adiag, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
     } else if (tid >= 128) {
         float r16[16], o16[16];
         for (int cs = (tid >> 7) - 1; cs < 8; cs += 3) {
@@ -138,8 +139,8 @@ __device__ __noinline__ void ut_inverse(const float *A, const float *Adiag, floa
         tmem_wait_st();
     }
     __syncthreads();
-    ut_level1(A, Tdiag, T, P, smem + OFF_TB, smem + OFF_TB16, beta, tid);
-    ut_level2(A, T, P, smem + OFF_TB, smem + OFF_TB16, beta, tid);
+    ut_level1(A, Tdiag, T, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    ut_level2(A, T, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
 }
 
 // kGate: the gate is computed in this kernel from the bf16 pre-activation f,
@@ -188,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         ctrl[3] = 0;
     }
     // The strictly upper blocks of the T beta tiles are zero for every chunk and
-    // are never written again (A_qk, which reuses the tf32 tile, is zero there too).
-    for (int e = tid; e < 16384 / 16; e += kThreads)
-        reinterpret_cast<float4 *>(smem + OFF_TB)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // are never written again (A_qk, which reuses the tf32 rows, is zero there too).
+    for (int e = tid; e < 49152 / 16; e += kThreads)
+        reinterpret_cast<float4 *>(smem + OFF_KH)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int e = tid; e < 16384 / 16; e += kThreads)
         reinterpret_cast<float4 *>(smem + OFF_TB16)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     fence_proxy_async_smem();
@@ -209,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint32_t a_qk = smem_addr(smem + OFF_QK);
     const uint32_t a_ks = smem_addr(smem + OFF_KS);
     const uint32_t a_kh = smem_addr(smem + OFF_KH);
-    const uint32_t a_tb = smem_addr(smem + OFF_TB);
     const uint32_t a_tb16 = smem_addr(smem + OFF_TB16);
     const uint32_t a_v = smem_addr(smem + OFF_V);
     // Shared-memory descriptors of every operand tile (128-byte swizzle), built
@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint64_t d_qk = smem_desc(a_qk, 16, 1024, kSwizzle128B);
     const uint64_t d_ks = smem_desc(a_ks, 16, 1024, kSwizzle128B);
     const uint64_t d_kh = smem_desc(a_kh, 16, 1024, kSwizzle128B);
-    const uint64_t d_tb = smem_desc(a_tb, 16, 1024, kSwizzle128B);
     const uint64_t d_tb16 = smem_desc(a_tb16, 16, 1024, kSwizzle128B);
     const uint64_t d_v = smem_desc(a_v, 8192, 1024, kSwizzle128B);  // MN-major, 64-wide M blocks
     float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
@@ -418,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             // Khat^T row ch, columns r = 16 grp .. +15: four 16-byte stores
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<float4 *>(smem + OFF_KH + sw128_offset(ch, 16 * grp + 4 * q4, 128, 4)) =
+                *reinterpret_cast<float4 *>(smem + OFF_KH + sw128_offset(ch, 16 * grp + 4 * q4, 192, 4)) =
                     make_float4(khv[4 * q4], khv[4 * q4 + 1], khv[4 * q4 + 2], khv[4 * q4 + 3]);
             tmem_st16(tmem + lane_base + T_W + 16 * grp, krt);
             tmem_wait_st();
@@ -471,11 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_after();
 
             // ---- S5: W'^T = Kr^T (T beta)^T ;  Ut^T = V^T (T beta)^T ----
+            // A_kk and T are consumed: the next chunk's g and beta are staged now.
+            if (Ln > 0) load_beta(tn, Ln);
             if (tid == 0) {
+                if (Ln > 0) issue_g(tn);
                 const uint32_t idw = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = (d_tb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
+                    const uint64_t bd = (d_kh + static_cast<uint64_t>(((kk >> 2) * 24576 + 16384 + (kk & 3) * 32) >> 4));
                     mma_tf32_ts(tmem + T_O, tmem + T_W + kk * 8, bd, idw, kk > 0);
                 }
                 if (!mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
@@ -501,33 +503,32 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             if (ctrl[2] != 0) break;
             if (tid == 0 && Ln > 0) issue_v(tn);
 
-            // ---- S6: W' to shared memory (K-major [r][k]) ----
+            // ---- S6: -W' into rows 64..127 of the [Qt ; Kr] tile (Kr is dead
+            // since D_A); the O columns are cleared for the accumulating MMA ----
             {
                 float w16[16];
                 tmem_ld16(tmem + lane_base + T_O + 16 * grp, w16);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    st_f32(smem + OFF_KS, sw128_offset(16 * grp + j, ch, 64, 4), to_tf32(w16[j]));
+                for (int j = 0; j < 16; ++j) {
+                    st_f32(smem + OFF_QK, sw128_offset(64 + 16 * grp + j, ch, 128, 4), -to_tf32(w16[j]));
+                    w16[j] = 0.f;
+                }
+                tmem_st16(tmem + lane_base + T_O + 16 * grp, w16);
+                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
 
-            // ---- S7: U^T -= S_op W'^T ;  O^T = S_op Qt^T ----
+            // ---- S7: [O^T | U^T] += S_op [Qt ; -W']^T (O columns start at zero) ----
             if (tid == 0) {
-                const uint32_t idn = instr_desc(128, 64, kFmtTF32, 0, 0, 1);
-                const uint32_t ido = instr_desc(128, 64, kFmtTF32, 0, 0);
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t bw = (d_ks + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_U, tmem + T_SOP + kk * 8, bw, idn, 1);
-                }
+                const uint32_t id = instr_desc(128, 128, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
                     const uint64_t bq = (d_qk + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_O, tmem + T_SOP + kk * 8, bq, ido, kk > 0);
+                    mma_tf32_ts(tmem + T_O, tmem + T_SOP + kk * 8, bq, id, 1);
                 }
                 mma_commit(bar_mma);
             }
@@ -541,17 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int s = 16 * grp + j;
-                    st_f32(smem + OFF_TB, sw128_offset(r, s, 64, 4), (s <= r) ? to_tf32(a16[j]) : 0.f);
+                    st_f32(smem + OFF_KH, sw128_offset(kTbRow0 + r, s, kTbRows, 4),
+                           (s <= r) ? to_tf32(a16[j]) : 0.f);
                 }
             }
             fence_proxy_async_smem();
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
-            // W' (in OFF_KS) is consumed: stage the next chunk's g and beta
-            if (Ln > 0) {
-                if (tid == 0) issue_g(tn);
-                load_beta(tn, Ln);
-            }
 
             // ---- S8: U rounded to tf32 in place (A operand of the next MMAs) ----
             {
@@ -568,19 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_after();
             if (ctrl[2] != 0) break;
 
-            // ---- S9: S_acc^T += U^T Khat ;  O^T += U^T A_qk^T ----
+            // ---- S9: [S_acc^T | O^T] += U^T [Khat^T ; A_qk]^T ----
             if (tid == 0) {
-                const uint32_t ids = instr_desc(128, 128, kFmtTF32, 0, 0);
-                const uint32_t ido = instr_desc(128, 64, kFmtTF32, 0, 0);
+                const uint32_t id = instr_desc(128, 192, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bk = (d_kh + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_SACC, tmem + T_U + kk * 8, bk, ids, 1);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ba = (d_tb + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_O, tmem + T_U + kk * 8, ba, ido, 1);
+                    const uint64_t bk = (d_kh + static_cast<uint64_t>(((kk >> 2) * 24576 + (kk & 3) * 32) >> 4));
+                    mma_tf32_ts(tmem + T_SACC, tmem + T_U + kk * 8, bk, id, 1);
                 }
                 mma_commit(bar_mma);
             }

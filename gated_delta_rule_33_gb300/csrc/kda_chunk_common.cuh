@@ -18,6 +18,11 @@ constexpr int kC = 64;              // chunk length
 constexpr int kD = 128;             // d_k = d_v
 constexpr float kMaxDecay = 160.f;  // largest per-channel chunk decay represented
 constexpr uint32_t kMaxPolls = 1u << 20;
+// The tf32 T beta tile lives in rows 128..191 of a 192-row K-major tile (the
+// chunk kernel's [Khat^T ; T beta -> A_qk] B operand), so its rows are
+// addressed with this offset and row count.
+constexpr uint32_t kTbRow0 = 128;
+constexpr uint32_t kTbRows = 192;
 
 __device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
@@ -58,7 +63,7 @@ __device__ __forceinline__ void store_tbeta4(uint8_t *tb, uint8_t *tb16, int r, 
                                              const float *beta) {
     const float x0 = t.x * beta[s4], x1 = t.y * beta[s4 + 1];
     const float x2 = t.z * beta[s4 + 2], x3 = t.w * beta[s4 + 3];
-    *reinterpret_cast<float4 *>(tb + sw128_offset(r, s4, 64, 4)) =
+    *reinterpret_cast<float4 *>(tb + sw128_offset(kTbRow0 + r, s4, kTbRows, 4)) =
         make_float4(to_tf32(x0), to_tf32(x1), to_tf32(x2), to_tf32(x3));
     const __nv_bfloat162 h01 = __floats2bfloat162_rn(x0, x1), h23 = __floats2bfloat162_rn(x2, x3);
     const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
@@ -202,7 +207,7 @@ __device__ __forceinline__ void ut_diag_solve(const float *Adiag, float *T, floa
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const float xb = x[r] * bj;
-            st_f32(tb, sw128_offset(base + r, base + j, 64, 4), to_tf32(xb));
+            st_f32(tb, sw128_offset(kTbRow0 + base + r, base + j, kTbRows, 4), to_tf32(xb));
             const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
             const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
             *reinterpret_cast<__nv_bfloat16 *>(tb16 + sw128_offset(base + r, base + j, 64, 2)) = hi;
