@@ -109,38 +109,48 @@ struct Params {
 // 16-byte loads.  Then the off-diagonal blocks in two levels: T_10 and T_32
 // (ut_level1), then the whole lower-left 32x32 block (ut_level2) -- the
 // 2x2-block inverse [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
-// applied at 16 and then at 32 rows.  T is row-major with stride 64; its strictly upper
-// blocks are left unwritten; Tdiag receives the diagonal blocks column-major.
+// applied at 16 and then at 32 rows.  T is row-major with stride 64 (only the
+// blocks that later steps read are written); Tdiag receives the diagonal blocks
+// column-major and Adiag, consumed by then, receives T_32 column-major.
 // Every lower block of T beta is written as soon as its block of T is final
 // (the strictly upper blocks of the T beta tiles hold zeros written once).
-// While warps 0-1 solve the diagonal blocks, warps 4-15 run the state pass:
-// S_op = tf32(e^{m_k} S[k][v]) and S_acc = e^{Gam_L,k} S[k][v] in tensor memory
-// (warp w: lane quarter w % 4, 16-column slices (w / 4 - 1) + 3 n).
-__device__ __noinline__ void ut_inverse(const float *A, const float *Adiag, float *T,
-                                        float *Tdiag, float *P, uint8_t *smem,
-                                        const float *beta, int tid, uint32_t tmem_lane,
-                                        const float *em, const float *dec) {
-    if (tid < 64) {
-        ut_diag_solve(Adiag, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
-    } else if (tid >= 128) {
-        float r16[16], o16[16];
-        for (int cs = (tid >> 7) - 1; cs < 8; cs += 3) {
-            const int c0 = 16 * cs;
-            tmem_ld16(tmem_lane + T_SACC + c0, r16);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                o16[j] = to_tf32(r16[j] * em[c0 + j]);
-                r16[j] = r16[j] * dec[c0 + j];
-            }
-            tmem_st16(tmem_lane + T_SOP + c0, o16);
-            tmem_st16(tmem_lane + T_SACC + c0, r16);
-        }
-        tmem_wait_st();
-    }
+// The operands are found from the shared-memory base inside the function (a
+// pointer argument would reach it as a generic address).
+__device__ __noinline__ void ut_inverse(int tid) {
+    uint8_t *smem = smem_base();
+    uint8_t *misc = smem + OFF_MISC;
+    float *A = reinterpret_cast<float *>(smem + OFF_KS);
+    float *T = A + 64 * 64;
+    float *Adiag = reinterpret_cast<float *>(misc + MISC_DIAG);
+    float *Tdiag = reinterpret_cast<float *>(misc + MISC_TDIAG);
+    float *P = reinterpret_cast<float *>(misc + MISC_P);
+    const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
+    if (tid < 64) ut_diag_solve(Adiag, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
     __syncthreads();
-    ut_level1(A, Tdiag, T, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
-    ut_level2(A, T, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    ut_level1(A, Tdiag, T, P, Adiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    ut_level2(A, T, Tdiag, Adiag, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+}
+
+// The state pass of a chunk, S_op = tf32(e^{m_k} S[k][v]) and
+// S_acc = e^{Gam_L,k} S[k][v] in tensor memory: warp w covers lane quarter
+// w % 4 and the 16-column slices w / 4 and w / 4 + 4.
+__device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const float *em,
+                                           const float *dec) {
+    float r16[16], o16[16];
+#pragma unroll 1
+    for (int cs = warp >> 2; cs < 8; cs += 4) {
+        const int c0 = 16 * cs;
+        tmem_ld16(tmem_lane + T_SACC + c0, r16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            o16[j] = to_tf32(r16[j] * em[c0 + j]);
+            r16[j] = r16[j] * dec[c0 + j];
+        }
+        tmem_st16(tmem_lane + T_SOP + c0, o16);
+        tmem_st16(tmem_lane + T_SACC + c0, r16);
+    }
+    tmem_wait_st();
 }
 
 // kGate: the gate is computed in this kernel from the bf16 pre-activation f,
@@ -153,14 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                                                             const __grid_constant__ CUtensorMap tm_v,
                                                             const __grid_constant__ CUtensorMap tm_g,
                                                             const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *smem = smem_base();
     uint8_t *misc = smem + OFF_MISC;
     float *s_beta = reinterpret_cast<float *>(misc + MISC_BETA);
     float *s_em = reinterpret_cast<float *>(misc + MISC_EM);
     float *s_dec = reinterpret_cast<float *>(misc + MISC_DEC);
-    float *s_P = reinterpret_cast<float *>(misc + MISC_P);
     uint64_t *bar_qk = reinterpret_cast<uint64_t *>(misc + MISC_BAR);
     uint64_t *bar_v = bar_qk + 1;
     uint64_t *bar_mma = bar_qk + 2;
@@ -220,9 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint64_t d_tb16 = smem_desc(a_tb16, 16, 1024, kSwizzle128B);
     const uint64_t d_v = smem_desc(a_v, 8192, 1024, kSwizzle128B);  // MN-major, 64-wide M blocks
     float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
-    float *Tm = Akk + 64 * 64;
     float *s_diag = reinterpret_cast<float *>(misc + MISC_DIAG);
-    float *s_tdiag = reinterpret_cast<float *>(misc + MISC_TDIAG);
 
     while (true) {
         __syncthreads();
@@ -462,8 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             __syncthreads();
 
             // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
-            ut_inverse(Akk, s_diag, Tm, s_tdiag, s_P, smem, s_beta, tid, tmem + lane_base, s_em,
-                       s_dec);
+            ut_inverse(tid);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -497,6 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
+            // the state pass touches only S_acc and S_op, which these products leave alone
+            state_pass(tmem + lane_base, warp, s_em, s_dec);
             ph_v++;
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;

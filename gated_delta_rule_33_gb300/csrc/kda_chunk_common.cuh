@@ -24,6 +24,16 @@ constexpr uint32_t kMaxPolls = 1u << 20;
 constexpr uint32_t kTbRow0 = 128;
 constexpr uint32_t kTbRows = 192;
 
+// The 1024-byte-aligned base of the dynamic shared memory (the launch asks for
+// 1024 bytes more than it uses).  It is formed by indexing the shared array,
+// not through an integer round trip, so that accesses derived from it stay
+// shared-memory accesses instead of generic ones.
+__device__ __forceinline__ uint8_t *smem_base() {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    return smem_raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
 }
@@ -78,9 +88,12 @@ __device__ __forceinline__ void store_tbeta4(uint8_t *tb, uint8_t *tb16, int r, 
 
 // Level 1 of the off-diagonal blocks: T_10 and T_32 (the block sub-diagonal
 // inside each 32x32 half), T_{t+1,t} = -T_{t+1,t+1} A_{t+1,t} T_tt, t = 0, 2.
-// 64 threads per target: 16 rows x 4 column quads.
+// 64 threads per target: 16 rows x 4 column quads.  T_10 goes to T (row-major,
+// read by level 2 as part of T_top); T_32 goes column-major to T32c (read by
+// level 2 as part of T_bot, a row per thread).
 __device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, float *T, float *P,
-                                          uint8_t *tb, uint8_t *tb16, const float *beta, int tid) {
+                                          float *T32c, uint8_t *tb, uint8_t *tb16,
+                                          const float *beta, int tid) {
     if (tid < 128) {
         const int t = 2 * (tid >> 6), r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
         const int arow = 16 * (t + 1) + r;
@@ -109,7 +122,14 @@ __device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, fl
             acc.x += a * pv.x; acc.y += a * pv.y; acc.z += a * pv.z; acc.w += a * pv.w;
         }
         const float4 tij = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        *reinterpret_cast<float4 *>(&T[(16 * (t + 1) + r) * 64 + 16 * t + c4]) = tij;
+        if (t == 0) {
+            *reinterpret_cast<float4 *>(&T[(16 + r) * 64 + c4]) = tij;
+        } else {
+            T32c[c4 * 16 + r] = tij.x;
+            T32c[(c4 + 1) * 16 + r] = tij.y;
+            T32c[(c4 + 2) * 16 + r] = tij.z;
+            T32c[(c4 + 3) * 16 + r] = tij.w;
+        }
         store_tbeta4(tb, tb16, 16 * (t + 1) + r, 16 * t + c4, tij, beta);
     }
     __syncthreads();
@@ -120,7 +140,9 @@ __device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, fl
 // triangular, complete after level 1) and A_bl = A[32:64, 0:32].
 // 256 threads, 32 rows x 8 column quads; every warp's rows and columns fall in
 // one 16-block, so the triangular bounds are compile-time per branch.
-// Y = A_bl T_top goes through P.
+// Y = A_bl T_top goes through P.  T_bot is read from its column-major blocks
+// (T_22 and T_33 in Tdiag, T_32 in T32c): the eight rows a warp covers then
+// fall in eight banks (a row-major read with stride 64 would hit one).
 template <int S0>
 __device__ __forceinline__ float4 level2_y(const float *Ar, int sw, const float *T, int c) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -133,19 +155,20 @@ __device__ __forceinline__ float4 level2_y(const float *Ar, int sw, const float 
     return acc;
 }
 
-template <int S1>
-__device__ __forceinline__ float4 level2_x(const float *Tr, const float *P, int c) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// acc += sum over 16 s of Tc[16 s] * P[s0 + s][c .. c + 3] (Tc: one row of a
+// column-major 16x16 block)
+__device__ __forceinline__ void level2_x16(float4 &acc, const float *Tc, const float *P, int s0,
+                                           int c) {
 #pragma unroll
-    for (int s = 0; s < S1; ++s) {
-        const float a = Tr[s];
-        const float4 yv = *reinterpret_cast<const float4 *>(&P[s * 32 + c]);
+    for (int s = 0; s < 16; ++s) {
+        const float a = Tc[16 * s];
+        const float4 yv = *reinterpret_cast<const float4 *>(&P[(s0 + s) * 32 + c]);
         acc.x += a * yv.x; acc.y += a * yv.y; acc.z += a * yv.z; acc.w += a * yv.w;
     }
-    return acc;
 }
 
-__device__ __forceinline__ void ut_level2(const float *A, float *T, float *P, uint8_t *tb,
+__device__ __forceinline__ void ut_level2(const float *A, const float *T, const float *Tdiag,
+                                          const float *T32c, float *P, uint8_t *tb,
                                           uint8_t *tb16, const float *beta, int tid) {
     // task: column block cb = tid / 128, row r = (tid / 4) % 32, quad q = tid % 4
     const int cb = tid >> 7, r = (tid >> 2) & 31, c = 16 * cb + 4 * (tid & 3);
@@ -158,11 +181,15 @@ __device__ __forceinline__ void ut_level2(const float *A, float *T, float *P, ui
     }
     __syncthreads();
     if (tid < 256) {
-        const float *Tr = T + (32 + r) * 64 + 32;   // T_bot[r][s]
         // T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
-        const float4 acc = (r < 16) ? level2_x<16>(Tr, P, c) : level2_x<32>(Tr, P, c);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < 16) {
+            level2_x16(acc, Tdiag + 2 * 256 + r, P, 0, c);
+        } else {
+            level2_x16(acc, T32c + (r - 16), P, 0, c);
+            level2_x16(acc, Tdiag + 3 * 256 + (r - 16), P, 16, c);
+        }
         const float4 x = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        *reinterpret_cast<float4 *>(&T[(32 + r) * 64 + c]) = x;
         store_tbeta4(tb, tb16, 32 + r, c, x, beta);
     }
     __syncthreads();
