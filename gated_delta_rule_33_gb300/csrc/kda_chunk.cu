@@ -114,8 +114,9 @@ struct Params {
 // column-major and Adiag, consumed by then, receives T_32 column-major.
 // Every lower block of T beta is written as soon as its block of T is final
 // (the strictly upper blocks of the T beta tiles hold zeros written once).
-// The operands are found from the shared-memory base inside the function (a
-// pointer argument would reach it as a generic address).
+// Warps 0-7 only (they meet at their own named barrier).  The operands are
+// found from the shared-memory base inside the function (a pointer argument
+// would reach it as a generic address).
 __device__ __noinline__ void ut_inverse(int tid) {
     uint8_t *smem = smem_base();
     uint8_t *misc = smem + OFF_MISC;
@@ -126,19 +127,20 @@ __device__ __noinline__ void ut_inverse(int tid) {
     float *P = reinterpret_cast<float *>(misc + MISC_P);
     const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
     if (tid < 64) ut_diag_solve(Adiag, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
-    __syncthreads();
+    inverse_sync();
     ut_level1(A, Tdiag, T, P, Adiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
     ut_level2(A, T, Tdiag, Adiag, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
 }
 
 // The state pass of a chunk, S_op = tf32(e^{m_k} S[k][v]) and
-// S_acc = e^{Gam_L,k} S[k][v] in tensor memory: warp w covers lane quarter
-// w % 4 and the 16-column slices w / 4 and w / 4 + 4.
+// S_acc = e^{Gam_L,k} S[k][v] in tensor memory, on warps 8-15 while warps 0-7
+// compute the UT inverse: warp w covers lane quarter w % 4 and the 16-column
+// slices w / 4 - 2 + 2 n.
 __device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const float *em,
                                            const float *dec) {
     float r16[16], o16[16];
 #pragma unroll 1
-    for (int cs = warp >> 2; cs < 8; cs += 4) {
+    for (int cs = (warp >> 2) - 2; cs < 8; cs += 2) {
         const int c0 = 16 * cs;
         tmem_ld16(tmem_lane + T_SACC + c0, r16);
         tmem_wait_ld();
@@ -357,15 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                         const int r = 16 * grp + i;
                         const float x = __bfloat162float(ft[r * kD + ch]) + gate_dt;
                         const float e = fast_exp2(-kLog2e * fabsf(x));
-                        // log2(1 + e) as log2(u) e / (u - 1), u = 1 + e (D. Goldberg,
-                        // "What every computer scientist should know about
-                        // floating-point arithmetic", 1991): exact-ish even when
-                        // 1 + e rounds; u == 1 leaves log2(1 + e) = e log2(e).
-                        const float u = 1.f + e;
-                        float lg;
-                        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(u));
-                        lg = (u == 1.f) ? kLog2e * e : lg * __fdividef(e, u - 1.f);
-                        const float g2 = -gate_a * (kLog2e * fmaxf(x, 0.f) + lg);
+                        const float g2 = -gate_a * (kLog2e * fmaxf(x, 0.f) + log2_1p_unit(e));
                         acc += (r < L) ? g2 : 0.f;
                         gam[i] = acc;
                     }
@@ -467,7 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             __syncthreads();
 
             // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
-            ut_inverse(tid);
+            if (warp < 8)
+                ut_inverse(tid);
+            else
+                state_pass(tmem + lane_base, warp, s_em, s_dec);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -501,8 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
-            // the state pass touches only S_acc and S_op, which these products leave alone
-            state_pass(tmem + lane_base, warp, s_em, s_dec);
             ph_v++;
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;

@@ -46,6 +46,27 @@ __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
 // one thread per row can write it without shared-memory bank conflicts.
 __device__ __forceinline__ int akk_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
 
+// log2(1 + e) for e in [0, 1], as e P(e) with P the degree-7 Chebyshev
+// interpolant of log2(1 + e) / e on [0, 1] in monomial form (coefficients from
+// gen_log2p1_poly.py; relative error of this fp32 evaluation below 4e-7).  It
+// runs on the FMA pipe, which the operand build leaves less loaded than the
+// special-function unit.
+__device__ __forceinline__ float log2_1p_unit(float e) {
+    float p = -0.0120770205f;
+    p = __fmaf_rn(p, e, 0.0627484322f);
+    p = __fmaf_rn(p, e, -0.154152006f);
+    p = __fmaf_rn(p, e, 0.255176336f);
+    p = __fmaf_rn(p, e, -0.353096366f);
+    p = __fmaf_rn(p, e, 0.480012447f);
+    p = __fmaf_rn(p, e, -0.721306741f);
+    p = __fmaf_rn(p, e, 1.44269478f);
+    return p * e;
+}
+
+// Barrier of the 256 threads (warps 0-7) that compute the UT inverse while
+// warps 8-15 run the state pass.
+__device__ __forceinline__ void inverse_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 // 2^x with the special-function unit (inputs here lie within +-116).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -109,7 +130,7 @@ __device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, fl
         }
         *reinterpret_cast<float4 *>(&P[((tid >> 6) << 8) + (r << 4) + c4]) = acc;
     }
-    __syncthreads();
+    inverse_sync();
     if (tid < 128) {
         const int t = 2 * (tid >> 6), r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
         const float *Ti = Tdiag + (t + 1) * 256 + r;   // T_{t+1,t+1}[r][s] at Ti[16 s]
@@ -132,7 +153,7 @@ __device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, fl
         }
         store_tbeta4(tb, tb16, 16 * (t + 1) + r, 16 * t + c4, tij, beta);
     }
-    __syncthreads();
+    inverse_sync();
 }
 
 // Level 2: the lower-left 32x32 block X = T[32:64, 0:32] = -T_bot (A_bl T_top),
@@ -179,7 +200,7 @@ __device__ __forceinline__ void ut_level2(const float *A, const float *T, const 
                                    : level2_y<16>(A + arow * 64, arow & 31, T, c);
         *reinterpret_cast<float4 *>(&P[r * 32 + c]) = y;
     }
-    __syncthreads();
+    inverse_sync();
     if (tid < 256) {
         // T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -192,7 +213,7 @@ __device__ __forceinline__ void ut_level2(const float *A, const float *T, const 
         const float4 x = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         store_tbeta4(tb, tb16, 32 + r, c, x, beta);
     }
-    __syncthreads();
+    inverse_sync();
 }
 
 // The four 16x16 diagonal blocks of T = (I + A)^{-1} (threads 0..63: block
