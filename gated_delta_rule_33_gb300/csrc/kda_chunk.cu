@@ -54,7 +54,7 @@ constexpr uint32_t OFF_Q = 0;            // raw q bf16 [64][128] (TMA, no swizzl
 constexpr uint32_t OFF_K = 16384;        // raw k bf16 [64][128] (TMA, no swizzle)
 constexpr uint32_t OFF_V = 32768;        // raw v bf16 [64 s][128 v] (TMA, 2 swizzled boxes)
 constexpr uint32_t OFF_QK = 49152;       // [Qt ; Kr] tf32, 128 rows (r) x 128 (channel)
-constexpr uint32_t OFF_KS = 114688;      // g fp32 64 x 128 (TMA) -> Ks tf32 -> A_kk | T fp32
+constexpr uint32_t OFF_KS = 114688;      // g fp32 64 x 128 (TMA) -> Ks tf32 -> A_kk^T | T fp32
 constexpr uint32_t OFF_KH = 147456;      // one tf32 tile, 192 rows x 64 (r), k-block stride 24576:
                                          // rows 0..127 Khat^T (channel), 128..191 T beta -> A_qk
 constexpr uint32_t OFF_TB16 = 196608;    // T beta bf16 hi 64 x 64 | lo 64 x 64
@@ -65,7 +65,7 @@ constexpr uint32_t MISC_DEC = 768;       // float[128] e^{Gam_L}
 constexpr uint32_t MISC_P = 1280;        // float[4][256] T-inverse partial products
 constexpr uint32_t MISC_PART = 5376;     // float[4][128] partial decay sums per row group
 constexpr uint32_t MISC_BNEXT = 7424;    // float[64] beta of the next chunk (cp.async)
-constexpr uint32_t MISC_DIAG = 7680;     // float[4][16][16] diagonal blocks of A_kk, column-major
+constexpr uint32_t MISC_T32 = 7680;      // float[16][16] T_32 column-major (1 KB of 4 KB used)
 constexpr uint32_t MISC_TDIAG = 11776;   // float[4][16][16] diagonal blocks of T, column-major
 constexpr uint32_t MISC_BAR = 15872;     // 4 mbarriers
 constexpr uint32_t MISC_CTRL = 15904;    // int[8]: tmem base, chain, abort, decay flag
@@ -101,46 +101,43 @@ struct Params {
     unsigned int *counter;
 };
 
-// T = (I + A)^{-1} for a 64x64 strictly lower-triangular A (fp32, akk_idx
-// layout; `Adiag` holds its four 16x16 diagonal blocks column-major), by 16x16
-// blocks.  Diagonal blocks by forward substitution in its right-looking form
-// (once x_s is final, subtract A[r][s] x_s from every later row): 15 steps of
-// independent FMAs, each step reading one block column as four broadcast
-// 16-byte loads.  Then the off-diagonal blocks in two levels: T_10 and T_32
-// (ut_level1), then the whole lower-left 32x32 block (ut_level2) -- the
-// 2x2-block inverse [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]]
-// applied at 16 and then at 32 rows.  T is row-major with stride 64 (only the
-// blocks that later steps read are written); Tdiag receives the diagonal blocks
-// column-major and Adiag, consumed by then, receives T_32 column-major.
-// Every lower block of T beta is written as soon as its block of T is final
-// (the strictly upper blocks of the T beta tiles hold zeros written once).
-// Warps 0-7 only (they meet at their own named barrier).  The operands are
-// found from the shared-memory base inside the function (a pointer argument
-// would reach it as a generic address).
-__device__ __noinline__ void ut_inverse(int tid) {
+// T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk (column-major
+// in the OFF_KS region), by 16 x 16 blocks, on warps 0-3: the diagonal blocks by
+// forward substitution (warps 0-1), then the off-diagonal blocks in two levels,
+// T_10 and T_32 (ut_level1, each warp on the blocks it solved), then the whole
+// lower-left 32 x 32 block (ut_level2) -- the 2 x 2-block inverse
+// [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]] applied at 16 and
+// then at 32 rows.  Every lower block of T beta is written as soon as its block
+// of T is final (the strictly upper blocks of the T beta tiles hold zeros
+// written once).  The operands are found from the shared-memory base inside
+// the function (a pointer argument would reach it as a generic address).
+__device__ __forceinline__ void ut_inverse(int tid) {
     uint8_t *smem = smem_base();
     uint8_t *misc = smem + OFF_MISC;
-    float *A = reinterpret_cast<float *>(smem + OFF_KS);
-    float *T = A + 64 * 64;
-    float *Adiag = reinterpret_cast<float *>(misc + MISC_DIAG);
+    const float *At = reinterpret_cast<const float *>(smem + OFF_KS);
+    float *T = reinterpret_cast<float *>(smem + OFF_KS) + 64 * 64;
     float *Tdiag = reinterpret_cast<float *>(misc + MISC_TDIAG);
+    float *T32c = reinterpret_cast<float *>(misc + MISC_T32);
     float *P = reinterpret_cast<float *>(misc + MISC_P);
     const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
-    if (tid < 64) ut_diag_solve(Adiag, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    if (tid < 64) {
+        ut_diag_solve(At, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+        __syncwarp();
+        ut_level1(At, T, Tdiag, P, T, T32c, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    }
     inverse_sync();
-    ut_level1(A, Tdiag, T, P, Adiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
-    ut_level2(A, T, Tdiag, Adiag, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    ut_level2(At, T, Tdiag, T32c, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
 }
 
 // The state pass of a chunk, S_op = tf32(e^{m_k} S[k][v]) and
-// S_acc = e^{Gam_L,k} S[k][v] in tensor memory, on warps 8-15 while warps 0-7
+// S_acc = e^{Gam_L,k} S[k][v] in tensor memory, on warps 4-15 while warps 0-3
 // compute the UT inverse: warp w covers lane quarter w % 4 and the 16-column
-// slices w / 4 - 2 + 2 n.
+// slices w / 4 - 1 + 3 n.
 __device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const float *em,
                                            const float *dec) {
     float r16[16], o16[16];
 #pragma unroll 1
-    for (int cs = (warp >> 2) - 2; cs < 8; cs += 2) {
+    for (int cs = (warp >> 2) - 1; cs < 8; cs += 3) {
         const int c0 = 16 * cs;
         tmem_ld16(tmem_lane + T_SACC + c0, r16);
         tmem_wait_ld();
@@ -215,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     // whether a TMA batch is in flight.
     uint32_t ph_qk = 0, ph_v = 0, ph_mma = 0, ph_g = 0;
     bool pend_qk = false, pend_v = false, pend_g = false;
+    // the last chunk's [S | O] product is in flight (identical in every thread)
+    bool pend_mma = false;
 
     const uint32_t a_qk = smem_addr(smem + OFF_QK);
     const uint32_t a_ks = smem_addr(smem + OFF_KS);
@@ -229,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint64_t d_tb16 = smem_desc(a_tb16, 16, 1024, kSwizzle128B);
     const uint64_t d_v = smem_desc(a_v, 8192, 1024, kSwizzle128B);  // MN-major, 64-wide M blocks
     float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
-    float *s_diag = reinterpret_cast<float *>(misc + MISC_DIAG);
 
     while (true) {
         __syncthreads();
@@ -413,6 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 khv[i] = kh;
                 krt[i] = kr;
             }
+            // The previous chunk's [S | O] product, which reads Khat^T, ran under
+            // this build; it is complete before Khat^T is overwritten.
+            if (pend_mma) {
+                cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
+                ph_mma++;
+                pend_mma = false;
+            }
             // Khat^T row ch, columns r = 16 grp .. +15: four 16-byte stores
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
@@ -449,19 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 float d16[16];
                 tmem_ld16(tmem + lane_base + T_A + 16 * grp, d16);
                 tmem_wait_ld();
-                // Ks is dead once D_A is complete; A_kk overwrites it
+                // Ks is dead once D_A is complete; A_kk (column-major) overwrites it
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int s = 16 * grp + j;
-                    const float a = (s < r) ? br * d16[j] : 0.f;
-                    Akk[akk_idx(r, s)] = a;
-                    if ((r >> 4) == grp) s_diag[grp * 256 + j * 16 + (r & 15)] = a;
+                    Akk[s * 64 + r] = (s < r) ? br * d16[j] : 0.f;
                 }
             }
             __syncthreads();
 
             // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
-            if (warp < 8)
+            if (warp < 4)
                 ut_inverse(tid);
             else
                 state_pass(tmem + lane_base, warp, s_em, s_dec);
@@ -576,13 +579,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
+            // ---- S10: the product completes under the next chunk's operand
+            // build, and this chunk's output is read out under the next MMA ----
+            pend_mma = true;
+        }
+        if (pend_mma) {
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
-
-            // ---- S10: (the output of this chunk is read out under the next MMA) ----
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
+            pend_mma = false;
         }
         if (ctrl[2] != 0) break;
         if (t1 > t0) {  // output of the last chunk

@@ -42,10 +42,6 @@ __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<float *>(base + off) = x;
 }
 
-// A_kk is stored row-major with its column index XOR-ed by (row % 32), so that
-// one thread per row can write it without shared-memory bank conflicts.
-__device__ __forceinline__ int akk_idx(int r, int s) { return r * 64 + (s ^ (r & 31)); }
-
 // log2(1 + e) for e in [0, 1], as e P(e) with P the degree-7 Chebyshev
 // interpolant of log2(1 + e) / e on [0, 1] in monomial form (coefficients from
 // gen_log2p1_poly.py; relative error of this fp32 evaluation below 4e-7).  It
@@ -63,9 +59,9 @@ __device__ __forceinline__ float log2_1p_unit(float e) {
     return p * e;
 }
 
-// Barrier of the 256 threads (warps 0-7) that compute the UT inverse while
-// warps 8-15 run the state pass.
-__device__ __forceinline__ void inverse_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier of the 128 threads (warps 0-3) that compute the UT inverse while
+// the other warps run the state pass.
+__device__ __forceinline__ void inverse_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // 2^x with the special-function unit (inputs here lie within +-116).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -107,160 +103,162 @@ __device__ __forceinline__ void store_tbeta4(uint8_t *tb, uint8_t *tb16, int r, 
     *reinterpret_cast<uint2 *>(tb16 + 8192 + sw128_offset(r, s4, 64, 2)) = lv;
 }
 
-// Level 1 of the off-diagonal blocks: T_10 and T_32 (the block sub-diagonal
-// inside each 32x32 half), T_{t+1,t} = -T_{t+1,t+1} A_{t+1,t} T_tt, t = 0, 2.
-// 64 threads per target: 16 rows x 4 column quads.  T_10 goes to T (row-major,
-// read by level 2 as part of T_top); T_32 goes column-major to T32c (read by
-// level 2 as part of T_bot, a row per thread).
-__device__ __forceinline__ void ut_level1(const float *A, const float *Tdiag, float *T, float *P,
-                                          float *T32c, uint8_t *tb, uint8_t *tb16,
-                                          const float *beta, int tid) {
-    if (tid < 128) {
-        const int t = 2 * (tid >> 6), r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        const int arow = 16 * (t + 1) + r;
-        const float *Ar = A + arow * 64;
-        const int sw = arow & 31;
-        const float *Tb = T + (16 * t) * 64 + 16 * t + c4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// ---- T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk ----
+// Layouts (fp32, shared memory):
+//   At     A column-major, At[s * 64 + r] = A[r][s] (zero for s >= r)
+//   T      row-major [64][64]; the blocks T_00, T_11, T_22 and T_10 are written
+//   Tdiag  the diagonal blocks column-major, Tdiag[b * 256 + s * 16 + r] = T_bb[r][s]
+//   T32c   T_32 column-major, T32c[s * 16 + r]
+//   P      scratch: level 1 two 16 x 16 row-major products; level 2 Y (32 x 32,
+//          row-major with the float4 group index XOR-ed by row % 8)
+// Products are register-blocked 2 rows x 4 columns per thread: per step one
+// 8-byte load of two rows of a column-major factor and one 16-byte load of a
+// row of the other feed eight FMAs.
+
+// acc{0,1} += sum over s < n of (Ac[s * ac_stride], Ac[s * ac_stride + 1]) x
+// B[s * b_stride .. + 3]: rows r0, r0 + 1 of a column-major left factor times
+// four columns of a row-major right factor.
+template <int kN>
+__device__ __forceinline__ void gemm_2x4(float4 &acc0, float4 &acc1, const float *Ac,
+                                         int ac_stride, const float *B, int b_stride) {
 #pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float a = Ar[(16 * t + s) ^ sw];
-            const float4 tv = *reinterpret_cast<const float4 *>(Tb + s * 64);
-            acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
-        }
-        *reinterpret_cast<float4 *>(&P[((tid >> 6) << 8) + (r << 4) + c4]) = acc;
+    for (int s = 0; s < kN; ++s) {
+        const float2 a = *reinterpret_cast<const float2 *>(Ac + s * ac_stride);
+        const float4 b = *reinterpret_cast<const float4 *>(B + s * b_stride);
+        acc0.x += a.x * b.x; acc0.y += a.x * b.y; acc0.z += a.x * b.z; acc0.w += a.x * b.w;
+        acc1.x += a.y * b.x; acc1.y += a.y * b.y; acc1.z += a.y * b.z; acc1.w += a.y * b.w;
     }
-    inverse_sync();
-    if (tid < 128) {
-        const int t = 2 * (tid >> 6), r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        const float *Ti = Tdiag + (t + 1) * 256 + r;   // T_{t+1,t+1}[r][s] at Ti[16 s]
-        const float *Pb = P + ((tid >> 6) << 8) + c4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float4 pv = *reinterpret_cast<const float4 *>(Pb + s * 16);
-            const float a = Ti[16 * s];   // zero above the diagonal
-            acc.x += a * pv.x; acc.y += a * pv.y; acc.z += a * pv.z; acc.w += a * pv.w;
-        }
-        const float4 tij = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        if (t == 0) {
-            *reinterpret_cast<float4 *>(&T[(16 + r) * 64 + c4]) = tij;
-        } else {
-            T32c[c4 * 16 + r] = tij.x;
-            T32c[(c4 + 1) * 16 + r] = tij.y;
-            T32c[(c4 + 2) * 16 + r] = tij.z;
-            T32c[(c4 + 3) * 16 + r] = tij.w;
-        }
-        store_tbeta4(tb, tb16, 16 * (t + 1) + r, 16 * t + c4, tij, beta);
-    }
-    inverse_sync();
 }
 
-// Level 2: the lower-left 32x32 block X = T[32:64, 0:32] = -T_bot (A_bl T_top),
-// with T_top = T[0:32, 0:32], T_bot = T[32:64, 32:64] (both block lower
-// triangular, complete after level 1) and A_bl = A[32:64, 0:32].
-// 256 threads, 32 rows x 8 column quads; every warp's rows and columns fall in
-// one 16-block, so the triangular bounds are compile-time per branch.
-// Y = A_bl T_top goes through P.  T_bot is read from its column-major blocks
-// (T_22 and T_33 in Tdiag, T_32 in T32c): the eight rows a warp covers then
-// fall in eight banks (a row-major read with stride 64 would hit one).
-template <int S0>
-__device__ __forceinline__ float4 level2_y(const float *Ar, int sw, const float *T, int c) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// Y index of (row r, columns c .. c + 3), c a multiple of 4
+__device__ __forceinline__ int y_idx(int r, int c) { return r * 32 + (((c >> 2) ^ (r & 7)) << 2); }
+
+// The four 16x16 diagonal blocks (warps 0-1: block tid / 16, column j = tid % 16)
+// by forward substitution in its right-looking form (once x_s is final,
+// subtract A[r][s] x_s from every later row): 15 steps of independent FMAs,
+// each reading one block column of At as four 16-byte loads, the next column
+// loaded while the current one is applied.  Writes T (row-major), Tdiag and
+// the T beta operand tiles.
+__device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *Tdiag, uint8_t *tb,
+                                              uint8_t *tb16, const float *beta, int tid) {
+    const int bb = tid >> 4, j = tid & 15, base = bb * 16;
+    const float *Ab = At + base * 64 + base;   // Ab[s * 64 + r] = A_bb[r][s]
+    float x[16];
 #pragma unroll
-    for (int s = S0; s < 32; ++s) {
-        const float a = Ar[s ^ sw];
-        const float4 tv = *reinterpret_cast<const float4 *>(&T[s * 64 + c]);
-        acc.x += a * tv.x; acc.y += a * tv.y; acc.z += a * tv.z; acc.w += a * tv.w;
+    for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+    float4 c[4], n[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const float4 *>(Ab + 4 * q);
+#pragma unroll
+    for (int s = 0; s < 15; ++s) {
+        if (s < 14) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                n[q] = *reinterpret_cast<const float4 *>(Ab + (s + 1) * 64 + 4 * q);
+        }
+        const float col[16] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w,
+                               c[2].x, c[2].y, c[2].z, c[2].w, c[3].x, c[3].y, c[3].z, c[3].w};
+        const float xs = x[s];
+#pragma unroll
+        for (int r = s + 1; r < 16; ++r) x[r] -= col[r] * xs;
+        if (s < 14) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) c[q] = n[q];
+        }
     }
-    return acc;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) T[(base + r) * 64 + base + j] = x[r];
+    float *Td = Tdiag + bb * 256 + j * 16;  // column j of T_bb
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+        *reinterpret_cast<float4 *>(Td + 4 * q4) =
+            make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+    // T beta of the diagonal block, column j (16 rows)
+    const float bj = beta[base + j];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float xb = x[r] * bj;
+        st_f32(tb, sw128_offset(kTbRow0 + base + r, base + j, kTbRows, 4), to_tf32(xb));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16 *>(tb16 + sw128_offset(base + r, base + j, 64, 2)) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(tb16 + 8192 + sw128_offset(base + r, base + j, 64, 2)) = lo;
+    }
 }
 
-// acc += sum over 16 s of Tc[16 s] * P[s0 + s][c .. c + 3] (Tc: one row of a
-// column-major 16x16 block)
-__device__ __forceinline__ void level2_x16(float4 &acc, const float *Tc, const float *P, int s0,
-                                           int c) {
+// Level 1 (warps 0-1, warp t / 2 for target t = 0, 2; it solved T_tt and
+// T_{t+1,t+1} itself): T_{t+1,t} = -T_{t+1,t+1} (A_{t+1,t} T_tt).  Lane l owns
+// rows r0 = 2 (l / 4), r0 + 1 and columns c0 = 4 (l % 4) .. + 3 of the block.
+// T_10 goes to T (row-major, part of T_top in level 2), T_32 to T32c.
+__device__ __forceinline__ void ut_level1(const float *At, const float *T, const float *Tdiag,
+                                          float *P, float *Tw, float *T32c, uint8_t *tb,
+                                          uint8_t *tb16, const float *beta, int tid) {
+    const int t = 2 * (tid >> 5), l = tid & 31, r0 = 2 * (l >> 2), c0 = 4 * (l & 3);
+    float *Pt = P + (t >> 1) * 256;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    // P_t = A_{t+1,t} T_tt (T_tt is zero above its diagonal)
+    gemm_2x4<16>(a0, a1, At + (16 * t) * 64 + 16 * (t + 1) + r0, 64, T + (16 * t) * 64 + 16 * t + c0, 64);
+    *reinterpret_cast<float4 *>(Pt + r0 * 16 + c0) = a0;
+    *reinterpret_cast<float4 *>(Pt + (r0 + 1) * 16 + c0) = a1;
+    __syncwarp();
+    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+    gemm_2x4<16>(b0, b1, Tdiag + (t + 1) * 256 + r0, 16, Pt + c0, 16);
+    const float4 x0 = make_float4(-b0.x, -b0.y, -b0.z, -b0.w);
+    const float4 x1 = make_float4(-b1.x, -b1.y, -b1.z, -b1.w);
+    if (t == 0) {
+        *reinterpret_cast<float4 *>(Tw + (16 + r0) * 64 + c0) = x0;
+        *reinterpret_cast<float4 *>(Tw + (17 + r0) * 64 + c0) = x1;
+    } else {
+        *reinterpret_cast<float2 *>(T32c + (c0 + 0) * 16 + r0) = make_float2(x0.x, x1.x);
+        *reinterpret_cast<float2 *>(T32c + (c0 + 1) * 16 + r0) = make_float2(x0.y, x1.y);
+        *reinterpret_cast<float2 *>(T32c + (c0 + 2) * 16 + r0) = make_float2(x0.z, x1.z);
+        *reinterpret_cast<float2 *>(T32c + (c0 + 3) * 16 + r0) = make_float2(x0.w, x1.w);
+    }
+    store_tbeta4(tb, tb16, 16 * (t + 1) + r0, 16 * t + c0, x0, beta);
+    store_tbeta4(tb, tb16, 16 * (t + 1) + r0 + 1, 16 * t + c0, x1, beta);
+}
+
+// Level 2 (warps 0-3): the lower-left 32x32 block X = T[32:64, 0:32] =
+// -T_bot (A_bl T_top), T_top = T[0:32, 0:32] and T_bot = T[32:64, 32:64] block
+// lower triangular (complete after level 1), A_bl = A[32:64, 0:32].  Warp w
+// owns rows 16 (w % 2) .. + 15 and columns 16 (w / 2) .. + 15 of Y and X, so
+// every triangular bound is warp-uniform; lane l owns rows r0 = 16 (w % 2) +
+// 2 (l / 4), r0 + 1 and columns c0 = 16 (w / 2) + 4 (l % 4) .. + 3.
+__device__ __forceinline__ void ut_level2(const float *At, const float *T, const float *Tdiag,
+                                          const float *T32c, float *Y, uint8_t *tb,
+                                          uint8_t *tb16, const float *beta, int tid) {
+    const int w = tid >> 5, l = tid & 31, rh = w & 1, cb = w >> 1;
+    const int r0 = 16 * rh + 2 * (l >> 2), c0 = 16 * cb + 4 * (l & 3);
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    // Y = A_bl T_top: T_top[s][c] is zero for s < 16 * block(c)
+    if (cb == 0)
+        gemm_2x4<32>(a0, a1, At + 32 + r0, 64, T + c0, 64);
+    else
+        gemm_2x4<16>(a0, a1, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
+    *reinterpret_cast<float4 *>(Y + y_idx(r0, c0)) = a0;
+    *reinterpret_cast<float4 *>(Y + y_idx(r0 + 1, c0)) = a1;
+    inverse_sync();
+    // X = -T_bot Y: T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
+    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
-        const float a = Tc[16 * s];
-        const float4 yv = *reinterpret_cast<const float4 *>(&P[(s0 + s) * 32 + c]);
-        acc.x += a * yv.x; acc.y += a * yv.y; acc.z += a * yv.z; acc.w += a * yv.w;
+        const float2 a = rh == 0 ? *reinterpret_cast<const float2 *>(Tdiag + 2 * 256 + s * 16 + r0)
+                                 : *reinterpret_cast<const float2 *>(T32c + s * 16 + r0 - 16);
+        const float4 y = *reinterpret_cast<const float4 *>(Y + y_idx(s, c0));
+        b0.x += a.x * y.x; b0.y += a.x * y.y; b0.z += a.x * y.z; b0.w += a.x * y.w;
+        b1.x += a.y * y.x; b1.y += a.y * y.y; b1.z += a.y * y.z; b1.w += a.y * y.w;
     }
-}
-
-__device__ __forceinline__ void ut_level2(const float *A, const float *T, const float *Tdiag,
-                                          const float *T32c, float *P, uint8_t *tb,
-                                          uint8_t *tb16, const float *beta, int tid) {
-    // task: column block cb = tid / 128, row r = (tid / 4) % 32, quad q = tid % 4
-    const int cb = tid >> 7, r = (tid >> 2) & 31, c = 16 * cb + 4 * (tid & 3);
-    if (tid < 256) {
-        const int arow = 32 + r;
-        // T_top[s][c] is zero for s < 16 * block(c)
-        const float4 y = (cb == 0) ? level2_y<0>(A + arow * 64, arow & 31, T, c)
-                                   : level2_y<16>(A + arow * 64, arow & 31, T, c);
-        *reinterpret_cast<float4 *>(&P[r * 32 + c]) = y;
+    if (rh == 1) {
+#pragma unroll
+        for (int s = 16; s < 32; ++s) {
+            const float2 a = *reinterpret_cast<const float2 *>(Tdiag + 3 * 256 + (s - 16) * 16 + r0 - 16);
+            const float4 y = *reinterpret_cast<const float4 *>(Y + y_idx(s, c0));
+            b0.x += a.x * y.x; b0.y += a.x * y.y; b0.z += a.x * y.z; b0.w += a.x * y.w;
+            b1.x += a.y * y.x; b1.y += a.y * y.y; b1.z += a.y * y.z; b1.w += a.y * y.w;
+        }
     }
-    inverse_sync();
-    if (tid < 256) {
-        // T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < 16) {
-            level2_x16(acc, Tdiag + 2 * 256 + r, P, 0, c);
-        } else {
-            level2_x16(acc, T32c + (r - 16), P, 0, c);
-            level2_x16(acc, Tdiag + 3 * 256 + (r - 16), P, 16, c);
-        }
-        const float4 x = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-        store_tbeta4(tb, tb16, 32 + r, c, x, beta);
-    }
-    inverse_sync();
-}
-
-// The four 16x16 diagonal blocks of T = (I + A)^{-1} (threads 0..63: block
-// tid / 16, column tid % 16) by forward substitution in its right-looking form
-// (once x_s is final, subtract A[r][s] x_s from every later row): 15 steps of
-// independent FMAs, each step reading one block column of `Adiag` (column-major
-// 16x16 blocks) as four broadcast 16-byte loads.  Writes the blocks into T
-// (row-major, stride 64), column-major into Tdiag, and T beta into the tf32 and
-// bf16 high/low operand tiles.
-__device__ __forceinline__ void ut_diag_solve(const float *Adiag, float *T, float *Tdiag,
-                                              uint8_t *tb, uint8_t *tb16, const float *beta,
-                                              int tid) {
-        const int bb = tid >> 4, j = tid & 15, base = bb * 16;
-        const float *Ab = Adiag + bb * 256;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
-#pragma unroll
-        for (int s = 0; s < 15; ++s) {
-            float col[16];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 v = *reinterpret_cast<const float4 *>(Ab + s * 16 + 4 * q4);
-                col[4 * q4] = v.x; col[4 * q4 + 1] = v.y; col[4 * q4 + 2] = v.z; col[4 * q4 + 3] = v.w;
-            }
-            const float xs = x[s];
-#pragma unroll
-            for (int r = s + 1; r < 16; ++r) x[r] -= col[r] * xs;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) T[(base + r) * 64 + base + j] = x[r];
-        float *Td = Tdiag + bb * 256 + j * 16;  // column j of T_bb
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<float4 *>(Td + 4 * q4) =
-                make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
-        // T beta of the diagonal block, column j (16 rows)
-        const float bj = beta[base + j];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float xb = x[r] * bj;
-            st_f32(tb, sw128_offset(kTbRow0 + base + r, base + j, kTbRows, 4), to_tf32(xb));
-            const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
-            *reinterpret_cast<__nv_bfloat16 *>(tb16 + sw128_offset(base + r, base + j, 64, 2)) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(tb16 + 8192 + sw128_offset(base + r, base + j, 64, 2)) = lo;
-        }
+    store_tbeta4(tb, tb16, 32 + r0, c0, make_float4(-b0.x, -b0.y, -b0.z, -b0.w), beta);
+    store_tbeta4(tb, tb16, 33 + r0, c0, make_float4(-b1.x, -b1.y, -b1.z, -b1.w), beta);
 }
 
 // ---- host: TMA tensor maps -------------------------------------------------------------
