@@ -142,9 +142,14 @@ __device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const f
         tmem_ld16(tmem_lane + T_SACC + c0, r16);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            o16[j] = to_tf32(r16[j] * em[c0 + j]);
-            r16[j] = r16[j] * dec[c0 + j];
+        for (int j = 0; j < 16; j += 2) {  // packed pairs of columns
+            const uint64_t rr = f2(r16[j], r16[j + 1]);
+            const float2 o = f2_split(f2_mul(rr, *reinterpret_cast<const uint64_t *>(em + c0 + j)));
+            const float2 d = f2_split(f2_mul(rr, *reinterpret_cast<const uint64_t *>(dec + c0 + j)));
+            o16[j] = to_tf32(o.x);
+            o16[j + 1] = to_tf32(o.y);
+            r16[j] = d.x;
+            r16[j + 1] = d.y;
         }
         tmem_st16(tmem_lane + T_SOP + c0, o16);
         tmem_st16(tmem_lane + T_SACC + c0, r16);
@@ -352,14 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                     // log2(e) g = -exp(A_log) (log2(e) max(x, 0) + log2(1 + 2^{-log2(e)|x|})),
                     // x = f + dt_bias
                     const __nv_bfloat16 *ft = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_KS);
+                    const uint64_t dt2 = f2(gate_dt, gate_dt), na2 = f2(-gate_a, -gate_a);
+                    const uint64_t l2e2 = f2(kLog2e, kLog2e);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 16; i += 2) {  // rows r, r + 1 as packed pairs
                         const int r = 16 * grp + i;
-                        const float x = __bfloat162float(ft[r * kD + ch]) + gate_dt;
-                        const float e = fast_exp2(-kLog2e * fabsf(x));
-                        const float g2 = -gate_a * (kLog2e * fmaxf(x, 0.f) + log2_1p_unit(e));
-                        acc += (r < L) ? g2 : 0.f;
+                        const float2 x = f2_split(f2_add(f2(__bfloat162float(ft[r * kD + ch]),
+                                                            __bfloat162float(ft[(r + 1) * kD + ch])),
+                                                         dt2));
+                        const uint64_t e = f2(fast_exp2(-kLog2e * fabsf(x.x)), fast_exp2(-kLog2e * fabsf(x.y)));
+                        const float2 g2 = f2_split(f2_mul(
+                            na2, f2_fma(l2e2, f2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log2_1p_unit2(e))));
+                        acc += (r < L) ? g2.x : 0.f;
                         gam[i] = acc;
+                        acc += (r + 1 < L) ? g2.y : 0.f;
+                        gam[i + 1] = acc;
                     }
                 } else {
                     const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
@@ -390,26 +402,34 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             const float ekh = fast_exp2(gam_l - m);
             const float qscale = p.scale;
             float krt[16], khv[16];
+            const uint64_t m2 = f2(m, m), pre2 = f2(prefix, prefix), qs2 = f2(qscale, qscale);
+            const uint64_t ekh2 = f2(ekh, ekh);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 16; i += 2) {  // rows r, r + 1 as packed pairs
                 const int r = 16 * grp + i;
-                float qt = 0.f, kr = 0.f, ks = 0.f, kh = 0.f;
-                if (r < L) {
-                    const float gr = prefix + gam[i];
-                    const float e_up = fast_exp2(gr - m);   // e^{Gam_r - m}
-                    const float e_dn = fast_exp2(m - gr);   // e^{m - Gam_r}
-                    const float qv = bf(smem + OFF_Q, (r * kD + ch) * 2);
-                    const float kv = bf(smem + OFF_K, (r * kD + ch) * 2);
-                    qt = to_tf32(qscale * qv * e_up);
-                    kr = to_tf32(kv * e_up);
-                    ks = to_tf32(kv * e_dn);
-                    kh = to_tf32(kv * (e_dn * ekh));
-                }
-                st_f32(smem + OFF_QK, sw128_offset(r, ch, 128, 4), qt);
-                st_f32(smem + OFF_QK, sw128_offset(r + 64, ch, 128, 4), kr);
-                st_f32(smem + OFF_KS, sw128_offset(r, ch, 64, 4), ks);
-                khv[i] = kh;
-                krt[i] = kr;
+                const bool v0 = r < L, v1 = r + 1 < L;  // rows past the sequence stay zero
+                const uint64_t gr = f2_add(pre2, f2(gam[i], gam[i + 1]));
+                const float2 du = f2_split(f2_sub(gr, m2)), dd = f2_split(f2_sub(m2, gr));
+                const uint64_t e_up = f2(fast_exp2(du.x), fast_exp2(du.y));  // e^{Gam_r - m}
+                const uint64_t e_dn = f2(fast_exp2(dd.x), fast_exp2(dd.y));  // e^{m - Gam_r}
+                const uint64_t qv = f2(v0 ? bf(smem + OFF_Q, (r * kD + ch) * 2) : 0.f,
+                                       v1 ? bf(smem + OFF_Q, ((r + 1) * kD + ch) * 2) : 0.f);
+                const uint64_t kv = f2(v0 ? bf(smem + OFF_K, (r * kD + ch) * 2) : 0.f,
+                                       v1 ? bf(smem + OFF_K, ((r + 1) * kD + ch) * 2) : 0.f);
+                const float2 qt = f2_split(f2_mul(f2_mul(qs2, qv), e_up));
+                const float2 kr = f2_split(f2_mul(kv, e_up));
+                const float2 ks = f2_split(f2_mul(kv, e_dn));
+                const float2 kh = f2_split(f2_mul(kv, f2_mul(e_dn, ekh2)));
+                st_f32(smem + OFF_QK, sw128_offset(r, ch, 128, 4), to_tf32(qt.x));
+                st_f32(smem + OFF_QK, sw128_offset(r + 1, ch, 128, 4), to_tf32(qt.y));
+                krt[i] = to_tf32(kr.x);
+                krt[i + 1] = to_tf32(kr.y);
+                st_f32(smem + OFF_QK, sw128_offset(r + 64, ch, 128, 4), krt[i]);
+                st_f32(smem + OFF_QK, sw128_offset(r + 65, ch, 128, 4), krt[i + 1]);
+                st_f32(smem + OFF_KS, sw128_offset(r, ch, 64, 4), to_tf32(ks.x));
+                st_f32(smem + OFF_KS, sw128_offset(r + 1, ch, 64, 4), to_tf32(ks.y));
+                khv[i] = to_tf32(kh.x);
+                khv[i + 1] = to_tf32(kh.y);
             }
             // The previous chunk's [S | O] product, which reads Khat^T, ran under
             // this build; it is complete before Khat^T is overwritten.

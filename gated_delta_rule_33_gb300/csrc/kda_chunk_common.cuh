@@ -42,6 +42,40 @@ __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<float *>(base + off) = x;
 }
 
+// Packed pairs of binary32 values: one instruction applies the IEEE
+// operation (round to nearest) to both halves, with the same results as two
+// scalar instructions.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // log2(1 + e) for e in [0, 1], as e P(e) with P the degree-7 Chebyshev
 // interpolant of log2(1 + e) / e on [0, 1] in monomial form (coefficients from
 // gen_log2p1_poly.py; relative error of this fp32 evaluation below 4e-7).  It
@@ -57,6 +91,19 @@ __device__ __forceinline__ float log2_1p_unit(float e) {
     p = __fmaf_rn(p, e, -0.721306741f);
     p = __fmaf_rn(p, e, 1.44269478f);
     return p * e;
+}
+
+// log2_1p_unit on a packed pair (the same operations, two lanes at a time)
+__device__ __forceinline__ uint64_t log2_1p_unit2(uint64_t e) {
+    uint64_t p = f2(-0.0120770205f, -0.0120770205f);
+    p = f2_fma(p, e, f2(0.0627484322f, 0.0627484322f));
+    p = f2_fma(p, e, f2(-0.154152006f, -0.154152006f));
+    p = f2_fma(p, e, f2(0.255176336f, 0.255176336f));
+    p = f2_fma(p, e, f2(-0.353096366f, -0.353096366f));
+    p = f2_fma(p, e, f2(0.480012447f, 0.480012447f));
+    p = f2_fma(p, e, f2(-0.721306741f, -0.721306741f));
+    p = f2_fma(p, e, f2(1.44269478f, 1.44269478f));
+    return f2_mul(p, e);
 }
 
 // Barrier of the 128 threads (warps 0-3) that compute the UT inverse while
