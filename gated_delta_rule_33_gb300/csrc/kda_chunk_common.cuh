@@ -165,16 +165,40 @@ __device__ __forceinline__ void store_tbeta4(uint8_t *tb, uint8_t *tb16, int r, 
 // acc{0,1} += sum over s < n of (Ac[s * ac_stride], Ac[s * ac_stride + 1]) x
 // B[s * b_stride .. + 3]: rows r0, r0 + 1 of a column-major left factor times
 // four columns of a row-major right factor.
-template <int kN>
-__device__ __forceinline__ void gemm_2x4(float4 &acc0, float4 &acc1, const float *Ac,
-                                         int ac_stride, const float *B, int b_stride) {
+// Accumulators as packed pairs: {acc0.xy, acc0.zw, acc1.xy, acc1.zw}.
+struct Acc2x4 {
+    uint64_t v[4];
+    __device__ __forceinline__ Acc2x4() {
 #pragma unroll
-    for (int s = 0; s < kN; ++s) {
-        const float2 a = *reinterpret_cast<const float2 *>(Ac + s * ac_stride);
-        const float4 b = *reinterpret_cast<const float4 *>(B + s * b_stride);
-        acc0.x += a.x * b.x; acc0.y += a.x * b.y; acc0.z += a.x * b.z; acc0.w += a.x * b.w;
-        acc1.x += a.y * b.x; acc1.y += a.y * b.y; acc1.z += a.y * b.z; acc1.w += a.y * b.w;
+        for (int i = 0; i < 4; ++i) v[i] = 0ull;  // +0.0f in both halves
     }
+    // rows (a.x, a.y) times the four columns b
+    __device__ __forceinline__ void step(float2 a, float4 b) {
+        const uint64_t ax = f2(a.x, a.x), ay = f2(a.y, a.y);
+        const uint64_t b01 = f2(b.x, b.y), b23 = f2(b.z, b.w);
+        v[0] = f2_fma(ax, b01, v[0]);
+        v[1] = f2_fma(ax, b23, v[1]);
+        v[2] = f2_fma(ay, b01, v[2]);
+        v[3] = f2_fma(ay, b23, v[3]);
+    }
+    // row 0 or 1, negated, as a float4
+    __device__ __forceinline__ float4 neg_row(int i) const {
+        const float2 lo = f2_split(v[2 * i]), hi = f2_split(v[2 * i + 1]);
+        return make_float4(-lo.x, -lo.y, -hi.x, -hi.y);
+    }
+    __device__ __forceinline__ float4 row(int i) const {
+        const float2 lo = f2_split(v[2 * i]), hi = f2_split(v[2 * i + 1]);
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+};
+
+template <int kN>
+__device__ __forceinline__ void gemm_2x4(Acc2x4 &acc, const float *Ac, int ac_stride,
+                                         const float *B, int b_stride) {
+#pragma unroll
+    for (int s = 0; s < kN; ++s)
+        acc.step(*reinterpret_cast<const float2 *>(Ac + s * ac_stride),
+                 *reinterpret_cast<const float4 *>(B + s * b_stride));
 }
 
 // Y index of (row r, columns c .. c + 3), c a multiple of 4
@@ -190,9 +214,11 @@ __device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *
                                               uint8_t *tb16, const float *beta, int tid) {
     const int bb = tid >> 4, j = tid & 15, base = bb * 16;
     const float *Ab = At + base * 64 + base;   // Ab[s * 64 + r] = A_bb[r][s]
-    float x[16];
+    // x as packed row pairs; a step updates whole pairs from the one holding
+    // row s + 1 on (when that is row s's pair, row s gets A_bb[s][s] x_s = 0)
+    uint64_t xp[8];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+    for (int q = 0; q < 8; ++q) xp[q] = f2((2 * q == j) ? 1.f : 0.f, (2 * q + 1 == j) ? 1.f : 0.f);
     float4 c[4], n[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const float4 *>(Ab + 4 * q);
@@ -203,15 +229,25 @@ __device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *
             for (int q = 0; q < 4; ++q)
                 n[q] = *reinterpret_cast<const float4 *>(Ab + (s + 1) * 64 + 4 * q);
         }
-        const float col[16] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w,
-                               c[2].x, c[2].y, c[2].z, c[2].w, c[3].x, c[3].y, c[3].z, c[3].w};
-        const float xs = x[s];
+        const uint64_t colp[8] = {f2(c[0].x, c[0].y), f2(c[0].z, c[0].w), f2(c[1].x, c[1].y),
+                                  f2(c[1].z, c[1].w), f2(c[2].x, c[2].y), f2(c[2].z, c[2].w),
+                                  f2(c[3].x, c[3].y), f2(c[3].z, c[3].w)};
+        const float2 ps = f2_split(xp[s >> 1]);
+        const float nxs = -((s & 1) ? ps.y : ps.x);
+        const uint64_t nx2 = f2(nxs, nxs);
 #pragma unroll
-        for (int r = s + 1; r < 16; ++r) x[r] -= col[r] * xs;
+        for (int q = (s + 1) >> 1; q < 8; ++q) xp[q] = f2_fma(colp[q], nx2, xp[q]);
         if (s < 14) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) c[q] = n[q];
         }
+    }
+    float x[16];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float2 v = f2_split(xp[q]);
+        x[2 * q] = v.x;
+        x[2 * q + 1] = v.y;
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) T[(base + r) * 64 + base + j] = x[r];
@@ -242,16 +278,15 @@ __device__ __forceinline__ void ut_level1(const float *At, const float *T, const
                                           uint8_t *tb16, const float *beta, int tid) {
     const int t = 2 * (tid >> 5), l = tid & 31, r0 = 2 * (l >> 2), c0 = 4 * (l & 3);
     float *Pt = P + (t >> 1) * 256;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    Acc2x4 a;
     // P_t = A_{t+1,t} T_tt (T_tt is zero above its diagonal)
-    gemm_2x4<16>(a0, a1, At + (16 * t) * 64 + 16 * (t + 1) + r0, 64, T + (16 * t) * 64 + 16 * t + c0, 64);
-    *reinterpret_cast<float4 *>(Pt + r0 * 16 + c0) = a0;
-    *reinterpret_cast<float4 *>(Pt + (r0 + 1) * 16 + c0) = a1;
+    gemm_2x4<16>(a, At + (16 * t) * 64 + 16 * (t + 1) + r0, 64, T + (16 * t) * 64 + 16 * t + c0, 64);
+    *reinterpret_cast<float4 *>(Pt + r0 * 16 + c0) = a.row(0);
+    *reinterpret_cast<float4 *>(Pt + (r0 + 1) * 16 + c0) = a.row(1);
     __syncwarp();
-    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
-    gemm_2x4<16>(b0, b1, Tdiag + (t + 1) * 256 + r0, 16, Pt + c0, 16);
-    const float4 x0 = make_float4(-b0.x, -b0.y, -b0.z, -b0.w);
-    const float4 x1 = make_float4(-b1.x, -b1.y, -b1.z, -b1.w);
+    Acc2x4 b;
+    gemm_2x4<16>(b, Tdiag + (t + 1) * 256 + r0, 16, Pt + c0, 16);
+    const float4 x0 = b.neg_row(0), x1 = b.neg_row(1);
     if (t == 0) {
         *reinterpret_cast<float4 *>(Tw + (16 + r0) * 64 + c0) = x0;
         *reinterpret_cast<float4 *>(Tw + (17 + r0) * 64 + c0) = x1;
@@ -276,36 +311,30 @@ __device__ __forceinline__ void ut_level2(const float *At, const float *T, const
                                           uint8_t *tb16, const float *beta, int tid) {
     const int w = tid >> 5, l = tid & 31, rh = w & 1, cb = w >> 1;
     const int r0 = 16 * rh + 2 * (l >> 2), c0 = 16 * cb + 4 * (l & 3);
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    Acc2x4 a;
     // Y = A_bl T_top: T_top[s][c] is zero for s < 16 * block(c)
     if (cb == 0)
-        gemm_2x4<32>(a0, a1, At + 32 + r0, 64, T + c0, 64);
+        gemm_2x4<32>(a, At + 32 + r0, 64, T + c0, 64);
     else
-        gemm_2x4<16>(a0, a1, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
-    *reinterpret_cast<float4 *>(Y + y_idx(r0, c0)) = a0;
-    *reinterpret_cast<float4 *>(Y + y_idx(r0 + 1, c0)) = a1;
+        gemm_2x4<16>(a, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
+    *reinterpret_cast<float4 *>(Y + y_idx(r0, c0)) = a.row(0);
+    *reinterpret_cast<float4 *>(Y + y_idx(r0 + 1, c0)) = a.row(1);
     inverse_sync();
     // X = -T_bot Y: T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
-    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+    Acc2x4 b;
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        const float2 a = rh == 0 ? *reinterpret_cast<const float2 *>(Tdiag + 2 * 256 + s * 16 + r0)
-                                 : *reinterpret_cast<const float2 *>(T32c + s * 16 + r0 - 16);
-        const float4 y = *reinterpret_cast<const float4 *>(Y + y_idx(s, c0));
-        b0.x += a.x * y.x; b0.y += a.x * y.y; b0.z += a.x * y.z; b0.w += a.x * y.w;
-        b1.x += a.y * y.x; b1.y += a.y * y.y; b1.z += a.y * y.z; b1.w += a.y * y.w;
-    }
+    for (int s = 0; s < 16; ++s)
+        b.step(rh == 0 ? *reinterpret_cast<const float2 *>(Tdiag + 2 * 256 + s * 16 + r0)
+                       : *reinterpret_cast<const float2 *>(T32c + s * 16 + r0 - 16),
+               *reinterpret_cast<const float4 *>(Y + y_idx(s, c0)));
     if (rh == 1) {
 #pragma unroll
-        for (int s = 16; s < 32; ++s) {
-            const float2 a = *reinterpret_cast<const float2 *>(Tdiag + 3 * 256 + (s - 16) * 16 + r0 - 16);
-            const float4 y = *reinterpret_cast<const float4 *>(Y + y_idx(s, c0));
-            b0.x += a.x * y.x; b0.y += a.x * y.y; b0.z += a.x * y.z; b0.w += a.x * y.w;
-            b1.x += a.y * y.x; b1.y += a.y * y.y; b1.z += a.y * y.z; b1.w += a.y * y.w;
-        }
+        for (int s = 16; s < 32; ++s)
+            b.step(*reinterpret_cast<const float2 *>(Tdiag + 3 * 256 + (s - 16) * 16 + r0 - 16),
+                   *reinterpret_cast<const float4 *>(Y + y_idx(s, c0)));
     }
-    store_tbeta4(tb, tb16, 32 + r0, c0, make_float4(-b0.x, -b0.y, -b0.z, -b0.w), beta);
-    store_tbeta4(tb, tb16, 33 + r0, c0, make_float4(-b1.x, -b1.y, -b1.z, -b1.w), beta);
+    store_tbeta4(tb, tb16, 32 + r0, c0, b.neg_row(0), beta);
+    store_tbeta4(tb, tb16, 33 + r0, c0, b.neg_row(1), beta);
 }
 
 // ---- host: TMA tensor maps -------------------------------------------------------------
