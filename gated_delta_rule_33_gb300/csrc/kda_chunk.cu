@@ -109,8 +109,11 @@ struct Params {
 // [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]] applied at 16 and
 // then at 32 rows.  Every lower block of T beta is written as soon as its block
 // of T is final (the strictly upper blocks of the T beta tiles hold zeros
-// written once).  The operands are found from the shared-memory base inside
-// the function (a pointer argument would reach it as a generic address).
+// written once), and the warp that issues the W' and U-tilde products is told
+// when each column block of T beta is complete: block 3 after the diagonal
+// solve, block 2 after level 1, blocks 0-1 after level 2.  The operands are
+// found from the shared-memory base inside the function (a pointer argument
+// would reach it as a generic address).
 __device__ __forceinline__ void ut_inverse(int tid) {
     uint8_t *smem = smem_base();
     uint8_t *misc = smem + OFF_MISC;
@@ -122,22 +125,28 @@ __device__ __forceinline__ void ut_inverse(int tid) {
     const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
     if (tid < 64) {
         ut_diag_solve(At, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+        fence_proxy_async_smem();
+        named_arrive(kBarDiag, 96);
         __syncwarp();
         ut_level1(At, T, Tdiag, P, T, T32c, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+        fence_proxy_async_smem();
+        named_arrive(kBarLevel1, 96);
     }
     inverse_sync();
     ut_level2(At, T, Tdiag, T32c, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    fence_proxy_async_smem();
+    named_arrive(kBarLevel2, 160);
 }
 
 // The state pass of a chunk, S_op = tf32(e^{m_k} S[k][v]) and
-// S_acc = e^{Gam_L,k} S[k][v] in tensor memory, on warps 4-15 while warps 0-3
+// S_acc = e^{Gam_L,k} S[k][v] in tensor memory, on warps 8-15 while warps 0-3
 // compute the UT inverse: warp w covers lane quarter w % 4 and the 16-column
-// slices w / 4 - 1 + 3 n.
+// slices w / 4 - 2 + 2 n.
 __device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const float *em,
                                            const float *dec) {
     float r16[16], o16[16];
 #pragma unroll 1
-    for (int cs = (warp >> 2) - 1; cs < 8; cs += 3) {
+    for (int cs = (warp >> 2) - 2; cs < 8; cs += 2) {
         const int c0 = 16 * cs;
         tmem_ld16(tmem_lane + T_SACC + c0, r16);
         tmem_wait_ld();
@@ -179,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     float *s_bnext = reinterpret_cast<float *>(misc + MISC_BNEXT);
     int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [3] decay
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, grp = warp >> 2;
     const int ch = quarter * 32 + (tid & 31);  // channel / tensor-memory lane
     const int H = p.H;
@@ -483,48 +492,71 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
             __syncthreads();
 
-            // ---- S4: UT inverse; T beta in tf32 and as bf16 high + low ----
-            if (warp < 4)
+            // ---- S4: UT inverse (warps 0-3); W'^T = Kr^T (T beta)^T and
+            // Ut^T = V^T (T beta)^T issued by warp 4 one column block of T beta
+            // (one K range of the products) at a time as the inverse completes
+            // it; the state pass (warps 8-15) ----
+            if (warp < 4) {
                 ut_inverse(tid);
-            else
+            } else if (warp == 4) {
+                const uint32_t idw = instr_desc(128, 64, kFmtTF32, 0, 0);
+                const uint32_t idu = instr_desc(128, 64, kFmtBF16, 1, 0);
+                bool v_ok = true;
+                // W' over tf32 k-steps kk (8 columns of T beta each), U-tilde over
+                // bf16 k-steps ku (16 columns) for the high and low halves
+                auto issue_w = [&](int kk, bool first) {
+                    const uint64_t bd = (d_kh + static_cast<uint64_t>(((kk >> 2) * 24576 + 16384 + (kk & 3) * 32) >> 4));
+                    mma_tf32_ts_w(tmem + T_O, tmem + T_W + kk * 8, bd, idw, first ? 0u : 1u);
+                };
+                auto issue_u = [&](int ku, bool first) {
+                    const uint64_t ad = (d_v + static_cast<uint64_t>((ku * 2048) >> 4));
+                    mma_f16_ss_w(tmem + T_U, ad, d_tb16 + static_cast<uint64_t>((ku * 32) >> 4), idu,
+                                 first ? 0u : 1u);
+                    mma_f16_ss_w(tmem + T_U, ad, d_tb16 + static_cast<uint64_t>((8192 + ku * 32) >> 4),
+                                 idu, 1u);
+                };
+                named_sync(kBarDiag, 96);
+                tc_fence_after();
+                issue_w(6, true);
+                issue_w(7, false);
+                int ok = 1;
+                if (lane == 0 && !mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
+                    ok = 0;
+                    ctrl[2] = 1;
+                    record_device_error(p.err, kDevTimeout);
+                }
+                v_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+                if (v_ok) issue_u(3, true);
+                named_sync(kBarLevel1, 96);
+                tc_fence_after();
+                issue_w(4, false);
+                issue_w(5, false);
+                if (v_ok) issue_u(2, false);
+                named_sync(kBarLevel2, 160);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) issue_w(kk, false);
+                if (v_ok) {
+                    issue_u(0, false);
+                    issue_u(1, false);
+                }
+                mma_commit_w(bar_mma);
+            } else if (warp >= 8) {
                 state_pass(tmem + lane_base, warp, s_em, s_dec);
-            fence_proxy_async_smem();
+            }
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
 
-            // ---- S5: W'^T = Kr^T (T beta)^T ;  Ut^T = V^T (T beta)^T ----
+            // ---- S5: the W' and U-tilde products complete ----
             // A_kk and T are consumed: the next chunk's g and beta are staged now.
             if (Ln > 0) load_beta(tn, Ln);
-            if (tid == 0) {
-                if (Ln > 0) issue_g(tn);
-                const uint32_t idw = instr_desc(128, 64, kFmtTF32, 0, 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = (d_kh + static_cast<uint64_t>(((kk >> 2) * 24576 + 16384 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_O, tmem + T_W + kk * 8, bd, idw, kk > 0);
-                }
-                if (!mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
-                    ctrl[2] = 1;
-                    record_device_error(p.err, kDevTimeout);
-                } else {
-                    pend_v = false;
-                    const uint32_t idu = instr_desc(128, 64, kFmtBF16, 1, 0);
-                    for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = (d_v + static_cast<uint64_t>((kk * 2048) >> 4));
-                            const uint64_t bd = (d_tb16 + static_cast<uint64_t>((part * 8192 + kk * 32) >> 4));
-                            mma_f16_ss(tmem + T_U, ad, bd, idu, (part | kk) != 0);
-                        }
-                    }
-                }
-                mma_commit(bar_mma);
-            }
+            if (tid == 0 && Ln > 0) issue_g(tn);
             ph_v++;
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
             ph_mma++;
             if (ctrl[2] != 0) break;
+            pend_v = false;
             if (tid == 0 && Ln > 0) issue_v(tn);
 
             // ---- S6: -W' into rows 64..127 of the [Qt ; Kr] tile (Kr is dead

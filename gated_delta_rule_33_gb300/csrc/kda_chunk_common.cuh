@@ -110,6 +110,17 @@ __device__ __forceinline__ uint64_t log2_1p_unit2(uint64_t e) {
 // the other warps run the state pass.
 __device__ __forceinline__ void inverse_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Named barriers between the inverse warps (which arrive) and the warp that
+// issues the W' and U-tilde products (which waits); n counts every thread of
+// both sides.
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+constexpr int kBarDiag = 2, kBarLevel1 = 3, kBarLevel2 = 4;
+
 // 2^x with the special-function unit (inputs here lie within +-116).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
