@@ -103,13 +103,17 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
-    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": 4 * 139.84e6,
-                      "sha256": ["0249a1d5c7d96af693a0ac274572e8e542305369099093f792305e80d5a7c953",
-                                 "1b42adeb58c6dbf45e946f4ab4b77d0169d66fd292fdb92c54d4c387190d085a"],
+    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh"],
+                      "bytes": 4 * 138.12e6,
+                      "sha256": ["51a136aa9376331c20ddae3aa63173a7c9897e8b87a0bbffb7c3363a6772d651",
+                                 "29b96e2fae45e0f01a5b1b6c39f43466ca2e3c2fef7c1dc633a3f702f9f1dd48",
+                                 "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4"],
                       "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
-    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh"], "bytes": 4 * 110.46e6,
-                    "sha256": ["0249a1d5c7d96af693a0ac274572e8e542305369099093f792305e80d5a7c953",
-                               "1b42adeb58c6dbf45e946f4ab4b77d0169d66fd292fdb92c54d4c387190d085a"],
+    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh"],
+                    "bytes": 4 * 109.96e6,
+                    "sha256": ["51a136aa9376331c20ddae3aa63173a7c9897e8b87a0bbffb7c3363a6772d651",
+                               "29b96e2fae45e0f01a5b1b6c39f43466ca2e3c2fef7c1dc633a3f702f9f1dd48",
+                               "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4"],
                     "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
     "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,
                "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
