@@ -7,6 +7,7 @@
 #include <cuda.h>
 
 #include "kda_internal.cuh"
+#include "kda_f32x2.cuh"
 #include "kda_sm100.cuh"
 
 namespace kda {
@@ -40,40 +41,6 @@ __device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
 
 __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<float *>(base + off) = x;
-}
-
-// Packed pairs of binary32 values: one instruction applies the IEEE
-// operation (round to nearest) to both halves, with the same results as two
-// scalar instructions.
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float2 f2_split(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
 }
 
 // log2(1 + e) for e in [0, 1], as e P(e) with P the degree-7 Chebyshev

@@ -75,7 +75,11 @@ __global__ void __launch_bounds__(256) gate_vec_kernel(
         }
         float out[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) out[j] = gate_g(fv[j], dt[j], a[j]);
+        for (int j = 0; j < 8; j += 2) {  // packed pairs, the same bits as gate_g
+            const float2 gp = gate_g_x2(fv[j], fv[j + 1], dt[j], dt[j + 1], a[j], a[j + 1]);
+            out[j] = gp.x;
+            out[j + 1] = gp.y;
+        }
         __stcs(reinterpret_cast<float4 *>(g + base), make_float4(out[0], out[1], out[2], out[3]));
         __stcs(reinterpret_cast<float4 *>(g + base + 4), make_float4(out[4], out[5], out[6], out[7]));
         if (do_beta) {
