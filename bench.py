@@ -218,30 +218,22 @@ class ClockSampler:
 
 
 # --- distributed helpers -----------------------------------------------------------------
+# Each rank runs its own sequences (weak scaling; no data-path exchange): the
+# helpers live in gated_delta_rule_33_gb300/sharding.py.
 
 def dist_setup(n_gpus):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    if world > 1:
-        import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        dist.init_process_group(backend)
-        return dist.get_rank(), world, int(os.environ.get("LOCAL_RANK", "0"))
-    return 0, 1, 0
+    from gated_delta_rule_33_gb300.sharding import dist_setup as _setup
+    return _setup()
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    from gated_delta_rule_33_gb300.sharding import barrier as _barrier
+    _barrier(world)
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from gated_delta_rule_33_gb300.sharding import max_over_ranks as _max
+    return _max(x, world, device)
 
 
 # --- reference arm (the CPU oracle) --------------------------------------------------------
