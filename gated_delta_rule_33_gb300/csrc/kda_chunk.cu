@@ -348,11 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
             // ---- S1: cumulative decay, references, operands ----
             cp_async_wait_all();
-            if (tid == 0 && !mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls)) {
+            // polled by warp 1: thread 0 may still be issuing the previous
+            // chunk's last product
+            if (tid == 32 && (!mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls) ||
+                              !mbar_wait_bounded(bar_g, ph_g & 1, kMaxPolls))) {
                 ctrl[2] = 1;
                 record_device_error(p.err, kDevTimeout);
             }
-            cta_wait(bar_g, ph_g & 1, &ctrl[2], p.err, tid);
+            __syncthreads();
+            tc_fence_after();
             ph_g++;
             ph_qk++;
             pend_g = false;
@@ -462,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 
             // ---- S2: D_A = [Qt; Kr] Ks^T ; next q/k loads ; previous chunk's output ----
             if (tid == 0) {
-                if (Ln > 0) issue_qk(tn);
                 const uint32_t id = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
@@ -471,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                     mma_tf32_ss(tmem + T_A, ad, bd, id, kk > 0);
                 }
                 mma_commit(bar_mma);
+                if (Ln > 0) issue_qk(tn);
             }
             if (tc > t0) write_output(tc - kC, kC);
 
