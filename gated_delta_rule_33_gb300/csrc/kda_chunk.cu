@@ -261,13 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         }
         const int64_t state_off = (static_cast<int64_t>(b) * H + h) * kD * kD;
         // O^T of the chunk starting at token tc (L valid rows) from tensor memory to o
-        auto write_output = [&](int64_t tcw, int Lw) {
+        // (rows 16 gw .. + 15 of the warp's lane quarter)
+        auto write_output = [&](int64_t tcw, int Lw, int gw) {
             float o16[16];
-            tmem_ld16(tmem + lane_base + T_O + 16 * grp, o16);
+            tmem_ld16(tmem + lane_base + T_O + 16 * gw, o16);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int r = 16 * grp + j;
+                const int r = 16 * gw + j;
                 if (r < Lw) {
                     const int64_t idx = ((tcw + r) * H + h) * kD + ch;
                     if (kOutBf16)
@@ -476,7 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 mma_commit(bar_mma);
                 if (Ln > 0) issue_qk(tn);
             }
-            if (tc > t0) write_output(tc - kC, kC);
+            // warp 0 issues the products; warp 4 (same lane quarter) takes its rows
+            if (tc > t0 && warp != 0) {
+                write_output(tc - kC, kC, grp);
+                if (warp == 4) write_output(tc - kC, kC, 0);
+            }
 
             // ---- S3: A_kk from the k-side rows of D_A ----
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
@@ -594,17 +599,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
             // A_qk (K-major [r][s], zero above the diagonal) while MMA1/MMA2 run;
             // the T beta tile it overwrites was consumed by the W' product.
-            if (quarter < 2) {
+            // (warp 0 issues the products; warp 4, same lane quarter, takes its columns)
+            auto store_aqk = [&](int gw) {
                 const int r = ch;
                 float a16[16];
-                tmem_ld16(tmem + lane_base + T_A + 16 * grp, a16);
+                tmem_ld16(tmem + lane_base + T_A + 16 * gw, a16);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int s = 16 * grp + j;
+                    const int s = 16 * gw + j;
                     st_f32(smem + OFF_KH, sw128_offset(kTbRow0 + r, s, kTbRows, 4),
                            (s <= r) ? to_tf32(a16[j]) : 0.f);
                 }
+            };
+            if (quarter < 2 && warp != 0) {
+                store_aqk(grp);
+                if (warp == 4) store_aqk(0);
             }
             fence_proxy_async_smem();
             cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
@@ -647,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         if (ctrl[2] != 0) break;
         if (t1 > t0) {  // output of the last chunk
             const int64_t tl = t0 + ((t1 - t0 - 1) / kC) * kC;
-            write_output(tl, static_cast<int>(t1 - tl));
+            write_output(tl, static_cast<int>(t1 - tl), grp);
         }
 
         // ---- final state ----
