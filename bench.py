@@ -103,18 +103,20 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
-    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh"],
-                      "bytes": 4 * 138.12e6,
-                      "sha256": ["51a136aa9376331c20ddae3aa63173a7c9897e8b87a0bbffb7c3363a6772d651",
-                                 "29b96e2fae45e0f01a5b1b6c39f43466ca2e3c2fef7c1dc633a3f702f9f1dd48",
-                                 "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4"],
-                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
-    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh"],
-                    "bytes": 4 * 109.96e6,
-                    "sha256": ["51a136aa9376331c20ddae3aa63173a7c9897e8b87a0bbffb7c3363a6772d651",
-                               "29b96e2fae45e0f01a5b1b6c39f43466ca2e3c2fef7c1dc633a3f702f9f1dd48",
-                               "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4"],
-                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
+    "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
+                     "bytes": 4 * 139.18e6,
+                     "sha256": ["e941a510ff91bd8b15b640e7bf660eb7447b6255c05489a05a2c8d19b9243f0f",
+                             "d9a06404aab5a35f50b521a94a3e0b03baa39e1f2e3b109bd4ab336152d2d471",
+                             "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4",
+                             "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
+                     "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
+    "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
+                   "bytes": 4 * 110.98e6,
+                   "sha256": ["e941a510ff91bd8b15b640e7bf660eb7447b6255c05489a05a2c8d19b9243f0f",
+                           "d9a06404aab5a35f50b521a94a3e0b03baa39e1f2e3b109bd4ab336152d2d471",
+                           "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4",
+                           "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
+                   "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
     "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,
                "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
                           "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
@@ -123,9 +125,12 @@ NCU_TRAFFIC = {
                     "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
                                "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
-    "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh"], "bytes": 246.81e6,
-             "sha256": ["4740ee00bfb7b6772d91a0e0309468ee3f2fb421f9ea1fae2c4ad50bdfa4bf80",
-                        "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
+    "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh", "kda_gate_spec_x2.cuh", "kda_f32x2.cuh"],
+             "bytes": 246.67e6,
+             "sha256": ["eb300c819670ac1a050c42847653314c1bb80e16d967403f83c881ac23a979d1",
+                        "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816",
+                        "f399e83c1e4aae348472e0801482dd513323e06dda80b6721213b1f41ebb401f",
+                        "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
              "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
     "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 559.92e6,
                    "sha256": ["af1058f9eb8c8df068075fb627961c0a26e972f1d2d7c6c2cb4b3f7e7208e6cc"],
@@ -234,6 +239,50 @@ def barrier(world):
 def max_over_ranks(x: float, world: int, device) -> float:
     from gated_delta_rule_33_gb300.sharding import max_over_ranks as _max
     return _max(x, world, device)
+
+
+def host_affinity_for(dev_index: int) -> dict:
+    """Restrict this process to the CPUs next to the GPU (its PCI device's
+    local_cpulist in sysfs), so that pinned host buffers allocated afterwards
+    sit in the memory nearest to the GPU; returns what was found."""
+    info = {}
+    try:
+        bus = None
+        props = torch.cuda.get_device_properties(dev_index)
+        if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            bus = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        else:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                                  "-i", str(dev_index)], capture_output=True, text=True, timeout=20)
+            raw = out.stdout.strip().lower()          # e.g. 00000009:01:00.0
+            if raw:
+                dom, rest = raw.split(":", 1)
+                bus = f"{int(dom, 16):04x}:{rest}"
+        if bus is None:
+            return {"note": "no PCI bus id"}
+        base = f"/sys/bus/pci/devices/{bus}"
+        info["pci"] = bus
+        with open(base + "/numa_node") as fh:
+            info["numa_node"] = int(fh.read().strip())
+        with open(base + "/local_cpulist") as fh:
+            cpulist = fh.read().strip()
+        cpus = set()
+        for part in cpulist.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        allowed = os.sched_getaffinity(0)
+        near = cpus & allowed
+        if near and near != allowed:
+            os.sched_setaffinity(0, near)
+            info["cpus"] = cpulist
+        else:
+            info["cpus"] = "unchanged"
+    except Exception as exc:  # best effort: the measurement still runs
+        info["note"] = f"affinity not set: {type(exc).__name__}"
+    return info
 
 
 # --- reference arm (the CPU oracle) --------------------------------------------------------
@@ -468,6 +517,8 @@ def run_ours(args):
     # compute stream, device-to-host copies on a third, so that step i+1's
     # inputs and step i-1's outputs move while step i computes.  Events order
     # each buffer set's reuse; every step still moves all of its bytes.
+    cpus_before = os.sched_getaffinity(0)
+    host_numa = host_affinity_for(local_rank)
     host_in = [t.pin_memory() for t in (x.q, x.k, x.v, x.f, x.b)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     slots = []
@@ -481,6 +532,7 @@ def run_ours(args):
             "d2h_done": torch.cuda.Event(), "used": False,
         })
     d2h = o.numel() * o.element_size() + Sf.numel() * Sf.element_size()
+    os.sched_setaffinity(0, cpus_before)   # the buffers stay where they were placed
     h2d_stream = torch.cuda.Stream(dev)
     d2h_stream = torch.cuda.Stream(dev)
 
@@ -620,7 +672,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "schedule": "steps pipelined over two buffer sets: H2D, prefill and D2H "
-                            "on three streams"},
+                            "on three streams", "host_memory": host_numa},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "peaks": peaks,

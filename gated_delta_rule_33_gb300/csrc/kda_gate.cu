@@ -16,7 +16,7 @@
 // (a 16-byte bf16 load of f, two 16-byte stores of g) and walks token rows with
 // a stride chosen so that its (head, channel) set never changes: exp(A_log) and
 // dt_bias are computed/loaded once per thread.
-#include "kda_gate_spec.cuh"
+#include "kda_gate_spec_x2.cuh"
 
 namespace kda {
 namespace {
