@@ -126,7 +126,7 @@ NCU_TRAFFIC = {
                                "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
     "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh", "kda_gate_spec_x2.cuh", "kda_f32x2.cuh"],
-             "bytes": 246.67e6,
+             "bytes": 246.60e6,
              "sha256": ["eb300c819670ac1a050c42847653314c1bb80e16d967403f83c881ac23a979d1",
                         "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816",
                         "f399e83c1e4aae348472e0801482dd513323e06dda80b6721213b1f41ebb401f",
