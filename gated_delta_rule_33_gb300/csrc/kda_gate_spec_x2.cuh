@@ -85,12 +85,67 @@ __device__ __forceinline__ uint64_t gate_log1p_x2(uint64_t y) {
     return f2(special(y2.x, v.x), special(y2.y, v.y));
 }
 
+// The common case, both |x| < 87: exp(-|x|) has n = round(-|x| / ln2) in
+// [-126, 0] and a normal result, and log1p sees y in (2^-126, 1].  There the
+// special-case branches of the specification cannot trigger and scaling p by
+// 2^n in one multiply gives the same bits as the two-step scaling (p 2^(n/2)
+// is exact, so only the final product rounds, in both forms).
+__device__ __forceinline__ uint64_t softplus_x2_common(float x0, float x1) {
+    const uint64_t x = f2(-fabsf(x0), -fabsf(x1));
+    const uint64_t n_f = f2_sub(f2_fma(x, f2(0x1.715476p+0f, 0x1.715476p+0f), f2(0x1.8p23f, 0x1.8p23f)),
+                                f2(0x1.8p23f, 0x1.8p23f));
+    uint64_t r = f2_fma(n_f, f2(-0x1.62e43p-1f, -0x1.62e43p-1f), x);
+    r = f2_fma(n_f, f2(0x1.05c61p-29f, 0x1.05c61p-29f), r);
+    uint64_t p = f2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
+    p = f2_fma(p, r, f2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    p = f2_fma(p, r, f2(0x1.111112p-7f, 0x1.111112p-7f));
+    p = f2_fma(p, r, f2(0x1.555556p-5f, 0x1.555556p-5f));
+    p = f2_fma(p, r, f2(0x1.555556p-3f, 0x1.555556p-3f));
+    p = f2_fma(p, r, f2(0.5f, 0.5f));
+    p = f2_fma(p, r, f2(1.0f, 1.0f));
+    p = f2_fma(p, r, f2(1.0f, 1.0f));
+    const float2 nf = f2_split(n_f);
+    const uint64_t y = f2_mul(p, f2(pow2_of(__float2int_rz(nf.x)), pow2_of(__float2int_rz(nf.y))));
+    // log1p(y), y in (2^-126, 1]
+    const uint64_t one = f2(1.0f, 1.0f);
+    const uint64_t u = f2_add(one, y);
+    const float2 u2 = f2_split(u);
+    float m0, m1;
+    const float e0 = log1p_reduce(u2.x, m0), e1 = log1p_reduce(u2.y, m1);
+    const uint64_t f = f2_sub(f2(m0, m1), one);
+    const float2 num = f2_split(f2_sub(y, f2_sub(u, one)));
+    const float2 fs = f2_split(f), den = f2_split(f2_add(f2(2.0f, 2.0f), f));
+    const float2 cp = make_float2(__fdiv_rn(num.x, u2.x), __fdiv_rn(num.y, u2.y));
+    const uint64_t s = f2(__fdiv_rn(fs.x, den.x), __fdiv_rn(fs.y, den.y));
+    const uint64_t z = f2_mul(s, s);
+    uint64_t R = f2(0x1.745d18p-3f, 0x1.745d18p-3f);
+    R = f2_fma(R, z, f2(0x1.c71c72p-3f, 0x1.c71c72p-3f));
+    R = f2_fma(R, z, f2(0x1.24924ap-2f, 0x1.24924ap-2f));
+    R = f2_fma(R, z, f2(0x1.99999ap-2f, 0x1.99999ap-2f));
+    R = f2_fma(R, z, f2(0x1.555556p-1f, 0x1.555556p-1f));
+    const float2 Rp = f2_split(R), zp = f2_split(z), sp = f2_split(s);
+    auto tail = [](float Ri, float zi, float si, float fi, float ci, float efi) {
+        const float Rz = __fmul_rn(Ri, zi);
+        const float t = __fmul_rn(si, __fsub_rn(fi, Rz));
+        const float low = __fsub_rn(__fmaf_rn(efi, -0x1.05c61p-29f, ci), t);
+        return __fmaf_rn(efi, 0x1.62e43p-1f, __fadd_rn(fi, low));
+    };
+    const uint64_t lg = f2(tail(Rp.x, zp.x, sp.x, fs.x, cp.x, e0), tail(Rp.y, zp.y, sp.y, fs.y, cp.y, e1));
+    // max(x, 0) + log1p: the sign of a zero max cannot show, log1p(e) > 0
+    return f2_add(f2(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f)), lg);
+}
+
 // g of two elements: gate_g(f0, dt0, a0) and gate_g(f1, dt1, a1)
 __device__ __forceinline__ float2 gate_g_x2(float f0, float f1, float dt0, float dt1, float a0,
                                             float a1) {
     const float2 x = f2_split(f2_add(f2(f0, f1), f2(dt0, dt1)));
-    const uint64_t e = gate_exp_x2(-fabsf(x.x), -fabsf(x.y));
-    const uint64_t sp = f2_add(f2(x.x > 0.0f ? x.x : 0.0f, x.y > 0.0f ? x.y : 0.0f), gate_log1p_x2(e));
+    uint64_t sp;
+    if (fabsf(x.x) < 87.0f && fabsf(x.y) < 87.0f) {
+        sp = softplus_x2_common(x.x, x.y);
+    } else {
+        const uint64_t e = gate_exp_x2(-fabsf(x.x), -fabsf(x.y));
+        sp = f2_add(f2(x.x > 0.0f ? x.x : 0.0f, x.y > 0.0f ? x.y : 0.0f), gate_log1p_x2(e));
+    }
     const float2 v = f2_split(f2_mul(f2(a0, a1), sp));
     return make_float2(-v.x, -v.y);
 }
