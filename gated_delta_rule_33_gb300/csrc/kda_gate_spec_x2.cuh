@@ -110,9 +110,11 @@ __device__ __forceinline__ uint64_t softplus_x2_common(float x0, float x1) {
     const uint64_t one = f2(1.0f, 1.0f);
     const uint64_t u = f2_add(one, y);
     const float2 u2 = f2_split(u);
-    float m0, m1;
-    const float e0 = log1p_reduce(u2.x, m0), e1 = log1p_reduce(u2.y, m1);
-    const uint64_t f = f2_sub(f2(m0, m1), one);
+    // u = 1 + y in (1, 2]: exponent 0 and m = u, or (u > sqrt 2, u = 2
+    // included) exponent 1 and m = u / 2 -- what log1p_reduce gives there
+    const bool h0 = u2.x > 0x1.6a09e6p+0f, h1 = u2.y > 0x1.6a09e6p+0f;
+    const float e0 = h0 ? 1.0f : 0.0f, e1 = h1 ? 1.0f : 0.0f;
+    const uint64_t f = f2_sub(f2_mul(u, f2(h0 ? 0.5f : 1.0f, h1 ? 0.5f : 1.0f)), one);
     const float2 num = f2_split(f2_sub(y, f2_sub(u, one)));
     const float2 fs = f2_split(f), den = f2_split(f2_add(f2(2.0f, 2.0f), f));
     const float2 cp = make_float2(__fdiv_rn(num.x, u2.x), __fdiv_rn(num.y, u2.y));
