@@ -445,8 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 khv[i] = to_tf32(kh.x);
                 khv[i + 1] = to_tf32(kh.y);
             }
-            // The previous chunk's [S | O] product, which reads Khat^T, ran under
-            // this build; it is complete before Khat^T is overwritten.
+            // The previous chunk's [S | O] product, which reads Khat^T, ran while
+            // these operands were formed; it is complete before Khat^T is overwritten.
             if (pend_mma) {
                 cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
                 ph_mma++;
