@@ -104,15 +104,15 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                     "bytes": 4 * 139.18e6,
-                     "sha256": ["e941a510ff91bd8b15b640e7bf660eb7447b6255c05489a05a2c8d19b9243f0f",
+                     "bytes": 4 * 138.80e6,
+                     "sha256": ["82db8085fb27161eb94341ea7f723e8c8c6d58ab3c2ad8a1c241ed51feeca65e",
                              "d9a06404aab5a35f50b521a94a3e0b03baa39e1f2e3b109bd4ab336152d2d471",
                              "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                   "bytes": 4 * 110.98e6,
-                   "sha256": ["e941a510ff91bd8b15b640e7bf660eb7447b6255c05489a05a2c8d19b9243f0f",
+                   "bytes": 4 * 111.02e6,
+                   "sha256": ["82db8085fb27161eb94341ea7f723e8c8c6d58ab3c2ad8a1c241ed51feeca65e",
                            "d9a06404aab5a35f50b521a94a3e0b03baa39e1f2e3b109bd4ab336152d2d471",
                            "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
@@ -126,10 +126,10 @@ NCU_TRAFFIC = {
                                "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
     "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh", "kda_gate_spec_x2.cuh", "kda_f32x2.cuh"],
-             "bytes": 246.60e6,
+             "bytes": 246.82e6,
              "sha256": ["eb300c819670ac1a050c42847653314c1bb80e16d967403f83c881ac23a979d1",
                         "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816",
-                        "f399e83c1e4aae348472e0801482dd513323e06dda80b6721213b1f41ebb401f",
+                        "3d6b65a9dfcc8c2e0ff562dd93aa28c5dad21e08b1edd9f0bffbe9f00f47dcfd",
                         "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
              "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
     "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 559.92e6,
