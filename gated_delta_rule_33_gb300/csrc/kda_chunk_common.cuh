@@ -43,24 +43,11 @@ __device__ __forceinline__ void st_f32(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<float *>(base + off) = x;
 }
 
-// log2(1 + e) for e in [0, 1], as e P(e) with P the degree-7 Chebyshev
-// interpolant of log2(1 + e) / e on [0, 1] in monomial form (coefficients from
-// gen_log2p1_poly.py; relative error of this fp32 evaluation below 4e-7).  It
-// runs on the FMA pipe, which the operand build leaves less loaded than the
-// special-function unit.
-__device__ __forceinline__ float log2_1p_unit(float e) {
-    float p = -0.0120770205f;
-    p = __fmaf_rn(p, e, 0.0627484322f);
-    p = __fmaf_rn(p, e, -0.154152006f);
-    p = __fmaf_rn(p, e, 0.255176336f);
-    p = __fmaf_rn(p, e, -0.353096366f);
-    p = __fmaf_rn(p, e, 0.480012447f);
-    p = __fmaf_rn(p, e, -0.721306741f);
-    p = __fmaf_rn(p, e, 1.44269478f);
-    return p * e;
-}
-
-// log2_1p_unit on a packed pair (the same operations, two lanes at a time)
+// log2(1 + e) of both halves of a packed pair, e in [0, 1], as e P(e) with P
+// the degree-7 Chebyshev interpolant of log2(1 + e) / e on [0, 1] in monomial
+// form (coefficients from gen_log2p1_poly.py; relative error of this fp32
+// evaluation below 4e-7).  It runs on the FMA pipe, which the operand build
+// leaves less loaded than the special-function unit.
 __device__ __forceinline__ uint64_t log2_1p_unit2(uint64_t e) {
     uint64_t p = f2(-0.0120770205f, -0.0120770205f);
     p = f2_fma(p, e, f2(0.0627484322f, 0.0627484322f));
