@@ -104,17 +104,17 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                     "bytes": 4 * 138.80e6,
+                     "bytes": 4 * 138.59e6,
                      "sha256": ["82db8085fb27161eb94341ea7f723e8c8c6d58ab3c2ad8a1c241ed51feeca65e",
-                             "d9a06404aab5a35f50b521a94a3e0b03baa39e1f2e3b109bd4ab336152d2d471",
-                             "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4",
+                             "436f5e167121af064c97dfe7473056041445553986b0e7372e24e3a8fbdeee1a",
+                             "ea28e7e55139d5d9b5dc2b66fb508aa4d932d6c4a6d5ca684b36b9a896c7ef9e",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                   "bytes": 4 * 111.02e6,
+                   "bytes": 4 * 110.61e6,
                    "sha256": ["82db8085fb27161eb94341ea7f723e8c8c6d58ab3c2ad8a1c241ed51feeca65e",
-                           "d9a06404aab5a35f50b521a94a3e0b03baa39e1f2e3b109bd4ab336152d2d471",
-                           "a10fa7eb02af38355f93795e9d2a8f29c8fa0e27617bdfbb153b2cf8ffee1ef4",
+                           "436f5e167121af064c97dfe7473056041445553986b0e7372e24e3a8fbdeee1a",
+                           "ea28e7e55139d5d9b5dc2b66fb508aa4d932d6c4a6d5ca684b36b9a896c7ef9e",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
     "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,
