@@ -26,6 +26,7 @@ from .kda import (  # noqa: F401
     kda_chunk_prefill_workspace_size,
     kda_gate_backward,
     kda_gate_backward_workspace_size,
+    kda_debug_set_wait_limit,
     kda_gate_fused,
     kda_get_last_device_error,
     kda_recurrent_backward,

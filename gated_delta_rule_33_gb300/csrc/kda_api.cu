@@ -3,6 +3,7 @@
 // Host-side argument checks, the per-device error word, and the launches.  No
 // CUDA allocation happens here; every buffer is the caller's.
 #include <mutex>
+#include <vector>
 
 #include "../../include/kda.h"
 #include "kda_internal.cuh"
@@ -69,7 +70,49 @@ kda_status from_cuda(cudaError_t e) {
     return KDA_ERR_CUDA;
 }
 
+// Host checks of kda_chunk_prefill's arguments other than the workspace.
+kda_status check_prefill_args(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const int32_t *cu_seqlens, int B, int64_t N,
+                              int H, int K, int V, const float *initial_state,
+                              const float *final_state, const void *o, kda_dtype o_dtype) {
+    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(o_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (cu_seqlens == nullptr && B != 1) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr ||
+                  beta == nullptr || o == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
+        !aligned16(cu_seqlens))
+        return KDA_ERR_MISALIGNED;
+    return KDA_OK;
+}
+
 }  // namespace
+
+namespace kda {
+
+cudaError_t ensure_dynamic_smem(const void *func, int bytes) {
+    struct Done {
+        int dev;
+        const void *func;
+        int bytes;
+    };
+    static std::mutex m;
+    static std::vector<Done> done;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(m);
+    for (const Done &d : done)
+        if (d.dev == dev && d.func == func && d.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back(Done{dev, func, bytes});
+    return e;
+}
+
+}  // namespace kda
 
 extern "C" {
 
@@ -126,22 +169,15 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
                              int K, int V, float scale, const float *initial_state,
                              float *final_state, void *o, kda_dtype o_dtype, void *workspace,
                              size_t workspace_bytes, void *stream) {
-    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
-    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
-    if (!valid_dtype(o_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
-    if (cu_seqlens == nullptr && B != 1) return KDA_ERR_INVALID_ARG;
-    if (N > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr ||
-                  beta == nullptr || o == nullptr))
-        return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
-        !aligned16(o) || !aligned16(initial_state) || !aligned16(final_state) ||
-        !aligned16(workspace) || !aligned16(cu_seqlens))
-        return KDA_ERR_MISALIGNED;
+    kda_status st = check_prefill_args(q, k, v, g, beta, cu_seqlens, B, N, H, K, V, initial_state,
+                                       final_state, o, o_dtype);
+    if (st != KDA_OK) return st;
+    if (!aligned16(workspace)) return KDA_ERR_MISALIGNED;
     const size_t need = kda::prefill_workspace_bytes(N, B, H);
     if (workspace_bytes < need || (need > 0 && workspace == nullptr))
         return KDA_ERR_WORKSPACE_TOO_SMALL;
     DeviceInfo *dev = nullptr;
-    kda_status st = current_device(&dev);
+    st = current_device(&dev);
     if (st != KDA_OK) return st;
     return from_cuda(kda::launch_prefill(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
@@ -193,8 +229,14 @@ kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v
                                      int64_t N, int H, int K, int V, float scale,
                                      const float *initial_state, float *final_state, void *o,
                                      kda_dtype o_dtype, void *stream) {
-    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
-    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    // The same argument and device checks as kda_chunk_prefill, in the same
+    // order, before the scratch lookup, so both return the same status codes.
+    kda_status st = check_prefill_args(q, k, v, g, beta, cu_seqlens, B, N, H, K, V, initial_state,
+                                       final_state, o, o_dtype);
+    if (st != KDA_OK) return st;
+    DeviceInfo *dev = nullptr;
+    st = current_device(&dev);
+    if (st != KDA_OK) return st;
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
     if (kda::builtin_prefill_scratch(&scratch, &scratch_bytes) != cudaSuccess) {
@@ -435,6 +477,11 @@ kda_status kda_recurrent_backward(const void *q, const void *k, const void *v, c
         static_cast<const __nv_bfloat16 *>(v), g, beta, cu_seqlens, B, N, H, scale, initial_state,
         dO, dO_dtype == KDA_BF16, dS_final, dq, dk, dv, dg, dbeta, dS0, workspace, ctas,
         dev->error_word, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_debug_set_wait_limit(int64_t copy_polls, int64_t product_polls) {
+    kda::set_prefill_wait_polls(copy_polls, product_polls);
+    return KDA_OK;
 }
 
 kda_status kda_get_last_device_error(void *stream) {

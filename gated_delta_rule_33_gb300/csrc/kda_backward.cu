@@ -401,15 +401,13 @@ cudaError_t launch_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     p.scratch = reinterpret_cast<float4 *>(ws + 256 + slots * H * state);
     p.err = err;
     constexpr size_t kDynSmem = 2 * kStateF4 * sizeof(float4);   // 128 KB
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(backward_kernel<true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+    {
+        cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(backward_kernel<true>),
+                                            static_cast<int>(kDynSmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(backward_kernel<false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+            e = ensure_dynamic_smem(reinterpret_cast<const void *>(backward_kernel<false>),
+                                    static_cast<int>(kDynSmem));
         if (e != cudaSuccess) return e;
-        attr_done = true;
     }
     cudaError_t e = cudaMemsetAsync(ws, 0, 256, s);
     if (e != cudaSuccess) return e;

@@ -16,8 +16,11 @@
 //
 // Numerics.  Every per-channel exponential is split around a per-channel
 // reference m = Gam_L / 2 so that each factor lies in [e^{-D/2}, e^{D/2}] with
-// D = -Gam_L the chunk's total decay (D <= 160 is representable; larger
-// decays are reported as KDA_ERR_DECAY_RANGE).  A_qk and A_kk come from one
+// D = -Gam_L the chunk's total decay.  D <= 160 is represented: a chunk whose
+// decay would exceed it in some channel is shortened to the rows before the
+// first one past it (the rest of its tile starts the next chunk), and each
+// token's decay is limited to 80 (e^{-80} is below fp32 resolution), so any
+// finite decay is computed.  A_qk and A_kk come from one
 // product [Qt; Kr] Ks^T with Qt = scale q e^{Gam-m}, Kr = k e^{Gam-m} and
 // Ks = k e^{m-Gam}.  The same Qt and Kr serve the state products because the
 // state operand is stored pre-scaled, S_op = Diag(e^m) S, and
@@ -34,6 +37,7 @@
 // of columns in every tensor-memory epilogue.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -68,7 +72,7 @@ constexpr uint32_t MISC_BNEXT = 7424;    // float[64] beta of the next chunk (cp
 constexpr uint32_t MISC_T32 = 7680;      // float[16][16] T_32 column-major (1 KB of 4 KB used)
 constexpr uint32_t MISC_TDIAG = 11776;   // float[4][16][16] diagonal blocks of T, column-major
 constexpr uint32_t MISC_BAR = 15872;     // 4 mbarriers
-constexpr uint32_t MISC_CTRL = 15904;    // int[8]: tmem base, chain, abort, decay flag
+constexpr uint32_t MISC_CTRL = 15904;    // int[8]: tmem base, chain, abort, split row
 constexpr uint32_t kSmemBytes = OFF_MISC + 15936;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
@@ -99,6 +103,8 @@ struct Params {
     void *o;
     unsigned int *err;
     unsigned int *counter;
+    uint32_t polls_tma;          // bound of the main loop's waits on copies
+    uint32_t polls_mma;          // and on products (the drain always uses kMaxPolls)
 };
 
 // T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk (column-major
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     uint64_t *bar_mma = bar_qk + 2;
     uint64_t *bar_g = bar_qk + 3;
     float *s_bnext = reinterpret_cast<float *>(misc + MISC_BNEXT);
-    int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [3] decay
+    int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [4] split
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, grp = warp >> 2;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
         ctrl[2] = 0;
-        ctrl[3] = 0;
+        ctrl[4] = kC;
     }
     // The strictly upper blocks of the T beta tiles are zero for every chunk and
     // are never written again (A_qk, which reuses the tf32 rows, is zero there too).
@@ -223,10 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     float *s_part = reinterpret_cast<float *>(misc + MISC_PART);
 
     // Phases consumed so far (identical in every thread) and, in thread 0,
-    // whether a TMA batch is in flight.
+    // whether a TMA batch is in flight.  A batch or product whose wait ran out
+    // stays marked in flight (its phase is not advanced), so the drain at the
+    // end waits for it before the CTA releases tensor memory and exits.
     uint32_t ph_qk = 0, ph_v = 0, ph_mma = 0, ph_g = 0;
     bool pend_qk = false, pend_v = false, pend_g = false;
-    // the last chunk's [S | O] product is in flight (identical in every thread)
+    // a product commit on bar_mma is not yet consumed (identical in every thread)
     bool pend_mma = false;
 
     const uint32_t a_qk = smem_addr(smem + OFF_QK);
@@ -242,13 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint64_t d_tb16 = smem_desc(a_tb16, 16, 1024, kSwizzle128B);
     const uint64_t d_v = smem_desc(a_v, 8192, 1024, kSwizzle128B);  // MN-major, 64-wide M blocks
     float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
+    // largest chunk decay and per-token decay represented, in log2 units
+    const float kMaxChunkLog2 = kMaxChunkDecay * 1.4426950408889634f;
+    const float kMinTokenLog2 = -kMaxTokenDecay * 1.4426950408889634f;
 
-    while (true) {
+    while (ctrl[2] == 0) {
         __syncthreads();
         if (tid == 0) ctrl[1] = static_cast<int>(atomicAdd(p.counter, 1u));
         __syncthreads();
         const int chain = ctrl[1];
-        if (chain >= num_chains || ctrl[2] != 0) break;
+        if (chain >= num_chains) break;
         const int b = chain / H, h = chain % H;
         int64_t t0 = 0, t1 = p.N;
         if (p.cu_seqlens != nullptr) {
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
         }
         const int64_t state_off = (static_cast<int64_t>(b) * H + h) * kD * kD;
-        // O^T of the chunk starting at token tc (L valid rows) from tensor memory to o
+        // O^T of the chunk starting at token tcw (Lw valid rows) from tensor memory to o
         // (rows 16 gw .. + 15 of the warp's lane quarter)
         auto write_output = [&](int64_t tcw, int Lw, int gw) {
             float o16[16];
@@ -342,27 +353,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             load_beta(t0, static_cast<int>((t1 - t0) < kC ? (t1 - t0) : kC));
         }
 
-        for (int64_t tc = t0; tc < t1; tc += kC) {
-            const int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
-            const int64_t tn = tc + kC;
-            const int Ln = static_cast<int>(tn >= t1 ? 0 : ((t1 - tn) < kC ? (t1 - tn) : kC));
+        // The chunk whose output is still in the O columns of tensor memory.
+        int64_t prev_tc = t0;
+        int prev_L = 0;
+        for (int64_t tc = t0; tc < t1;) {
+            // L tokens from tc; a chunk whose decay exceeds the represented
+            // range in some channel is shortened below (and the rest of its
+            // tile starts the next chunk)
+            int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
 
             // ---- S1: cumulative decay, references, operands ----
             cp_async_wait_all();
             // polled by warp 1: thread 0 may still be issuing the previous
-            // chunk's last product
-            if (tid == 32 && (!mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls) ||
-                              !mbar_wait_bounded(bar_g, ph_g & 1, kMaxPolls))) {
+            // chunk's last product.  Thread 0 also resets the split row here:
+            // every read of it (after S1's last barrier) is long past.
+            if (tid == 0) ctrl[4] = kC;
+            if (tid == 32 && (!mbar_wait_bounded(bar_qk, ph_qk & 1, p.polls_tma) ||
+                              !mbar_wait_bounded(bar_g, ph_g & 1, p.polls_tma))) {
                 ctrl[2] = 1;
                 record_device_error(p.err, kDevTimeout);
             }
             __syncthreads();
             tc_fence_after();
+            if (ctrl[2] != 0) break;  // the batches stay pending for the drain
             ph_g++;
             ph_qk++;
             pend_g = false;
             pend_qk = false;
-            // cumulative decay in log2 units: gam = log2(e) * sum g
+            // cumulative decay in log2 units: gam = log2(e) * sum g, each token's
+            // decay limited to kMaxTokenDecay (below fp32 resolution)
             float gam[16];
             {
                 const float kLog2e = 1.4426950408889634f;
@@ -382,88 +401,130 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                         const uint64_t e = f2(fast_exp2(-kLog2e * fabsf(x.x)), fast_exp2(-kLog2e * fabsf(x.y)));
                         const float2 g2 = f2_split(f2_mul(
                             na2, f2_fma(l2e2, f2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log2_1p_unit2(e))));
-                        acc += (r < L) ? g2.x : 0.f;
+                        // (the comparisons keep a NaN, which then reaches the outputs)
+                        acc += (r < L) ? (g2.x < kMinTokenLog2 ? kMinTokenLog2 : g2.x) : 0.f;
                         gam[i] = acc;
-                        acc += (r + 1 < L) ? g2.y : 0.f;
+                        acc += (r + 1 < L) ? (g2.y < kMinTokenLog2 ? kMinTokenLog2 : g2.y) : 0.f;
                         gam[i + 1] = acc;
                     }
                 } else {
                     const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
+                    // g must be a decay (g <= 0): a positive or NaN g is
+                    // reported; a positive one is taken as 0, a NaN kept
+                    bool bad = false;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
                         const int r = 16 * grp + i;
-                        acc += (r < L) ? kLog2e * gt[r * kD + ch] : 0.f;
+                        const float gv = kLog2e * gt[r * kD + ch];
+                        bad |= (r < L) && !(gv <= 0.f);
+                        const float gc = gv < kMinTokenLog2 ? kMinTokenLog2 : (gv > 0.f ? 0.f : gv);
+                        acc += (r < L) ? gc : 0.f;
                         gam[i] = acc;
                     }
+                    if (bad) record_device_error(p.err, kDevInvalidArg);
                 }
-                s_part[grp * kD + ch] = acc;
             }
-            if (tid < kC) s_beta[tid] = kGate ? 1.f / (1.f + __expf(-blog_reg)) : s_bnext[tid];
-            __syncthreads();  // every g read is done before Ks overwrites the tile
-            float prefix = 0.f, gam_l = 0.f;
+            float beta_r = 0.f;  // beta of row tid (threads 0..63)
+            if (tid < kC) beta_r = kGate ? 1.f / (1.f + __expf(-blog_reg)) : s_bnext[tid];
+            // Builds the operands of the chunk's first L rows from gam; runs a
+            // second time, with a shorter L, for a chunk that is split.
+            bool again;
+            do {
+                s_part[grp * kD + ch] = gam[15];
+                if (tid < kC) s_beta[tid] = (tid < L) ? beta_r : 0.f;
+                __syncthreads();  // every g read is done before Ks overwrites the tile
+                float prefix = 0.f, gam_l = 0.f;
 #pragma unroll
-            for (int g2 = 0; g2 < 4; ++g2) {
-                const float pg = s_part[g2 * kD + ch];
-                if (g2 < grp) prefix += pg;
-                gam_l += pg;
-            }
-            if (-gam_l > kMaxDecay * 1.4426950408889634f) ctrl[3] = 1;
-            const float m = 0.5f * gam_l;
-            if (grp == 0) {
-                s_em[ch] = fast_exp2(m);
-                s_dec[ch] = fast_exp2(gam_l);
-            }
-            const float ekh = fast_exp2(gam_l - m);
-            const float qscale = p.scale;
-            float krt[16], khv[16];
-            const uint64_t m2 = f2(m, m), pre2 = f2(prefix, prefix), qs2 = f2(qscale, qscale);
-            const uint64_t ekh2 = f2(ekh, ekh);
+                for (int g2 = 0; g2 < 4; ++g2) {
+                    const float pg = s_part[g2 * kD + ch];
+                    if (g2 < grp) prefix += pg;
+                    gam_l += pg;
+                }
+                if (-gam_l > kMaxChunkLog2) {
+                    // the first of this thread's rows beyond the range
+                    int first = kC;
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {  // rows r, r + 1 as packed pairs
-                const int r = 16 * grp + i;
-                const bool v0 = r < L, v1 = r + 1 < L;  // rows past the sequence stay zero
-                const uint64_t gr = f2_add(pre2, f2(gam[i], gam[i + 1]));
-                const float2 du = f2_split(f2_sub(gr, m2)), dd = f2_split(f2_sub(m2, gr));
-                const uint64_t e_up = f2(fast_exp2(du.x), fast_exp2(du.y));  // e^{Gam_r - m}
-                const uint64_t e_dn = f2(fast_exp2(dd.x), fast_exp2(dd.y));  // e^{m - Gam_r}
-                const uint64_t qv = f2(v0 ? bf(smem + OFF_Q, (r * kD + ch) * 2) : 0.f,
-                                       v1 ? bf(smem + OFF_Q, ((r + 1) * kD + ch) * 2) : 0.f);
-                const uint64_t kv = f2(v0 ? bf(smem + OFF_K, (r * kD + ch) * 2) : 0.f,
-                                       v1 ? bf(smem + OFF_K, ((r + 1) * kD + ch) * 2) : 0.f);
-                const float2 qt = f2_split(f2_mul(f2_mul(qs2, qv), e_up));
-                const float2 kr = f2_split(f2_mul(kv, e_up));
-                const float2 ks = f2_split(f2_mul(kv, e_dn));
-                const float2 kh = f2_split(f2_mul(kv, f2_mul(e_dn, ekh2)));
-                st_f32(smem + OFF_QK, sw128_offset(r, ch, 128, 4), to_tf32(qt.x));
-                st_f32(smem + OFF_QK, sw128_offset(r + 1, ch, 128, 4), to_tf32(qt.y));
-                krt[i] = to_tf32(kr.x);
-                krt[i + 1] = to_tf32(kr.y);
-                st_f32(smem + OFF_QK, sw128_offset(r + 64, ch, 128, 4), krt[i]);
-                st_f32(smem + OFF_QK, sw128_offset(r + 65, ch, 128, 4), krt[i + 1]);
-                st_f32(smem + OFF_KS, sw128_offset(r, ch, 64, 4), to_tf32(ks.x));
-                st_f32(smem + OFF_KS, sw128_offset(r + 1, ch, 64, 4), to_tf32(ks.y));
-                khv[i] = to_tf32(kh.x);
-                khv[i + 1] = to_tf32(kh.y);
-            }
-            // The previous chunk's [S | O] product, which reads Khat^T, ran while
-            // these operands were formed; it is complete before Khat^T is overwritten.
-            if (pend_mma) {
-                cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
-                ph_mma++;
-                pend_mma = false;
-            }
-            // Khat^T row ch, columns r = 16 grp .. +15: four 16-byte stores
+                    for (int i = 15; i >= 0; --i) {
+                        const int r = 16 * grp + i;
+                        if (r < L && -(prefix + gam[i]) > kMaxChunkLog2) first = r;
+                    }
+                    if (first < kC) atomicMin(&ctrl[4], first);
+                }
+                const float m = 0.5f * gam_l;
+                if (grp == 0) {
+                    s_em[ch] = fast_exp2(m);
+                    s_dec[ch] = fast_exp2(gam_l);
+                }
+                const float ekh = fast_exp2(gam_l - m);
+                const float qscale = p.scale;
+                float krt[16], khv[16];
+                const uint64_t m2 = f2(m, m), pre2 = f2(prefix, prefix), qs2 = f2(qscale, qscale);
+                const uint64_t ekh2 = f2(ekh, ekh);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<float4 *>(smem + OFF_KH + sw128_offset(ch, 16 * grp + 4 * q4, 192, 4)) =
-                    make_float4(khv[4 * q4], khv[4 * q4 + 1], khv[4 * q4 + 2], khv[4 * q4 + 3]);
-            tmem_st16(tmem + lane_base + T_W + 16 * grp, krt);
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
+                for (int i = 0; i < 16; i += 2) {  // rows r, r + 1 as packed pairs
+                    const int r = 16 * grp + i;
+                    const bool v0 = r < L, v1 = r + 1 < L;  // rows past the chunk stay zero
+                    const uint64_t gr = f2_add(pre2, f2(gam[i], gam[i + 1]));
+                    const float2 du = f2_split(f2_sub(gr, m2)), dd = f2_split(f2_sub(m2, gr));
+                    const uint64_t e_up = f2(fast_exp2(du.x), fast_exp2(du.y));  // e^{Gam_r - m}
+                    const uint64_t e_dn = f2(fast_exp2(dd.x), fast_exp2(dd.y));  // e^{m - Gam_r}
+                    const uint64_t qv = f2(v0 ? bf(smem + OFF_Q, (r * kD + ch) * 2) : 0.f,
+                                           v1 ? bf(smem + OFF_Q, ((r + 1) * kD + ch) * 2) : 0.f);
+                    const uint64_t kv = f2(v0 ? bf(smem + OFF_K, (r * kD + ch) * 2) : 0.f,
+                                           v1 ? bf(smem + OFF_K, ((r + 1) * kD + ch) * 2) : 0.f);
+                    const float2 qt = f2_split(f2_mul(f2_mul(qs2, qv), e_up));
+                    const float2 kr = f2_split(f2_mul(kv, e_up));
+                    const float2 ks = f2_split(f2_mul(kv, e_dn));
+                    const float2 kh = f2_split(f2_mul(kv, f2_mul(e_dn, ekh2)));
+                    st_f32(smem + OFF_QK, sw128_offset(r, ch, 128, 4), to_tf32(qt.x));
+                    st_f32(smem + OFF_QK, sw128_offset(r + 1, ch, 128, 4), to_tf32(qt.y));
+                    krt[i] = to_tf32(kr.x);
+                    krt[i + 1] = to_tf32(kr.y);
+                    st_f32(smem + OFF_QK, sw128_offset(r + 64, ch, 128, 4), krt[i]);
+                    st_f32(smem + OFF_QK, sw128_offset(r + 65, ch, 128, 4), krt[i + 1]);
+                    st_f32(smem + OFF_KS, sw128_offset(r, ch, 64, 4), to_tf32(ks.x));
+                    st_f32(smem + OFF_KS, sw128_offset(r + 1, ch, 64, 4), to_tf32(ks.y));
+                    khv[i] = to_tf32(kh.x);
+                    khv[i + 1] = to_tf32(kh.y);
+                }
+                // The previous chunk's [S | O] product, which reads Khat^T, ran while
+                // these operands were formed; it is complete before Khat^T is overwritten.
+                if (pend_mma) {
+                    if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) break;
+                    ph_mma++;
+                    pend_mma = false;
+                }
+                // Khat^T row ch, columns r = 16 grp .. +15: four 16-byte stores
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<float4 *>(smem + OFF_KH + sw128_offset(ch, 16 * grp + 4 * q4, 192, 4)) =
+                        make_float4(khv[4 * q4], khv[4 * q4 + 1], khv[4 * q4 + 2], khv[4 * q4 + 3]);
+                tmem_st16(tmem + lane_base + T_W + 16 * grp, krt);
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                // A chunk split: the rows from ctrl[4] on start the next chunk.
+                // gam keeps its values up to the new last row and repeats the
+                // last one after it (those rows add no decay), and the
+                // operands are formed again; no channel exceeds the range now.
+                again = ctrl[4] < L;
+                if (again) {
+                    L = ctrl[4];
+                    float last = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (16 * grp + i < L)
+                            last = gam[i];
+                        else
+                            gam[i] = last;
+                    }
+                }
+            } while (again);
             if (ctrl[2] != 0) break;
+            const int64_t tn = tc + L;
+            const int Ln = static_cast<int>(tn >= t1 ? 0 : ((t1 - tn) < kC ? (t1 - tn) : kC));
 
             // ---- S2: D_A = [Qt; Kr] Ks^T ; next q/k loads ; previous chunk's output ----
             if (tid == 0) {
@@ -477,15 +538,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 mma_commit(bar_mma);
                 if (Ln > 0) issue_qk(tn);
             }
+            pend_mma = true;
             // warp 0 issues the products; warp 4 (same lane quarter) takes its rows
-            if (tc > t0 && warp != 0) {
-                write_output(tc - kC, kC, grp);
-                if (warp == 4) write_output(tc - kC, kC, 0);
+            if (prev_L > 0 && warp != 0) {
+                write_output(prev_tc, prev_L, grp);
+                if (warp == 4) write_output(prev_tc, prev_L, 0);
             }
 
             // ---- S3: A_kk from the k-side rows of D_A ----
-            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
+            if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) break;
             ph_mma++;
+            pend_mma = false;
             if (quarter >= 2) {
                 const int r = ch - 64;
                 const float br = s_beta[r];
@@ -529,11 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 issue_w(6, true);
                 issue_w(7, false);
                 int ok = 1;
-                if (lane == 0 && !mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls)) {
+                if (lane == 0 && !mbar_wait_bounded(bar_v, ph_v & 1, p.polls_tma)) {
                     ok = 0;
                     ctrl[2] = 1;
                     record_device_error(p.err, kDevTimeout);
                 }
+                // no product reads V unless its copy is known to be complete
                 v_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
                 if (v_ok) issue_u(3, true);
                 named_sync(kBarLevel1, 96);
@@ -556,16 +620,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
+            pend_mma = true;
+            // a V copy that did not arrive stays pending for the drain
+            if (ctrl[2] != 0) break;
+            ph_v++;
+            pend_v = false;
 
             // ---- S5: the W' and U-tilde products complete ----
             // A_kk and T are consumed: the next chunk's g and beta are staged now.
             if (Ln > 0) load_beta(tn, Ln);
             if (tid == 0 && Ln > 0) issue_g(tn);
-            ph_v++;
-            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
+            if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) break;
             ph_mma++;
-            if (ctrl[2] != 0) break;
-            pend_v = false;
+            pend_mma = false;
             if (tid == 0 && Ln > 0) issue_v(tn);
 
             // ---- S6: -W' into rows 64..127 of the [Qt ; Kr] tile (Kr is dead
@@ -597,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit(bar_mma);
             }
+            pend_mma = true;
             // A_qk (K-major [r][s], zero above the diagonal) while MMA1/MMA2 run;
             // the T beta tile it overwrites was consumed by the W' product.
             // (warp 0 issues the products; warp 4, same lane quarter, takes its columns)
@@ -617,8 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 if (warp == 4) store_aqk(0);
             }
             fence_proxy_async_smem();
-            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
+            if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) break;
             ph_mma++;
+            pend_mma = false;
 
             // ---- S8: U rounded to tf32 in place (A operand of the next MMAs) ----
             {
@@ -633,7 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
-            if (ctrl[2] != 0) break;
 
             // ---- S9: [S_acc^T | O^T] += U^T [Khat^T ; A_qk]^T ----
             if (tid == 0) {
@@ -648,17 +716,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             // ---- S10: the product completes under the next chunk's operand
             // build, and this chunk's output is read out under the next MMA ----
             pend_mma = true;
+            prev_tc = tc;
+            prev_L = L;
+            tc = tn;
         }
+        if (ctrl[2] != 0) break;  // to the drain
         if (pend_mma) {
-            cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid);
+            if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) break;
             ph_mma++;
             pend_mma = false;
         }
-        if (ctrl[2] != 0) break;
-        if (t1 > t0) {  // output of the last chunk
-            const int64_t tl = t0 + ((t1 - t0 - 1) / kC) * kC;
-            write_output(tl, static_cast<int>(t1 - tl), grp);
-        }
+        if (prev_L > 0) write_output(prev_tc, prev_L, grp);  // output of the last chunk
 
         // ---- final state ----
         if (p.Sf != nullptr) {
@@ -670,14 +738,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         }
     }
 
-    // Drain: after an abort, wait (bounded) for TMA batches still in flight so
-    // that no copy lands in shared memory after this CTA has exited.
+    // Drain: after an abort, wait for every TMA batch and product still in
+    // flight, with the full bound whatever limit the main loop used, so that
+    // no copy lands in shared memory after this CTA has exited and no product
+    // is running when the tensor memory is released.
     cp_async_wait_all();
     if (tid == 0) {
         if (pend_qk) mbar_wait_bounded(bar_qk, ph_qk & 1, kMaxPolls);
         if (pend_v) mbar_wait_bounded(bar_v, ph_v & 1, kMaxPolls);
         if (pend_g) mbar_wait_bounded(bar_g, ph_g & 1, kMaxPolls);
-        if (ctrl[3] != 0) record_device_error(p.err, kDevDecayRange);
+        if (pend_mma) mbar_wait_bounded(bar_mma, ph_mma & 1, kMaxPolls);
     }
     tc_fence_before();
     __syncthreads();
@@ -686,6 +756,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
 }
 
 }  // namespace
+
+namespace {
+// Bounds of the main loop's waits for the next launches (kMaxPolls unless a
+// test shortens them to make a wait run out).
+std::atomic<uint32_t> g_polls_tma{kMaxPolls};
+std::atomic<uint32_t> g_polls_mma{kMaxPolls};
+}  // namespace
+
+void set_prefill_wait_polls(int64_t copy_polls, int64_t product_polls) {
+    auto clamp = [](int64_t v) -> uint32_t {
+        if (v < 0 || v > static_cast<int64_t>(kMaxPolls)) return kMaxPolls;
+        return static_cast<uint32_t>(v);
+    };
+    g_polls_tma.store(clamp(copy_polls));
+    g_polls_mma.store(clamp(product_polls));
+}
 
 size_t prefill_workspace_bytes(int64_t N, int B, int H) {
     (void)N;
@@ -699,17 +785,11 @@ cudaError_t launch_chunk(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
                          const void *g_or_f, const Params &p, bool o_bf16, int num_sms,
                          cudaStream_t s) {
     if (p.B == 0 || p.H == 0) return cudaSuccess;
-    static bool attr_done[2] = {false, false};
-    if (!attr_done[o_bf16 ? 1 : 0]) {
-        cudaError_t e = o_bf16 ? cudaFuncSetAttribute(chunk_kernel<true, kGate>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                      kSmemAlloc)
-                               : cudaFuncSetAttribute(chunk_kernel<false, kGate>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                      kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        attr_done[o_bf16 ? 1 : 0] = true;
-    }
+    cudaError_t ea = o_bf16 ? ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_kernel<true, kGate>),
+                                                  static_cast<int>(kSmemAlloc))
+                            : ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_kernel<false, kGate>),
+                                                  static_cast<int>(kSmemAlloc));
+    if (ea != cudaSuccess) return ea;
     CUtensorMap mq, mk, mv, mg;
     const int64_t Nmap = p.N > 0 ? p.N : 1;
     if (!make_map(&mq, q, Nmap, p.H, 128, false) || !make_map(&mk, k, Nmap, p.H, 128, false) ||
@@ -718,12 +798,15 @@ cudaError_t launch_chunk(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
+    Params pl = p;
+    pl.polls_tma = g_polls_tma.load();
+    pl.polls_mma = g_polls_mma.load();
     const int chains = p.B * p.H;
     const int grid = chains < num_sms ? chains : num_sms;
     if (o_bf16)
-        chunk_kernel<true, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
+        chunk_kernel<true, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, pl);
     else
-        chunk_kernel<false, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, p);
+        chunk_kernel<false, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, pl);
     return cudaGetLastError();
 }
 
@@ -735,7 +818,8 @@ cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            const float *initial_state, float *final_state, void *o, bool o_bf16,
                            void *workspace, unsigned int *err, int num_sms, cudaStream_t s) {
     const Params p{g, beta, nullptr, nullptr, 0, nullptr, 0, nullptr, cu_seqlens, B, N, H, scale,
-                   initial_state, final_state, o, err, static_cast<unsigned int *>(workspace)};
+                   initial_state, final_state, o, err, static_cast<unsigned int *>(workspace),
+                   kMaxPolls, kMaxPolls};
     return launch_chunk<false>(q, k, v, g, p, o_bf16, num_sms, s);
 }
 
@@ -748,7 +832,7 @@ cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                  unsigned int *err, int num_sms, cudaStream_t s) {
     const Params p{nullptr, nullptr, f, b, b_bf16 ? 1 : 0, A_log, alog_mode, dt_bias, cu_seqlens,
                    B, N, H, scale, initial_state, final_state, o, err,
-                   static_cast<unsigned int *>(workspace)};
+                   static_cast<unsigned int *>(workspace), kMaxPolls, kMaxPolls};
     return launch_chunk<true>(q, k, v, f, p, o_bf16, num_sms, s);
 }
 

@@ -17,7 +17,16 @@ using namespace sm100;
 
 constexpr int kC = 64;              // chunk length
 constexpr int kD = 128;             // d_k = d_v
-constexpr float kMaxDecay = 160.f;  // largest per-channel chunk decay represented
+// Largest per-channel decay -sum(g) of one chunk that the midpoint-referenced
+// factors represent (every factor within e^{+-80}); a chunk that would exceed
+// it in some channel is shortened.
+constexpr float kMaxChunkDecay = 160.f;
+// Each token's decay -g is limited to this value: e^{-80} (1.8e-35) is far
+// below fp32 resolution relative to the state and the new token's term, so
+// the limit changes no result at fp32 precision, and it guarantees that any
+// single token fits a chunk.
+constexpr float kMaxTokenDecay = 80.f;
+// Bound of every mbarrier wait (polls of try_wait, each itself a bounded wait).
 constexpr uint32_t kMaxPolls = 1u << 20;
 // The tf32 T beta tile lives in rows 128..191 of a 192-row K-major tile (the
 // chunk kernel's [Khat^T ; T beta -> A_qk] B operand), so its rows are
@@ -82,18 +91,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// Thread 0 waits (bounded) on an mbarrier phase, then the whole CTA meets at a
-// barrier; a time-out raises the CTA abort flag, which every thread reads
-// after the barrier.  Only one thread polls, so the other warps do not compete
-// with the tensor core for shared-memory bandwidth while they wait.
-__device__ __forceinline__ void cta_wait(uint64_t *bar, uint32_t parity, int *abort_flag,
-                                         unsigned int *err, int tid) {
-    if (tid == 0 && !mbar_wait_bounded(bar, parity, kMaxPolls)) {
+// Thread 0 waits (bounded, `polls` polls) on an mbarrier phase, then the
+// whole CTA meets at a barrier; a time-out raises the CTA abort flag, which
+// every thread reads after the barrier.  Returns false (in every thread) when
+// the CTA is aborting.  Only one thread polls, so the other warps do not
+// compete with the tensor core for shared-memory bandwidth while they wait.
+__device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, int *abort_flag,
+                                         unsigned int *err, int tid, uint32_t polls) {
+    if (tid == 0 && !mbar_wait_bounded(bar, parity, polls)) {
         *abort_flag = 1;
         record_device_error(err, kDevTimeout);
     }
     __syncthreads();
     tc_fence_after();
+    return *abort_flag == 0;
 }
 
 // T beta[r][s] = T[r][s] beta_s as a tf32 operand tile and as bf16 high + low

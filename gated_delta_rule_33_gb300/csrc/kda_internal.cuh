@@ -14,7 +14,6 @@ enum : unsigned int {
     kDevOk = 0,
     kDevInvalidArg = 1,      // KDA_ERR_INVALID_ARG: a bad cu_seqlens entry
     kDevTimeout = 7,         // KDA_ERR_DEVICE_TIMEOUT: a bounded wait ran out
-    kDevDecayRange = 11,     // KDA_ERR_DECAY_RANGE: a chunk's decay is out of range
 };
 
 __device__ __forceinline__ void record_device_error(unsigned int *err, unsigned int code) {
@@ -22,6 +21,12 @@ __device__ __forceinline__ void record_device_error(unsigned int *err, unsigned 
 }
 
 __device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current device.
+// The attribute belongs to the device, so a process that drives several GPUs
+// needs it on each: the call is made once per (device, kernel) under a lock
+// (kda_api.cu) and later calls return at once.
+cudaError_t ensure_dynamic_smem(const void *func, int bytes);
 
 // Launchers (defined next to their kernels).  All are asynchronous on `s`.
 cudaError_t launch_gate(const void *f, bool f_bf16, const void *b, bool b_bf16,
@@ -92,6 +97,10 @@ cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                  int H, float scale, const float *initial_state,
                                  float *final_state, void *o, bool o_bf16, void *workspace,
                                  unsigned int *err, int num_sms, cudaStream_t s);
+
+// Bounds of the chunked prefill's main-loop waits for later launches (copies,
+// products; a negative value restores the default).  Test use only.
+void set_prefill_wait_polls(int64_t copy_polls, int64_t product_polls);
 
 // Device address and size of the built-in prefill scratch on the current device
 // (looked up once per device; see kda_chunk.cu).

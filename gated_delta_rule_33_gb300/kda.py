@@ -101,6 +101,8 @@ def load():
         lib.kda_gate_backward.argtypes = [P, I, P, I, P, I, P, P, P, P, P, P, P, I64, I, I, P,
                                           ctypes.c_size_t, P]
         lib.kda_gate_backward.restype = I
+        lib.kda_debug_set_wait_limit.argtypes = [I64, I64]
+        lib.kda_debug_set_wait_limit.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
         lib.kda_get_last_device_error.restype = I
         _lib = lib
@@ -285,6 +287,12 @@ def kda_gate_backward(f, b, A_log, alog_mode, dt_bias, dg, dbeta, df, db, dA_log
         N, H, K, _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream, f.device))
     _check(st, "kda_gate_backward")
+
+
+def kda_debug_set_wait_limit(copy_polls: int = -1, product_polls: int = -1):
+    """Test hook: bound of the chunked prefill's main-loop waits (negative = default)."""
+    _check(load().kda_debug_set_wait_limit(int(copy_polls), int(product_polls)),
+           "kda_debug_set_wait_limit")
 
 
 def kda_get_last_device_error(stream=None) -> int:

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define KDA_VERSION 10000 /* 1.0.0 */
+#define KDA_VERSION 10100 /* 1.1.0 */
 
 typedef enum kda_status {
     KDA_OK = 0,
@@ -57,8 +57,8 @@ typedef enum kda_status {
     KDA_ERR_NONFINITE = 8,          /* reserved for debug checks */
     KDA_ERR_NOT_IMPLEMENTED = 9,
     KDA_ERR_NO_DEVICE = 10,         /* no usable sm_103 device / driver */
-    KDA_ERR_DECAY_RANGE = 11        /* prefill: in some channel the decay summed over one
-                                       64-token chunk is below -160 (device-side check) */
+    KDA_ERR_DECAY_RANGE = 11        /* reserved: no entry point returns it (the chunked
+                                       prefill computes chunks of any decay) */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -120,7 +120,13 @@ size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V);
  * as the token recurrence above would, chunk by chunk.
  *
  *   q, k, v       bf16 [N, H, 128]; q and k are used as given (no normalisation)
- *   g             fp32 [N, H, 128] log-decay (g <= 0 for a decay)
+ *   g             fp32 [N, H, 128] log-decay, g <= 0.  A positive or NaN entry
+ *                 sets INVALID_ARG in the device error word (a positive one is
+ *                 computed as 0).  Each token's g is taken as at least -80
+ *                 (e^-80 = 1.8e-35 lies far below fp32 resolution, so results
+ *                 are unchanged at fp32 precision); chunks whose decay in some
+ *                 channel exceeds what one chunk represents are split on the
+ *                 device, so every decay is computed.
  *   beta          fp32 [N, H], already passed through the sigmoid
  *   cu_seqlens    int32 [B+1] device offsets of B packed sequences
  *                 (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = N); NULL
@@ -413,6 +419,22 @@ kda_status kda_short_conv_qkv_step(const void *x_q, const void *x_k, const void 
                                    void *conv_state_pool, const int32_t *state_indices,
                                    int num_slots, int B, int C,
                                    void *q, void *k, void *v, void *stream);
+
+/*
+ * kda_debug_set_wait_limit -- test hook for the bounded device waits.  Every
+ * wait of the chunked prefill kernels on a copy (TMA) or a tensor-core product
+ * gives up after a bounded number of polls and records KDA_ERR_DEVICE_TIMEOUT
+ * in the device error word instead of hanging (a failure is reported, never
+ * turned into silent wrong numbers: the EP-adapter review, finding IMPORTANT
+ * 1, asks for loud failure).  This call sets the bound of the main-loop waits
+ * of later kda_chunk_prefill* launches in this process: copy_polls for copies,
+ * product_polls for products; 0 gives up at the first poll, a negative value
+ * restores the default.  A kernel that gives up stops issuing work and, before
+ * it exits, waits for everything it had in flight with the default bound (this
+ * drain is never shortened).  For tests only: the outputs of an aborted launch
+ * are incomplete.  Always returns KDA_OK.
+ */
+kda_status kda_debug_set_wait_limit(int64_t copy_polls, int64_t product_polls);
 
 /*
  * Synchronises `stream`, then returns and clears the device error word of the

@@ -23,6 +23,44 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / denom)
 
 
+def per_unit_rel_l2(a, b, cu_seqlens=None):
+    """Largest relative L2 error over the (sequence, head) units of a token
+    tensor [N, H, D] (``cu_seqlens`` splits N; None = one sequence) or of a
+    state tensor [B, H, K, V] (``cu_seqlens`` ignored).  Units whose reference
+    is all zero (empty sequences) are skipped.  One wrong chunk, head or
+    sequence shows here even where the error pooled over the whole tensor stays
+    under its bound."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    worst = 0.0
+    if a.ndim == 4:
+        units = [(a[i, h], b[i, h]) for i in range(a.shape[0]) for h in range(a.shape[1])]
+    else:
+        cu = [0, a.shape[0]] if cu_seqlens is None else [int(c) for c in np.asarray(cu_seqlens)]
+        units = [(a[cu[i]:cu[i + 1], h], b[cu[i]:cu[i + 1], h])
+                 for i in range(len(cu) - 1) for h in range(a.shape[1])]
+    for ua, ub in units:
+        nb = np.linalg.norm(ub)
+        if nb == 0:
+            continue
+        worst = max(worst, float(np.linalg.norm(ua - ub) / nb))
+    return worst
+
+
+def assert_parity(o_g, o_ref, S_g, S_ref, cu_seqlens=None):
+    """The prefill bounds, pooled over the tensors and for every (sequence,
+    head) unit on its own: o within O_TOL and the final state within
+    STATE_TOL."""
+    cu = None if cu_seqlens is None else np.asarray(cu_seqlens)
+    e_o, e_s = rel_l2(o_g, o_ref), rel_l2(S_g, S_ref)
+    u_o, u_s = per_unit_rel_l2(o_g, o_ref, cu), per_unit_rel_l2(S_g, S_ref)
+    assert e_o <= O_TOL, f"o rel-L2 {e_o:.3e}"
+    assert e_s <= STATE_TOL, f"state rel-L2 {e_s:.3e}"
+    assert u_o <= O_TOL, f"o rel-L2 of the worst (sequence, head) {u_o:.3e}"
+    assert u_s <= STATE_TOL, f"state rel-L2 of the worst (sequence, head) {u_s:.3e}"
+    return e_o, e_s
+
+
 def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().double().numpy()
 

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(clib):
 
 def test_version_and_status_strings(clib):
     import gated_delta_rule_33_gb300 as kda
-    assert kda.kda_version() == 10000
+    assert kda.kda_version() == 10100
     assert kda.kda_status_string(0) == "KDA_OK"
     assert kda.kda_status_string(5) == "KDA_ERR_WORKSPACE_TOO_SMALL"
     assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 from gated_delta_rule_33_gb300 import synth
-from parity_utils import DEV, O_TOL, STATE_TOL, f64, oracle_gate, oracle_prefill, rel_l2
+from parity_utils import (DEV, O_TOL, STATE_TOL, assert_parity, f64, oracle_gate, oracle_prefill,
+                          rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +34,7 @@ def check_gated(lib, x, scale=1.0, o_dtype=torch.bfloat16, b_bf16=False, heads=N
     o_g, S_g = f64(o), f64(Sf)
     if heads is not None:
         o_g, S_g = o_g[:, heads], S_g[:, heads]
-    assert rel_l2(o_g, o_ref) <= O_TOL
-    assert rel_l2(S_g, S_ref) <= STATE_TOL
+    assert_parity(o_g, o_ref, S_g, S_ref, x.cu_seqlens)
 
 
 @pytest.mark.parametrize("lengths,H", [([16], 1), ([65], 2), ([17, 31], 2), ([200], 3)])

@@ -9,8 +9,8 @@ import torch
 
 import oracle
 from gated_delta_rule_33_gb300 import synth
-from parity_utils import (DEV, O_TOL, STATE_TOL, f64, gpu_gate, oracle_gate, oracle_prefill,
-                          rel_l2)
+from parity_utils import (DEV, O_TOL, STATE_TOL, assert_parity, f64, gpu_gate, oracle_gate,
+                          oracle_prefill, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,11 +80,8 @@ def check_prefill(lib, x, scale=1.0, o_dtype=torch.bfloat16, heads=None):
     o_g, S_g = f64(o), f64(Sf)
     if heads is not None:
         o_g, S_g = o_g[:, heads], S_g[:, heads]
-    e_o, e_s = rel_l2(o_g, o_ref), rel_l2(S_g, S_ref)
-    assert e_o <= O_TOL, f"o rel-L2 {e_o:.3e}"
-    assert e_s <= STATE_TOL, f"state rel-L2 {e_s:.3e}"
     assert np.isfinite(o_g).all() and np.isfinite(S_g).all()
-    return e_o, e_s
+    return assert_parity(o_g, o_ref, S_g, S_ref, x.cu_seqlens)
 
 
 # The exact-match shape set of K3_ARTIFACT_AUDIT.md section 7.3: one chunk, a
@@ -109,8 +106,7 @@ def test_prefill_varlen_with_empty_sequences(lib):
     o, Sf, g, beta = run_prefill(lib, x, o_dtype=torch.float32)
     g_ref, beta_ref = oracle_gate(x)
     o_ref, S_ref = oracle_prefill(x, g_ref, beta_ref)
-    assert rel_l2(f64(o), o_ref) <= O_TOL
-    assert rel_l2(f64(Sf), S_ref) <= STATE_TOL
+    assert_parity(f64(o), o_ref, f64(Sf), S_ref, x.cu_seqlens)
     # empty sequences: final state equals the initial state
     for i in (0, 2, 5):
         np.testing.assert_array_equal(Sf[i].cpu().numpy(), x.initial_state[i].numpy())
@@ -233,21 +229,70 @@ def test_prefill_many_short_sequences(lib):
     check_prefill(lib, x, o_dtype=torch.float32)
 
 
-@pytest.mark.parametrize("gated", [False, True])
-def test_prefill_decay_out_of_range_is_reported(lib, gated):
-    """A chunk whose per-channel decay exceeds the represented range (sum of g
-    below -160 within 64 tokens) sets KDA_ERR_DECAY_RANGE instead of
-    returning wrong numbers silently."""
-    x = synth.make_inputs(128, H=2, D=128, seed=8)
-    q, k, v = x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
-    if gated:
-        # A_log = 2, f = 30: g = -e^2 softplus(30 + dt_bias) ~ -190 per token
-        f = torch.full_like(x.f, 30.0).to(DEV)
-        A_log = torch.full_like(x.A_log, 2.0).to(DEV)
-        lib.prefill_gated(q, k, v, f, x.b.to(DEV), A_log, x.dt_bias.to(DEV), x.alog_mode)
+# --- strong decay: chunks whose decay exceeds what one chunk represents ----------------------
+
+def _strong_decay_g(x, g_ref, case):
+    """g for the strong-decay cases: every channel at -5 per token (-320 over a
+    64-token chunk), or one head with a mix of hard channels (-5 per token;
+    -300 every seventh token in a few) and the soft K3 channels."""
+    g = np.array(g_ref, dtype=np.float32, copy=True)
+    if case == "all_hard":
+        g[:] = -5.0
     else:
-        g = torch.full((128, 2, 128), -5.0, device=DEV)      # -320 per 64-token chunk
-        beta = torch.full((128, 2), 0.5, device=DEV)
-        lib.prefill(q, k, v, g, beta)
-    assert lib.kda_get_last_device_error() == 11   # KDA_ERR_DECAY_RANGE
+        g[:, 0, :32] = -5.0
+        g[::7, 0, 32:40] = -300.0
+    return g
+
+
+@pytest.mark.parametrize("case", ["all_hard", "mixed"])
+@pytest.mark.parametrize("o_dtype", [torch.bfloat16, torch.float32])
+def test_prefill_strong_decay_matches_oracle(lib, case, o_dtype):
+    """Per-channel chunk decays far beyond one chunk's range (and single tokens
+    beyond e^-80) are computed, not refused: the kernel shortens such chunks.
+    Parity with the fp64 recurrence on the same g."""
+    x = synth.make_inputs(lengths=[200, 77, 1], H=2, D=128, seed=8, s0_std=0.05)
+    g_ref, beta_ref = oracle_gate(x)
+    g_np = _strong_decay_g(x, g_ref, case)
+    g, beta = torch.from_numpy(g_np).to(DEV), torch.from_numpy(beta_ref).to(DEV)
+    o, Sf = lib.prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g, beta, x.cu_seqlens.to(DEV), 1.0,
+                        x.initial_state.to(DEV), o_dtype=o_dtype)
+    assert lib.kda_get_last_device_error() == 0
+    o_ref, S_ref = oracle_prefill(x, g_np, beta_ref)
+    assert np.isfinite(f64(o)).all() and np.isfinite(f64(Sf)).all()
+    assert_parity(f64(o), o_ref, f64(Sf), S_ref, x.cu_seqlens)
+
+
+@pytest.mark.parametrize("hard", ["all", "some_channels"])
+def test_prefill_gated_strong_decay_matches_oracle(lib, hard):
+    """The gate fused into the kernel with A_log = 2 and f = 30 (g about -190
+    per token, clamped at -80 in the kernel), in every channel or in the first
+    32 channels of each head beside the soft K3 ones."""
+    x = synth.make_inputs(lengths=[130, 64, 9], H=2, D=128, seed=12, s0_std=0.05)
+    f = x.f.float()
+    A_log = x.A_log.clone()
+    sl = slice(None) if hard == "all" else slice(0, 32)
+    f[..., sl] = 30.0
+    A_log[sl] = 2.0
+    x.f = f.to(torch.bfloat16)
+    x.A_log = A_log
+    o, Sf = lib.prefill_gated(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.f.to(DEV), x.b.to(DEV),
+                              x.A_log.to(DEV), x.dt_bias.to(DEV), x.alog_mode,
+                              x.cu_seqlens.to(DEV), 1.0, x.initial_state.to(DEV),
+                              o_dtype=torch.float32)
+    assert lib.kda_get_last_device_error() == 0
+    g_ref, beta_ref = oracle_gate(x)
+    assert g_ref[..., sl].max() < -100.0
+    o_ref, S_ref = oracle_prefill(x, g_ref, beta_ref)
+    assert np.isfinite(f64(o)).all() and np.isfinite(f64(Sf)).all()
+    assert_parity(f64(o), o_ref, f64(Sf), S_ref, x.cu_seqlens)
+
+
+def test_prefill_positive_g_is_reported(lib):
+    """g must be a log-decay (g <= 0): a positive entry sets INVALID_ARG in the
+    device error word."""
+    x = synth.make_inputs(96, H=2, D=128, seed=13)
+    g, beta = gpu_gate(lib, x)
+    g[40, 1, 7] = 0.25
+    lib.prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g, beta)
+    assert lib.kda_get_last_device_error() == 1   # KDA_ERR_INVALID_ARG
     assert lib.kda_get_last_device_error() == 0
