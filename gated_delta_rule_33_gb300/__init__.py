@@ -14,12 +14,15 @@ from .kda import (  # noqa: F401
     KDA_FP32,
     KDAError,
     backward,
+    backward_chunked,
     build,
     decode,
     decode_gated,
     decode_indexed,
     gate,
     gate_backward,
+    kda_chunk_backward,
+    kda_chunk_backward_workspace_size,
     kda_chunk_prefill,
     kda_chunk_prefill_gated,
     kda_chunk_prefill_noalloc,

@@ -105,6 +105,8 @@ struct Params {
     unsigned int *counter;
     uint32_t polls_tma;          // bound of the main loop's waits on copies
     uint32_t polls_mma;          // and on products (the drain always uses kMaxPolls)
+    float *ckpt;                 // chunk-start states for a backward pass, or NULL
+    int *split;                  // per chain: set when a chunk was shortened (with ckpt)
 };
 
 // T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk (column-major
@@ -129,17 +131,18 @@ __device__ __forceinline__ void ut_inverse(int tid) {
     float *T32c = reinterpret_cast<float *>(misc + MISC_T32);
     float *P = reinterpret_cast<float *>(misc + MISC_P);
     const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
+    const TbetaTiles out{smem + OFF_KH, smem + OFF_TB16, beta};
     if (tid < 64) {
-        ut_diag_solve(At, T, Tdiag, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+        ut_diag_solve(At, T, Tdiag, out, tid);
         fence_proxy_async_smem();
         named_arrive(kBarDiag, 96);
         __syncwarp();
-        ut_level1(At, T, Tdiag, P, T, T32c, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+        ut_level1(At, T, Tdiag, P, T, T32c, out, tid);
         fence_proxy_async_smem();
         named_arrive(kBarLevel1, 96);
     }
     inverse_sync();
-    ut_level2(At, T, Tdiag, T32c, P, smem + OFF_KH, smem + OFF_TB16, beta, tid);
+    ut_level2(At, T, Tdiag, T32c, P, out, tid);
     fence_proxy_async_smem();
     named_arrive(kBarLevel2, 160);
 }
@@ -147,15 +150,20 @@ __device__ __forceinline__ void ut_inverse(int tid) {
 // The state pass of a chunk, S_op = tf32(e^{m_k} S[k][v]) and
 // S_acc = e^{Gam_L,k} S[k][v] in tensor memory, on warps 8-15 while warps 0-3
 // compute the UT inverse: warp w covers lane quarter w % 4 and the 16-column
-// slices w / 4 - 2 + 2 n.
+// slices w / 4 - 2 + 2 n.  With `ckpt`, the chunk-start state S[k][v] is also
+// stored there (fp32 [128][128]) for the chunked backward.
 __device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const float *em,
-                                           const float *dec) {
+                                           const float *dec, float *ckpt, int v) {
     float r16[16], o16[16];
 #pragma unroll 1
     for (int cs = (warp >> 2) - 2; cs < 8; cs += 2) {
         const int c0 = 16 * cs;
         tmem_ld16(tmem_lane + T_SACC + c0, r16);
         tmem_wait_ld();
+        if (ckpt != nullptr) {  // S[k][v] at the chunk start, k = c0 + j
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ckpt[(c0 + j) * kD + v] = r16[j];
+        }
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {  // packed pairs of columns
             const uint64_t rr = f2(r16[j], r16[j + 1]);
@@ -274,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         // O^T of the chunk starting at token tcw (Lw valid rows) from tensor memory to o
         // (rows 16 gw .. + 15 of the warp's lane quarter)
         auto write_output = [&](int64_t tcw, int Lw, int gw) {
+            if (p.o == nullptr) return;
             float o16[16];
             tmem_ld16(tmem + lane_base + T_O + 16 * gw, o16);
             tmem_wait_ld();
@@ -356,6 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         // The chunk whose output is still in the O columns of tensor memory.
         int64_t prev_tc = t0;
         int prev_L = 0;
+        // checkpoint slot of this sequence's first chunk (see kda_chunk_bwd.cu)
+        bool ckpt_ok = p.ckpt != nullptr;
+        const int64_t ckpt_slot0 = t0 / kC + b;
         for (int64_t tc = t0; tc < t1;) {
             // L tokens from tc; a chunk whose decay exceeds the represented
             // range in some channel is shortened below (and the rest of its
@@ -523,6 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
             } while (again);
             if (ctrl[2] != 0) break;
+            // a shortened chunk: later chunk starts are no longer 64-token aligned,
+            // so this chain's checkpoints stop here and the chain is marked
+            if (L < kC && tc + L < t1 && p.ckpt != nullptr) {
+                if (tid == 0) p.split[chain] = 1;
+                ckpt_ok = false;
+            }
             const int64_t tn = tc + L;
             const int Ln = static_cast<int>(tn >= t1 ? 0 : ((t1 - tn) < kC ? (t1 - tn) : kC));
 
@@ -615,7 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 }
                 mma_commit_w(bar_mma);
             } else if (warp >= 8) {
-                state_pass(tmem + lane_base, warp, s_em, s_dec);
+                float *ck = nullptr;
+                if (ckpt_ok && ((tc - t0) % kC) == 0)
+                    ck = p.ckpt + ((ckpt_slot0 + (tc - t0) / kC) * H + h) * (kD * kD);
+                state_pass(tmem + lane_base, warp, s_em, s_dec, ck, ch);
             }
             tc_fence_before();
             __syncthreads();
@@ -773,6 +794,8 @@ void set_prefill_wait_polls(int64_t copy_polls, int64_t product_polls) {
     g_polls_mma.store(clamp(product_polls));
 }
 
+uint32_t prefill_wait_polls() { return g_polls_mma.load(); }
+
 size_t prefill_workspace_bytes(int64_t N, int B, int H) {
     (void)N;
     return (B > 0 && H > 0) ? 256 : 0;
@@ -819,8 +842,19 @@ cudaError_t launch_prefill(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                            void *workspace, unsigned int *err, int num_sms, cudaStream_t s) {
     const Params p{g, beta, nullptr, nullptr, 0, nullptr, 0, nullptr, cu_seqlens, B, N, H, scale,
                    initial_state, final_state, o, err, static_cast<unsigned int *>(workspace),
-                   kMaxPolls, kMaxPolls};
+                   kMaxPolls, kMaxPolls, nullptr, nullptr};
     return launch_chunk<false>(q, k, v, g, p, o_bf16, num_sms, s);
+}
+
+cudaError_t launch_prefill_checkpoints(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                       const __nv_bfloat16 *v, const float *g, const float *beta,
+                                       const int32_t *cu_seqlens, int B, int64_t N, int H,
+                                       float scale, const float *initial_state, float *ckpt,
+                                       int *split, unsigned int *counter, unsigned int *err,
+                                       int num_sms, cudaStream_t s) {
+    const Params p{g, beta, nullptr, nullptr, 0, nullptr, 0, nullptr, cu_seqlens, B, N, H, scale,
+                   initial_state, nullptr, nullptr, err, counter, kMaxPolls, kMaxPolls, ckpt, split};
+    return launch_chunk<false>(q, k, v, g, p, false, num_sms, s);
 }
 
 cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
@@ -832,7 +866,7 @@ cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                  unsigned int *err, int num_sms, cudaStream_t s) {
     const Params p{nullptr, nullptr, f, b, b_bf16 ? 1 : 0, A_log, alog_mode, dt_bias, cu_seqlens,
                    B, N, H, scale, initial_state, final_state, o, err,
-                   static_cast<unsigned int *>(workspace), kMaxPolls, kMaxPolls};
+                   static_cast<unsigned int *>(workspace), kMaxPolls, kMaxPolls, nullptr, nullptr};
     return launch_chunk<true>(q, k, v, f, p, o_bf16, num_sms, s);
 }
 

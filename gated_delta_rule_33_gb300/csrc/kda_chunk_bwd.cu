@@ -1,0 +1,837 @@
+// kda_chunk_bwd.cu -- chunked KDA backward on tcgen05 tensor cores (sm_103a).
+//
+// The training regime of Kimi Delta Attention in chunked form
+// (data/code-audit.json, finding "dual-kda-execution-regimes": chunked KDA for
+// prefill and training).  The pages print no gradient; this is the exact
+// reverse mode of the chunk-level forward of kda_chunk.cu.  For one chunk of
+// L <= 64 tokens of one (sequence, head) with start state S (k x v), the
+// chunk-end state gradient dS' and the output gradient dO, with the per-channel
+// reference m = Gam_L / 2 and the referenced operands
+//   Qt = scale q e^{Gam - m}, Kr = k e^{Gam - m}, Ks = k e^{m - Gam},
+//   Kh = k e^{Gam_L - Gam},  S_op = Diag(e^m) S,
+//   A_qk = tril(Qt Ks^T),  kk = Kr Ks^T,  A_kk = strict_tril(diag(beta) kk),
+//   T = (I + A_kk)^{-1},  W' = T diag(beta) Kr,  Ut = T diag(beta) V,
+//   U = Ut - W' S_op,
+// the gradients are
+//   dU    = A_qk^T dO + Kh dS'
+//   dS    = Diag(e^{Gam_L}) dS' + Diag(e^m) (Qt^T dO - W'^T dU)      (to the previous chunk)
+//   dA_qk = tril(dO U^T),  dQt = dO S_op^T + dA_qk Ks,  dW' = -dU S_op^T,
+//   dKh   = U dS'^T,
+//   dT    = (dW' Kr^T + dU V^T) diag(beta),  d(beta Kr) = T^T dW',  d(beta V) = T^T dU,
+//   dA_kk = -strict_tril(T^T dT T^T),
+//   dKs   = dA_qk^T Qt + (diag(beta) dA_kk)^T Kr,  dKr = diag(beta) (dA_kk Ks + d(beta Kr)),
+//   dbeta = rowsum(dA_kk . kk) + rowsum(d(beta Kr) . Kr) + rowsum(d(beta V) . V),
+//   dv = diag(beta) d(beta V),  dq = scale dQt e^{Gam - m},
+//   dk = dKr e^{Gam - m} + dKs e^{m - Gam} + dKh e^{Gam_L - Gam},
+//   dGam = dKr.Kr - dKs.Ks - dKh.Kh + dQt.Qt,
+//   dGam_L += colsum(dKh.Kh) + rowsum_v(dS' . Diag(e^{Gam_L}) S),
+//   dg = the reverse cumulative sum of dGam over the chunk's tokens.
+// (The e^{+-m} factors cancel in every product, so these equal the
+// unreferenced formulas term by term.)
+//
+// Products.  Every matrix above is stored once, as an "image": a bf16 tile
+// pair hi = bf16(x), lo = bf16(x - hi) in the 128-byte-swizzled layout of a
+// [rows][cols] operand tile (cols in blocks of 64).  bf16 tcgen05 operands may
+// be K-major or MN-major, so one image serves a matrix and its transpose, and
+// every product is three kind::f16 MMAs per k-step (hi.hi + hi.lo + lo.hi, a
+// 16-bit mantissa; the raw bf16 inputs are exact and need no low part).
+// Images live in a per-CTA scratch area of the workspace (about 530 KB, L2
+// resident); a product copies its two operand images into two 64 KB shared
+// slots with bulk copies, runs its MMAs into tensor memory, and an epilogue
+// writes the result's image(s).  The chain's state gradient dS stays in
+// tensor memory in fp32 for the whole sequence.
+//
+// The chunk-start states S come from the forward prefill kernel, which writes
+// them to the workspace (fp32 [k][v] per chunk) when asked; chains whose
+// forward pass had to shorten a chunk (a per-channel chunk decay beyond the
+// represented range) have no 64-token-aligned states: they are reported as
+// KDA_ERR_DECAY_RANGE and their gradients are written as zeros.
+//
+// Work decomposition: one CTA of 512 threads per (sequence, head) chain at a
+// time, chains from a counter, chunks last to first.  Warp w serves lane
+// quarter w % 4 (tensor-memory lanes 32 (w % 4) .. + 31, also the channel of
+// the element-wise passes) and group w / 4 (16 chunk rows / columns).
+#include <cuda.h>
+
+#include "kda_internal.cuh"
+#include "kda_sm100.cuh"
+#include "kda_chunk_common.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+using namespace chunk;
+
+constexpr int kThreads = 512;
+
+// ---- operand images in the per-CTA scratch ----------------------------------------------
+// rows x cols, split (hi tile then lo tile) unless exact; every size a multiple of 8 KB.
+enum Img : int {
+    I_QK,    // [128][128] rows 0-63 Qt (later dW'), rows 64-127 Kr
+    I_KS,    // [64][128]  Ks
+    I_KH,    // [64][128]  Kh
+    I_V,     // [64][128]  v (exact bf16)
+    I_TB,    // [64][64]   T diag(beta)
+    I_T,     // [64][64]   T
+    I_AQ,    // [64][64]   A_qk
+    I_WT,    // [128][64]  -W'^T
+    I_UT,    // [128][64]  U^T
+    I_SO,    // [128][128] S_op = Diag(e^m) S
+    I_DS,    // [128][128] dS' (chunk-end state gradient)
+    I_DU2,   // [128][128] rows 0-63 dU, rows 64-127 dO
+    I_DAQ,   // [64][64]   dA_qk
+    I_DT,    // [64][64]   dT
+    I_Y,     // [64][64]   dT T^T
+    I_DKK,   // [64][64]   dA_kk
+    I_BDKK,  // [64][64]   diag(beta) dA_kk
+    kNumImg
+};
+__host__ __device__ constexpr uint32_t img_rows(int i) {
+    return (i == I_QK || i == I_WT || i == I_UT || i == I_SO || i == I_DS || i == I_DU2) ? 128 : 64;
+}
+__host__ __device__ constexpr uint32_t img_cols(int i) {
+    return (i == I_TB || i == I_T || i == I_AQ || i == I_WT || i == I_UT || i == I_DAQ ||
+            i == I_DT || i == I_Y || i == I_DKK || i == I_BDKK)
+               ? 64
+               : 128;
+}
+__host__ __device__ constexpr bool img_exact(int i) { return i == I_V; }
+// bytes of one bf16 tile of the image (hi or lo)
+__host__ __device__ constexpr uint32_t img_half(int i) { return img_rows(i) * img_cols(i) * 2; }
+__host__ __device__ constexpr uint32_t img_bytes(int i) {
+    return img_exact(i) ? img_half(i) : 2 * img_half(i);
+}
+__host__ __device__ constexpr uint32_t img_off(int i) {
+    uint32_t o = 0;
+    for (int j = 0; j < i; ++j) o += img_bytes(j);
+    return o;
+}
+constexpr uint32_t kScratchPerCta = img_off(kNumImg);  // 540672
+
+// ---- shared memory (bytes from a 1024-aligned base) -------------------------------------
+constexpr uint32_t SLOT_A = 0;            // operand slot, 64 KB
+constexpr uint32_t SLOT_B = 65536;        // operand slot, 64 KB
+constexpr uint32_t OFF_AT = 131072;       // A_kk column-major fp32 [64][64]
+constexpr uint32_t OFF_TT = 147456;       // T row-major fp32 (inverse work area)
+constexpr uint32_t OFF_KK = 163840;       // kk fp32 [64][64] row-major
+constexpr uint32_t OFF_MISC = 180224;
+constexpr uint32_t M_BETA = 0;            // float[64]
+constexpr uint32_t M_EM = 256;            // float[128] e^{m}
+constexpr uint32_t M_DEC = 768;           // float[128] e^{Gam_L}
+constexpr uint32_t M_PART = 1280;         // float[4][128] partial decay sums per row group
+constexpr uint32_t M_DGL = 3328;          // float[128] sum_v dS'[k][v] S[k][v]
+constexpr uint32_t M_DBETA = 3840;        // float[64]
+constexpr uint32_t M_SUF = 4096;          // float[4][128] dGam sums per row group
+constexpr uint32_t M_P = 6144;            // float[4][256] inverse partial products
+constexpr uint32_t M_T32 = 10240;         // float[16][16]
+constexpr uint32_t M_TDIAG = 11264;       // float[4][16][16]
+constexpr uint32_t M_BAR = 15360;         // 2 mbarriers
+constexpr uint32_t M_CTRL = 15376;        // int[8]: tmem base, chain, abort
+constexpr uint32_t M_KHS = 15424;         // float[128] colsum(dKh . Kh)
+constexpr uint32_t kSmemBytes = OFF_MISC + 15936;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+
+// ---- tensor memory columns (lane = M row of each product) ----
+constexpr uint32_t C_DS = 0;      // dS^T fp32 (lane v, column k), the chain
+constexpr uint32_t C_VB = 128;    // d(beta V)^T (lane v, column r)            transient
+constexpr uint32_t C_H = 192;     // dKh^T (lane k, column r)
+constexpr uint32_t C_S = 256;     // dKs^T (lane k, column s)
+constexpr uint32_t C_R = 320;     // d(beta Kr)^T + (dA_kk Ks)^T (lane k, column r)
+constexpr uint32_t C_TA = 384;    // transient 64 columns
+constexpr uint32_t C_TB = 448;    // Ut^T -> U^T, later dQt^T (lane k, column r)
+
+struct BwdParams {
+    const __nv_bfloat16 *q, *k, *v;
+    const float *g, *beta;
+    const int32_t *cu_seqlens;
+    int B;
+    int64_t N;
+    int H;
+    float scale;
+    const void *dO;
+    int dO_bf16;
+    const float *dSf;
+    const float *ckpt;      // chunk-start states from the forward pass
+    const int *split;       // per chain: the forward pass shortened a chunk
+    float *dq, *dk, *dv, *dg, *dbeta, *dS0;
+    uint8_t *scratch;       // kScratchPerCta bytes per CTA
+    unsigned int *counter;
+    unsigned int *err;
+    uint32_t polls;
+};
+
+// ---- image stores (generic pointers into the global scratch) ------------------------------
+
+__device__ __forceinline__ void put1(uint8_t *img, uint32_t half, uint32_t rows, int i, int j,
+                                     float x) {
+    const uint32_t o = sw128_offset(i, j, rows, 2);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    *reinterpret_cast<__nv_bfloat16 *>(img + o) = hi;
+    if (half != 0)
+        *reinterpret_cast<__nv_bfloat16 *>(img + half + o) =
+            __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// eight consecutive columns j0 .. j0 + 7 (j0 % 8 == 0) of row i: one 16-byte chunk each
+__device__ __forceinline__ void put8(uint8_t *img, uint32_t half, uint32_t rows, int i, int j0,
+                                     const float *x) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+        hw[e] = *reinterpret_cast<const uint32_t *>(&h);
+        lw[e] = *reinterpret_cast<const uint32_t *>(&l);
+    }
+    const uint32_t o = sw128_offset(i, j0, rows, 2);
+    *reinterpret_cast<uint4 *>(img + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    if (half != 0) *reinterpret_cast<uint4 *>(img + half + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// The UT inverse's output policy here: T diag(beta) and T as split images.
+struct TSplitImages {
+    uint8_t *tb, *t;
+    const float *beta;
+    __device__ __forceinline__ void one(int r, int s, float x) const {
+        put1(tb, 8192, 64, r, s, x * beta[s]);
+        put1(t, 8192, 64, r, s, x);
+    }
+    __device__ __forceinline__ void four(int r, int s4, float4 x) const {
+        one(r, s4, x.x);
+        one(r, s4 + 1, x.y);
+        one(r, s4 + 2, x.z);
+        one(r, s4 + 3, x.w);
+    }
+};
+
+// ---- product issue ---------------------------------------------------------------------
+
+// One operand of a product: an image (or a row range of it) in a shared slot.
+// K-major: rows are M / N, `blk` the bytes between 64-column K blocks.
+// MN-major: rows are K, `blk` the bytes between 64-column M / N blocks (LBO).
+struct Opd {
+    uint32_t hi, lo;   // shared addresses of the hi and lo tiles (lo = 0: exact)
+    uint32_t blk;
+    uint32_t mn;
+};
+
+__device__ __forceinline__ Opd opd(uint32_t slot, int img, uint32_t row0, bool mn) {
+    Opd o;
+    o.hi = slot + row0 * 128;
+    o.lo = img_exact(img) ? 0u : o.hi + img_half(img);
+    o.blk = img_rows(img) * 128;
+    o.mn = mn ? 1u : 0u;
+    return o;
+}
+
+__device__ __forceinline__ uint64_t kdesc(const Opd &o, uint32_t base, int kk) {
+    if (o.mn) return smem_desc(base + kk * 2048, o.blk, 1024, kSwizzle128B);
+    return smem_desc(base + (kk >> 2) * o.blk + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+}
+
+// D[tmem d] (+)= A B over `ksteps` k-steps of 16 (M = 128, N columns), as
+// hi.hi + hi.lo + lo.hi per k-step.  Issued by one thread.
+__device__ __forceinline__ void issue(uint32_t d, const Opd &A, const Opd &B, uint32_t N,
+                                     int ksteps, bool accumulate) {
+    const uint32_t id = instr_desc(128, N, kFmtBF16, A.mn, B.mn);
+    uint32_t acc = accumulate ? 1u : 0u;
+    for (int kk = 0; kk < ksteps; ++kk) {
+        const uint64_t ah = kdesc(A, A.hi, kk), bh = kdesc(B, B.hi, kk);
+        mma_f16_ss(d, ah, bh, id, acc);
+        acc = 1u;
+        if (B.lo != 0) mma_f16_ss(d, ah, kdesc(B, B.lo, kk), id, 1u);
+        if (A.lo != 0) mma_f16_ss(d, kdesc(A, A.lo, kk), bh, id, 1u);
+    }
+}
+
+// Sum over the 32 lanes of a warp (every lane gets the total).
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams p) {
+    uint8_t *smem = smem_base();
+    uint8_t *misc = smem + OFF_MISC;
+    float *s_beta = reinterpret_cast<float *>(misc + M_BETA);
+    float *s_em = reinterpret_cast<float *>(misc + M_EM);
+    float *s_dec = reinterpret_cast<float *>(misc + M_DEC);
+    float *s_part = reinterpret_cast<float *>(misc + M_PART);
+    float *s_dgl = reinterpret_cast<float *>(misc + M_DGL);
+    float *s_dbeta = reinterpret_cast<float *>(misc + M_DBETA);
+    float *s_suf = reinterpret_cast<float *>(misc + M_SUF);
+    float *s_khs = reinterpret_cast<float *>(misc + M_KHS);
+    float *s_kk = reinterpret_cast<float *>(smem + OFF_KK);
+    float *s_at = reinterpret_cast<float *>(smem + OFF_AT);
+    uint64_t *bar_load = reinterpret_cast<uint64_t *>(misc + M_BAR);
+    uint64_t *bar_mma = bar_load + 1;
+    int *ctrl = reinterpret_cast<int *>(misc + M_CTRL);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, grp = warp >> 2;
+    const int ch = quarter * 32 + lane;  // channel / tensor-memory lane
+    const int H = p.H;
+    const int num_chains = p.B * H;
+    uint8_t *scr = p.scratch + static_cast<size_t>(blockIdx.x) * kScratchPerCta;
+    auto img = [&](int i) { return scr + img_off(i); };
+
+    if (warp == 0) tmem_alloc(reinterpret_cast<uint32_t *>(&ctrl[0]), 512);
+    if (tid == 0) {
+        mbar_init(bar_load, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        ctrl[2] = 0;
+    }
+    // The strictly upper blocks of T and T diag(beta) are zero in every chunk and
+    // are never written again.
+    for (int e = tid; e < 2 * 16384 / 16; e += kThreads)
+        reinterpret_cast<uint4 *>(img(I_TB))[e] = make_uint4(0u, 0u, 0u, 0u);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = static_cast<uint32_t>(ctrl[0]);
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tl = tmem + lane_base;  // this warp's lane quarter
+    const uint32_t sa = smem_addr(smem + SLOT_A), sb = smem_addr(smem + SLOT_B);
+
+    uint32_t ph_load = 0, ph_mma = 0;
+    bool pend_load = false, pend_mma = false;  // identical in every thread
+    const float kLog2e = 1.4426950408889634f;
+    const float kMaxChunkLog2 = kMaxChunkDecay * kLog2e;
+    const float kMinTokenLog2 = -kMaxTokenDecay * kLog2e;
+
+    // Makes every thread's image and tensor-memory writes visible to the next
+    // bulk copy / product.
+    auto publish = [&]() {
+        fence_proxy_async_global();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    // Copies images ia -> slot A and ib -> slot B (ib < 0: none; ib == ia: once).
+    auto load = [&](int ia, int ib) -> bool {
+        if (tid == 0) {
+            uint32_t bytes = img_bytes(ia) + ((ib >= 0 && ib != ia) ? img_bytes(ib) : 0u);
+            mbar_arrive_expect_tx(bar_load, bytes);
+            bulk_load(smem + SLOT_A, img(ia), img_bytes(ia), bar_load);
+            if (ib >= 0 && ib != ia) bulk_load(smem + SLOT_B, img(ib), img_bytes(ib), bar_load);
+        }
+        pend_load = true;
+        if (!cta_wait(bar_load, ph_load & 1, &ctrl[2], p.err, tid, p.polls)) return false;
+        ph_load++;
+        pend_load = false;
+        return true;
+    };
+    auto mma_done = [&]() -> bool {
+        if (tid == 0) mma_commit(bar_mma);
+        pend_mma = true;
+        if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls)) return false;
+        ph_mma++;
+        pend_mma = false;
+        return true;
+    };
+
+    while (ctrl[2] == 0) {
+        __syncthreads();
+        if (tid == 0) ctrl[1] = static_cast<int>(atomicAdd(p.counter, 1u));
+        __syncthreads();
+        const int chain = ctrl[1];
+        if (chain >= num_chains) break;
+        const int b = chain / H, h = chain % H;
+        int64_t t0 = 0, t1 = p.N;
+        if (p.cu_seqlens != nullptr) {
+            t0 = p.cu_seqlens[b];
+            t1 = p.cu_seqlens[b + 1];
+            if (t0 < 0 || t1 < t0 || t1 > p.N) {
+                if (tid == 0) record_device_error(p.err, kDevInvalidArg);
+                continue;
+            }
+        }
+        const int64_t state_off = (static_cast<int64_t>(b) * H + h) * kD * kD;
+        const bool skip = p.split[chain] != 0;
+        if (skip && tid == 0) record_device_error(p.err, kDevDecayRange);
+
+        // ---- dS^T <- dS_final (lane v, column k holds dS[k][v]) ----
+        {
+            float r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                r[j] = (p.dSf != nullptr) ? p.dSf[state_off + (32 * grp + j) * kD + ch] : 0.f;
+            tmem_st32(tl + C_DS + 32 * grp, r);
+            tmem_wait_st();
+        }
+
+        const int64_t nchunks = (t1 - t0 + kC - 1) / kC;
+        const int64_t slot0 = t0 / kC + b;
+        for (int64_t c = skip ? -1 : nchunks - 1; c >= 0; --c) {
+            const int64_t tc = t0 + c * kC;
+            const int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
+            const float *Sc = p.ckpt + ((slot0 + c) * H + h) * (kD * kD);
+
+            // ---- B1: cumulative decay and the chunk operand images ----
+            float gam[16];
+            {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {  // the forward kernel's clamp and order
+                    const int r = 16 * grp + i;
+                    float gc = 0.f;
+                    if (r < L) {
+                        const float gv = kLog2e * p.g[((tc + r) * H + h) * kD + ch];
+                        gc = gv < kMinTokenLog2 ? kMinTokenLog2 : (gv > 0.f ? 0.f : gv);
+                    }
+                    acc += gc;
+                    gam[i] = acc;
+                }
+                s_part[grp * kD + ch] = acc;
+            }
+            if (tid < kC) s_beta[tid] = tid < L ? p.beta[(tc + tid) * H + h] : 0.f;
+            if (tid < kC) s_dbeta[tid] = 0.f;
+            if (tid < kD) s_dgl[tid] = 0.f;
+            if (tid < kD) s_khs[tid] = 0.f;
+            __syncthreads();
+            float prefix = 0.f, gam_l = 0.f;
+#pragma unroll
+            for (int g2 = 0; g2 < 4; ++g2) {
+                const float pg = s_part[g2 * kD + ch];
+                if (g2 < grp) prefix += pg;
+                gam_l += pg;
+            }
+            if (-gam_l > kMaxChunkLog2 && tid == 0) record_device_error(p.err, kDevDecayRange);
+            const float m = 0.5f * gam_l;
+            if (grp == 0) {
+                s_em[ch] = fast_exp2(m);
+                s_dec[ch] = fast_exp2(gam_l);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                gam[i] += prefix;  // Gam_r in log2 units from here on
+                const int r = 16 * grp + i;
+                float qv = 0.f, kv = 0.f, vv = 0.f, dov = 0.f;
+                if (r < L) {
+                    const int64_t e = ((tc + r) * H + h) * kD + ch;
+                    qv = __bfloat162float(p.q[e]);
+                    kv = __bfloat162float(p.k[e]);
+                    vv = __bfloat162float(p.v[e]);
+                    dov = p.dO_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.dO)[e])
+                                    : static_cast<const float *>(p.dO)[e];
+                }
+                const float eu = fast_exp2(gam[i] - m), ed = fast_exp2(m - gam[i]);
+                const float eh = fast_exp2(gam_l - gam[i]);
+                put1(img(I_QK), img_half(I_QK), 128, r, ch, p.scale * qv * eu);
+                put1(img(I_QK), img_half(I_QK), 128, 64 + r, ch, kv * eu);
+                put1(img(I_KS), img_half(I_KS), 64, r, ch, kv * ed);
+                put1(img(I_KH), img_half(I_KH), 64, r, ch, kv * eh);
+                put1(img(I_V), 0, 64, r, ch, vv);
+                put1(img(I_DU2), img_half(I_DU2), 128, 64 + r, ch, dov);
+            }
+
+            // ---- B2: S_op and dS' images; sum_v dS'[k][v] S[k][v] ----
+            __syncthreads();  // e^{m} of every channel
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float ds[16];
+                tmem_ld16(tl + C_DS + 32 * grp + 16 * half, ds);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int kq = 32 * grp + 16 * half + j;
+                    const float sv = Sc[kq * kD + ch];
+                    put1(img(I_SO), img_half(I_SO), 128, kq, ch, s_em[kq] * sv);
+                    put1(img(I_DS), img_half(I_DS), 128, kq, ch, ds[j]);
+                    const float t = warp_sum(ds[j] * sv);
+                    if (lane == 0) atomicAdd(&s_dgl[kq], t);
+                }
+            }
+            publish();
+
+            // ---- D_A = [Qt; Kr] Ks^T ----
+            if (!load(I_QK, I_KS)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_QK, 0, false), opd(sb, I_KS, 0, false), 64, 8, false);
+            if (!mma_done()) break;
+            {
+                float d16[16];
+                tmem_ld16(tl + C_TA + 16 * grp, d16);
+                tmem_wait_ld();
+                if (quarter < 2) {  // A_qk rows r = ch
+                    float a[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[j] = (16 * grp + j <= ch) ? d16[j] : 0.f;
+                    put8(img(I_AQ), img_half(I_AQ), 64, ch, 16 * grp, a);
+                    put8(img(I_AQ), img_half(I_AQ), 64, ch, 16 * grp + 8, a + 8);
+                } else {  // kk rows r = ch - 64: kept, and A_kk column-major for the inverse
+                    const int r = ch - 64;
+                    const float br = s_beta[r];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = 16 * grp + j;
+                        s_kk[r * 64 + s] = d16[j];
+                        s_at[s * 64 + r] = (s < r) ? br * d16[j] : 0.f;
+                    }
+                }
+            }
+            __syncthreads();
+
+            // ---- T = (I + A_kk)^{-1} on warps 0-3: T and T diag(beta) images ----
+            if (warp < 4) {
+                float *T = reinterpret_cast<float *>(smem + OFF_TT);
+                float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
+                float *T32c = reinterpret_cast<float *>(misc + M_T32);
+                float *P = reinterpret_cast<float *>(misc + M_P);
+                const TSplitImages out{img(I_TB), img(I_T), s_beta};
+                if (tid < 64) {
+                    ut_diag_solve(s_at, T, Tdiag, out, tid);
+                    __syncwarp();
+                    ut_level1(s_at, T, Tdiag, P, T, T32c, out, tid);
+                }
+                inverse_sync();
+                ut_level2(s_at, T, Tdiag, T32c, P, out, tid);
+            }
+            publish();
+
+            // ---- W'^T = Kr^T (T beta)^T ; -W'^T image ----
+            if (!load(I_QK, I_TB)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_QK, 64, true), opd(sb, I_TB, 0, false), 64, 4, false);
+            if (!mma_done()) break;
+            {
+                float w16[16];
+                tmem_ld16(tl + C_TA + 16 * grp, w16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w16[j] = -w16[j];
+                put8(img(I_WT), img_half(I_WT), 128, ch, 16 * grp, w16);
+                put8(img(I_WT), img_half(I_WT), 128, ch, 16 * grp + 8, w16 + 8);
+            }
+            publish();
+
+            // ---- Ut^T = V^T (T beta)^T, then U^T = Ut^T + S_op^T (-W'^T) ----
+            if (!load(I_V, I_TB)) break;
+            if (tid == 0) issue(tmem + C_TB, opd(sa, I_V, 0, true), opd(sb, I_TB, 0, false), 64, 4, false);
+            if (!mma_done()) break;
+            if (!load(I_SO, I_WT)) break;
+            if (tid == 0) issue(tmem + C_TB, opd(sa, I_SO, 0, true), opd(sb, I_WT, 0, true), 64, 8, true);
+            if (!mma_done()) break;
+            {
+                float u16[16];
+                tmem_ld16(tl + C_TB + 16 * grp, u16);
+                tmem_wait_ld();
+                put8(img(I_UT), img_half(I_UT), 128, ch, 16 * grp, u16);
+                put8(img(I_UT), img_half(I_UT), 128, ch, 16 * grp + 8, u16 + 8);
+            }
+            publish();
+
+            // ---- dU^T = dO^T A_qk + dS'^T Kh ; dU image (rows 0-63 of DU2) ----
+            if (!load(I_DU2, I_AQ)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 64, true), opd(sb, I_AQ, 0, true), 64, 4, false);
+            if (!mma_done()) break;
+            if (!load(I_DS, I_KH)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DS, 0, true), opd(sb, I_KH, 0, false), 64, 8, true);
+            if (!mma_done()) break;
+            {
+                float d16[16];
+                tmem_ld16(tl + C_TA + 16 * grp, d16);  // dU^T[v = ch][r]
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) put1(img(I_DU2), img_half(I_DU2), 128, 16 * grp + j, ch, d16[j]);
+            }
+            publish();
+
+            // ---- P^T = dO^T Qt - dU^T W'^T... ; dS <- e^{Gam_L} dS' + e^m P ----
+            if (!load(I_DU2, I_QK)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 64, true), opd(sb, I_QK, 0, true), 128, 4, false);
+            if (!mma_done()) break;
+            if (!load(I_DU2, I_WT)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 0, true), opd(sb, I_WT, 0, false), 128, 4, true);
+            if (!mma_done()) break;
+            {
+                float pv[32], ds[32];
+                tmem_ld32(tl + C_TA + 32 * grp, pv);
+                tmem_ld32(tl + C_DS + 32 * grp, ds);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int kq = 32 * grp + j;
+                    ds[j] = s_dec[kq] * ds[j] + s_em[kq] * pv[j];
+                }
+                tmem_st32(tl + C_DS + 32 * grp, ds);
+                tmem_wait_st();
+            }
+            publish();
+
+            // ---- dA_qk = tril(dO U^T) (lanes 64-127 of [dU; dO] U^T) ----
+            if (!load(I_DU2, I_UT)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 0, false), opd(sb, I_UT, 0, true), 64, 8, false);
+            if (!mma_done()) break;
+            if (quarter >= 2) {
+                const int r = ch - 64;
+                float d16[16];
+                tmem_ld16(tl + C_TA + 16 * grp, d16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) d16[j] = (16 * grp + j <= r) ? d16[j] : 0.f;
+                put8(img(I_DAQ), img_half(I_DAQ), 64, r, 16 * grp, d16);
+                put8(img(I_DAQ), img_half(I_DAQ), 64, r, 16 * grp + 8, d16 + 8);
+            }
+            publish();
+
+            // ---- dKs^T = Qt^T dA_qk ----
+            if (!load(I_QK, I_DAQ)) break;
+            if (tid == 0) issue(tmem + C_S, opd(sa, I_QK, 0, true), opd(sb, I_DAQ, 0, true), 64, 4, false);
+            if (!mma_done()) break;
+
+            // ---- [-dW'^T | dQt^T] = S_op [dU; dO]^T ; dQt^T += Ks^T dA_qk^T ----
+            if (!load(I_SO, I_DU2)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_SO, 0, false), opd(sb, I_DU2, 0, false), 128, 8, false);
+            if (!mma_done()) break;
+            if (!load(I_KS, I_DAQ)) break;
+            if (tid == 0) issue(tmem + C_TB, opd(sa, I_KS, 0, true), opd(sb, I_DAQ, 0, false), 64, 4, true);
+            if (!mma_done()) break;
+            {
+                float d16[16];  // -dW'^T[k = ch][r]: dW'[r][k] into rows 0-63 of the QK image (Qt is dead)
+                tmem_ld16(tl + C_TA + 16 * grp, d16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) put1(img(I_QK), img_half(I_QK), 128, 16 * grp + j, ch, -d16[j]);
+            }
+            publish();
+
+            // ---- dKh^T = dS' U^T ----
+            if (!load(I_DS, I_UT)) break;
+            if (tid == 0) issue(tmem + C_H, opd(sa, I_DS, 0, false), opd(sb, I_UT, 0, true), 64, 8, false);
+            if (!mma_done()) break;
+
+            // ---- dT = (dW' Kr^T + dU V^T) diag(beta) (lanes 0-63) ----
+            if (!load(I_QK, I_V)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_QK, 0, false), opd(sa, I_QK, 64, false), 64, 8, false);
+            if (!mma_done()) break;
+            if (!load(I_DU2, I_V)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 0, false), opd(sb, I_V, 0, false), 64, 8, true);
+            if (!mma_done()) break;
+            if (quarter < 2) {
+                float d16[16];
+                tmem_ld16(tl + C_TA + 16 * grp, d16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) d16[j] *= s_beta[16 * grp + j];
+                put8(img(I_DT), img_half(I_DT), 64, ch, 16 * grp, d16);
+                put8(img(I_DT), img_half(I_DT), 64, ch, 16 * grp + 8, d16 + 8);
+            }
+            publish();
+
+            // ---- d(beta Kr)^T = dW'^T T and d(beta V)^T = dU^T T ----
+            if (!load(I_QK, I_T)) break;
+            if (tid == 0) issue(tmem + C_R, opd(sa, I_QK, 0, true), opd(sb, I_T, 0, true), 64, 4, false);
+            if (!mma_done()) break;
+            if (!load(I_DU2, I_T)) break;
+            if (tid == 0) issue(tmem + C_VB, opd(sa, I_DU2, 0, true), opd(sb, I_T, 0, true), 64, 4, false);
+            if (!mma_done()) break;
+            {
+                // d(beta V)^T[v = ch][r]: dv = beta_r d(beta V); dbeta += sum_v d(beta V) v.
+                // d(beta Kr)^T[k = ch][r]: dbeta += sum_k d(beta Kr) Kr.
+                float vb[16], rb[16];
+                tmem_ld16(tl + C_VB + 16 * grp, vb);
+                tmem_ld16(tl + C_R + 16 * grp, rb);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * grp + j;
+                    float vv = 0.f, kr = 0.f;
+                    if (r < L) {
+                        const int64_t e = ((tc + r) * H + h) * kD + ch;
+                        vv = __bfloat162float(p.v[e]);
+                        kr = __bfloat162float(p.k[e]) * fast_exp2(gam[j] - m);
+                        p.dv[e] = s_beta[r] * vb[j];
+                    }
+                    const float t = warp_sum(vb[j] * vv + rb[j] * kr);
+                    if (lane == 0) atomicAdd(&s_dbeta[r], t);
+                }
+            }
+
+            // ---- Y = dT T^T (lanes 0-63) ----
+            if (!load(I_DT, I_T)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DT, 0, false), opd(sb, I_T, 0, false), 64, 4, false);
+            if (!mma_done()) break;
+            if (quarter < 2) {
+                float d16[16];
+                tmem_ld16(tl + C_TA + 16 * grp, d16);
+                tmem_wait_ld();
+                put8(img(I_Y), img_half(I_Y), 64, ch, 16 * grp, d16);
+                put8(img(I_Y), img_half(I_Y), 64, ch, 16 * grp + 8, d16 + 8);
+            }
+            publish();
+
+            // ---- dA_kk = -strict_tril(T^T Y) (lanes 0-63); dbeta += rowsum(dA_kk kk) ----
+            if (!load(I_T, I_Y)) break;
+            if (tid == 0) issue(tmem + C_TA, opd(sa, I_T, 0, true), opd(sb, I_Y, 0, true), 64, 4, false);
+            if (!mma_done()) break;
+            if (quarter < 2) {
+                const int r = ch;
+                float d16[16], bd[16];
+                tmem_ld16(tl + C_TA + 16 * grp, d16);
+                tmem_wait_ld();
+                float part = 0.f;
+                const float br = s_beta[r];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s = 16 * grp + j;
+                    d16[j] = (s < r) ? -d16[j] : 0.f;
+                    bd[j] = br * d16[j];
+                    part += d16[j] * s_kk[r * 64 + s];
+                }
+                atomicAdd(&s_dbeta[r], part);
+                put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp, d16);
+                put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp + 8, d16 + 8);
+                put8(img(I_BDKK), img_half(I_BDKK), 64, r, 16 * grp, bd);
+                put8(img(I_BDKK), img_half(I_BDKK), 64, r, 16 * grp + 8, bd + 8);
+            }
+            publish();
+
+            // ---- dKs^T += Kr^T (beta dA_kk) ; (dA_kk Ks)^T into C_R ----
+            if (!load(I_QK, I_BDKK)) break;
+            if (tid == 0) issue(tmem + C_S, opd(sa, I_QK, 64, true), opd(sb, I_BDKK, 0, true), 64, 4, true);
+            if (!mma_done()) break;
+            if (!load(I_KS, I_DKK)) break;
+            if (tid == 0) issue(tmem + C_R, opd(sa, I_KS, 0, true), opd(sb, I_DKK, 0, false), 64, 4, true);
+            if (!mma_done()) break;
+
+            // ---- assembly: dq, dk, dg, dbeta (lane k = ch, rows r = 16 grp + j) ----
+            {
+                float dqt[16], dkh[16], dks[16], dkr[16];
+                tmem_ld16(tl + C_TB + 16 * grp, dqt);
+                tmem_ld16(tl + C_H + 16 * grp, dkh);
+                tmem_ld16(tl + C_S + 16 * grp, dks);
+                tmem_ld16(tl + C_R + 16 * grp, dkr);
+                tmem_wait_ld();
+                float dgam[16], khsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * grp + j;
+                    dgam[j] = 0.f;
+                    if (r < L) {
+                        const int64_t e = ((tc + r) * H + h) * kD + ch;
+                        const float qv = __bfloat162float(p.q[e]), kv = __bfloat162float(p.k[e]);
+                        const float eu = fast_exp2(gam[j] - m), ed = fast_exp2(m - gam[j]);
+                        const float eh = fast_exp2(gam_l - gam[j]);
+                        const float Qt = p.scale * qv * eu, Kr = kv * eu, Ks = kv * ed, Kh = kv * eh;
+                        const float dKr = s_beta[r] * dkr[j];
+                        p.dq[e] = p.scale * dqt[j] * eu;
+                        p.dk[e] = dKr * eu + dks[j] * ed + dkh[j] * eh;
+                        const float khp = dkh[j] * Kh;
+                        dgam[j] = dKr * Kr - dks[j] * Ks - khp + dqt[j] * Qt;
+                        khsum += khp;
+                    }
+                }
+                // suffix sums over the chunk's rows: this group's rows, then the later groups
+                float run = 0.f;
+#pragma unroll
+                for (int j = 15; j >= 0; --j) {
+                    run += dgam[j];
+                    dgam[j] = run;
+                }
+                s_suf[grp * kD + ch] = run;
+                atomicAdd(&s_khs[ch], khsum);
+                __syncthreads();
+                float later = 0.f;
+#pragma unroll
+                for (int g2 = 0; g2 < 4; ++g2)
+                    if (g2 > grp) later += s_suf[g2 * kD + ch];
+                // dGam_L = colsum(dKh . Kh) + e^{Gam_L} sum_v dS' S, added to every row
+                const float dgl = s_khs[ch] + s_dec[ch] * s_dgl[ch];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * grp + j;
+                    if (r < L) p.dg[((tc + r) * H + h) * kD + ch] = dgam[j] + later + dgl;
+                }
+                if (tid < L) p.dbeta[(tc + tid) * H + h] = s_dbeta[tid];
+            }
+            publish();
+        }
+        if (ctrl[2] != 0) break;
+
+        // ---- dS0 ----
+        if (p.dS0 != nullptr) {
+            float r[32];
+            tmem_ld32(tl + C_DS + 32 * grp, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p.dS0[state_off + (32 * grp + j) * kD + ch] = skip ? 0.f : r[j];
+        }
+        if (skip) {  // chains without 64-token-aligned checkpoints: zero gradients
+            for (int64_t e = t0 * kD + tid; e < t1 * kD; e += kThreads) {
+                const int64_t t = e / kD, c2 = e % kD;
+                const int64_t i = (t * H + h) * kD + c2;
+                p.dq[i] = 0.f;
+                p.dk[i] = 0.f;
+                p.dv[i] = 0.f;
+                p.dg[i] = 0.f;
+                if (c2 == 0) p.dbeta[t * H + h] = 0.f;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    // Drain: wait for a copy or product still in flight (full bound) before the
+    // tensor memory is released and the CTA exits.
+    if (tid == 0) {
+        if (pend_load) mbar_wait_bounded(bar_load, ph_load & 1, kMaxPolls);
+        if (pend_mma) mbar_wait_bounded(bar_mma, ph_mma & 1, kMaxPolls);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace_bytes(int64_t N, int B, int H, int ctas) {
+    const size_t head = 512 + ((static_cast<size_t>(B) * H * sizeof(int) + 255) / 256) * 256;
+    const size_t ckpt = (static_cast<size_t>(N / kC) + static_cast<size_t>(B)) * H * kD * kD * sizeof(float);
+    return head + ckpt + static_cast<size_t>(ctas) * kScratchPerCta;
+}
+
+cudaError_t launch_chunk_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                  const __nv_bfloat16 *v, const float *g, const float *beta,
+                                  const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+                                  const float *S0, const void *dO, bool dO_bf16, const float *dSf,
+                                  float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                                  float *dS0, void *workspace, int ctas, unsigned int *err,
+                                  int num_sms, cudaStream_t s) {
+    if (B == 0 || H == 0) return cudaSuccess;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t flags_bytes = ((static_cast<size_t>(B) * H * sizeof(int) + 255) / 256) * 256;
+    unsigned int *counters = reinterpret_cast<unsigned int *>(ws);  // [0] forward, [64] backward
+    int *split = reinterpret_cast<int *>(ws + 512);
+    float *ckpt = reinterpret_cast<float *>(ws + 512 + flags_bytes);
+    const size_t ckpt_bytes = (static_cast<size_t>(N / kC) + static_cast<size_t>(B)) * H * kD * kD * sizeof(float);
+    uint8_t *scratch = ws + 512 + flags_bytes + ckpt_bytes;
+
+    cudaError_t e = cudaMemsetAsync(ws, 0, 512 + flags_bytes, s);
+    if (e != cudaSuccess) return e;
+    // forward pass: chunk-start states only
+    e = launch_prefill_checkpoints(q, k, v, g, beta, cu_seqlens, B, N, H, scale, S0, ckpt, split,
+                                   counters, err, num_sms, s);
+    if (e != cudaSuccess) return e;
+
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_bwd_kernel), static_cast<int>(kSmemAlloc));
+    if (e != cudaSuccess) return e;
+    BwdParams p;
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = cu_seqlens; p.B = B; p.N = N; p.H = H; p.scale = scale;
+    p.dO = dO; p.dO_bf16 = dO_bf16 ? 1 : 0; p.dSf = dSf;
+    p.ckpt = ckpt; p.split = split;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dg; p.dbeta = dbeta; p.dS0 = dS0;
+    p.scratch = scratch;
+    p.counter = counters + 64;
+    p.err = err;
+    p.polls = prefill_wait_polls();
+    chunk_bwd_kernel<<<ctas, kThreads, kSmemAlloc, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -126,6 +126,27 @@ __device__ __forceinline__ void store_tbeta4(uint8_t *tb, uint8_t *tb16, int r, 
     *reinterpret_cast<uint2 *>(tb16 + 8192 + sw128_offset(r, s4, 64, 2)) = lv;
 }
 
+// Where the UT inverse writes its result, as each block of T is final: the
+// forward kernel's T beta operand tiles in shared memory.  (The chunked
+// backward supplies its own policy with the same two members.)
+struct TbetaTiles {
+    uint8_t *tb, *tb16;
+    const float *beta;
+    // one element T[r][s]
+    __device__ __forceinline__ void one(int r, int s, float t) const {
+        const float xb = t * beta[s];
+        st_f32(tb, sw128_offset(kTbRow0 + r, s, kTbRows, 4), to_tf32(xb));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16 *>(tb16 + sw128_offset(r, s, 64, 2)) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(tb16 + 8192 + sw128_offset(r, s, 64, 2)) = lo;
+    }
+    // T[r][s4 .. s4 + 3]
+    __device__ __forceinline__ void four(int r, int s4, float4 t) const {
+        store_tbeta4(tb, tb16, r, s4, t, beta);
+    }
+};
+
 // ---- T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk ----
 // Layouts (fp32, shared memory):
 //   At     A column-major, At[s * 64 + r] = A[r][s] (zero for s >= r)
@@ -186,8 +207,9 @@ __device__ __forceinline__ int y_idx(int r, int c) { return r * 32 + (((c >> 2) 
 // each reading one block column of At as four 16-byte loads, the next column
 // loaded while the current one is applied.  Writes T (row-major), Tdiag and
 // the T beta operand tiles.
-__device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *Tdiag, uint8_t *tb,
-                                              uint8_t *tb16, const float *beta, int tid) {
+template <class Out>
+__device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *Tdiag, const Out &out,
+                                              int tid) {
     const int bb = tid >> 4, j = tid & 15, base = bb * 16;
     const float *Ab = At + base * 64 + base;   // Ab[s * 64 + r] = A_bb[r][s]
     // x as packed row pairs; a step updates whole pairs from the one holding
@@ -232,26 +254,19 @@ __device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *
     for (int q4 = 0; q4 < 4; ++q4)
         *reinterpret_cast<float4 *>(Td + 4 * q4) =
             make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
-    // T beta of the diagonal block, column j (16 rows)
-    const float bj = beta[base + j];
+    // T (beta) of the diagonal block, column j (16 rows)
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const float xb = x[r] * bj;
-        st_f32(tb, sw128_offset(kTbRow0 + base + r, base + j, kTbRows, 4), to_tf32(xb));
-        const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
-        *reinterpret_cast<__nv_bfloat16 *>(tb16 + sw128_offset(base + r, base + j, 64, 2)) = hi;
-        *reinterpret_cast<__nv_bfloat16 *>(tb16 + 8192 + sw128_offset(base + r, base + j, 64, 2)) = lo;
-    }
+    for (int r = 0; r < 16; ++r) out.one(base + r, base + j, x[r]);
 }
 
 // Level 1 (warps 0-1, warp t / 2 for target t = 0, 2; it solved T_tt and
 // T_{t+1,t+1} itself): T_{t+1,t} = -T_{t+1,t+1} (A_{t+1,t} T_tt).  Lane l owns
 // rows r0 = 2 (l / 4), r0 + 1 and columns c0 = 4 (l % 4) .. + 3 of the block.
 // T_10 goes to T (row-major, part of T_top in level 2), T_32 to T32c.
+template <class Out>
 __device__ __forceinline__ void ut_level1(const float *At, const float *T, const float *Tdiag,
-                                          float *P, float *Tw, float *T32c, uint8_t *tb,
-                                          uint8_t *tb16, const float *beta, int tid) {
+                                          float *P, float *Tw, float *T32c, const Out &out,
+                                          int tid) {
     const int t = 2 * (tid >> 5), l = tid & 31, r0 = 2 * (l >> 2), c0 = 4 * (l & 3);
     float *Pt = P + (t >> 1) * 256;
     Acc2x4 a;
@@ -272,8 +287,8 @@ __device__ __forceinline__ void ut_level1(const float *At, const float *T, const
         *reinterpret_cast<float2 *>(T32c + (c0 + 2) * 16 + r0) = make_float2(x0.z, x1.z);
         *reinterpret_cast<float2 *>(T32c + (c0 + 3) * 16 + r0) = make_float2(x0.w, x1.w);
     }
-    store_tbeta4(tb, tb16, 16 * (t + 1) + r0, 16 * t + c0, x0, beta);
-    store_tbeta4(tb, tb16, 16 * (t + 1) + r0 + 1, 16 * t + c0, x1, beta);
+    out.four(16 * (t + 1) + r0, 16 * t + c0, x0);
+    out.four(16 * (t + 1) + r0 + 1, 16 * t + c0, x1);
 }
 
 // Level 2 (warps 0-3): the lower-left 32x32 block X = T[32:64, 0:32] =
@@ -282,9 +297,9 @@ __device__ __forceinline__ void ut_level1(const float *At, const float *T, const
 // owns rows 16 (w % 2) .. + 15 and columns 16 (w / 2) .. + 15 of Y and X, so
 // every triangular bound is warp-uniform; lane l owns rows r0 = 16 (w % 2) +
 // 2 (l / 4), r0 + 1 and columns c0 = 16 (w / 2) + 4 (l % 4) .. + 3.
+template <class Out>
 __device__ __forceinline__ void ut_level2(const float *At, const float *T, const float *Tdiag,
-                                          const float *T32c, float *Y, uint8_t *tb,
-                                          uint8_t *tb16, const float *beta, int tid) {
+                                          const float *T32c, float *Y, const Out &out, int tid) {
     const int w = tid >> 5, l = tid & 31, rh = w & 1, cb = w >> 1;
     const int r0 = 16 * rh + 2 * (l >> 2), c0 = 16 * cb + 4 * (l & 3);
     Acc2x4 a;
@@ -309,8 +324,8 @@ __device__ __forceinline__ void ut_level2(const float *At, const float *T, const
             b.step(*reinterpret_cast<const float2 *>(Tdiag + 3 * 256 + (s - 16) * 16 + r0 - 16),
                    *reinterpret_cast<const float4 *>(Y + y_idx(s, c0)));
     }
-    store_tbeta4(tb, tb16, 32 + r0, c0, b.neg_row(0), beta);
-    store_tbeta4(tb, tb16, 33 + r0, c0, b.neg_row(1), beta);
+    out.four(32 + r0, c0, b.neg_row(0));
+    out.four(33 + r0, c0, b.neg_row(1));
 }
 
 // ---- host: TMA tensor maps -------------------------------------------------------------

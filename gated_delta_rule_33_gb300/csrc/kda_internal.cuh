@@ -14,6 +14,7 @@ enum : unsigned int {
     kDevOk = 0,
     kDevInvalidArg = 1,      // KDA_ERR_INVALID_ARG: a bad cu_seqlens entry
     kDevTimeout = 7,         // KDA_ERR_DEVICE_TIMEOUT: a bounded wait ran out
+    kDevDecayRange = 11,     // KDA_ERR_DECAY_RANGE: chunked backward, a chain it cannot take
 };
 
 __device__ __forceinline__ void record_device_error(unsigned int *err, unsigned int code) {
@@ -101,6 +102,33 @@ cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
 // Bounds of the chunked prefill's main-loop waits for later launches (copies,
 // products; a negative value restores the default).  Test use only.
 void set_prefill_wait_polls(int64_t copy_polls, int64_t product_polls);
+
+// Bound of the product waits set by set_prefill_wait_polls (the chunked
+// backward uses it for all its waits).
+uint32_t prefill_wait_polls();
+
+// The chunked prefill as the forward pass of the chunked backward: no output,
+// no final state; the state at the start of every 64-token chunk of chain
+// (b, h) goes to ckpt[((cu[b] / 64 + b + c) * H + h) * 128 * 128 ..], and
+// split[b * H + h] is set if a chunk had to be shortened.  counter: one zeroed
+// unsigned int.
+cudaError_t launch_prefill_checkpoints(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                       const __nv_bfloat16 *v, const float *g, const float *beta,
+                                       const int32_t *cu_seqlens, int B, int64_t N, int H,
+                                       float scale, const float *initial_state, float *ckpt,
+                                       int *split, unsigned int *counter, unsigned int *err,
+                                       int num_sms, cudaStream_t s);
+
+// Chunked backward (kda_chunk_bwd.cu).
+constexpr int kChunkBwdMaxCtas = 160;
+size_t chunk_bwd_workspace_bytes(int64_t N, int B, int H, int ctas);
+cudaError_t launch_chunk_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                  const __nv_bfloat16 *v, const float *g, const float *beta,
+                                  const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+                                  const float *S0, const void *dO, bool dO_bf16, const float *dSf,
+                                  float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                                  float *dS0, void *workspace, int ctas, unsigned int *err,
+                                  int num_sms, cudaStream_t s);
 
 // Device address and size of the built-in prefill scratch on the current device
 // (looked up once per device; see kda_chunk.cu).

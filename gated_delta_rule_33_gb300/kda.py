@@ -93,6 +93,11 @@ def load():
         lib.kda_recurrent_backward.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, I, P,
                                                P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.kda_recurrent_backward.restype = I
+        lib.kda_chunk_backward_workspace_size.argtypes = [I64, I, I, I, I]
+        lib.kda_chunk_backward_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_backward.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, I, P,
+                                           P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.kda_chunk_backward.restype = I
         lib.kda_recurrent_decode_gated.argtypes = [P, P, P, P, I, P, I, P, I, P, P, I, P, I, I, I,
                                                    I, I, F, P, I, P]
         lib.kda_recurrent_decode_gated.restype = I
@@ -261,6 +266,23 @@ def kda_recurrent_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, d
     _check(st, "kda_recurrent_backward")
 
 
+def kda_chunk_backward_workspace_size(N, B, H, K=128, V=128) -> int:
+    return int(load().kda_chunk_backward_workspace_size(N, B, H, K, V))
+
+
+def kda_chunk_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final,
+                       dq, dk, dv, dg, dbeta, dS0, workspace, stream=None):
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_chunk_backward(
+        _p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), B, N, H, K, V, float(scale),
+        _p(initial_state), _p(dO), _dtype_code(dO), _p(dS_final), _p(dq), _p(dk), _p(dv), _p(dg),
+        _p(dbeta), _p(dS0), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, q.device))
+    _check(st, "kda_chunk_backward")
+
+
 def kda_recurrent_decode_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, state_pool,
                                state_indices, scale, o, stream=None):
     """state_indices None: slot b for sequence b."""
@@ -384,6 +406,25 @@ def backward(q, k, v, g, beta, dO, cu_seqlens=None, scale=1.0, initial_state=Non
                      device=dev)
     kda_recurrent_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final, dq,
                            dk, dv, dg, dbeta, dS0, ws, stream)
+    return dq, dk, dv, dg, dbeta, dS0
+
+
+def backward_chunked(q, k, v, g, beta, dO, cu_seqlens=None, scale=1.0, initial_state=None,
+                     dS_final=None, want_dS0=True, stream=None):
+    """Gradients of the recurrence by the chunked tensor-core backward;
+    returns (dq, dk, dv, dg, dbeta, dS0 or None)."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.device
+    dq, dk, dg = (torch.empty(N, H, K, device=dev) for _ in range(3))
+    dv = torch.empty(N, H, V, device=dev)
+    dbeta = torch.empty(N, H, device=dev)
+    dS0 = torch.empty(B, H, K, V, device=dev) if want_dS0 else None
+    ws = torch.empty(kda_chunk_backward_workspace_size(N, B, H, K, V), dtype=torch.uint8,
+                     device=dev)
+    kda_chunk_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final, dq, dk,
+                       dv, dg, dbeta, dS0, ws, stream)
     return dq, dk, dv, dg, dbeta, dS0
 
 

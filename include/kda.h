@@ -57,8 +57,8 @@ typedef enum kda_status {
     KDA_ERR_NONFINITE = 8,          /* reserved for debug checks */
     KDA_ERR_NOT_IMPLEMENTED = 9,
     KDA_ERR_NO_DEVICE = 10,         /* no usable sm_103 device / driver */
-    KDA_ERR_DECAY_RANGE = 11        /* reserved: no entry point returns it (the chunked
-                                       prefill computes chunks of any decay) */
+    KDA_ERR_DECAY_RANGE = 11        /* kda_chunk_backward: a (sequence, head) whose chunk
+                                       decay exceeds one chunk's range (device-side) */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -329,6 +329,47 @@ kda_status kda_recurrent_backward(const void *q, const void *k, const void *v,
                                   float *dq, float *dk, float *dv, float *dg, float *dbeta,
                                   float *dS0, void *workspace, size_t workspace_bytes,
                                   void *stream);
+
+/*
+ * kda_chunk_backward -- the same gradients as kda_recurrent_backward (same
+ * arguments, layouts and results), in the chunked form the pages name for
+ * training ("chunked KDA for training", code-audit.json, finding
+ * "dual-kda-execution-regimes"), on the tensor cores.  A forward pass of the
+ * chunked prefill keeps the state at the start of every 64-token chunk in the
+ * workspace; then each (sequence, head) walks its chunks last to first, with
+ * the state gradient in tensor memory, and per chunk forms the reverse mode
+ * of the chunk-level (WY/UT) forward: dU = A_qk^T dO + Khat dS',
+ * dS = Diag(e^{Gam_L}) dS' + Qbar^T dO - W^T dU, and the gradients of
+ * A_qk, A_kk (through T = (I + A_kk)^-1), W, U-tilde and the decay factors,
+ * down to dq, dk, dv, dg, dbeta.  Every product runs as tcgen05 bf16 MMAs on
+ * operands split in a high and a low bf16 part (three products per pair,
+ * a 16-bit significand) with fp32 accumulation; the chunk-start states come
+ * from the tf32 forward, so the gradients agree with the exact reverse mode
+ * to about 1e-3 relative L2 (the forward's state precision), not to fp32
+ * rounding as kda_recurrent_backward does.
+ *
+ * A (sequence, head) whose forward pass had to shorten a chunk (a chunk's
+ * decay -sum(g) in some channel above 160) has no 64-token-aligned states:
+ * its gradients are written as zeros and the device error word is set to
+ * KDA_ERR_DECAY_RANGE; kda_recurrent_backward computes those.
+ *
+ *   workspace  device, >= kda_chunk_backward_workspace_size() bytes, 16-byte
+ *              aligned: the chunk-start states ((N / 64 + B) H 64 KB, 400 MB
+ *              for N = 4096, H = 96) plus 528 KB of operand scratch for each
+ *              of up to min(B H, 160) CTAs; its contents are scratch.
+ * The bounded waits use the product limit of kda_debug_set_wait_limit.
+ */
+size_t kda_chunk_backward_workspace_size(int64_t N, int B, int H, int K, int V);
+
+kda_status kda_chunk_backward(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta,
+                              const int32_t *cu_seqlens, int B,
+                              int64_t N, int H, int K, int V, float scale,
+                              const float *initial_state,
+                              const void *dO, kda_dtype dO_dtype, const float *dS_final,
+                              float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                              float *dS0, void *workspace, size_t workspace_bytes,
+                              void *stream);
 
 /*
  * kda_gate_backward -- gradients of the gate (the training regime, after
