@@ -77,8 +77,8 @@ enum Img : int {
     I_AQ,    // [64][64]   A_qk
     I_WT,    // [128][64]  -W'^T
     I_UT,    // [128][64]  U^T
-    I_SO,    // [128][128] S_op = Diag(e^m) S
-    I_DS,    // [128][128] dS' (chunk-end state gradient)
+    I_SO,    // [128][128] S_op^T: row v holds e^{m_k} S[k][v] over k
+    I_DS,    // [128][128] dS'^T: row v holds dS'[k][v] over k (chunk-end state gradient)
     I_DU2,   // [128][128] rows 0-63 dU, rows 64-127 dO
     I_DAQ,   // [64][64]   dA_qk
     I_DT,    // [64][64]   dT
@@ -114,7 +114,7 @@ constexpr uint32_t SLOT_A = 0;            // operand slot, 64 KB
 constexpr uint32_t SLOT_B = 65536;        // operand slot, 64 KB
 constexpr uint32_t OFF_AT = 131072;       // A_kk column-major fp32 [64][64]
 constexpr uint32_t OFF_TT = 147456;       // T row-major fp32 (inverse work area)
-constexpr uint32_t OFF_KK = 163840;       // kk fp32 [64][64] row-major
+constexpr uint32_t OFF_KK = 163840;       // kk fp32 [64][64] column-major
 constexpr uint32_t OFF_MISC = 180224;
 constexpr uint32_t M_BETA = 0;            // float[64]
 constexpr uint32_t M_EM = 256;            // float[128] e^{m}
@@ -129,7 +129,8 @@ constexpr uint32_t M_TDIAG = 11264;       // float[4][16][16]
 constexpr uint32_t M_BAR = 15360;         // 2 mbarriers
 constexpr uint32_t M_CTRL = 15376;        // int[8]: tmem base, chain, abort
 constexpr uint32_t M_KHS = 15424;         // float[128] colsum(dKh . Kh)
-constexpr uint32_t kSmemBytes = OFF_MISC + 15936;
+constexpr uint32_t M_GL = 15936;          // float[128] Gam_L (log2 units)
+constexpr uint32_t kSmemBytes = OFF_MISC + 16448;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 // ---- tensor memory columns (lane = M row of each product) ----
@@ -190,6 +191,23 @@ __device__ __forceinline__ void put8(uint8_t *img, uint32_t half, uint32_t rows,
     if (half != 0) *reinterpret_cast<uint4 *>(img + half + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
+// four consecutive columns j0 .. j0 + 3 (j0 % 4 == 0) of row i: one 8-byte store each
+__device__ __forceinline__ void put4(uint8_t *img, uint32_t half, uint32_t rows, int i, int j0,
+                                     const float *x) {
+    uint32_t hw[2], lw[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+        hw[e] = *reinterpret_cast<const uint32_t *>(&h);
+        lw[e] = *reinterpret_cast<const uint32_t *>(&l);
+    }
+    const uint32_t o = sw128_offset(i, j0, rows, 2);
+    *reinterpret_cast<uint2 *>(img + o) = make_uint2(hw[0], hw[1]);
+    if (half != 0) *reinterpret_cast<uint2 *>(img + half + o) = make_uint2(lw[0], lw[1]);
+}
+
 // The UT inverse's output policy here: T diag(beta) and T as split images.
 struct TSplitImages {
     uint8_t *tb, *t;
@@ -199,10 +217,11 @@ struct TSplitImages {
         put1(t, 8192, 64, r, s, x);
     }
     __device__ __forceinline__ void four(int r, int s4, float4 x) const {
-        one(r, s4, x.x);
-        one(r, s4 + 1, x.y);
-        one(r, s4 + 2, x.z);
-        one(r, s4 + 3, x.w);
+        const float v[4] = {x.x, x.y, x.z, x.w};
+        const float vb[4] = {x.x * beta[s4], x.y * beta[s4 + 1], x.z * beta[s4 + 2],
+                             x.w * beta[s4 + 3]};
+        put4(tb, 8192, 64, r, s4, vb);
+        put4(t, 8192, 64, r, s4, v);
     }
 };
 
@@ -226,31 +245,135 @@ __device__ __forceinline__ Opd opd(uint32_t slot, int img, uint32_t row0, bool m
     return o;
 }
 
-__device__ __forceinline__ uint64_t kdesc(const Opd &o, uint32_t base, int kk) {
-    if (o.mn) return smem_desc(base + kk * 2048, o.blk, 1024, kSwizzle128B);
-    return smem_desc(base + (kk >> 2) * o.blk + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+// Descriptor of k-step kk (16 elements) of an operand, from its descriptor at
+// k-step 0 (`d0`, built for the hi or lo tile): the start address advances by
+// whole 8-row groups (MN-major) or by 32 bytes inside the 128-byte rows and a
+// block per four steps (K-major).
+__device__ __forceinline__ uint64_t kstep(const Opd &o, uint64_t d0, int kk) {
+    const uint32_t off = o.mn ? kk * 2048u : (kk >> 2) * o.blk + (kk & 3) * 32u;
+    return d0 + static_cast<uint64_t>(off >> 4);
+}
+__device__ __forceinline__ uint64_t desc0(const Opd &o, uint32_t base) {
+    return smem_desc(base, o.mn ? o.blk : 16u, 1024, kSwizzle128B);
 }
 
 // D[tmem d] (+)= A B over `ksteps` k-steps of 16 (M = 128, N columns), as
 // hi.hi + hi.lo + lo.hi per k-step.  Issued by one thread.
-__device__ __forceinline__ void issue(uint32_t d, const Opd &A, const Opd &B, uint32_t N,
-                                     int ksteps, bool accumulate) {
+__device__ __forceinline__ void issue(uint32_t d, const Opd &A, const Opd &B, uint32_t N, int ksteps,
+                                  bool accumulate) {
     const uint32_t id = instr_desc(128, N, kFmtBF16, A.mn, B.mn);
+    const uint64_t ah0 = desc0(A, A.hi), bh0 = desc0(B, B.hi);
+    const uint64_t al0 = A.lo ? desc0(A, A.lo) : 0, bl0 = B.lo ? desc0(B, B.lo) : 0;
     uint32_t acc = accumulate ? 1u : 0u;
     for (int kk = 0; kk < ksteps; ++kk) {
-        const uint64_t ah = kdesc(A, A.hi, kk), bh = kdesc(B, B.hi, kk);
+        const uint64_t ah = kstep(A, ah0, kk), bh = kstep(B, bh0, kk);
         mma_f16_ss(d, ah, bh, id, acc);
         acc = 1u;
-        if (B.lo != 0) mma_f16_ss(d, ah, kdesc(B, B.lo, kk), id, 1u);
-        if (A.lo != 0) mma_f16_ss(d, kdesc(A, A.lo, kk), bh, id, 1u);
+        if (B.lo != 0) mma_f16_ss(d, ah, kstep(B, bl0, kk), id, 1u);
+        if (A.lo != 0) mma_f16_ss(d, kstep(A, al0, kk), bh, id, 1u);
     }
 }
 
-// Sum over the 32 lanes of a warp (every lane gets the total).
-__device__ __forceinline__ float warp_sum(float x) {
+// One halving step of a sum across lanes: lanes with bit `off` set keep the
+// upper N of their 2N values, the others the lower N, each adding its
+// partner's copy of the half it keeps.
+template <int N>
+__device__ __forceinline__ void fold(float *x, int lane, int off) {
+    const bool up = (lane & off) != 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
+    for (int i = 0; i < N; ++i) {
+        const float a = x[i], b = x[i + N];
+        x[i] = (up ? b : a) + __shfl_xor_sync(0xffffffffu, up ? a : b, off);
+    }
+}
+
+// Sums over the 32 lanes of a warp of 16 values per lane: on return x[0] of
+// lane l holds the total of value l >> 1 (16 shuffles instead of 16 x 5).
+__device__ __forceinline__ float lanes_sum16(float (&x)[16], int lane) {
+    fold<8>(x, lane, 16);
+    fold<4>(x, lane, 8);
+    fold<2>(x, lane, 4);
+    fold<1>(x, lane, 2);
+    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
+}
+
+// The product engine's state (identical in every thread): the image each of
+// the two operand slots holds (-1: none), the barrier phases, and what is in
+// flight for the drain.
+struct Sched {
+    uint8_t *smem, *scr;
+    uint64_t *bar_load, *bar_mma;
+    int *abort_flag;
+    unsigned int *err;
+    uint32_t polls, sa, sb;
+    int tid;
+    int sl0, sl1;
+    uint32_t ph_load, ph_mma;
+    bool pend_load, pend_mma;
+    bool t_store;  // thread 0: the bulk store of the T image is in flight
+};
+
+// An operand: image, first row used, MN-major.
+struct OpSpec {
+    int img, row0, mn;
+};
+
+__device__ __forceinline__ void dirty(Sched &S, int i) {
+    if (S.sl0 == i) S.sl0 = -1;
+    if (S.sl1 == i) S.sl1 = -1;
+}
+
+// One product term, D[tmem d] (+)= A B: bulk-copies the operand images that are
+// not already in a slot (a slot keeps its image until it is reused or the image
+// is rewritten), issues the MMAs from thread 0 and waits for them.  Returns
+// false when a wait ran out (the CTA is aborting).
+__device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d, uint32_t N,
+                                     int ksteps, bool accumulate) {
+    const int ia = A.img, ib = B.img;
+    int pa = (S.sl0 == ia) ? 0 : (S.sl1 == ia) ? 1 : -1;
+    int pb = (S.sl0 == ib) ? 0 : (S.sl1 == ib) ? 1 : -1;
+    int la = -1, lb = -1;
+    if (pa < 0) {
+        pa = (pb == 0) ? 1 : 0;
+        la = pa;
+    }
+    if (ib == ia) pb = pa;
+    if (pb < 0) {
+        pb = (pa == 0) ? 1 : 0;
+        lb = pb;
+    }
+    if (la >= 0 || lb >= 0) {
+        if (S.tid == 0) {
+            if (S.t_store && (ia == I_T || ib == I_T)) {
+                bulk_wait_all();
+                S.t_store = false;
+            }
+            const uint32_t bytes = (la >= 0 ? img_bytes(ia) : 0u) + (lb >= 0 ? img_bytes(ib) : 0u);
+            mbar_arrive_expect_tx(S.bar_load, bytes);
+            if (la >= 0)
+                bulk_load(S.smem + (la ? SLOT_B : SLOT_A), S.scr + img_off(ia), img_bytes(ia), S.bar_load);
+            if (lb >= 0)
+                bulk_load(S.smem + (lb ? SLOT_B : SLOT_A), S.scr + img_off(ib), img_bytes(ib), S.bar_load);
+        }
+        if (la == 0) S.sl0 = ia;
+        if (la == 1) S.sl1 = ia;
+        if (lb == 0) S.sl0 = ib;
+        if (lb == 1) S.sl1 = ib;
+        S.pend_load = true;
+        if (!cta_wait(S.bar_load, S.ph_load & 1, S.abort_flag, S.err, S.tid, S.polls)) return false;
+        S.ph_load++;
+        S.pend_load = false;
+    }
+    if (S.tid == 0) {
+        issue(d, opd(pa ? S.sb : S.sa, ia, A.row0, A.mn != 0), opd(pb ? S.sb : S.sa, ib, B.row0, B.mn != 0),
+              N, ksteps, accumulate);
+        mma_commit(S.bar_mma);
+    }
+    S.pend_mma = true;
+    if (!cta_wait(S.bar_mma, S.ph_mma & 1, S.abort_flag, S.err, S.tid, S.polls)) return false;
+    S.ph_mma++;
+    S.pend_mma = false;
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams p) {
@@ -264,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     float *s_dbeta = reinterpret_cast<float *>(misc + M_DBETA);
     float *s_suf = reinterpret_cast<float *>(misc + M_SUF);
     float *s_khs = reinterpret_cast<float *>(misc + M_KHS);
+    float *s_gl = reinterpret_cast<float *>(misc + M_GL);
     float *s_kk = reinterpret_cast<float *>(smem + OFF_KK);
     float *s_at = reinterpret_cast<float *>(smem + OFF_AT);
     uint64_t *bar_load = reinterpret_cast<uint64_t *>(misc + M_BAR);
@@ -285,10 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
         fence_mbar_init();
         ctrl[2] = 0;
     }
-    // The strictly upper blocks of T and T diag(beta) are zero in every chunk and
-    // are never written again.
-    for (int e = tid; e < 2 * 16384 / 16; e += kThreads)
-        reinterpret_cast<uint4 *>(img(I_TB))[e] = make_uint4(0u, 0u, 0u, 0u);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -297,8 +417,21 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     const uint32_t tl = tmem + lane_base;  // this warp's lane quarter
     const uint32_t sa = smem_addr(smem + SLOT_A), sb = smem_addr(smem + SLOT_B);
 
-    uint32_t ph_load = 0, ph_mma = 0;
-    bool pend_load = false, pend_mma = false;  // identical in every thread
+    Sched S;
+    S.smem = smem;
+    S.scr = scr;
+    S.bar_load = bar_load;
+    S.bar_mma = bar_mma;
+    S.abort_flag = &ctrl[2];
+    S.err = p.err;
+    S.polls = p.polls;
+    S.sa = sa;
+    S.sb = sb;
+    S.tid = tid;
+    S.sl0 = S.sl1 = -1;
+    S.ph_load = S.ph_mma = 0;
+    S.pend_load = S.pend_mma = false;
+    S.t_store = false;
     const float kLog2e = 1.4426950408889634f;
     const float kMaxChunkLog2 = kMaxChunkDecay * kLog2e;
     const float kMinTokenLog2 = -kMaxTokenDecay * kLog2e;
@@ -311,29 +444,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
         __syncthreads();
         tc_fence_after();
     };
-    // Copies images ia -> slot A and ib -> slot B (ib < 0: none; ib == ia: once).
-    auto load = [&](int ia, int ib) -> bool {
-        if (tid == 0) {
-            uint32_t bytes = img_bytes(ia) + ((ib >= 0 && ib != ia) ? img_bytes(ib) : 0u);
-            mbar_arrive_expect_tx(bar_load, bytes);
-            bulk_load(smem + SLOT_A, img(ia), img_bytes(ia), bar_load);
-            if (ib >= 0 && ib != ia) bulk_load(smem + SLOT_B, img(ib), img_bytes(ib), bar_load);
-        }
-        pend_load = true;
-        if (!cta_wait(bar_load, ph_load & 1, &ctrl[2], p.err, tid, p.polls)) return false;
-        ph_load++;
-        pend_load = false;
-        return true;
-    };
-    auto mma_done = [&]() -> bool {
-        if (tid == 0) mma_commit(bar_mma);
-        pend_mma = true;
-        if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls)) return false;
-        ph_mma++;
-        pend_mma = false;
-        return true;
-    };
-
     while (ctrl[2] == 0) {
         __syncthreads();
         if (tid == 0) ctrl[1] = static_cast<int>(atomicAdd(p.counter, 1u));
@@ -370,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             const int64_t tc = t0 + c * kC;
             const int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
             const float *Sc = p.ckpt + ((slot0 + c) * H + h) * (kD * kD);
+            S.sl0 = S.sl1 = -1;  // every image is rewritten for this chunk
 
             // ---- B1: cumulative decay and the chunk operand images ----
             float gam[16];
@@ -405,53 +516,95 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             if (grp == 0) {
                 s_em[ch] = fast_exp2(m);
                 s_dec[ch] = fast_exp2(gam_l);
+                s_gl[ch] = gam_l;
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                gam[i] += prefix;  // Gam_r in log2 units from here on
-                const int r = 16 * grp + i;
-                float qv = 0.f, kv = 0.f, vv = 0.f, dov = 0.f;
+            for (int i = 0; i < 16; ++i) gam[i] += prefix;  // Gam_r in log2 units from here on
+            // Gam [64][128] to slot B, then the operand images eight channels of one
+            // row at a time (unit u: row u / 16, channels 8 (u % 16) .. + 7)
+            {
+                float *gt = reinterpret_cast<float *>(smem + SLOT_B);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) gt[(16 * grp + i) * kD + ch] = gam[i];
+            }
+            __syncthreads();
+#pragma unroll 1
+            for (int u = tid; u < kC * 16; u += kThreads) {
+                const int r = u >> 4, c0 = (u & 15) * 8;
+                float qv[8], kv[8], vv[8], dov[8];
                 if (r < L) {
-                    const int64_t e = ((tc + r) * H + h) * kD + ch;
-                    qv = __bfloat162float(p.q[e]);
-                    kv = __bfloat162float(p.k[e]);
-                    vv = __bfloat162float(p.v[e]);
-                    dov = p.dO_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.dO)[e])
-                                    : static_cast<const float *>(p.dO)[e];
+                    const int64_t e = ((tc + r) * H + h) * kD + c0;
+                    const uint4 q8 = *reinterpret_cast<const uint4 *>(p.q + e);
+                    const uint4 k8 = *reinterpret_cast<const uint4 *>(p.k + e);
+                    const uint4 v8 = *reinterpret_cast<const uint4 *>(p.v + e);
+                    const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&q8);
+                    const __nv_bfloat16 *kb = reinterpret_cast<const __nv_bfloat16 *>(&k8);
+                    const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(&v8);
+                    if (p.dO_bf16) {
+                        const uint4 d8 = *reinterpret_cast<const uint4 *>(
+                            static_cast<const __nv_bfloat16 *>(p.dO) + e);
+                        const __nv_bfloat16 *db = reinterpret_cast<const __nv_bfloat16 *>(&d8);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) dov[j] = __bfloat162float(db[j]);
+                    } else {
+                        const float4 d0 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.dO) + e);
+                        const float4 d1 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.dO) + e + 4);
+                        dov[0] = d0.x; dov[1] = d0.y; dov[2] = d0.z; dov[3] = d0.w;
+                        dov[4] = d1.x; dov[5] = d1.y; dov[6] = d1.z; dov[7] = d1.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        qv[j] = __bfloat162float(qb[j]);
+                        kv[j] = __bfloat162float(kb[j]);
+                        vv[j] = __bfloat162float(vb[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) qv[j] = kv[j] = vv[j] = dov[j] = 0.f;
                 }
-                const float eu = fast_exp2(gam[i] - m), ed = fast_exp2(m - gam[i]);
-                const float eh = fast_exp2(gam_l - gam[i]);
-                put1(img(I_QK), img_half(I_QK), 128, r, ch, p.scale * qv * eu);
-                put1(img(I_QK), img_half(I_QK), 128, 64 + r, ch, kv * eu);
-                put1(img(I_KS), img_half(I_KS), 64, r, ch, kv * ed);
-                put1(img(I_KH), img_half(I_KH), 64, r, ch, kv * eh);
-                put1(img(I_V), 0, 64, r, ch, vv);
-                put1(img(I_DU2), img_half(I_DU2), 128, 64 + r, ch, dov);
+                const float *gt = reinterpret_cast<const float *>(smem + SLOT_B) + r * kD + c0;
+                float qt[8], kr[8], ks[8], kh[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float gr = gt[j], gl = s_gl[c0 + j], mj = 0.5f * gl;
+                    const float eu = fast_exp2(gr - mj);
+                    qt[j] = p.scale * qv[j] * eu;
+                    kr[j] = kv[j] * eu;
+                    ks[j] = kv[j] * fast_exp2(mj - gr);
+                    kh[j] = kv[j] * fast_exp2(gl - gr);
+                }
+                put8(img(I_QK), img_half(I_QK), 128, r, c0, qt);
+                put8(img(I_QK), img_half(I_QK), 128, 64 + r, c0, kr);
+                put8(img(I_KS), img_half(I_KS), 64, r, c0, ks);
+                put8(img(I_KH), img_half(I_KH), 64, r, c0, kh);
+                put8(img(I_V), 0, 64, r, c0, vv);
+                put8(img(I_DU2), img_half(I_DU2), 128, 64 + r, c0, dov);
             }
 
-            // ---- B2: S_op and dS' images; sum_v dS'[k][v] S[k][v] ----
-            __syncthreads();  // e^{m} of every channel
+            // ---- B2: S_op^T and dS'^T images (row v = this lane); sum_v dS' S ----
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-                float ds[16];
-                tmem_ld16(tl + C_DS + 32 * grp + 16 * half, ds);
+                const int k0 = 32 * grp + 16 * half;
+                float ds[16], sv[16], so[16];
+                tmem_ld16(tl + C_DS + k0, ds);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sv[j] = Sc[(k0 + j) * kD + ch];
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int kq = 32 * grp + 16 * half + j;
-                    const float sv = Sc[kq * kD + ch];
-                    put1(img(I_SO), img_half(I_SO), 128, kq, ch, s_em[kq] * sv);
-                    put1(img(I_DS), img_half(I_DS), 128, kq, ch, ds[j]);
-                    const float t = warp_sum(ds[j] * sv);
-                    if (lane == 0) atomicAdd(&s_dgl[kq], t);
-                }
+                for (int j = 0; j < 16; ++j) so[j] = s_em[k0 + j] * sv[j];
+                put8(img(I_SO), img_half(I_SO), 128, ch, k0, so);
+                put8(img(I_SO), img_half(I_SO), 128, ch, k0 + 8, so + 8);
+                put8(img(I_DS), img_half(I_DS), 128, ch, k0, ds);
+                put8(img(I_DS), img_half(I_DS), 128, ch, k0 + 8, ds + 8);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) so[j] = ds[j] * sv[j];
+                const float t = lanes_sum16(so, lane);
+                if ((lane & 1) == 0) atomicAdd(&s_dgl[k0 + (lane >> 1)], t);
             }
             publish();
 
             // ---- D_A = [Qt; Kr] Ks^T ----
-            if (!load(I_QK, I_KS)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_QK, 0, false), opd(sb, I_KS, 0, false), 64, 8, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_QK, 0, 0}, {I_KS, 0, 0}, tmem + C_TA, 64, 8, false)) break;
             {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
@@ -468,20 +621,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int s = 16 * grp + j;
-                        s_kk[r * 64 + s] = d16[j];
+                        s_kk[s * 64 + r] = d16[j];
                         s_at[s * 64 + r] = (s < r) ? br * d16[j] : 0.f;
                     }
                 }
             }
+            dirty(S, I_AQ);
             __syncthreads();
 
-            // ---- T = (I + A_kk)^{-1} on warps 0-3: T and T diag(beta) images ----
+            // ---- T = (I + A_kk)^{-1} on warps 0-3: T diag(beta) and T staged in
+            // slot B (strictly upper blocks zero), T stored to its image ----
+            for (int e = tid; e < 32768 / 16; e += kThreads)
+                reinterpret_cast<uint4 *>(smem + SLOT_B)[e] = make_uint4(0u, 0u, 0u, 0u);
+            __syncthreads();
             if (warp < 4) {
                 float *T = reinterpret_cast<float *>(smem + OFF_TT);
                 float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
                 float *T32c = reinterpret_cast<float *>(misc + M_T32);
                 float *P = reinterpret_cast<float *>(misc + M_P);
-                const TSplitImages out{img(I_TB), img(I_T), s_beta};
+                const TSplitImages out{smem + SLOT_B, smem + SLOT_B + img_bytes(I_TB), s_beta};
                 if (tid < 64) {
                     ut_diag_solve(s_at, T, Tdiag, out, tid);
                     __syncwarp();
@@ -490,12 +648,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 inverse_sync();
                 ut_level2(s_at, T, Tdiag, T32c, P, out, tid);
             }
+            fence_proxy_async_smem();
             publish();
+            if (tid == 0) {
+                bulk_store(img(I_T), smem + SLOT_B + img_bytes(I_TB), img_bytes(I_T));
+                bulk_wait_read();
+                S.t_store = true;
+            }
+            S.sl1 = I_TB;
 
             // ---- W'^T = Kr^T (T beta)^T ; -W'^T image ----
-            if (!load(I_QK, I_TB)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_QK, 64, true), opd(sb, I_TB, 0, false), 64, 4, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_QK, 64, 1}, {I_TB, 0, 0}, tmem + C_TA, 64, 4, false)) break;
             {
                 float w16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, w16);
@@ -505,15 +668,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_WT), img_half(I_WT), 128, ch, 16 * grp, w16);
                 put8(img(I_WT), img_half(I_WT), 128, ch, 16 * grp + 8, w16 + 8);
             }
+            dirty(S, I_WT);
             publish();
 
             // ---- Ut^T = V^T (T beta)^T, then U^T = Ut^T + S_op^T (-W'^T) ----
-            if (!load(I_V, I_TB)) break;
-            if (tid == 0) issue(tmem + C_TB, opd(sa, I_V, 0, true), opd(sb, I_TB, 0, false), 64, 4, false);
-            if (!mma_done()) break;
-            if (!load(I_SO, I_WT)) break;
-            if (tid == 0) issue(tmem + C_TB, opd(sa, I_SO, 0, true), opd(sb, I_WT, 0, true), 64, 8, true);
-            if (!mma_done()) break;
+            if (!product(S, {I_V, 0, 1}, {I_TB, 0, 0}, tmem + C_TB, 64, 4, false)) break;
+            if (!product(S, {I_SO, 0, 0}, {I_WT, 0, 1}, tmem + C_TB, 64, 8, true)) break;
             {
                 float u16[16];
                 tmem_ld16(tl + C_TB + 16 * grp, u16);
@@ -521,31 +681,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_UT), img_half(I_UT), 128, ch, 16 * grp, u16);
                 put8(img(I_UT), img_half(I_UT), 128, ch, 16 * grp + 8, u16 + 8);
             }
+            dirty(S, I_UT);
             publish();
 
             // ---- dU^T = dO^T A_qk + dS'^T Kh ; dU image (rows 0-63 of DU2) ----
-            if (!load(I_DU2, I_AQ)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 64, true), opd(sb, I_AQ, 0, true), 64, 4, false);
-            if (!mma_done()) break;
-            if (!load(I_DS, I_KH)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DS, 0, true), opd(sb, I_KH, 0, false), 64, 8, true);
-            if (!mma_done()) break;
+            if (!product(S, {I_DU2, 64, 1}, {I_AQ, 0, 1}, tmem + C_TA, 64, 4, false)) break;
+            if (!product(S, {I_DS, 0, 0}, {I_KH, 0, 0}, tmem + C_TA, 64, 8, true)) break;
             {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);  // dU^T[v = ch][r]
                 tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j < 16; ++j) put1(img(I_DU2), img_half(I_DU2), 128, 16 * grp + j, ch, d16[j]);
             }
+            dirty(S, I_DU2);
             publish();
 
             // ---- P^T = dO^T Qt - dU^T W'^T... ; dS <- e^{Gam_L} dS' + e^m P ----
-            if (!load(I_DU2, I_QK)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 64, true), opd(sb, I_QK, 0, true), 128, 4, false);
-            if (!mma_done()) break;
-            if (!load(I_DU2, I_WT)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 0, true), opd(sb, I_WT, 0, false), 128, 4, true);
-            if (!mma_done()) break;
+            if (!product(S, {I_DU2, 64, 1}, {I_QK, 0, 1}, tmem + C_TA, 128, 4, false)) break;
+            if (!product(S, {I_DU2, 0, 1}, {I_WT, 0, 0}, tmem + C_TA, 128, 4, true)) break;
             {
                 float pv[32], ds[32];
                 tmem_ld32(tl + C_TA + 32 * grp, pv);
@@ -562,9 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             publish();
 
             // ---- dA_qk = tril(dO U^T) (lanes 64-127 of [dU; dO] U^T) ----
-            if (!load(I_DU2, I_UT)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 0, false), opd(sb, I_UT, 0, true), 64, 8, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_DU2, 0, 0}, {I_UT, 0, 1}, tmem + C_TA, 64, 8, false)) break;
             if (quarter >= 2) {
                 const int r = ch - 64;
                 float d16[16];
@@ -575,41 +727,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_DAQ), img_half(I_DAQ), 64, r, 16 * grp, d16);
                 put8(img(I_DAQ), img_half(I_DAQ), 64, r, 16 * grp + 8, d16 + 8);
             }
+            dirty(S, I_DAQ);
             publish();
 
             // ---- dKs^T = Qt^T dA_qk ----
-            if (!load(I_QK, I_DAQ)) break;
-            if (tid == 0) issue(tmem + C_S, opd(sa, I_QK, 0, true), opd(sb, I_DAQ, 0, true), 64, 4, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_QK, 0, 1}, {I_DAQ, 0, 1}, tmem + C_S, 64, 4, false)) break;
 
             // ---- [-dW'^T | dQt^T] = S_op [dU; dO]^T ; dQt^T += Ks^T dA_qk^T ----
-            if (!load(I_SO, I_DU2)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_SO, 0, false), opd(sb, I_DU2, 0, false), 128, 8, false);
-            if (!mma_done()) break;
-            if (!load(I_KS, I_DAQ)) break;
-            if (tid == 0) issue(tmem + C_TB, opd(sa, I_KS, 0, true), opd(sb, I_DAQ, 0, false), 64, 4, true);
-            if (!mma_done()) break;
+            if (!product(S, {I_SO, 0, 1}, {I_DU2, 0, 0}, tmem + C_TA, 128, 8, false)) break;
+            if (!product(S, {I_KS, 0, 1}, {I_DAQ, 0, 0}, tmem + C_TB, 64, 4, true)) break;
             {
                 float d16[16];  // -dW'^T[k = ch][r]: dW'[r][k] into rows 0-63 of the QK image (Qt is dead)
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
                 tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j < 16; ++j) put1(img(I_QK), img_half(I_QK), 128, 16 * grp + j, ch, -d16[j]);
             }
+            dirty(S, I_QK);
             publish();
 
             // ---- dKh^T = dS' U^T ----
-            if (!load(I_DS, I_UT)) break;
-            if (tid == 0) issue(tmem + C_H, opd(sa, I_DS, 0, false), opd(sb, I_UT, 0, true), 64, 8, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_DS, 0, 1}, {I_UT, 0, 1}, tmem + C_H, 64, 8, false)) break;
 
             // ---- dT = (dW' Kr^T + dU V^T) diag(beta) (lanes 0-63) ----
-            if (!load(I_QK, I_V)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_QK, 0, false), opd(sa, I_QK, 64, false), 64, 8, false);
-            if (!mma_done()) break;
-            if (!load(I_DU2, I_V)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DU2, 0, false), opd(sb, I_V, 0, false), 64, 8, true);
-            if (!mma_done()) break;
+            if (!product(S, {I_QK, 0, 0}, {I_QK, 64, 0}, tmem + C_TA, 64, 8, false)) break;
+            if (!product(S, {I_DU2, 0, 0}, {I_V, 0, 0}, tmem + C_TA, 64, 8, true)) break;
             if (quarter < 2) {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
@@ -619,41 +761,42 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_DT), img_half(I_DT), 64, ch, 16 * grp, d16);
                 put8(img(I_DT), img_half(I_DT), 64, ch, 16 * grp + 8, d16 + 8);
             }
+            dirty(S, I_DT);
             publish();
 
             // ---- d(beta Kr)^T = dW'^T T and d(beta V)^T = dU^T T ----
-            if (!load(I_QK, I_T)) break;
-            if (tid == 0) issue(tmem + C_R, opd(sa, I_QK, 0, true), opd(sb, I_T, 0, true), 64, 4, false);
-            if (!mma_done()) break;
-            if (!load(I_DU2, I_T)) break;
-            if (tid == 0) issue(tmem + C_VB, opd(sa, I_DU2, 0, true), opd(sb, I_T, 0, true), 64, 4, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_QK, 0, 1}, {I_T, 0, 1}, tmem + C_R, 64, 4, false)) break;
+            if (!product(S, {I_DU2, 0, 1}, {I_T, 0, 1}, tmem + C_VB, 64, 4, false)) break;
             {
                 // d(beta V)^T[v = ch][r]: dv = beta_r d(beta V); dbeta += sum_v d(beta V) v.
                 // d(beta Kr)^T[k = ch][r]: dbeta += sum_k d(beta Kr) Kr.
-                float vb[16], rb[16];
+                float vb[16], rb[16], vv[16], kr[16];
                 tmem_ld16(tl + C_VB + 16 * grp, vb);
                 tmem_ld16(tl + C_R + 16 * grp, rb);
-                tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int r = 16 * grp + j;
-                    float vv = 0.f, kr = 0.f;
+                    vv[j] = kr[j] = 0.f;
                     if (r < L) {
                         const int64_t e = ((tc + r) * H + h) * kD + ch;
-                        vv = __bfloat162float(p.v[e]);
-                        kr = __bfloat162float(p.k[e]) * fast_exp2(gam[j] - m);
-                        p.dv[e] = s_beta[r] * vb[j];
+                        vv[j] = __bfloat162float(p.v[e]);
+                        kr[j] = __bfloat162float(p.k[e]);
                     }
-                    const float t = warp_sum(vb[j] * vv + rb[j] * kr);
-                    if (lane == 0) atomicAdd(&s_dbeta[r], t);
                 }
+                tmem_wait_ld();
+                float sum[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r = 16 * grp + j;
+                    if (r < L) p.dv[((tc + r) * H + h) * kD + ch] = s_beta[r] * vb[j];
+                    sum[j] = vb[j] * vv[j] + rb[j] * kr[j] * fast_exp2(gam[j] - m);
+                }
+                const float t = lanes_sum16(sum, lane);
+                if ((lane & 1) == 0) atomicAdd(&s_dbeta[16 * grp + (lane >> 1)], t);
             }
 
             // ---- Y = dT T^T (lanes 0-63) ----
-            if (!load(I_DT, I_T)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_DT, 0, false), opd(sb, I_T, 0, false), 64, 4, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_DT, 0, 0}, {I_T, 0, 0}, tmem + C_TA, 64, 4, false)) break;
             if (quarter < 2) {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
@@ -661,12 +804,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_Y), img_half(I_Y), 64, ch, 16 * grp, d16);
                 put8(img(I_Y), img_half(I_Y), 64, ch, 16 * grp + 8, d16 + 8);
             }
+            dirty(S, I_Y);
             publish();
 
             // ---- dA_kk = -strict_tril(T^T Y) (lanes 0-63); dbeta += rowsum(dA_kk kk) ----
-            if (!load(I_T, I_Y)) break;
-            if (tid == 0) issue(tmem + C_TA, opd(sa, I_T, 0, true), opd(sb, I_Y, 0, true), 64, 4, false);
-            if (!mma_done()) break;
+            if (!product(S, {I_T, 0, 1}, {I_Y, 0, 1}, tmem + C_TA, 64, 4, false)) break;
             if (quarter < 2) {
                 const int r = ch;
                 float d16[16], bd[16];
@@ -679,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     const int s = 16 * grp + j;
                     d16[j] = (s < r) ? -d16[j] : 0.f;
                     bd[j] = br * d16[j];
-                    part += d16[j] * s_kk[r * 64 + s];
+                    part += d16[j] * s_kk[s * 64 + r];
                 }
                 atomicAdd(&s_dbeta[r], part);
                 put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp, d16);
@@ -687,41 +829,53 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_BDKK), img_half(I_BDKK), 64, r, 16 * grp, bd);
                 put8(img(I_BDKK), img_half(I_BDKK), 64, r, 16 * grp + 8, bd + 8);
             }
+            dirty(S, I_DKK);
+            dirty(S, I_BDKK);
             publish();
 
             // ---- dKs^T += Kr^T (beta dA_kk) ; (dA_kk Ks)^T into C_R ----
-            if (!load(I_QK, I_BDKK)) break;
-            if (tid == 0) issue(tmem + C_S, opd(sa, I_QK, 64, true), opd(sb, I_BDKK, 0, true), 64, 4, true);
-            if (!mma_done()) break;
-            if (!load(I_KS, I_DKK)) break;
-            if (tid == 0) issue(tmem + C_R, opd(sa, I_KS, 0, true), opd(sb, I_DKK, 0, false), 64, 4, true);
-            if (!mma_done()) break;
+            if (!product(S, {I_QK, 64, 1}, {I_BDKK, 0, 1}, tmem + C_S, 64, 4, true)) break;
+            if (!product(S, {I_KS, 0, 1}, {I_DKK, 0, 0}, tmem + C_R, 64, 4, true)) break;
 
             // ---- assembly: dq, dk, dg, dbeta (lane k = ch, rows r = 16 grp + j) ----
             {
-                float dqt[16], dkh[16], dks[16], dkr[16];
-                tmem_ld16(tl + C_TB + 16 * grp, dqt);
-                tmem_ld16(tl + C_H + 16 * grp, dkh);
-                tmem_ld16(tl + C_S + 16 * grp, dks);
-                tmem_ld16(tl + C_R + 16 * grp, dkr);
-                tmem_wait_ld();
                 float dgam[16], khsum = 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r = 16 * grp + j;
-                    dgam[j] = 0.f;
-                    if (r < L) {
-                        const int64_t e = ((tc + r) * H + h) * kD + ch;
-                        const float qv = __bfloat162float(p.q[e]), kv = __bfloat162float(p.k[e]);
-                        const float eu = fast_exp2(gam[j] - m), ed = fast_exp2(m - gam[j]);
-                        const float eh = fast_exp2(gam_l - gam[j]);
-                        const float Qt = p.scale * qv * eu, Kr = kv * eu, Ks = kv * ed, Kh = kv * eh;
-                        const float dKr = s_beta[r] * dkr[j];
-                        p.dq[e] = p.scale * dqt[j] * eu;
-                        p.dk[e] = dKr * eu + dks[j] * ed + dkh[j] * eh;
-                        const float khp = dkh[j] * Kh;
-                        dgam[j] = dKr * Kr - dks[j] * Ks - khp + dqt[j] * Qt;
-                        khsum += khp;
+                for (int j0 = 0; j0 < 16; j0 += 8) {  // eight rows at a time
+                    float dqt[8], dkh[8], dks[8], dkr[8], qv[8], kv[8];
+                    tmem_ld8(tl + C_TB + 16 * grp + j0, dqt);
+                    tmem_ld8(tl + C_H + 16 * grp + j0, dkh);
+                    tmem_ld8(tl + C_S + 16 * grp + j0, dks);
+                    tmem_ld8(tl + C_R + 16 * grp + j0, dkr);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int r = 16 * grp + j0 + j;
+                        qv[j] = kv[j] = 0.f;
+                        if (r < L) {
+                            const int64_t e = ((tc + r) * H + h) * kD + ch;
+                            qv[j] = __bfloat162float(p.q[e]);
+                            kv[j] = __bfloat162float(p.k[e]);
+                        }
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int r = 16 * grp + j0 + j;
+                        const float gr = gam[j0 + j];
+                        dgam[j0 + j] = 0.f;
+                        if (r < L) {
+                            const int64_t e = ((tc + r) * H + h) * kD + ch;
+                            const float eu = fast_exp2(gr - m), ed = fast_exp2(m - gr);
+                            const float eh = fast_exp2(gam_l - gr);
+                            const float Qt = p.scale * qv[j] * eu, Kr = kv[j] * eu, Ks = kv[j] * ed;
+                            const float Kh = kv[j] * eh;
+                            const float dKr = s_beta[r] * dkr[j];
+                            p.dq[e] = p.scale * dqt[j] * eu;
+                            p.dk[e] = dKr * eu + dks[j] * ed + dkh[j] * eh;
+                            const float khp = dkh[j] * Kh;
+                            dgam[j0 + j] = dKr * Kr - dks[j] * Ks - khp + dqt[j] * Qt;
+                            khsum += khp;
+                        }
                     }
                 }
                 // suffix sums over the chunk's rows: this group's rows, then the later groups
@@ -778,8 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     // Drain: wait for a copy or product still in flight (full bound) before the
     // tensor memory is released and the CTA exits.
     if (tid == 0) {
-        if (pend_load) mbar_wait_bounded(bar_load, ph_load & 1, kMaxPolls);
-        if (pend_mma) mbar_wait_bounded(bar_mma, ph_mma & 1, kMaxPolls);
+        if (S.pend_load) mbar_wait_bounded(bar_load, S.ph_load & 1, kMaxPolls);
+        if (S.pend_mma) mbar_wait_bounded(bar_mma, S.ph_mma & 1, kMaxPolls);
+        bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();

@@ -87,6 +87,23 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` from shared to global memory (bulk-group
+// completion); both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+                 "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the committed bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Makes this thread's generic-proxy global writes visible to later
 // async-proxy reads (bulk copies) once the CTA has synchronised.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -163,6 +180,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) 
         "r"(u[22]), "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]),
         "r"(u[29]), "r"(u[30]), "r"(u[31])
         : "memory");
+}
+
+// 32 lanes x 8 columns of 32-bit values.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                   "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr));
 }
 
 // 32 lanes x 16 columns of 32-bit values.
