@@ -18,9 +18,10 @@
 // reference m = Gam_L / 2 so that each factor lies in [e^{-D/2}, e^{D/2}] with
 // D = -Gam_L the chunk's total decay.  D <= 160 is represented: a chunk whose
 // decay would exceed it in some channel is shortened to the rows before the
-// first one past it (the rest of its tile starts the next chunk), and each
-// token's decay is limited to 80 (e^{-80} is below fp32 resolution), so any
-// finite decay is computed.  A_qk and A_kk come from one
+// first one past it (the rest of its tile starts the next chunk); a token
+// whose own decay exceeds 160 forms a chunk of one with its decay taken as 160
+// (e^{-160} underflows fp32 like any larger decay), so every decay is
+// computed.  A_qk and A_kk come from one
 // product [Qt; Kr] Ks^T with Qt = scale q e^{Gam-m}, Kr = k e^{Gam-m} and
 // Ks = k e^{m-Gam}.  The same Qt and Kr serve the state products because the
 // state operand is stored pre-scaled, S_op = Diag(e^m) S, and
@@ -72,7 +73,7 @@ constexpr uint32_t MISC_BNEXT = 7424;    // float[64] beta of the next chunk (cp
 constexpr uint32_t MISC_T32 = 7680;      // float[16][16] T_32 column-major (1 KB of 4 KB used)
 constexpr uint32_t MISC_TDIAG = 11776;   // float[4][16][16] diagonal blocks of T, column-major
 constexpr uint32_t MISC_BAR = 15872;     // 4 mbarriers
-constexpr uint32_t MISC_CTRL = 15904;    // int[8]: tmem base, chain, abort, split row
+constexpr uint32_t MISC_CTRL = 15904;    // int[8]: tmem base, chain, abort, -, split row
 constexpr uint32_t kSmemBytes = OFF_MISC + 15936;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
@@ -183,8 +184,9 @@ __device__ __forceinline__ void state_pass(uint32_t tmem_lane, int warp, const f
 // kGate: the gate is computed in this kernel from the bf16 pre-activation f,
 // A_log, dt_bias and the beta logits (g = -exp(A_log) softplus(f + dt_bias),
 // beta = sigmoid(logit)) with the special-function unit, instead of reading a
-// precomputed fp32 g and beta.
-template <bool kOutBf16, bool kGate>
+// precomputed fp32 g and beta.  kCkpt: the forward pass of the chunked
+// backward (chunk-start states to p.ckpt, shortened chunks to p.split).
+template <bool kOutBf16, bool kGate, bool kCkpt>
 __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                             const __grid_constant__ CUtensorMap tm_k,
                                                             const __grid_constant__ CUtensorMap tm_v,
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     uint64_t *bar_mma = bar_qk + 2;
     uint64_t *bar_g = bar_qk + 3;
     float *s_bnext = reinterpret_cast<float *>(misc + MISC_BNEXT);
-    int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [4] split
+    int *ctrl = reinterpret_cast<int *>(misc + MISC_CTRL);  // [0] tmem [1] chain [2] abort [4] split row
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, grp = warp >> 2;
@@ -258,9 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
     const uint64_t d_tb16 = smem_desc(a_tb16, 16, 1024, kSwizzle128B);
     const uint64_t d_v = smem_desc(a_v, 8192, 1024, kSwizzle128B);  // MN-major, 64-wide M blocks
     float *Akk = reinterpret_cast<float *>(smem + OFF_KS);
-    // largest chunk decay and per-token decay represented, in log2 units
+    // largest chunk decay represented, in log2 units
     const float kMaxChunkLog2 = kMaxChunkDecay * 1.4426950408889634f;
-    const float kMinTokenLog2 = -kMaxTokenDecay * 1.4426950408889634f;
 
     while (ctrl[2] == 0) {
         __syncthreads();
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
         int64_t prev_tc = t0;
         int prev_L = 0;
         // checkpoint slot of this sequence's first chunk (see kda_chunk_bwd.cu)
-        bool ckpt_ok = p.ckpt != nullptr;
+        bool ckpt_ok = kCkpt;
         const int64_t ckpt_slot0 = t0 / kC + b;
         for (int64_t tc = t0; tc < t1;) {
             // L tokens from tc; a chunk whose decay exceeds the represented
@@ -377,23 +378,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             // ---- S1: cumulative decay, references, operands ----
             cp_async_wait_all();
             // polled by warp 1: thread 0 may still be issuing the previous
-            // chunk's last product.  Thread 0 also resets the split row here:
-            // every read of it (after S1's last barrier) is long past.
-            if (tid == 0) ctrl[4] = kC;
+            // chunk's last product
+            bool copies_ok = true;
             if (tid == 32 && (!mbar_wait_bounded(bar_qk, ph_qk & 1, p.polls_tma) ||
                               !mbar_wait_bounded(bar_g, ph_g & 1, p.polls_tma))) {
                 ctrl[2] = 1;
                 record_device_error(p.err, kDevTimeout);
+                copies_ok = false;
             }
-            __syncthreads();
+            copies_ok = __syncthreads_and(copies_ok);
             tc_fence_after();
-            if (ctrl[2] != 0) break;  // the batches stay pending for the drain
+            if (!copies_ok) break;  // the batches stay pending for the drain
             ph_g++;
             ph_qk++;
             pend_g = false;
             pend_qk = false;
-            // cumulative decay in log2 units: gam = log2(e) * sum g, each token's
-            // decay limited to kMaxTokenDecay (below fp32 resolution)
+            // cumulative decay in log2 units: gam = log2(e) * sum g
             float gam[16];
             {
                 const float kLog2e = 1.4426950408889634f;
@@ -413,55 +413,49 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                         const uint64_t e = f2(fast_exp2(-kLog2e * fabsf(x.x)), fast_exp2(-kLog2e * fabsf(x.y)));
                         const float2 g2 = f2_split(f2_mul(
                             na2, f2_fma(l2e2, f2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log2_1p_unit2(e))));
-                        // (the comparisons keep a NaN, which then reaches the outputs)
-                        acc += (r < L) ? (g2.x < kMinTokenLog2 ? kMinTokenLog2 : g2.x) : 0.f;
+                        acc += (r < L) ? g2.x : 0.f;
                         gam[i] = acc;
-                        acc += (r + 1 < L) ? (g2.y < kMinTokenLog2 ? kMinTokenLog2 : g2.y) : 0.f;
+                        acc += (r + 1 < L) ? g2.y : 0.f;
                         gam[i + 1] = acc;
                     }
                 } else {
                     const float *gt = reinterpret_cast<const float *>(smem + OFF_KS);
-                    // g must be a decay (g <= 0): a positive or NaN g is
-                    // reported; a positive one is taken as 0, a NaN kept
-                    bool bad = false;
+                    // g must be a decay (g <= 0): a positive or NaN g in the
+                    // chunk's rows is reported (rows past the sequence belong
+                    // to the next one or are zero-filled)
+                    float gmax = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {  // rows >= L carry g = 0
+                    for (int i = 0; i < 16; ++i) {
                         const int r = 16 * grp + i;
                         const float gv = kLog2e * gt[r * kD + ch];
-                        bad |= (r < L) && !(gv <= 0.f);
-                        const float gc = gv < kMinTokenLog2 ? kMinTokenLog2 : (gv > 0.f ? 0.f : gv);
-                        acc += (r < L) ? gc : 0.f;
+                        gmax = fmaxf(gmax, gv);
+                        acc += (r < L) ? gv : 0.f;
                         gam[i] = acc;
                     }
-                    if (bad) record_device_error(p.err, kDevInvalidArg);
+                    if (gmax > 0.f || acc != acc) record_device_error(p.err, kDevInvalidArg);
                 }
             }
             float beta_r = 0.f;  // beta of row tid (threads 0..63)
             if (tid < kC) beta_r = kGate ? 1.f / (1.f + __expf(-blog_reg)) : s_bnext[tid];
-            // Builds the operands of the chunk's first L rows from gam; runs a
-            // second time, with a shorter L, for a chunk that is split.
-            bool again;
-            do {
+            // Builds the operands of the chunk's first L rows from gam and finds
+            // (wide) whether some channel's decay exceeds the represented range;
+            // runs a second time for a chunk that is split.  Returns false when
+            // the CTA is aborting.
+            float prefix = 0.f;  // decay before this thread's rows, log2 units
+            bool wide = false;
+            auto build = [&]() -> bool {
                 s_part[grp * kD + ch] = gam[15];
-                if (tid < kC) s_beta[tid] = (tid < L) ? beta_r : 0.f;
+                if (tid < kC) s_beta[tid] = beta_r;
                 __syncthreads();  // every g read is done before Ks overwrites the tile
-                float prefix = 0.f, gam_l = 0.f;
+                float gam_l = 0.f;
+                prefix = 0.f;
 #pragma unroll
                 for (int g2 = 0; g2 < 4; ++g2) {
                     const float pg = s_part[g2 * kD + ch];
                     if (g2 < grp) prefix += pg;
                     gam_l += pg;
                 }
-                if (-gam_l > kMaxChunkLog2) {
-                    // the first of this thread's rows beyond the range
-                    int first = kC;
-#pragma unroll
-                    for (int i = 15; i >= 0; --i) {
-                        const int r = 16 * grp + i;
-                        if (r < L && -(prefix + gam[i]) > kMaxChunkLog2) first = r;
-                    }
-                    if (first < kC) atomicMin(&ctrl[4], first);
-                }
+                const bool over = -gam_l > kMaxChunkLog2;
                 const float m = 0.5f * gam_l;
                 if (grp == 0) {
                     s_em[ch] = fast_exp2(m);
@@ -502,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 // The previous chunk's [S | O] product, which reads Khat^T, ran while
                 // these operands were formed; it is complete before Khat^T is overwritten.
                 if (pend_mma) {
-                    if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) break;
+                    if (!cta_wait(bar_mma, ph_mma & 1, &ctrl[2], p.err, tid, p.polls_mma)) return false;
                     ph_mma++;
                     pend_mma = false;
                 }
@@ -515,29 +509,52 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                __syncthreads();
+                wide = __syncthreads_or(over) != 0;
                 tc_fence_after();
-                // A chunk split: the rows from ctrl[4] on start the next chunk.
-                // gam keeps its values up to the new last row and repeats the
-                // last one after it (those rows add no decay), and the
-                // operands are formed again; no channel exceeds the range now.
-                again = ctrl[4] < L;
-                if (again) {
-                    L = ctrl[4];
-                    float last = 0.f;
+                return true;
+            };
+            if (!build()) break;
+            if (wide) {
+                // A chunk split (rare: some channel's decay exceeds the range).
+                // The rows from the first one beyond the range in any channel
+                // start the next chunk; gam keeps its values up to the new last
+                // row and repeats the last one after it (those rows add no
+                // decay), and the operands are formed again.  A first token
+                // whose own decay exceeds the range makes a chunk of one token
+                // with its decay taken as the range: e^-160 vanishes in fp32
+                // like any larger decay.
+                int first = kC;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (16 * grp + i < L)
-                            last = gam[i];
-                        else
-                            gam[i] = last;
-                    }
+                for (int i = 15; i >= 0; --i) {
+                    const int r = 16 * grp + i;
+                    if (r < L && -(prefix + gam[i]) > kMaxChunkLog2) first = r;
                 }
-            } while (again);
-            if (ctrl[2] != 0) break;
+                if (first < kC) atomicMin(&ctrl[4], first);
+                __syncthreads();
+                int Ls = ctrl[4];
+                __syncthreads();  // every thread has read the split row
+                if (tid == 0) ctrl[4] = kC;
+                if (Ls == 0) {
+                    Ls = 1;
+                    if (grp == 0) gam[0] = fmaxf(gam[0], -kMaxChunkLog2);
+                }
+                if (Ls < L) {
+                    L = Ls;
+                    if (tid >= L) beta_r = 0.f;
+                }
+                float last = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (16 * grp + i < L)
+                        last = gam[i];
+                    else
+                        gam[i] = last;
+                }
+                if (!build()) break;
+            }
             // a shortened chunk: later chunk starts are no longer 64-token aligned,
             // so this chain's checkpoints stop here and the chain is marked
-            if (L < kC && tc + L < t1 && p.ckpt != nullptr) {
+            if (kCkpt && L < kC && tc + L < t1) {
                 if (tid == 0) p.split[chain] = 1;
                 ckpt_ok = false;
             }
@@ -558,7 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
             pend_mma = true;
             // warp 0 issues the products; warp 4 (same lane quarter) takes its rows
-            if (prev_L > 0 && warp != 0) {
+            // (a full chunk's rows are stored without a per-row test)
+            if (prev_L == kC && warp != 0) {
+                write_output(prev_tc, kC, grp);
+                if (warp == 4) write_output(prev_tc, kC, 0);
+            } else if (prev_L > 0 && warp != 0) {
                 write_output(prev_tc, prev_L, grp);
                 if (warp == 4) write_output(prev_tc, prev_L, 0);
             }
@@ -634,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                 mma_commit_w(bar_mma);
             } else if (warp >= 8) {
                 float *ck = nullptr;
-                if (ckpt_ok && ((tc - t0) % kC) == 0)
+                if (kCkpt && ckpt_ok && ((tc - t0) % kC) == 0)
                     ck = p.ckpt + ((ckpt_slot0 + (tc - t0) / kC) * H + h) * (kD * kD);
                 state_pass(tmem + lane_base, warp, s_em, s_dec, ck, ch);
             }
@@ -803,14 +824,14 @@ size_t prefill_workspace_bytes(int64_t N, int B, int H) {
 
 namespace {
 
-template <bool kGate>
+template <bool kGate, bool kCkpt = false>
 cudaError_t launch_chunk(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                          const void *g_or_f, const Params &p, bool o_bf16, int num_sms,
                          cudaStream_t s) {
     if (p.B == 0 || p.H == 0) return cudaSuccess;
-    cudaError_t ea = o_bf16 ? ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_kernel<true, kGate>),
+    cudaError_t ea = o_bf16 ? ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_kernel<true, kGate, kCkpt>),
                                                   static_cast<int>(kSmemAlloc))
-                            : ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_kernel<false, kGate>),
+                            : ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_kernel<false, kGate, kCkpt>),
                                                   static_cast<int>(kSmemAlloc));
     if (ea != cudaSuccess) return ea;
     CUtensorMap mq, mk, mv, mg;
@@ -827,9 +848,9 @@ cudaError_t launch_chunk(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
     const int chains = p.B * p.H;
     const int grid = chains < num_sms ? chains : num_sms;
     if (o_bf16)
-        chunk_kernel<true, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, pl);
+        chunk_kernel<true, kGate, kCkpt><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, pl);
     else
-        chunk_kernel<false, kGate><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, pl);
+        chunk_kernel<false, kGate, kCkpt><<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, mg, pl);
     return cudaGetLastError();
 }
 
@@ -854,7 +875,7 @@ cudaError_t launch_prefill_checkpoints(const __nv_bfloat16 *q, const __nv_bfloat
                                        int num_sms, cudaStream_t s) {
     const Params p{g, beta, nullptr, nullptr, 0, nullptr, 0, nullptr, cu_seqlens, B, N, H, scale,
                    initial_state, nullptr, nullptr, err, counter, kMaxPolls, kMaxPolls, ckpt, split};
-    return launch_chunk<false>(q, k, v, g, p, false, num_sms, s);
+    return launch_chunk<false, true>(q, k, v, g, p, false, num_sms, s);
 }
 
 cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,

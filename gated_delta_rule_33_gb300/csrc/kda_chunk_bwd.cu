@@ -216,6 +216,10 @@ struct TSplitImages {
         put1(tb, 8192, 64, r, s, x * beta[s]);
         put1(t, 8192, 64, r, s, x);
     }
+    __device__ __forceinline__ void col(int r0, int j, const float (&x)[16]) const {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) one(r0 + i, j, x[i]);
+    }
     __device__ __forceinline__ void four(int r, int s4, float4 x) const {
         const float v[4] = {x.x, x.y, x.z, x.w};
         const float vb[4] = {x.x * beta[s4], x.y * beta[s4 + 1], x.z * beta[s4 + 2],
@@ -434,7 +438,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.t_store = false;
     const float kLog2e = 1.4426950408889634f;
     const float kMaxChunkLog2 = kMaxChunkDecay * kLog2e;
-    const float kMinTokenLog2 = -kMaxTokenDecay * kLog2e;
 
     // Makes every thread's image and tensor-memory writes visible to the next
     // bulk copy / product.
@@ -487,14 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             {
                 float acc = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {  // the forward kernel's clamp and order
+                for (int i = 0; i < 16; ++i) {  // the forward kernel's order
                     const int r = 16 * grp + i;
-                    float gc = 0.f;
-                    if (r < L) {
-                        const float gv = kLog2e * p.g[((tc + r) * H + h) * kD + ch];
-                        gc = gv < kMinTokenLog2 ? kMinTokenLog2 : (gv > 0.f ? 0.f : gv);
-                    }
-                    acc += gc;
+                    if (r < L) acc += kLog2e * p.g[((tc + r) * H + h) * kD + ch];
                     gam[i] = acc;
                 }
                 s_part[grp * kD + ch] = acc;

@@ -19,13 +19,10 @@ constexpr int kC = 64;              // chunk length
 constexpr int kD = 128;             // d_k = d_v
 // Largest per-channel decay -sum(g) of one chunk that the midpoint-referenced
 // factors represent (every factor within e^{+-80}); a chunk that would exceed
-// it in some channel is shortened.
+// it in some channel is shortened.  A single token whose own decay exceeds it
+// forms a chunk of one token with its decay taken as this value: e^{-160}
+// underflows fp32 exactly as any larger decay does.
 constexpr float kMaxChunkDecay = 160.f;
-// Each token's decay -g is limited to this value: e^{-80} (1.8e-35) is far
-// below fp32 resolution relative to the state and the new token's term, so
-// the limit changes no result at fp32 precision, and it guarantees that any
-// single token fits a chunk.
-constexpr float kMaxTokenDecay = 80.f;
 // Bound of every mbarrier wait (polls of try_wait, each itself a bounded wait).
 constexpr uint32_t kMaxPolls = 1u << 20;
 // The tf32 T beta tile lives in rows 128..191 of a 192-row K-major tile (the
@@ -92,19 +89,21 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Thread 0 waits (bounded, `polls` polls) on an mbarrier phase, then the
-// whole CTA meets at a barrier; a time-out raises the CTA abort flag, which
-// every thread reads after the barrier.  Returns false (in every thread) when
-// the CTA is aborting.  Only one thread polls, so the other warps do not
+// whole CTA meets at a barrier; a time-out raises the CTA abort flag and
+// records the error.  Returns false (in every thread, through the barrier's
+// AND reduction) when this wait ran out.  Only one thread polls, so the other warps do not
 // compete with the tensor core for shared-memory bandwidth while they wait.
 __device__ __forceinline__ bool cta_wait(uint64_t *bar, uint32_t parity, int *abort_flag,
                                          unsigned int *err, int tid, uint32_t polls) {
+    bool ok = true;
     if (tid == 0 && !mbar_wait_bounded(bar, parity, polls)) {
         *abort_flag = 1;
         record_device_error(err, kDevTimeout);
+        ok = false;
     }
-    __syncthreads();
+    ok = __syncthreads_and(ok);
     tc_fence_after();
-    return *abort_flag == 0;
+    return ok;
 }
 
 // T beta[r][s] = T[r][s] beta_s as a tf32 operand tile and as bf16 high + low
@@ -144,6 +143,19 @@ struct TbetaTiles {
     // T[r][s4 .. s4 + 3]
     __device__ __forceinline__ void four(int r, int s4, float4 t) const {
         store_tbeta4(tb, tb16, r, s4, t, beta);
+    }
+    // column j of a diagonal block: T[r0 + i][j] = x[i], i < 16
+    __device__ __forceinline__ void col(int r0, int j, const float (&x)[16]) const {
+        const float bj = beta[j];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float xb = x[i] * bj;
+            st_f32(tb, sw128_offset(kTbRow0 + r0 + i, j, kTbRows, 4), to_tf32(xb));
+            const __nv_bfloat16 hi = __float2bfloat16_rn(xb);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(xb - __bfloat162float(hi));
+            *reinterpret_cast<__nv_bfloat16 *>(tb16 + sw128_offset(r0 + i, j, 64, 2)) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(tb16 + 8192 + sw128_offset(r0 + i, j, 64, 2)) = lo;
+        }
     }
 };
 
@@ -255,8 +267,7 @@ __device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *
         *reinterpret_cast<float4 *>(Td + 4 * q4) =
             make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
     // T (beta) of the diagonal block, column j (16 rows)
-#pragma unroll
-    for (int r = 0; r < 16; ++r) out.one(base + r, base + j, x[r]);
+    out.col(base, base + j, x);
 }
 
 // Level 1 (warps 0-1, warp t / 2 for target t = 0, 2; it solved T_tt and

@@ -121,12 +121,12 @@ size_t kda_chunk_prefill_workspace_size(int64_t N, int B, int H, int K, int V);
  *
  *   q, k, v       bf16 [N, H, 128]; q and k are used as given (no normalisation)
  *   g             fp32 [N, H, 128] log-decay, g <= 0.  A positive or NaN entry
- *                 sets INVALID_ARG in the device error word (a positive one is
- *                 computed as 0).  Each token's g is taken as at least -80
- *                 (e^-80 = 1.8e-35 lies far below fp32 resolution, so results
- *                 are unchanged at fp32 precision); chunks whose decay in some
- *                 channel exceeds what one chunk represents are split on the
- *                 device, so every decay is computed.
+ *                 sets INVALID_ARG in the device error word (that sequence's
+ *                 results are then unspecified).  Chunks whose decay in some
+ *                 channel exceeds what one chunk represents (160) are split on
+ *                 the device, and a token whose own g is below -160 is taken
+ *                 as -160 (e^-160 underflows fp32 as any stronger decay does),
+ *                 so every decay is computed.
  *   beta          fp32 [N, H], already passed through the sigmoid
  *   cu_seqlens    int32 [B+1] device offsets of B packed sequences
  *                 (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = N); NULL

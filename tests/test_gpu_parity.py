@@ -248,7 +248,7 @@ def _strong_decay_g(x, g_ref, case):
 @pytest.mark.parametrize("o_dtype", [torch.bfloat16, torch.float32])
 def test_prefill_strong_decay_matches_oracle(lib, case, o_dtype):
     """Per-channel chunk decays far beyond one chunk's range (and single tokens
-    beyond e^-80) are computed, not refused: the kernel shortens such chunks.
+    beyond e^-160) are computed, not refused: the kernel shortens such chunks.
     Parity with the fp64 recurrence on the same g."""
     x = synth.make_inputs(lengths=[200, 77, 1], H=2, D=128, seed=8, s0_std=0.05)
     g_ref, beta_ref = oracle_gate(x)
@@ -265,7 +265,7 @@ def test_prefill_strong_decay_matches_oracle(lib, case, o_dtype):
 @pytest.mark.parametrize("hard", ["all", "some_channels"])
 def test_prefill_gated_strong_decay_matches_oracle(lib, hard):
     """The gate fused into the kernel with A_log = 2 and f = 30 (g about -190
-    per token, clamped at -80 in the kernel), in every channel or in the first
+    per token: each token a chunk of its own), in every channel or in the first
     32 channels of each head beside the soft K3 ones."""
     x = synth.make_inputs(lengths=[130, 64, 9], H=2, D=128, seed=12, s0_std=0.05)
     f = x.f.float()
