@@ -77,6 +77,35 @@ def prefill_flops_per_head(lengths, K=D, V=D, C=CHUNK):
     return total
 
 
+def chunk_backward_flops_per_head(lengths, K=D, V=D, C=CHUNK):
+    """Algorithmic flops of the chunked backward for one head: the forward pass
+    that keeps the chunk-start states (prefill_flops_per_head), then per chunk of
+    L tokens the recomputed products (A_qk and A_kk, W, U-tilde, U = U-tilde - W S)
+    and the gradient products (dU, dS, dA_qk, dQbar, dW, dKhat, dT, d(beta K),
+    d(beta V), the two dA_kk products, dKtilde and dK), each counted as a dense
+    product of its operand shapes (2 flops per multiply-add)."""
+    total = prefill_flops_per_head(lengths, K, V, C)
+    for n in lengths:
+        for c0 in range(0, n, C):
+            L = min(C, n - c0)
+            macs = (2 * L * L * K            # [Qt; Kr] Ks^T
+                    + L * L * (K + V)        # W', U-tilde
+                    + L * K * V              # U
+                    + L * L * V + L * K * V  # dU
+                    + 2 * L * K * V          # dS
+                    + L * L * V              # dA_qk
+                    + L * K * V + L * L * K  # dQt
+                    + L * K * V              # dW'
+                    + L * K * V              # dKh
+                    + L * L * (K + V)        # dT
+                    + L * L * (K + V)        # d(beta Kr), d(beta V)
+                    + 2 * L * L * L          # T^T dT T^T
+                    + 2 * L * L * K          # dKs
+                    + L * L * K)             # dA_kk Ks
+            total += 2 * macs
+    return total
+
+
 def prefill_io_bytes(T, Hh=H, K=D, V=D, o_bytes=2):
     """Minimal HBM bytes of gate+prefill: f (bf16) read by the gate, g (fp32)
     written by the gate and read by prefill, b/beta, q/k/v (bf16) read, o written."""
@@ -348,10 +377,17 @@ def cpu_baseline(heads: int):
     g, beta = oracle.gate(f, b, x.A_log.numpy(), dt, x.alog_mode)
     oracle.recurrent(q, k, v, g, beta, nthreads=cores)
     elapsed = time.perf_counter() - t0
+    # one thread, on a sample of 4 heads
+    t1 = time.perf_counter()
+    g1, b1 = oracle.gate(f[:, :4], b[:, :4], x.A_log.numpy(), dt[:4], x.alog_mode)
+    oracle.recurrent(q[:, :4], k[:, :4], v[:, :4], g1, b1, nthreads=1)
+    one = time.perf_counter() - t1
     return {"value": T_PREFILL * heads / H / elapsed, "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
             "sample": f"gate + fp64 recurrence on {heads} of {H} heads, T={T_PREFILL}, d={D} "
-                      f"({elapsed:.1f} s); tokens/s scaled to all {H} heads"}
+                      f"({elapsed:.1f} s); tokens/s scaled to all {H} heads",
+            "one_thread": {"value": T_PREFILL * 4 / H / one, "unit": "tokens/s", "cores": 1,
+                           "sample": f"4 of {H} heads ({one:.1f} s), scaled to all {H} heads"}}
 
 
 # --- our arm -------------------------------------------------------------------------------
@@ -474,6 +510,44 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
+    def protocol(fn, warmup=20, iters=100, repeats=3):
+        """The timing protocol of the pages' FlashKDA measurements
+        (K3_ARTIFACT_AUDIT.md section 7.4): `warmup` untimed calls, then `repeats`
+        runs of `iters` calls, each call bracketed by CUDA events on the stream;
+        mean and 95th percentile over all calls, and the spread of the repeat
+        means (max / min)."""
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times, means = [], []
+        for _ in range(repeats):
+            evs = []
+            for _ in range(iters):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            rep = [a.elapsed_time(b) for a, b in evs]
+            times += rep
+            means.append(statistics.mean(rep))
+        times.sort()
+        return {"mean_ms": statistics.mean(times),
+                "p95_ms": times[min(len(times) - 1, int(0.95 * len(times)))],
+                "repeat_spread": max(means) / min(means), "calls": len(times),
+                "protocol": f"warm-up {warmup}, {repeats} x {iters} calls, CUDA events"}
+
+    proto = {}
+    proto["prefill_gated"] = protocol(lambda: kda.kda_chunk_prefill_gated(
+        q, k, v, f, b, A_log, x.alog_mode, dt_bias, None, 1.0, None, Sf, o, ws, stream))
+    proto["prefill_unfused"] = protocol(lambda: kda.kda_chunk_prefill(
+        q, k, v, g, beta, None, 1.0, None, Sf, o, ws, stream))
+    proto["gate"] = protocol(lambda: kda.kda_gate_fused(f, b, A_log, x.alog_mode, dt_bias, g, beta,
+                                                        stream))
+    proto["decode"] = protocol(lambda: kda.kda_recurrent_decode(dq, dk, dv, dg, dbeta, state, 1.0,
+                                                                dout, stream))
+
     # decode from a bf16 state pool addressed by slot (reversed order); its own
     # timed loop, not part of `value`
     pool = state.to(torch.bfloat16)
@@ -503,7 +577,12 @@ def run_ours(args):
     bwd_ms = timed(lambda: kda.kda_recurrent_backward(q, k, v, g, beta, None, 1.0, None, bdO, None,
                                                       *bgrads, bdbeta, None, bws, stream),
                    max(args.steps // 3, 1))
-    del bgrads, bws, bdO
+    cws = torch.empty(kda.kda_chunk_backward_workspace_size(T_PREFILL, 1, H), dtype=torch.uint8,
+                      device=dev)
+    proto["backward_chunked"] = protocol(
+        lambda: kda.kda_chunk_backward(q, k, v, g, beta, None, 1.0, None, bdO, None, *bgrads,
+                                       bdbeta, None, cws, stream), warmup=3, iters=10, repeats=3)
+    del bgrads, bws, bdO, cws
 
     prefill_leg_ms = max_over_ranks(fused_ms, world, dev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
@@ -584,7 +663,9 @@ def run_ours(args):
         return 0
     peaks = measured_peaks()
     hbm = peaks["hbm_gbs"]
-    # tf32 dense peak = measured bf16 peak x the nominal tf32/bf16 ratio (1.1/2.25)
+    # tf32 dense peak = measured bf16 peak x the ratio of NVIDIA's published dense
+    # rates for GB300 (tf32 1.1, bf16 2.25 PFLOP/s per GPU; the per-8-GPU figures of
+    # 18 and 36 PFLOP/s are with 2:4 sparsity)
     tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
     pf_flops = H * prefill_flops_per_head([T_PREFILL])
     pf_tflops = pf_flops / (fused_ms * 1e-3) / 1e12
@@ -598,6 +679,16 @@ def run_ours(args):
                   "hbm_achieved_gbs": pf_bytes / (fused_ms * 1e-3) / 1e9,
                   "hbm_frac": pf_bytes / (fused_ms * 1e-3) / 1e9 / hbm,
                   "algorithmic_bytes_per_launch": pf_bytes}
+    # the fraction of the binding roof: the time the kernel would take at the
+    # slower of its two roofs (tf32 tensor or HBM), over the measured time
+    t_tensor_ms = pf_flops / (tf32_peak * 1e12) * 1e3
+    t_hbm_ms = pf_bytes / (hbm * 1e9) * 1e3
+    roof_ms = max(t_tensor_ms, t_hbm_ms)
+    rl_prefill["binding_roof"] = "tensor" if t_tensor_ms >= t_hbm_ms else "hbm"
+    rl_prefill["roof_ms"] = {"tensor_tf32": t_tensor_ms, "hbm": t_hbm_ms}
+    rl_prefill["binding_roof_frac"] = roof_ms / fused_ms
+    rl_prefill["frac_of_bf16_peak"] = pf_tflops / peaks["bf16_tflops"]
+    rl_prefill["protocol"] = proto["prefill_gated"]
     up_bytes = prefill_kernel_bytes(T_PREFILL)
     rl_prefill_unfused = {"kernel": "kda chunked prefill, precomputed g and beta",
                           "bound": "tensor",
@@ -606,13 +697,14 @@ def run_ours(args):
                           "frac": pf_flops / (prefill_ms * 1e-3) / 1e12 / tf32_peak,
                           "traffic": None, "algorithmic_flops_per_launch": pf_flops,
                           "hbm_frac": up_bytes / (prefill_ms * 1e-3) / 1e9 / hbm,
-                          "algorithmic_bytes_per_launch": up_bytes}
+                          "algorithmic_bytes_per_launch": up_bytes,
+                          "protocol": proto["prefill_unfused"]}
     dec_bytes = decode_bytes()
     dec_gbs = dec_bytes / (decode_ms_max * 1e-3) / 1e9
     rl_decode = {"kernel": "kda recurrent decode", "bound": "hbm",
                  "achieved": dec_gbs, "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm,
                  "traffic": None, "peak_source": peaks["source"],
-                 "algorithmic_bytes_per_launch": dec_bytes}
+                 "algorithmic_bytes_per_launch": dec_bytes, "protocol": proto["decode"]}
     pool_bytes = decode_bytes(state_bytes=2) + B_DECODE * 4
     pool_gbs = pool_bytes / (pool_ms * 1e-3) / 1e9
     rl_pool = {"kernel": "kda recurrent decode, bf16 state pool by slot", "bound": "hbm",
@@ -644,10 +736,22 @@ def run_ours(args):
     gate_gbs = gate_bytes / (gate_ms * 1e-3) / 1e9
     rl_gate = {"kernel": "kda gate", "bound": "hbm", "achieved": gate_gbs, "peak": hbm,
                "unit": "GB/s", "frac": gate_gbs / hbm, "traffic": None,
-               "peak_source": peaks["source"], "algorithmic_bytes_per_launch": gate_bytes}
+               "peak_source": peaks["source"], "algorithmic_bytes_per_launch": gate_bytes,
+               "protocol": proto["gate"]}
+    cb_ms = proto["backward_chunked"]["mean_ms"]
+    cb_flops = H * chunk_backward_flops_per_head([T_PREFILL])
+    cb_tflops = cb_flops / (cb_ms * 1e-3) / 1e12
+    rl_cbwd = {"kernel": "kda chunked backward (tcgen05 bf16 high/low products; with its "
+                         "checkpointing forward pass)", "bound": "tensor",
+               "achieved": cb_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+               "frac": cb_tflops / peaks["bf16_tflops"], "traffic": None,
+               "peak_source": f"{peaks['source']} bf16 burst",
+               "algorithmic_flops_per_launch": cb_flops, "ms": cb_ms,
+               "tokens_per_s": T_PREFILL / (cb_ms * 1e-3),
+               "protocol": proto["backward_chunked"]}
     for rl, kid in ((rl_prefill, "chunk_gated"), (rl_prefill_unfused, "chunk_unfused"),
                     (rl_decode, "decode"), (rl_pool, "decode_pool"), (rl_gate, "gate"),
-                    (rl_conv, "short_conv"), (rl_bwd, "backward")):
+                    (rl_conv, "short_conv"), (rl_bwd, "backward"), (rl_cbwd, "backward_chunked")):
         rl["traffic"], rl["traffic_note"] = measured_traffic(kid)
     # the dominant kernel is the one with the largest share of the step
     roofline = rl_prefill if fused_ms >= decode_ms_max else rl_decode
@@ -668,7 +772,8 @@ def run_ours(args):
         "roofline": roofline,
         "rooflines": {"gate": rl_gate, "prefill_gated": rl_prefill,
                       "prefill_unfused": rl_prefill_unfused, "decode": rl_decode,
-                      "decode_bf16_pool": rl_pool, "short_conv": rl_conv, "backward": rl_bwd},
+                      "decode_bf16_pool": rl_pool, "short_conv": rl_conv, "backward": rl_bwd,
+                      "backward_chunked": rl_cbwd},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "schedule": "steps pipelined over two buffer sets: H2D, prefill and D2H "
@@ -696,10 +801,10 @@ def run_profile_case(args):
         ws = [t.to(dev) for t in sx.w]
         for _ in range(args.warmup + 1):
             kda.short_conv(*xs, *ws)
-    elif args.profile in ("gate", "prefill", "prefill_gated", "backward"):
+    elif args.profile in ("gate", "prefill", "prefill_gated", "backward", "backward_chunked"):
         x = synth.make_inputs(args.size, H=H, D=D, seed=0, device=dev)
         g, beta = kda.gate(x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
-        dO = torch.randn_like(x.q) if args.profile == "backward" else None
+        dO = torch.randn_like(x.q) if args.profile.startswith("backward") else None
         for _ in range(args.warmup + 1):
             if args.profile == "gate":
                 kda.gate(x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
@@ -707,8 +812,10 @@ def run_profile_case(args):
                 kda.prefill(x.q, x.k, x.v, g, beta)
             elif args.profile == "prefill_gated":
                 kda.prefill_gated(x.q, x.k, x.v, x.f, x.b, x.A_log, x.dt_bias, x.alog_mode)
-            else:
+            elif args.profile == "backward":
                 kda.backward(x.q, x.k, x.v, g, beta, dO, want_dS0=False)
+            else:
+                kda.backward_chunked(x.q, x.k, x.v, g, beta, dO, want_dS0=False)
     else:
         d = synth.make_decode_inputs(args.size, H=H, D=D, seed=0, state_device=dev)
         q, k, v, f, b = (t.to(dev) for t in (d.q, d.k, d.v, d.f, d.b))
@@ -740,7 +847,8 @@ def main():
                     help="heads of the T=4096 workload timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["gate", "prefill", "prefill_gated", "decode",
-                                                  "decode_pool", "short_conv", "backward"], default=None,
+                                          "decode_pool", "short_conv", "backward",
+                                          "backward_chunked"], default=None,
                     help="run only this kernel (warm-up + 1 launch) for an ncu capture")
     ap.add_argument("--size", type=int, default=1024,
                     help="--profile size: tokens (gate, prefill) or sequences (decode)")
