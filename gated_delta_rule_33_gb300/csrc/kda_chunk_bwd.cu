@@ -112,7 +112,7 @@ constexpr uint32_t kScratchPerCta = img_off(kNumImg);  // 540672
 // ---- shared memory (bytes from a 1024-aligned base) -------------------------------------
 constexpr uint32_t SLOT_A = 0;            // operand slot, 64 KB
 constexpr uint32_t SLOT_B = 65536;        // operand slot, 64 KB
-constexpr uint32_t OFF_AT = 131072;       // A_kk column-major fp32 [64][64]
+constexpr uint32_t OFF_AT = 131072;       // A_kk column-major fp32 [64][64]; q staged outside the inverse
 constexpr uint32_t OFF_TT = 147456;       // T row-major fp32 (inverse work area)
 constexpr uint32_t OFF_KK = 163840;       // kk fp32 [64][64] column-major
 constexpr uint32_t OFF_MISC = 180224;
@@ -130,7 +130,8 @@ constexpr uint32_t M_BAR = 15360;         // 2 mbarriers
 constexpr uint32_t M_CTRL = 15376;        // int[8]: tmem base, chain, abort
 constexpr uint32_t M_KHS = 15424;         // float[128] colsum(dKh . Kh)
 constexpr uint32_t M_GL = 15936;          // float[128] Gam_L (log2 units)
-constexpr uint32_t kSmemBytes = OFF_MISC + 16448;
+constexpr uint32_t OFF_STG = OFF_MISC + 16448;  // k, v bf16 [64][128] each, the whole chunk
+constexpr uint32_t kSmemBytes = OFF_STG + 32768;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 // ---- tensor memory columns (lane = M row of each product) ----
@@ -191,41 +192,15 @@ __device__ __forceinline__ void put8(uint8_t *img, uint32_t half, uint32_t rows,
     if (half != 0) *reinterpret_cast<uint4 *>(img + half + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-// four consecutive columns j0 .. j0 + 3 (j0 % 4 == 0) of row i: one 8-byte store each
-__device__ __forceinline__ void put4(uint8_t *img, uint32_t half, uint32_t rows, int i, int j0,
-                                     const float *x) {
-    uint32_t hw[2], lw[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        const float2 hf = __bfloat1622float2(h);
-        const __nv_bfloat162 l = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
-        hw[e] = *reinterpret_cast<const uint32_t *>(&h);
-        lw[e] = *reinterpret_cast<const uint32_t *>(&l);
-    }
-    const uint32_t o = sw128_offset(i, j0, rows, 2);
-    *reinterpret_cast<uint2 *>(img + o) = make_uint2(hw[0], hw[1]);
-    if (half != 0) *reinterpret_cast<uint2 *>(img + half + o) = make_uint2(lw[0], lw[1]);
-}
-
-// The UT inverse's output policy here: T diag(beta) and T as split images.
-struct TSplitImages {
-    uint8_t *tb, *t;
-    const float *beta;
-    __device__ __forceinline__ void one(int r, int s, float x) const {
-        put1(tb, 8192, 64, r, s, x * beta[s]);
-        put1(t, 8192, 64, r, s, x);
-    }
-    __device__ __forceinline__ void col(int r0, int j, const float (&x)[16]) const {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) one(r0 + i, j, x[i]);
-    }
+// The UT inverse's output policy here: the blocks it does not keep in its
+// row-major T itself (T_32 and the lower-left 32 x 32 block) are written there,
+// so that T is complete (fp32, row-major, zero above the diagonal) when the
+// inverse returns; the split images are formed from it by the whole CTA.
+struct TRowMajor {
+    float *t;
+    __device__ __forceinline__ void col(int, int, const float (&)[16]) const {}  // already in T
     __device__ __forceinline__ void four(int r, int s4, float4 x) const {
-        const float v[4] = {x.x, x.y, x.z, x.w};
-        const float vb[4] = {x.x * beta[s4], x.y * beta[s4 + 1], x.z * beta[s4 + 2],
-                             x.w * beta[s4 + 3]};
-        put4(tb, 8192, 64, r, s4, vb);
-        put4(t, 8192, 64, r, s4, v);
+        *reinterpret_cast<float4 *>(t + r * 64 + s4) = x;
     }
 };
 
@@ -302,8 +277,8 @@ __device__ __forceinline__ float lanes_sum16(float (&x)[16], int lane) {
 }
 
 // The product engine's state (identical in every thread): the image each of
-// the two operand slots holds (-1: none), the barrier phases, and what is in
-// flight for the drain.
+// the two operand slots holds (-1: none), the barrier phases, what is in
+// flight for the drain, and the bulk stores of images staged in a slot.
 struct Sched {
     uint8_t *smem, *scr;
     uint64_t *bar_load, *bar_mma;
@@ -314,7 +289,8 @@ struct Sched {
     int sl0, sl1;
     uint32_t ph_load, ph_mma;
     bool pend_load, pend_mma;
-    bool t_store;  // thread 0: the bulk store of the T image is in flight
+    bool st_read;      // a bulk store may still be reading its slot
+    uint32_t st_imgs;  // images whose bulk store may still be writing (bit per image)
 };
 
 // An operand: image, first row used, MN-major.
@@ -325,6 +301,45 @@ struct OpSpec {
 __device__ __forceinline__ void dirty(Sched &S, int i) {
     if (S.sl0 == i) S.sl0 = -1;
     if (S.sl1 == i) S.sl1 = -1;
+}
+
+__device__ __forceinline__ uint8_t *slot_ptr(const Sched &S, int sl) {
+    return S.smem + (sl ? SLOT_B : SLOT_A);
+}
+
+// After an epilogue wrote image `i` (or the row range [r0, r1) of it) into slot
+// `sl` in the image's own byte layout: makes the writes visible to the async
+// proxy, and thread 0 bulk-stores the written bytes to the image in the
+// scratch.  A whole image stays in the slot for the next products.
+__device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0, uint32_t r1) {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t rows = img_rows(i), nblk = img_cols(i) / 64;
+    const bool whole = r0 == 0 && r1 == rows;
+    if (S.tid == 0) {
+        uint8_t *src = slot_ptr(S, sl), *dst = S.scr + img_off(i);
+        if (whole) {
+            bulk_store(dst, src, img_bytes(i));
+        } else {
+            // rows [r0, r1) of each 64-column block of the hi (and lo) tile
+            const uint32_t tiles = img_exact(i) ? 1u : 2u;
+            for (uint32_t t = 0; t < tiles; ++t)
+                for (uint32_t b = 0; b < nblk; ++b) {
+                    const uint32_t o = t * img_half(i) + b * rows * 128 + r0 * 128;
+                    bulk_store(dst + o, src + o, (r1 - r0) * 128);
+                }
+        }
+    }
+    S.st_read = true;
+    S.st_imgs |= 1u << i;
+    if (sl) S.sl1 = whole ? i : (S.sl1 == i ? i : -1); else S.sl0 = whole ? i : (S.sl0 == i ? i : -1);
+    // any other copy of a partly rewritten image is stale
+    if (!whole) {
+        if (sl && S.sl0 == i) S.sl0 = -1;
+        if (!sl && S.sl1 == i) S.sl1 = -1;
+    }
 }
 
 // One product term, D[tmem d] (+)= A B: bulk-copies the operand images that are
@@ -346,12 +361,20 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         pb = (pa == 0) ? 1 : 0;
         lb = pb;
     }
+    // a staged image's store finishes reading its slot before the slot is
+    // reloaded or rewritten (after this product), and finishes writing before
+    // the image is copied back
+    const bool reload_stored = (la >= 0 && ((S.st_imgs >> ia) & 1u)) || (lb >= 0 && ((S.st_imgs >> ib) & 1u));
+    if (S.tid == 0) {
+        if (reload_stored)
+            bulk_wait_all();
+        else if (S.st_read)
+            bulk_wait_read();
+    }
+    if (reload_stored) S.st_imgs = 0;
+    S.st_read = false;
     if (la >= 0 || lb >= 0) {
         if (S.tid == 0) {
-            if (S.t_store && (ia == I_T || ib == I_T)) {
-                bulk_wait_all();
-                S.t_store = false;
-            }
             const uint32_t bytes = (la >= 0 ? img_bytes(ia) : 0u) + (lb >= 0 ? img_bytes(ib) : 0u);
             mbar_arrive_expect_tx(S.bar_load, bytes);
             if (la >= 0)
@@ -413,6 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
         fence_mbar_init();
         ctrl[2] = 0;
     }
+    // the inverse's T: the blocks above the diagonal stay zero for every chunk
+    for (int e = tid; e < 4096 / 4; e += kThreads)
+        reinterpret_cast<float4 *>(smem + OFF_TT)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -435,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.sl0 = S.sl1 = -1;
     S.ph_load = S.ph_mma = 0;
     S.pend_load = S.pend_mma = false;
-    S.t_store = false;
+    S.st_read = false;
+    S.st_imgs = 0;
     const float kLog2e = 1.4426950408889634f;
     const float kMaxChunkLog2 = kMaxChunkDecay * kLog2e;
 
@@ -484,15 +511,43 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             const int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
             const float *Sc = p.ckpt + ((slot0 + c) * H + h) * (kD * kD);
             S.sl0 = S.sl1 = -1;  // every image is rewritten for this chunk
+            // ---- B0: the chunk's rows into shared memory by 16-byte cp.async
+            // (rows past the sequence zero-filled): g and dO to slot A, q to the
+            // A_kk area (free until the D_A epilogue), k and v to the staging
+            // area (read again later) ----
+            {
+                const int dob = p.dO_bf16 ? 2 : 4;  // bytes per dO element
+                auto src_row = [&](int r) { return ((tc + (r < L ? r : 0)) * H + h) * kD; };
+                for (int u = tid; u < kC * 32; u += kThreads) {
+                    const int r = u >> 5, pc = u & 31;
+                    cp_async_16(smem + SLOT_A + u * 16, p.g + src_row(r) + pc * 4, r < L);
+                }
+                const int dpr = 8 * dob;  // 16-byte pieces per dO row
+                for (int u = tid; u < kC * dpr; u += kThreads) {
+                    const int r = u / dpr, pc = u - r * dpr;
+                    cp_async_16(smem + SLOT_A + 32768 + u * 16,
+                                static_cast<const uint8_t *>(p.dO) + src_row(r) * dob + pc * 16, r < L);
+                }
+                for (int u = tid; u < kC * 16; u += kThreads) {
+                    const int r = u >> 4, pc = u & 15;
+                    const int64_t e = src_row(r) + pc * 8;
+                    cp_async_16(smem + OFF_AT + u * 16, p.q + e, r < L);
+                    cp_async_16(smem + OFF_STG + u * 16, p.k + e, r < L);
+                    cp_async_16(smem + OFF_STG + 16384 + u * 16, p.v + e, r < L);
+                }
+                cp_async_wait_all();
+            }
+            __syncthreads();
 
             // ---- B1: cumulative decay and the chunk operand images ----
             float gam[16];
+            float *gA = reinterpret_cast<float *>(smem + SLOT_A);  // g, then Gam in place
             {
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {  // the forward kernel's order
                     const int r = 16 * grp + i;
-                    if (r < L) acc += kLog2e * p.g[((tc + r) * H + h) * kD + ch];
+                    if (r < L) acc += kLog2e * gA[r * kD + ch];
                     gam[i] = acc;
                 }
                 s_part[grp * kD + ch] = acc;
@@ -518,35 +573,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) gam[i] += prefix;  // Gam_r in log2 units from here on
-            // Gam [64][128] to slot B, then the operand images eight channels of one
-            // row at a time (unit u: row u / 16, channels 8 (u % 16) .. + 7)
-            {
-                float *gt = reinterpret_cast<float *>(smem + SLOT_B);
+            // Gam [64][128] over g in slot A (each thread its own elements), then
+            // the operand images eight channels of one row at a time (unit u: row
+            // u / 16, channels 8 (u % 16) .. + 7)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) gt[(16 * grp + i) * kD + ch] = gam[i];
-            }
+            for (int i = 0; i < 16; ++i) gA[(16 * grp + i) * kD + ch] = gam[i];
             __syncthreads();
 #pragma unroll 1
             for (int u = tid; u < kC * 16; u += kThreads) {
                 const int r = u >> 4, c0 = (u & 15) * 8;
-                float qv[8], kv[8], vv[8], dov[8];
-                if (r < L) {
-                    const int64_t e = ((tc + r) * H + h) * kD + c0;
-                    const uint4 q8 = *reinterpret_cast<const uint4 *>(p.q + e);
-                    const uint4 k8 = *reinterpret_cast<const uint4 *>(p.k + e);
-                    const uint4 v8 = *reinterpret_cast<const uint4 *>(p.v + e);
+                float qv[8], kv[8], vv[8], dov[8];  // rows past the sequence are zero
+                {
+                    const uint4 q8 = *reinterpret_cast<const uint4 *>(smem + OFF_AT + u * 16);
+                    const uint4 k8 = *reinterpret_cast<const uint4 *>(smem + OFF_STG + u * 16);
+                    const uint4 v8 = *reinterpret_cast<const uint4 *>(smem + OFF_STG + 16384 + u * 16);
                     const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(&q8);
                     const __nv_bfloat16 *kb = reinterpret_cast<const __nv_bfloat16 *>(&k8);
                     const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(&v8);
                     if (p.dO_bf16) {
-                        const uint4 d8 = *reinterpret_cast<const uint4 *>(
-                            static_cast<const __nv_bfloat16 *>(p.dO) + e);
+                        const uint4 d8 = *reinterpret_cast<const uint4 *>(smem + SLOT_A + 32768 + u * 16);
                         const __nv_bfloat16 *db = reinterpret_cast<const __nv_bfloat16 *>(&d8);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) dov[j] = __bfloat162float(db[j]);
                     } else {
-                        const float4 d0 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.dO) + e);
-                        const float4 d1 = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.dO) + e + 4);
+                        const float4 d0 = *reinterpret_cast<const float4 *>(smem + SLOT_A + 32768 + u * 32);
+                        const float4 d1 = *reinterpret_cast<const float4 *>(smem + SLOT_A + 32768 + u * 32 + 16);
                         dov[0] = d0.x; dov[1] = d0.y; dov[2] = d0.z; dov[3] = d0.w;
                         dov[4] = d1.x; dov[5] = d1.y; dov[6] = d1.z; dov[7] = d1.w;
                     }
@@ -556,11 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                         kv[j] = __bfloat162float(kb[j]);
                         vv[j] = __bfloat162float(vb[j]);
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) qv[j] = kv[j] = vv[j] = dov[j] = 0.f;
                 }
-                const float *gt = reinterpret_cast<const float *>(smem + SLOT_B) + r * kD + c0;
+                const float *gt = gA + r * kD + c0;
                 float qt[8], kr[8], ks[8], kh[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -571,35 +619,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     ks[j] = kv[j] * fast_exp2(mj - gr);
                     kh[j] = kv[j] * fast_exp2(gl - gr);
                 }
-                put8(img(I_QK), img_half(I_QK), 128, r, c0, qt);
-                put8(img(I_QK), img_half(I_QK), 128, 64 + r, c0, kr);
+                put8(smem + SLOT_B, img_half(I_QK), 128, r, c0, qt);  // staged (slot B is free)
+                put8(smem + SLOT_B, img_half(I_QK), 128, 64 + r, c0, kr);
                 put8(img(I_KS), img_half(I_KS), 64, r, c0, ks);
                 put8(img(I_KH), img_half(I_KH), 64, r, c0, kh);
                 put8(img(I_V), 0, 64, r, c0, vv);
                 put8(img(I_DU2), img_half(I_DU2), 128, 64 + r, c0, dov);
             }
-
-            // ---- B2: S_op^T and dS'^T images (row v = this lane); sum_v dS' S ----
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                const int k0 = 32 * grp + 16 * half;
-                float ds[16], sv[16], so[16];
-                tmem_ld16(tl + C_DS + k0, ds);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) sv[j] = Sc[(k0 + j) * kD + ch];
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) so[j] = s_em[k0 + j] * sv[j];
-                put8(img(I_SO), img_half(I_SO), 128, ch, k0, so);
-                put8(img(I_SO), img_half(I_SO), 128, ch, k0 + 8, so + 8);
-                put8(img(I_DS), img_half(I_DS), 128, ch, k0, ds);
-                put8(img(I_DS), img_half(I_DS), 128, ch, k0 + 8, ds + 8);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) so[j] = ds[j] * sv[j];
-                const float t = lanes_sum16(so, lane);
-                if ((lane & 1) == 0) atomicAdd(&s_dgl[k0 + (lane >> 1)], t);
-            }
-            publish();
+            fence_proxy_async_global();
+            stage_store(S, 1, I_QK, 0, 128);
 
             // ---- D_A = [Qt; Kr] Ks^T ----
             if (!product(S, {I_QK, 0, 0}, {I_KS, 0, 0}, tmem + C_TA, 64, 8, false)) break;
@@ -627,73 +655,124 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             dirty(S, I_AQ);
             __syncthreads();
 
-            // ---- T = (I + A_kk)^{-1} on warps 0-3: T diag(beta) and T staged in
-            // slot B (strictly upper blocks zero), T stored to its image ----
-            for (int e = tid; e < 32768 / 16; e += kThreads)
-                reinterpret_cast<uint4 *>(smem + SLOT_B)[e] = make_uint4(0u, 0u, 0u, 0u);
-            __syncthreads();
-            if (warp < 4) {
+            // ---- T = (I + A_kk)^{-1} on warps 0-3 (fp32, row-major); meanwhile
+            // warps 4-15 (B2) form the S_op^T and dS'^T images (row v = the
+            // lane) and sum_v dS' S from the chunk-start state S, brought into
+            // slot B (free since D_A).  Then T diag(beta) and T as split images
+            // staged in slot B by every thread (row tid / 8, columns 8 (tid % 8)
+            // .. + 7), T stored to its image ----
+            {
                 float *T = reinterpret_cast<float *>(smem + OFF_TT);
-                float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
-                float *T32c = reinterpret_cast<float *>(misc + M_T32);
-                float *P = reinterpret_cast<float *>(misc + M_P);
-                const TSplitImages out{smem + SLOT_B, smem + SLOT_B + img_bytes(I_TB), s_beta};
-                if (tid < 64) {
-                    ut_diag_solve(s_at, T, Tdiag, out, tid);
-                    __syncwarp();
-                    ut_level1(s_at, T, Tdiag, P, T, T32c, out, tid);
+                if (warp >= 4) {
+                    for (int u = tid - 128; u < 4096; u += kThreads - 128)
+                        cp_async_16(smem + SLOT_B + u * 16, Sc + u * 4, true);
+                    cp_async_wait_all();
+                    named_sync(2, kThreads - 128);
+                    // 16-column units of k: warps 4-7 take units 0, 3, 6, warps
+                    // 8-11 units 1, 4, 7 and warps 12-15 units 2, 5
+#pragma unroll 1
+                    for (int u = grp - 1; u < 8; u += 3) {
+                        const int k0 = 16 * u;
+                        float ds[16], sv[16], so[16];
+                        tmem_ld16(tl + C_DS + k0, ds);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            sv[j] = reinterpret_cast<const float *>(smem + SLOT_B)[(k0 + j) * kD + ch];
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) so[j] = s_em[k0 + j] * sv[j];
+                        put8(img(I_SO), img_half(I_SO), 128, ch, k0, so);
+                        put8(img(I_SO), img_half(I_SO), 128, ch, k0 + 8, so + 8);
+                        put8(img(I_DS), img_half(I_DS), 128, ch, k0, ds);
+                        put8(img(I_DS), img_half(I_DS), 128, ch, k0 + 8, ds + 8);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) so[j] = ds[j] * sv[j];
+                        const float t = lanes_sum16(so, lane);
+                        if ((lane & 1) == 0) atomicAdd(&s_dgl[k0 + (lane >> 1)], t);
+                    }
+                } else {
+                    float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
+                    float *T32c = reinterpret_cast<float *>(misc + M_T32);
+                    float *P = reinterpret_cast<float *>(misc + M_P);
+                    const TRowMajor out{T};
+                    if (tid < 64) {
+                        ut_diag_solve(s_at, T, Tdiag, out, tid);
+                        __syncwarp();
+                        ut_level1(s_at, T, Tdiag, P, T, T32c, out, tid);
+                    }
+                    inverse_sync();
+                    ut_level2(s_at, T, Tdiag, T32c, P, out, tid);
                 }
-                inverse_sync();
-                ut_level2(s_at, T, Tdiag, T32c, P, out, tid);
+                __syncthreads();
+                // A_kk is consumed: q again into its area for the assembly
+                for (int u = tid; u < kC * 16; u += kThreads) {
+                    const int r = u >> 4, pc = u & 15;
+                    cp_async_16(smem + OFF_AT + u * 16, p.q + ((tc + (r < L ? r : 0)) * H + h) * kD + pc * 8,
+                                r < L);
+                }
+                const int r = tid >> 3, c0 = (tid & 7) * 8;
+                const float4 t0 = *reinterpret_cast<const float4 *>(T + r * 64 + c0);
+                const float4 t1 = *reinterpret_cast<const float4 *>(T + r * 64 + c0 + 4);
+                const float t8[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                float tb8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tb8[j] = t8[j] * s_beta[c0 + j];
+                put8(smem + SLOT_B, img_half(I_TB), 64, r, c0, tb8);
+                put8(smem + SLOT_B + img_bytes(I_TB), img_half(I_T), 64, r, c0, t8);
             }
             fence_proxy_async_smem();
             publish();
-            if (tid == 0) {
-                bulk_store(img(I_T), smem + SLOT_B + img_bytes(I_TB), img_bytes(I_T));
-                bulk_wait_read();
-                S.t_store = true;
-            }
+            if (tid == 0) bulk_store(img(I_T), smem + SLOT_B + img_bytes(I_TB), img_bytes(I_T));
+            S.st_read = true;
+            S.st_imgs |= 1u << I_T;
             S.sl1 = I_TB;
 
-            // ---- W'^T = Kr^T (T beta)^T ; -W'^T image ----
+            // Epilogues below write their image into a slot whose operand is
+            // dead (the image's own byte layout) and bulk-store it from there;
+            // a whole image stays in the slot for the products that follow.
+
+            // ---- W'^T = Kr^T (T beta)^T and Ut^T = V^T (T beta)^T; -W'^T image
+            // in V's slot ----
             if (!product(S, {I_QK, 64, 1}, {I_TB, 0, 0}, tmem + C_TA, 64, 4, false)) break;
+            if (!product(S, {I_V, 0, 1}, {I_TB, 0, 0}, tmem + C_TB, 64, 4, false)) break;
             {
+                const int sl = (S.sl0 == I_V) ? 0 : 1;
                 float w16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, w16);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) w16[j] = -w16[j];
-                put8(img(I_WT), img_half(I_WT), 128, ch, 16 * grp, w16);
-                put8(img(I_WT), img_half(I_WT), 128, ch, 16 * grp + 8, w16 + 8);
+                put8(slot_ptr(S, sl), img_half(I_WT), 128, ch, 16 * grp, w16);
+                put8(slot_ptr(S, sl), img_half(I_WT), 128, ch, 16 * grp + 8, w16 + 8);
+                stage_store(S, sl, I_WT, 0, 128);
             }
-            dirty(S, I_WT);
-            publish();
 
-            // ---- Ut^T = V^T (T beta)^T, then U^T = Ut^T + S_op^T (-W'^T) ----
-            if (!product(S, {I_V, 0, 1}, {I_TB, 0, 0}, tmem + C_TB, 64, 4, false)) break;
+            // ---- U^T = Ut^T + S_op^T (-W'^T); U^T image in S_op's slot ----
             if (!product(S, {I_SO, 0, 0}, {I_WT, 0, 1}, tmem + C_TB, 64, 8, true)) break;
             {
+                const int sl = (S.sl0 == I_SO) ? 0 : 1;
                 float u16[16];
                 tmem_ld16(tl + C_TB + 16 * grp, u16);
                 tmem_wait_ld();
-                put8(img(I_UT), img_half(I_UT), 128, ch, 16 * grp, u16);
-                put8(img(I_UT), img_half(I_UT), 128, ch, 16 * grp + 8, u16 + 8);
+                put8(slot_ptr(S, sl), img_half(I_UT), 128, ch, 16 * grp, u16);
+                put8(slot_ptr(S, sl), img_half(I_UT), 128, ch, 16 * grp + 8, u16 + 8);
+                stage_store(S, sl, I_UT, 0, 128);
             }
-            dirty(S, I_UT);
-            publish();
 
-            // ---- dU^T = dO^T A_qk + dS'^T Kh ; dU image (rows 0-63 of DU2) ----
-            if (!product(S, {I_DU2, 64, 1}, {I_AQ, 0, 1}, tmem + C_TA, 64, 4, false)) break;
-            if (!product(S, {I_DS, 0, 0}, {I_KH, 0, 0}, tmem + C_TA, 64, 8, true)) break;
+            // ---- dU^T = dS'^T Kh + dO^T A_qk ; dU into rows 0-63 of DU2, which
+            // stays in its slot ----
+            if (!product(S, {I_DS, 0, 0}, {I_KH, 0, 0}, tmem + C_TA, 64, 8, false)) break;
+            if (!product(S, {I_DU2, 64, 1}, {I_AQ, 0, 1}, tmem + C_TA, 64, 4, true)) break;
             {
+                const int sl = (S.sl0 == I_DU2) ? 0 : 1;
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);  // dU^T[v = ch][r]
                 tmem_wait_ld();
-#pragma unroll 1
-                for (int j = 0; j < 16; ++j) put1(img(I_DU2), img_half(I_DU2), 128, 16 * grp + j, ch, d16[j]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    put1(slot_ptr(S, sl), img_half(I_DU2), 128, 16 * grp + j, ch, d16[j]);
+                stage_store(S, sl, I_DU2, 0, 64);
             }
-            dirty(S, I_DU2);
-            publish();
 
             // ---- P^T = dO^T Qt - dU^T W'^T... ; dS <- e^{Gam_L} dS' + e^m P ----
             if (!product(S, {I_DU2, 64, 1}, {I_QK, 0, 1}, tmem + C_TA, 128, 4, false)) break;
@@ -711,38 +790,44 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 tmem_st32(tl + C_DS + 32 * grp, ds);
                 tmem_wait_st();
             }
-            publish();
+            tc_fence_before();  // (no global image was written since the last publish)
+            __syncthreads();
+            tc_fence_after();
 
             // ---- dA_qk = tril(dO U^T) (lanes 64-127 of [dU; dO] U^T) ----
             if (!product(S, {I_DU2, 0, 0}, {I_UT, 0, 1}, tmem + C_TA, 64, 8, false)) break;
-            if (quarter >= 2) {
-                const int r = ch - 64;
+            {
+                const int sl = (S.sl0 == I_UT) ? 0 : 1;
+                if (quarter >= 2) {
+                    const int r = ch - 64;
+                    float d16[16];
+                    tmem_ld16(tl + C_TA + 16 * grp, d16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) d16[j] = (16 * grp + j <= r) ? d16[j] : 0.f;
+                    put8(slot_ptr(S, sl), img_half(I_DAQ), 64, r, 16 * grp, d16);
+                    put8(slot_ptr(S, sl), img_half(I_DAQ), 64, r, 16 * grp + 8, d16 + 8);
+                }
+                stage_store(S, sl, I_DAQ, 0, 64);
+            }
+
+            // ---- [-dW'^T | dQt^T] = S_op [dU; dO]^T (DU2 still in its slot) ;
+            // dKs^T = Qt^T dA_qk ; dQt^T += Ks^T dA_qk^T ----
+            if (!product(S, {I_SO, 0, 1}, {I_DU2, 0, 0}, tmem + C_TA, 128, 8, false)) break;
+            if (!product(S, {I_QK, 0, 1}, {I_DAQ, 0, 1}, tmem + C_S, 64, 4, false)) break;
+            if (!product(S, {I_KS, 0, 1}, {I_DAQ, 0, 0}, tmem + C_TB, 64, 4, true)) break;
+            {
+                // -dW'^T[k = ch][r]: dW'[r][k] into rows 0-63 of the QK image (Qt is
+                // dead), staged in the slot dA_qk used
+                const int sl = (S.sl0 == I_DAQ) ? 0 : 1;
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) d16[j] = (16 * grp + j <= r) ? d16[j] : 0.f;
-                put8(img(I_DAQ), img_half(I_DAQ), 64, r, 16 * grp, d16);
-                put8(img(I_DAQ), img_half(I_DAQ), 64, r, 16 * grp + 8, d16 + 8);
+                for (int j = 0; j < 16; ++j)
+                    put1(slot_ptr(S, sl), img_half(I_QK), 128, 16 * grp + j, ch, -d16[j]);
+                stage_store(S, sl, I_QK, 0, 64);
             }
-            dirty(S, I_DAQ);
-            publish();
-
-            // ---- dKs^T = Qt^T dA_qk ----
-            if (!product(S, {I_QK, 0, 1}, {I_DAQ, 0, 1}, tmem + C_S, 64, 4, false)) break;
-
-            // ---- [-dW'^T | dQt^T] = S_op [dU; dO]^T ; dQt^T += Ks^T dA_qk^T ----
-            if (!product(S, {I_SO, 0, 1}, {I_DU2, 0, 0}, tmem + C_TA, 128, 8, false)) break;
-            if (!product(S, {I_KS, 0, 1}, {I_DAQ, 0, 0}, tmem + C_TB, 64, 4, true)) break;
-            {
-                float d16[16];  // -dW'^T[k = ch][r]: dW'[r][k] into rows 0-63 of the QK image (Qt is dead)
-                tmem_ld16(tl + C_TA + 16 * grp, d16);
-                tmem_wait_ld();
-#pragma unroll 1
-                for (int j = 0; j < 16; ++j) put1(img(I_QK), img_half(I_QK), 128, 16 * grp + j, ch, -d16[j]);
-            }
-            dirty(S, I_QK);
-            publish();
 
             // ---- dKh^T = dS' U^T ----
             if (!product(S, {I_DS, 0, 1}, {I_UT, 0, 1}, tmem + C_H, 64, 8, false)) break;
@@ -756,11 +841,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) d16[j] *= s_beta[16 * grp + j];
-                put8(img(I_DT), img_half(I_DT), 64, ch, 16 * grp, d16);
-                put8(img(I_DT), img_half(I_DT), 64, ch, 16 * grp + 8, d16 + 8);
+                put8(slot_ptr(S, S.sl0 == I_V ? 0 : 1), img_half(I_DT), 64, ch, 16 * grp, d16);
+                put8(slot_ptr(S, S.sl0 == I_V ? 0 : 1), img_half(I_DT), 64, ch, 16 * grp + 8, d16 + 8);
             }
-            dirty(S, I_DT);
-            publish();
+            stage_store(S, S.sl0 == I_V ? 0 : 1, I_DT, 0, 64);
 
             // ---- d(beta Kr)^T = dW'^T T and d(beta V)^T = dU^T T ----
             if (!product(S, {I_QK, 0, 1}, {I_T, 0, 1}, tmem + C_R, 64, 4, false)) break;
@@ -771,15 +855,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 float vb[16], rb[16], vv[16], kr[16];
                 tmem_ld16(tl + C_VB + 16 * grp, vb);
                 tmem_ld16(tl + C_R + 16 * grp, rb);
+                const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_STG);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 16; ++j) {  // staged rows (zero past the sequence)
                     const int r = 16 * grp + j;
-                    vv[j] = kr[j] = 0.f;
-                    if (r < L) {
-                        const int64_t e = ((tc + r) * H + h) * kD + ch;
-                        vv[j] = __bfloat162float(p.v[e]);
-                        kr[j] = __bfloat162float(p.k[e]);
-                    }
+                    vv[j] = __bfloat162float(ks[8192 + r * kD + ch]);
+                    kr[j] = __bfloat162float(ks[r * kD + ch]);
                 }
                 tmem_wait_ld();
                 float sum[16];
@@ -799,11 +880,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
                 tmem_wait_ld();
-                put8(img(I_Y), img_half(I_Y), 64, ch, 16 * grp, d16);
-                put8(img(I_Y), img_half(I_Y), 64, ch, 16 * grp + 8, d16 + 8);
+                put8(slot_ptr(S, S.sl0 == I_DT ? 0 : 1), img_half(I_Y), 64, ch, 16 * grp, d16);
+                put8(slot_ptr(S, S.sl0 == I_DT ? 0 : 1), img_half(I_Y), 64, ch, 16 * grp + 8, d16 + 8);
             }
-            dirty(S, I_Y);
-            publish();
+            stage_store(S, S.sl0 == I_DT ? 0 : 1, I_Y, 0, 64);
 
             // ---- dA_kk = -strict_tril(T^T Y) (lanes 0-63); dbeta += rowsum(dA_kk kk) ----
             if (!product(S, {I_T, 0, 1}, {I_Y, 0, 1}, tmem + C_TA, 64, 4, false)) break;
@@ -822,21 +902,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     part += d16[j] * s_kk[s * 64 + r];
                 }
                 atomicAdd(&s_dbeta[r], part);
-                put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp, d16);
-                put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp + 8, d16 + 8);
-                put8(img(I_BDKK), img_half(I_BDKK), 64, r, 16 * grp, bd);
-                put8(img(I_BDKK), img_half(I_BDKK), 64, r, 16 * grp + 8, bd + 8);
+                uint8_t *sk = slot_ptr(S, S.sl0 == I_Y ? 0 : 1), *sb = slot_ptr(S, S.sl0 == I_Y ? 1 : 0);
+                put8(sk, img_half(I_DKK), 64, r, 16 * grp, d16);
+                put8(sk, img_half(I_DKK), 64, r, 16 * grp + 8, d16 + 8);
+                put8(sb, img_half(I_BDKK), 64, r, 16 * grp, bd);
+                put8(sb, img_half(I_BDKK), 64, r, 16 * grp + 8, bd + 8);
             }
-            dirty(S, I_DKK);
-            dirty(S, I_BDKK);
-            publish();
+            {
+                const int sk = S.sl0 == I_Y ? 0 : 1;
+                stage_store(S, sk, I_DKK, 0, 64);
+                stage_store(S, 1 - sk, I_BDKK, 0, 64);
+            }
 
             // ---- dKs^T += Kr^T (beta dA_kk) ; (dA_kk Ks)^T into C_R ----
             if (!product(S, {I_QK, 64, 1}, {I_BDKK, 0, 1}, tmem + C_S, 64, 4, true)) break;
             if (!product(S, {I_KS, 0, 1}, {I_DKK, 0, 0}, tmem + C_R, 64, 4, true)) break;
 
             // ---- assembly: dq, dk, dg, dbeta (lane k = ch, rows r = 16 grp + j) ----
+            cp_async_wait_all();  // q staged after the inverse
+            __syncthreads();
             {
+                const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_AT);
+                const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_STG);
                 float dgam[16], khsum = 0.f;
 #pragma unroll
                 for (int j0 = 0; j0 < 16; j0 += 8) {  // eight rows at a time
@@ -848,12 +935,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int r = 16 * grp + j0 + j;
-                        qv[j] = kv[j] = 0.f;
-                        if (r < L) {
-                            const int64_t e = ((tc + r) * H + h) * kD + ch;
-                            qv[j] = __bfloat162float(p.q[e]);
-                            kv[j] = __bfloat162float(p.k[e]);
-                        }
+                        qv[j] = __bfloat162float(qs[r * kD + ch]);
+                        kv[j] = __bfloat162float(ks[r * kD + ch]);
                     }
                     tmem_wait_ld();
 #pragma unroll
@@ -899,7 +982,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 }
                 if (tid < L) p.dbeta[(tc + tid) * H + h] = s_dbeta[tid];
             }
-            publish();
+            // the gradients are not read back: a plain barrier before the next chunk
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
         }
         if (ctrl[2] != 0) break;
 

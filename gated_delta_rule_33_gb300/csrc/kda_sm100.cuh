@@ -104,6 +104,15 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Brings `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+// Brings the line holding `gmem` into L2.
+__device__ __forceinline__ void prefetch_l2(const void *gmem) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem) : "memory");
+}
+
 // Makes this thread's generic-proxy global writes visible to later
 // async-proxy reads (bulk copies) once the CTA has synchronised.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -120,6 +129,13 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
 __device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src, bool valid) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(smem_dst)),
                  "l"(gmem_src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+// 16 bytes, zero-filled when !valid (the source is then not read).
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem_dst)),
+                 "l"(gmem_src), "r"(valid ? 16 : 0)
                  : "memory");
 }
 
