@@ -17,10 +17,11 @@
 // streams, ~12 instructions of arithmetic).  Lane l of a warp owns 8
 // consecutive channels (one 16-byte load or store of bf16), so a warp covers
 // two heads of 128 channels and the per-head norm is a reduction over 16 lanes
-// by shuffles.  A warp walks 32 consecutive tokens, requesting 8 rows at a
-// time (the taps and the three-token halo before the first row are loaded
-// once per 32 tokens; the halo comes from L2, as the neighbouring warp of the
-// same block reads those rows as its last ones).
+// by shuffles.  A warp walks 128 consecutive tokens in segments that stay
+// inside one sequence, requesting 4 rows at a time; the rows two batches
+// ahead are brought into L2 by bulk prefetches, so each load waits on L2
+// rather than HBM (the taps and the three-token halo before the first row are
+// loaded once per segment).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -32,8 +33,8 @@ constexpr int kHeadDim = 128;
 constexpr int kLaneCh = 8;                 // channels per lane
 constexpr int kWarpCh = 32 * kLaneCh;      // 256 channels per warp
 constexpr int kWarps = 8;
-constexpr int kTT = 32;                    // tokens per warp
-constexpr int kBatch = 8;                  // rows requested together
+constexpr int kTT = 128;                   // tokens per warp
+constexpr int kBatch = 4;                  // rows requested together
 constexpr float kNormEps = 1e-6f;
 
 static_assert(kWarpCh == 2 * kHeadDim, "a warp covers two heads; the norm reduces 16 lanes");
@@ -129,7 +130,7 @@ __device__ __forceinline__ int64_t state_index(int64_t s, int z, int r, int C, i
 // Prefill over a packed batch.  grid = (token tiles of kWarps * kTT tokens,
 // channel groups of kWarpCh channels, 3 streams); warp w of a block takes
 // tokens [tile * kWarps * kTT + w * kTT, + kTT) of the group's channels.
-__global__ void __launch_bounds__(kWarps * 32) short_conv_kernel(
+__global__ void __launch_bounds__(kWarps * 32, 2) short_conv_kernel(
     ConvStreams io, const int32_t *__restrict__ cu, int B, int64_t N, int C,
     const __nv_bfloat16 *__restrict__ state_in, __nv_bfloat16 *__restrict__ state_out,
     unsigned int *err) {
@@ -202,45 +203,58 @@ __global__ void __launch_bounds__(kWarps * 32) short_conv_kernel(
             }
         }
     };
-    load_window(t_begin, s);
-    int64_t next = seq_end(s);
+    // The warp's rows of this channel group (512 bytes at most) are brought
+    // into L2 ahead of their loads by bulk prefetches, one row per lane.
+    const int gc0 = blockIdx.y * kWarpCh;
+    const uint32_t row_bytes = static_cast<uint32_t>(min(kWarpCh, C - gc0)) * 2u;
+    auto prefetch_row = [&](int64_t t) {
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(x + t * C + gc0), "r"(row_bytes)
+                     : "memory");
+    };
 
-    // Tokens in batches of kBatch: every row of a batch is requested before the
-    // first is used, so a warp keeps kBatch 16-byte loads in flight.
-    for (int64_t tb = t_begin; tb < t_end; tb += kBatch) {
-        uint4 raw[kBatch];
+    // The warp's tokens in segments that lie inside one sequence: each segment
+    // loads its window once, then runs batches of kBatch rows with every row of
+    // a batch requested before the first is used and no per-row test beyond
+    // the segment bound; rows two batches ahead are prefetched into L2.
+    for (int64_t a = t_begin; a < t_end;) {
+        while (s < B - 1 && seq_end(s) <= a) ++s;
+        const int64_t send = seq_end(s);
+        const int64_t b = min(t_end, send);
+        if (lane < 2 * kBatch && a + lane < b) prefetch_row(a + lane);  // the first two batches
+        load_window(a, s);
+        for (int64_t tb = a; tb < b; tb += kBatch) {
+            if (lane < kBatch && tb + 2 * kBatch + lane < b) prefetch_row(tb + 2 * kBatch + lane);
+            uint4 raw[kBatch];
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j)
-            raw[j] = (active && tb + j < t_end)
-                         ? __ldcs(reinterpret_cast<const uint4 *>(x + (tb + j) * C + c))
-                         : make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < kBatch; ++j)
+                raw[j] = (active && tb + j < b)
+                             ? __ldcs(reinterpret_cast<const uint4 *>(x + (tb + j) * C + c))
+                             : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-            const int64_t t = tb + j;
-            if (t >= t_end) break;
-            if (t >= next) {   // a new sequence starts at t
-                while (s < B - 1 && seq_end(s) <= t) ++s;
-                next = seq_end(s);
-                load_window(t, s);
-            }
-            float xt[kLaneCh], out[kLaneCh];
-            unpack_row(raw[j], xt);
-            conv_row(w, win, xt, norm, out);
-            if (active) store_row(y + t * C + c, out);
+            for (int j = 0; j < kBatch; ++j) {
+                float xt[kLaneCh], out[kLaneCh];
+                unpack_row(raw[j], xt);
+                conv_row(w, win, xt, norm, out);
+                if (active && tb + j < b) store_row(y + (tb + j) * C + c, out);
+                // (rows past the segment only shift the window, which the
+                // next segment reloads)
 #pragma unroll
-            for (int i = 0; i < kLaneCh; ++i) {
-                win[0][i] = win[1][i];
-                win[1][i] = win[2][i];
-                win[2][i] = xt[i];
-            }
-            if (t == next - 1) {   // the last token of sequence s: its carried state
-                if (state_out != nullptr && active) {
-#pragma unroll
-                    for (int r = 0; r < kHalo; ++r) store_row(state_out + state_index(s, z, r, C, c), win[r]);
+                for (int i = 0; i < kLaneCh; ++i) {
+                    win[0][i] = win[1][i];
+                    win[1][i] = win[2][i];
+                    win[2][i] = xt[i];
                 }
-                for (int s2 = s + 1; s2 < B && seq_end(s2) <= next; ++s2) pass_state(s2);
             }
         }
+        if (b == send) {  // the last token of sequence s: its carried state
+            if (state_out != nullptr && active) {
+                load_window(b, s);
+#pragma unroll
+                for (int r = 0; r < kHalo; ++r) store_row(state_out + state_index(s, z, r, C, c), win[r]);
+            }
+            for (int s2 = s + 1; s2 < B && seq_end(s2) <= send; ++s2) pass_state(s2);
+        }
+        a = b;
     }
 }
 
