@@ -133,17 +133,17 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                     "bytes": 4 * 138.59e6,
-                     "sha256": ["82db8085fb27161eb94341ea7f723e8c8c6d58ab3c2ad8a1c241ed51feeca65e",
-                             "436f5e167121af064c97dfe7473056041445553986b0e7372e24e3a8fbdeee1a",
-                             "ea28e7e55139d5d9b5dc2b66fb508aa4d932d6c4a6d5ca684b36b9a896c7ef9e",
+                     "bytes": 4 * 138.88e6,
+                     "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
+                             "2c08ecee71ff165d965818832203d45381f1b8411cd06d8ba06d24bdfa04cb03",
+                             "2e8c65c935ee4d7b3cfc9d2bca83976f27519751adc8c75f5083f6a2180b4b5b",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                   "bytes": 4 * 110.61e6,
-                   "sha256": ["82db8085fb27161eb94341ea7f723e8c8c6d58ab3c2ad8a1c241ed51feeca65e",
-                           "436f5e167121af064c97dfe7473056041445553986b0e7372e24e3a8fbdeee1a",
-                           "ea28e7e55139d5d9b5dc2b66fb508aa4d932d6c4a6d5ca684b36b9a896c7ef9e",
+                   "bytes": 4 * 110.55e6,
+                   "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
+                           "2c08ecee71ff165d965818832203d45381f1b8411cd06d8ba06d24bdfa04cb03",
+                           "2e8c65c935ee4d7b3cfc9d2bca83976f27519751adc8c75f5083f6a2180b4b5b",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
     "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,
@@ -161,9 +161,16 @@ NCU_TRAFFIC = {
                         "3d6b65a9dfcc8c2e0ff562dd93aa28c5dad21e08b1edd9f0bffbe9f00f47dcfd",
                         "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
              "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
-    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 559.92e6,
-                   "sha256": ["af1058f9eb8c8df068075fb627961c0a26e972f1d2d7c6c2cb4b3f7e7208e6cc"],
+    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 552.06e6,
+                   "sha256": ["094b0cd14e6dc076b32a65ea2c43e303f58b69df86299636d303604ef5ecdea3"],
                    "note": "T=4096 capture (profiles/short_conv_T4096_H96.md)"},
+    "backward": {"src": ["kda_backward.cu"], "bytes": 16 * 2.067e9,
+                 "sha256": ["58f242b881fc2d1b1acb1532ced68f7c8a83e5dd92b3b19f71833997525eacc1"],
+                 "note": "T=256 capture x 16 (per-token state scratch; profiles/backward_T256_H96.md)"},
+    "backward_chunked": {"src": ["kda_chunk_bwd.cu"], "bytes": None, "sha256": [],
+                         "note": "T=256 capture (profiles/chunk_backward_T256_H96.md): the per-CTA "
+                                 "scratch stays in L2 at T=4096, so its traffic does not scale "
+                                 "with the tokens"},
 }
 
 
@@ -172,8 +179,10 @@ def measured_traffic(kernel_id):
     source file of the kernel has changed since the capture."""
     import hashlib
     ent = NCU_TRAFFIC.get(kernel_id)
-    if ent is None or ent["bytes"] is None:
+    if ent is None:
         return None, "not captured"
+    if ent["bytes"] is None:
+        return None, ent["note"]
     digests = []
     for name in ent["src"]:
         path = os.path.join(ROOT, "gated_delta_rule_33_gb300", "csrc", name)
