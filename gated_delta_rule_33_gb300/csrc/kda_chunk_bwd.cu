@@ -37,8 +37,10 @@
 // 16-bit mantissa; the raw bf16 inputs are exact and need no low part).
 // Images live in a per-CTA scratch area of the workspace (about 530 KB, L2
 // resident); a product copies its two operand images into two 64 KB shared
-// slots with bulk copies, runs its MMAs into tensor memory, and an epilogue
-// writes the result's image(s).  The chain's state gradient dS stays in
+// slots (16-byte cp.async by every thread) unless a slot already holds them,
+// runs its MMAs into tensor memory, and an epilogue writes the result's
+// image(s), mostly into a slot whose operand is dead, bulk-storing it from
+// there.  The chain's state gradient dS stays in
 // tensor memory in fp32 for the whole sequence.
 //
 // The chunk-start states S come from the forward prefill kernel, which writes
@@ -126,7 +128,7 @@ constexpr uint32_t M_SUF = 4096;          // float[4][128] dGam sums per row gro
 constexpr uint32_t M_P = 6144;            // float[4][256] inverse partial products
 constexpr uint32_t M_T32 = 10240;         // float[16][16]
 constexpr uint32_t M_TDIAG = 11264;       // float[4][16][16]
-constexpr uint32_t M_BAR = 15360;         // 2 mbarriers
+constexpr uint32_t M_BAR = 15360;         // the product mbarrier
 constexpr uint32_t M_CTRL = 15376;        // int[8]: tmem base, chain, abort
 constexpr uint32_t M_KHS = 15424;         // float[128] colsum(dKh . Kh)
 constexpr uint32_t M_GL = 15936;          // float[128] Gam_L (log2 units)
@@ -281,14 +283,14 @@ __device__ __forceinline__ float lanes_sum16(float (&x)[16], int lane) {
 // flight for the drain, and the bulk stores of images staged in a slot.
 struct Sched {
     uint8_t *smem, *scr;
-    uint64_t *bar_load, *bar_mma;
+    uint64_t *bar_mma;
     int *abort_flag;
     unsigned int *err;
     uint32_t polls, sa, sb;
     int tid;
     int sl0, sl1;
-    uint32_t ph_load, ph_mma;
-    bool pend_load, pend_mma;
+    uint32_t ph_mma;
+    bool pend_mma;
     bool st_read;      // a bulk store may still be reading its slot
     uint32_t st_imgs;  // images whose bulk store may still be writing (bit per image)
 };
@@ -342,9 +344,9 @@ __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0
     }
 }
 
-// One product term, D[tmem d] (+)= A B: bulk-copies the operand images that are
-// not already in a slot (a slot keeps its image until it is reused or the image
-// is rewritten), issues the MMAs from thread 0 and waits for them.  Returns
+// One product term, D[tmem d] (+)= A B: copies the operand images that are not
+// already in a slot (a slot keeps its image until it is reused or the image is
+// rewritten), issues the MMAs from thread 0 and waits for them.  Returns
 // false when a wait ran out (the CTA is aborting).
 __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d, uint32_t N,
                                      int ksteps, bool accumulate) {
@@ -365,6 +367,7 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
     // reloaded or rewritten (after this product), and finishes writing before
     // the image is copied back
     const bool reload_stored = (la >= 0 && ((S.st_imgs >> ia) & 1u)) || (lb >= 0 && ((S.st_imgs >> ib) & 1u));
+    const bool waited = reload_stored || S.st_read;
     if (S.tid == 0) {
         if (reload_stored)
             bulk_wait_all();
@@ -374,22 +377,23 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
     if (reload_stored) S.st_imgs = 0;
     S.st_read = false;
     if (la >= 0 || lb >= 0) {
-        if (S.tid == 0) {
-            const uint32_t bytes = (la >= 0 ? img_bytes(ia) : 0u) + (lb >= 0 ? img_bytes(ib) : 0u);
-            mbar_arrive_expect_tx(S.bar_load, bytes);
-            if (la >= 0)
-                bulk_load(S.smem + (la ? SLOT_B : SLOT_A), S.scr + img_off(ia), img_bytes(ia), S.bar_load);
-            if (lb >= 0)
-                bulk_load(S.smem + (lb ? SLOT_B : SLOT_A), S.scr + img_off(ib), img_bytes(ib), S.bar_load);
-        }
+        // every thread copies 16-byte pieces of the images with cp.async
+        if (waited) __syncthreads();  // after thread 0's wait on the bulk stores
+        auto copy = [&](int sl, int i) {
+            uint8_t *dst = S.smem + (sl ? SLOT_B : SLOT_A);
+            const uint8_t *src = S.scr + img_off(i);
+            for (uint32_t u = S.tid; u < img_bytes(i) / 16; u += kThreads)
+                cp_async_16(dst + u * 16, src + u * 16, true);
+        };
+        if (la >= 0) copy(la, ia);
+        if (lb >= 0) copy(lb, ib);
+        cp_async_wait_all();
+        fence_proxy_async_smem();  // read by the tensor core
+        __syncthreads();
         if (la == 0) S.sl0 = ia;
         if (la == 1) S.sl1 = ia;
         if (lb == 0) S.sl0 = ib;
         if (lb == 1) S.sl1 = ib;
-        S.pend_load = true;
-        if (!cta_wait(S.bar_load, S.ph_load & 1, S.abort_flag, S.err, S.tid, S.polls)) return false;
-        S.ph_load++;
-        S.pend_load = false;
     }
     if (S.tid == 0) {
         issue(d, opd(pa ? S.sb : S.sa, ia, A.row0, A.mn != 0), opd(pb ? S.sb : S.sa, ib, B.row0, B.mn != 0),
@@ -417,8 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     float *s_gl = reinterpret_cast<float *>(misc + M_GL);
     float *s_kk = reinterpret_cast<float *>(smem + OFF_KK);
     float *s_at = reinterpret_cast<float *>(smem + OFF_AT);
-    uint64_t *bar_load = reinterpret_cast<uint64_t *>(misc + M_BAR);
-    uint64_t *bar_mma = bar_load + 1;
+    uint64_t *bar_mma = reinterpret_cast<uint64_t *>(misc + M_BAR);
     int *ctrl = reinterpret_cast<int *>(misc + M_CTRL);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -431,7 +434,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 
     if (warp == 0) tmem_alloc(reinterpret_cast<uint32_t *>(&ctrl[0]), 512);
     if (tid == 0) {
-        mbar_init(bar_load, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         ctrl[2] = 0;
@@ -450,7 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     Sched S;
     S.smem = smem;
     S.scr = scr;
-    S.bar_load = bar_load;
     S.bar_mma = bar_mma;
     S.abort_flag = &ctrl[2];
     S.err = p.err;
@@ -459,8 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.sb = sb;
     S.tid = tid;
     S.sl0 = S.sl1 = -1;
-    S.ph_load = S.ph_mma = 0;
-    S.pend_load = S.pend_mma = false;
+    S.ph_mma = 0;
+    S.pend_mma = false;
     S.st_read = false;
     S.st_imgs = 0;
     const float kLog2e = 1.4426950408889634f;
@@ -1016,7 +1017,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     // Drain: wait for a copy or product still in flight (full bound) before the
     // tensor memory is released and the CTA exits.
     if (tid == 0) {
-        if (S.pend_load) mbar_wait_bounded(bar_load, S.ph_load & 1, kMaxPolls);
         if (S.pend_mma) mbar_wait_bounded(bar_mma, S.ph_mma & 1, kMaxPolls);
         bulk_wait_all();
     }
