@@ -291,8 +291,6 @@ struct Sched {
     int sl0, sl1;
     uint32_t ph_mma;
     bool pend_mma;
-    bool st_read;      // a bulk store may still be reading its slot
-    uint32_t st_imgs;  // images whose bulk store may still be writing (bit per image)
 };
 
 // An operand: image, first row used, MN-major.
@@ -311,8 +309,9 @@ __device__ __forceinline__ uint8_t *slot_ptr(const Sched &S, int sl) {
 
 // After an epilogue wrote image `i` (or the row range [r0, r1) of it) into slot
 // `sl` in the image's own byte layout: makes the writes visible to the async
-// proxy, and thread 0 bulk-stores the written bytes to the image in the
-// scratch.  A whole image stays in the slot for the next products.
+// proxy (the tensor core reads the slot), and the CTA copies the written bytes
+// to the image in the scratch.  A whole image stays in the slot for the next
+// products.
 __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0, uint32_t r1) {
     fence_proxy_async_smem();
     tc_fence_before();
@@ -320,22 +319,22 @@ __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0
     tc_fence_after();
     const uint32_t rows = img_rows(i), nblk = img_cols(i) / 64;
     const bool whole = r0 == 0 && r1 == rows;
-    if (S.tid == 0) {
-        uint8_t *src = slot_ptr(S, sl), *dst = S.scr + img_off(i);
-        if (whole) {
-            bulk_store(dst, src, img_bytes(i));
-        } else {
-            // rows [r0, r1) of each 64-column block of the hi (and lo) tile
-            const uint32_t tiles = img_exact(i) ? 1u : 2u;
-            for (uint32_t t = 0; t < tiles; ++t)
-                for (uint32_t b = 0; b < nblk; ++b) {
-                    const uint32_t o = t * img_half(i) + b * rows * 128 + r0 * 128;
-                    bulk_store(dst + o, src + o, (r1 - r0) * 128);
-                }
+    // every thread copies 16-byte pieces: the whole image, or rows [r0, r1)
+    // of each 64-column block of the hi (and lo) tile
+    const uint8_t *src = slot_ptr(S, sl);
+    uint8_t *dst = S.scr + img_off(i);
+    if (whole) {
+        for (uint32_t u = S.tid; u < img_bytes(i) / 16; u += kThreads)
+            *reinterpret_cast<uint4 *>(dst + u * 16) = *reinterpret_cast<const uint4 *>(src + u * 16);
+    } else {
+        const uint32_t per = (r1 - r0) * 8;  // pieces per (tile, block) range
+        const uint32_t n = (img_exact(i) ? 1u : 2u) * nblk * per;
+        for (uint32_t u = S.tid; u < n; u += kThreads) {
+            const uint32_t q = u / per, w = u - q * per;  // q = tile * nblk + block
+            const uint32_t o = (q / nblk) * img_half(i) + (q % nblk) * rows * 128 + r0 * 128 + w * 16;
+            *reinterpret_cast<uint4 *>(dst + o) = *reinterpret_cast<const uint4 *>(src + o);
         }
     }
-    S.st_read = true;
-    S.st_imgs |= 1u << i;
     if (sl) S.sl1 = whole ? i : (S.sl1 == i ? i : -1); else S.sl0 = whole ? i : (S.sl0 == i ? i : -1);
     // any other copy of a partly rewritten image is stale
     if (!whole) {
@@ -363,22 +362,9 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         pb = (pa == 0) ? 1 : 0;
         lb = pb;
     }
-    // a staged image's store finishes reading its slot before the slot is
-    // reloaded or rewritten (after this product), and finishes writing before
-    // the image is copied back
-    const bool reload_stored = (la >= 0 && ((S.st_imgs >> ia) & 1u)) || (lb >= 0 && ((S.st_imgs >> ib) & 1u));
-    const bool waited = reload_stored || S.st_read;
-    if (S.tid == 0) {
-        if (reload_stored)
-            bulk_wait_all();
-        else if (S.st_read)
-            bulk_wait_read();
-    }
-    if (reload_stored) S.st_imgs = 0;
-    S.st_read = false;
     if (la >= 0 || lb >= 0) {
         // every thread copies 16-byte pieces of the images with cp.async
-        if (waited) __syncthreads();  // after thread 0's wait on the bulk stores
+        // (the images were written by this CTA's threads before a barrier)
         auto copy = [&](int sl, int i) {
             uint8_t *dst = S.smem + (sl ? SLOT_B : SLOT_A);
             const uint8_t *src = S.scr + img_off(i);
@@ -462,15 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.sl0 = S.sl1 = -1;
     S.ph_mma = 0;
     S.pend_mma = false;
-    S.st_read = false;
-    S.st_imgs = 0;
     const float kLog2e = 1.4426950408889634f;
     const float kMaxChunkLog2 = kMaxChunkDecay * kLog2e;
 
     // Makes every thread's image and tensor-memory writes visible to the next
-    // bulk copy / product.
+    // copy / product (the images are read back by the same CTA's cp.async, in
+    // the generic proxy, so a CTA barrier orders them).
     auto publish = [&]() {
-        fence_proxy_async_global();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -627,7 +611,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(img(I_V), 0, 64, r, c0, vv);
                 put8(img(I_DU2), img_half(I_DU2), 128, 64 + r, c0, dov);
             }
-            fence_proxy_async_global();
             stage_store(S, 1, I_QK, 0, 128);
 
             // ---- D_A = [Qt; Kr] Ks^T ----
@@ -720,12 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 for (int j = 0; j < 8; ++j) tb8[j] = t8[j] * s_beta[c0 + j];
                 put8(smem + SLOT_B, img_half(I_TB), 64, r, c0, tb8);
                 put8(smem + SLOT_B + img_bytes(I_TB), img_half(I_T), 64, r, c0, t8);
+                put8(img(I_T), img_half(I_T), 64, r, c0, t8);
             }
             fence_proxy_async_smem();
             publish();
-            if (tid == 0) bulk_store(img(I_T), smem + SLOT_B + img_bytes(I_TB), img_bytes(I_T));
-            S.st_read = true;
-            S.st_imgs |= 1u << I_T;
             S.sl1 = I_TB;
 
             // Epilogues below write their image into a slot whose operand is
@@ -1014,12 +995,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
         tc_fence_after();
     }
 
-    // Drain: wait for a copy or product still in flight (full bound) before the
-    // tensor memory is released and the CTA exits.
-    if (tid == 0) {
-        if (S.pend_mma) mbar_wait_bounded(bar_mma, S.ph_mma & 1, kMaxPolls);
-        bulk_wait_all();
-    }
+    // Drain: wait for a product still in flight (full bound) and this thread's
+    // copies before the tensor memory is released and the CTA exits.
+    cp_async_wait_all();
+    if (tid == 0 && S.pend_mma) mbar_wait_bounded(bar_mma, S.ph_mma & 1, kMaxPolls);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
