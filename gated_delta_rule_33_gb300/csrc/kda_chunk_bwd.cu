@@ -289,6 +289,7 @@ struct Sched {
     uint32_t polls, sa, sb;
     int tid;
     int sl0, sl1;
+    int lo0, hi0, lo1, hi1;  // the rows of its image each slot holds
     uint32_t ph_mma;
     bool pend_mma;
 };
@@ -307,6 +308,48 @@ __device__ __forceinline__ uint8_t *slot_ptr(const Sched &S, int sl) {
     return S.smem + (sl ? SLOT_B : SLOT_A);
 }
 
+// Slot `sl` holds rows [lo, hi) of image i.
+__device__ __forceinline__ void set_slot(Sched &S, int sl, int i, int lo, int hi) {
+    if (sl) {
+        S.sl1 = i; S.lo1 = lo; S.hi1 = hi;
+    } else {
+        S.sl0 = i; S.lo0 = lo; S.hi0 = hi;
+    }
+}
+__device__ __forceinline__ bool slot_has(const Sched &S, int sl, int i, int lo, int hi) {
+    return sl ? (S.sl1 == i && S.lo1 <= lo && hi <= S.hi1) : (S.sl0 == i && S.lo0 <= lo && hi <= S.hi0);
+}
+
+// Every thread copies 16-byte pieces between a slot and the image in the
+// scratch: rows [r0, r1) of each 64-column block of the hi (and lo) tile, in
+// the image's byte layout; cp.async into the slot (load) or plain 16-byte
+// stores to the scratch (store).
+template <bool kLoad>
+__device__ __forceinline__ void copy_rows(const Sched &S, int sl, int i, uint32_t r0, uint32_t r1) {
+    uint8_t *slot = slot_ptr(S, sl);
+    uint8_t *glob = S.scr + img_off(i);
+    const uint32_t rows = img_rows(i);
+    if (r0 == 0 && r1 == rows) {
+        for (uint32_t u = S.tid; u < img_bytes(i) / 16; u += kThreads) {
+            if (kLoad)
+                cp_async_16(slot + u * 16, glob + u * 16, true);
+            else
+                *reinterpret_cast<uint4 *>(glob + u * 16) = *reinterpret_cast<const uint4 *>(slot + u * 16);
+        }
+        return;
+    }
+    const uint32_t nblk = img_cols(i) / 64, per = (r1 - r0) * 8;  // pieces per (tile, block) range
+    const uint32_t n = (img_exact(i) ? 1u : 2u) * nblk * per;
+    for (uint32_t u = S.tid; u < n; u += kThreads) {
+        const uint32_t q = u / per, w = u - q * per;  // q = tile * nblk + block
+        const uint32_t o = (q / nblk) * img_half(i) + (q % nblk) * rows * 128 + r0 * 128 + w * 16;
+        if (kLoad)
+            cp_async_16(slot + o, glob + o, true);
+        else
+            *reinterpret_cast<uint4 *>(glob + o) = *reinterpret_cast<const uint4 *>(slot + o);
+    }
+}
+
 // After an epilogue wrote image `i` (or the row range [r0, r1) of it) into slot
 // `sl` in the image's own byte layout: makes the writes visible to the async
 // proxy (the tensor core reads the slot), and the CTA copies the written bytes
@@ -317,27 +360,19 @@ __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t rows = img_rows(i), nblk = img_cols(i) / 64;
-    const bool whole = r0 == 0 && r1 == rows;
-    // every thread copies 16-byte pieces: the whole image, or rows [r0, r1)
-    // of each 64-column block of the hi (and lo) tile
-    const uint8_t *src = slot_ptr(S, sl);
-    uint8_t *dst = S.scr + img_off(i);
-    if (whole) {
-        for (uint32_t u = S.tid; u < img_bytes(i) / 16; u += kThreads)
-            *reinterpret_cast<uint4 *>(dst + u * 16) = *reinterpret_cast<const uint4 *>(src + u * 16);
-    } else {
-        const uint32_t per = (r1 - r0) * 8;  // pieces per (tile, block) range
-        const uint32_t n = (img_exact(i) ? 1u : 2u) * nblk * per;
-        for (uint32_t u = S.tid; u < n; u += kThreads) {
-            const uint32_t q = u / per, w = u - q * per;  // q = tile * nblk + block
-            const uint32_t o = (q / nblk) * img_half(i) + (q % nblk) * rows * 128 + r0 * 128 + w * 16;
-            *reinterpret_cast<uint4 *>(dst + o) = *reinterpret_cast<const uint4 *>(src + o);
-        }
+    const int rows = static_cast<int>(img_rows(i));
+    copy_rows<false>(S, sl, i, r0, r1);
+    // the slot's rows of image i: the written ones, with those it held if the
+    // two ranges touch; any other slot's copy of the image is stale
+    int lo = static_cast<int>(r0), hi = static_cast<int>(r1);
+    const bool had = sl ? S.sl1 == i : S.sl0 == i;
+    const int plo = sl ? S.lo1 : S.lo0, phi = sl ? S.hi1 : S.hi0;
+    if (had && plo <= hi && lo <= phi) {
+        lo = min(lo, plo);
+        hi = max(hi, phi);
     }
-    if (sl) S.sl1 = whole ? i : (S.sl1 == i ? i : -1); else S.sl0 = whole ? i : (S.sl0 == i ? i : -1);
-    // any other copy of a partly rewritten image is stale
-    if (!whole) {
+    set_slot(S, sl, i, lo, hi);
+    if (!(r0 == 0 && static_cast<int>(r1) == rows)) {
         if (sl && S.sl0 == i) S.sl0 = -1;
         if (!sl && S.sl1 == i) S.sl1 = -1;
     }
@@ -348,10 +383,20 @@ __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0
 // rewritten), issues the MMAs from thread 0 and waits for them.  Returns
 // false when a wait ran out (the CTA is aborting).
 __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d, uint32_t N,
-                                     int ksteps, bool accumulate) {
+                                     int ksteps, bool accumulate, int a_lo = 0, int a_hi = 128) {
     const int ia = A.img, ib = B.img;
-    int pa = (S.sl0 == ia) ? 0 : (S.sl1 == ia) ? 1 : -1;
-    int pb = (S.sl0 == ib) ? 0 : (S.sl1 == ib) ? 1 : -1;
+    // the rows each operand reads: K rows for an MN-major operand, the M rows
+    // whose results are used (a_lo .. a_hi) for A, N rows for B
+    int alo = A.mn ? A.row0 : A.row0 + a_lo, ahi = A.mn ? A.row0 + 16 * ksteps : A.row0 + a_hi;
+    int blo = B.row0, bhi = B.row0 + (B.mn ? 16 * ksteps : static_cast<int>(N));
+    ahi = min(ahi, static_cast<int>(img_rows(ia)));
+    bhi = min(bhi, static_cast<int>(img_rows(ib)));
+    if (ia == ib) {
+        alo = blo = min(alo, blo);
+        ahi = bhi = max(ahi, bhi);
+    }
+    int pa = slot_has(S, 0, ia, alo, ahi) ? 0 : slot_has(S, 1, ia, alo, ahi) ? 1 : -1;
+    int pb = slot_has(S, 0, ib, blo, bhi) ? 0 : slot_has(S, 1, ib, blo, bhi) ? 1 : -1;
     int la = -1, lb = -1;
     if (pa < 0) {
         pa = (pb == 0) ? 1 : 0;
@@ -363,23 +408,15 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         lb = pb;
     }
     if (la >= 0 || lb >= 0) {
-        // every thread copies 16-byte pieces of the images with cp.async
-        // (the images were written by this CTA's threads before a barrier)
-        auto copy = [&](int sl, int i) {
-            uint8_t *dst = S.smem + (sl ? SLOT_B : SLOT_A);
-            const uint8_t *src = S.scr + img_off(i);
-            for (uint32_t u = S.tid; u < img_bytes(i) / 16; u += kThreads)
-                cp_async_16(dst + u * 16, src + u * 16, true);
-        };
-        if (la >= 0) copy(la, ia);
-        if (lb >= 0) copy(lb, ib);
+        // the rows it reads of each image not in a slot, by cp.async (the
+        // images were written by this CTA's threads before a barrier)
+        if (la >= 0) copy_rows<true>(S, la, ia, alo, ahi);
+        if (lb >= 0) copy_rows<true>(S, lb, ib, blo, bhi);
         cp_async_wait_all();
         fence_proxy_async_smem();  // read by the tensor core
         __syncthreads();
-        if (la == 0) S.sl0 = ia;
-        if (la == 1) S.sl1 = ia;
-        if (lb == 0) S.sl0 = ib;
-        if (lb == 1) S.sl1 = ib;
+        if (la >= 0) set_slot(S, la, ia, alo, ahi);
+        if (lb >= 0) set_slot(S, lb, ib, blo, bhi);
     }
     if (S.tid == 0) {
         issue(d, opd(pa ? S.sb : S.sa, ia, A.row0, A.mn != 0), opd(pb ? S.sb : S.sa, ib, B.row0, B.mn != 0),
@@ -446,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.sb = sb;
     S.tid = tid;
     S.sl0 = S.sl1 = -1;
+    S.lo0 = S.hi0 = S.lo1 = S.hi1 = 0;
     S.ph_mma = 0;
     S.pend_mma = false;
     const float kLog2e = 1.4426950408889634f;
@@ -707,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             }
             fence_proxy_async_smem();
             publish();
-            S.sl1 = I_TB;
+            set_slot(S, 1, I_TB, 0, 64);
 
             // Epilogues below write their image into a slot whose operand is
             // dead (the image's own byte layout) and bulk-store it from there;
@@ -777,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             tc_fence_after();
 
             // ---- dA_qk = tril(dO U^T) (lanes 64-127 of [dU; dO] U^T) ----
-            if (!product(S, {I_DU2, 0, 0}, {I_UT, 0, 1}, tmem + C_TA, 64, 8, false)) break;
+            if (!product(S, {I_DU2, 0, 0}, {I_UT, 0, 1}, tmem + C_TA, 64, 8, false, 64, 128)) break;  // lanes 64-127
             {
                 const int sl = (S.sl0 == I_UT) ? 0 : 1;
                 if (quarter >= 2) {
@@ -815,8 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             if (!product(S, {I_DS, 0, 1}, {I_UT, 0, 1}, tmem + C_H, 64, 8, false)) break;
 
             // ---- dT = (dW' Kr^T + dU V^T) diag(beta) (lanes 0-63) ----
-            if (!product(S, {I_QK, 0, 0}, {I_QK, 64, 0}, tmem + C_TA, 64, 8, false)) break;
-            if (!product(S, {I_DU2, 0, 0}, {I_V, 0, 0}, tmem + C_TA, 64, 8, true)) break;
+            if (!product(S, {I_QK, 0, 0}, {I_QK, 64, 0}, tmem + C_TA, 64, 8, false, 0, 64)) break;  // lanes 0-63
+            if (!product(S, {I_DU2, 0, 0}, {I_V, 0, 0}, tmem + C_TA, 64, 8, true, 0, 64)) break;  // lanes 0-63
             if (quarter < 2) {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
