@@ -680,16 +680,30 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // ---- T = (I + A_kk)^{-1} on warps 0-3 (fp32, row-major); meanwhile
             // warps 4-15 (B2) form the S_op^T and dS'^T images (row v = the
             // lane) and sum_v dS' S from the chunk-start state S, brought into
-            // slot B (free since D_A).  Then T diag(beta) and T as split images
-            // staged in slot B by every thread (row tid / 8, columns 8 (tid % 8)
-            // .. + 7), T stored to its image ----
+            // slot A.  Then T diag(beta) and T as split images staged in slot B
+            // by every thread (row tid / 8, columns 8 (tid % 8) .. + 7), T
+            // also stored to its image ----
             {
                 float *T = reinterpret_cast<float *>(smem + OFF_TT);
                 if (warp >= 4) {
-                    for (int u = tid - 128; u < 4096; u += kThreads - 128)
-                        cp_async_16(smem + SLOT_B + u * 16, Sc + u * 4, true);
+                    // the checkpoint S into slot A (its Ks is dead since D_A);
+                    // each image is staged in slot B (QK's copy there is given
+                    // up: the W' product copies its rows back) and then copied
+                    // to the scratch with coalesced stores
+                    const int bt = tid - 128;  // 0 .. 383
+                    for (int u = bt; u < 4096; u += kThreads - 128)
+                        cp_async_16(smem + SLOT_A + u * 16, Sc + u * 4, true);
                     cp_async_wait_all();
                     named_sync(2, kThreads - 128);
+                    const float *Ss = reinterpret_cast<const float *>(smem + SLOT_A);
+                    uint8_t *stage = smem + SLOT_B;
+                    auto copy_out = [&](int i) {
+                        named_sync(2, kThreads - 128);
+                        for (uint32_t u = bt; u < img_bytes(i) / 16; u += kThreads - 128)
+                            *reinterpret_cast<uint4 *>(img(i) + u * 16) =
+                                *reinterpret_cast<const uint4 *>(stage + u * 16);
+                        named_sync(2, kThreads - 128);
+                    };
                     // 16-column units of k: warps 4-7 take units 0, 3, 6, warps
                     // 8-11 units 1, 4, 7 and warps 12-15 units 2, 5
 #pragma unroll 1
@@ -698,20 +712,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                         float ds[16], sv[16], so[16];
                         tmem_ld16(tl + C_DS + k0, ds);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            sv[j] = reinterpret_cast<const float *>(smem + SLOT_B)[(k0 + j) * kD + ch];
+                        for (int j = 0; j < 16; ++j) sv[j] = Ss[(k0 + j) * kD + ch];
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) so[j] = s_em[k0 + j] * sv[j];
-                        put8(img(I_SO), img_half(I_SO), 128, ch, k0, so);
-                        put8(img(I_SO), img_half(I_SO), 128, ch, k0 + 8, so + 8);
-                        put8(img(I_DS), img_half(I_DS), 128, ch, k0, ds);
-                        put8(img(I_DS), img_half(I_DS), 128, ch, k0 + 8, ds + 8);
+                        put8(stage, img_half(I_SO), 128, ch, k0, so);
+                        put8(stage, img_half(I_SO), 128, ch, k0 + 8, so + 8);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) so[j] = ds[j] * sv[j];
                         const float t = lanes_sum16(so, lane);
                         if ((lane & 1) == 0) atomicAdd(&s_dgl[k0 + (lane >> 1)], t);
                     }
+                    copy_out(I_SO);
+#pragma unroll 1
+                    for (int u = grp - 1; u < 8; u += 3) {
+                        const int k0 = 16 * u;
+                        float ds[16];
+                        tmem_ld16(tl + C_DS + k0, ds);
+                        tmem_wait_ld();
+                        put8(stage, img_half(I_DS), 128, ch, k0, ds);
+                        put8(stage, img_half(I_DS), 128, ch, k0 + 8, ds + 8);
+                    }
+                    copy_out(I_DS);
                 } else {
                     float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
                     float *T32c = reinterpret_cast<float *>(misc + M_T32);
@@ -745,6 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             }
             fence_proxy_async_smem();
             publish();
+            S.sl0 = -1;  // slot A holds the checkpoint
             set_slot(S, 1, I_TB, 0, 64);
 
             // Epilogues below write their image into a slot whose operand is
