@@ -246,6 +246,9 @@ __device__ __forceinline__ void issue(uint32_t d, const Opd &A, const Opd &B, ui
     const uint64_t ah0 = desc0(A, A.hi), bh0 = desc0(B, B.hi);
     const uint64_t al0 = A.lo ? desc0(A, A.lo) : 0, bl0 = B.lo ? desc0(B, B.lo) : 0;
     uint32_t acc = accumulate ? 1u : 0u;
+    // (kept rolled: the kernel's code size, not the issuing loop, is what
+    // costs; every copy of it fills the instruction cache)
+#pragma unroll 1
     for (int kk = 0; kk < ksteps; ++kk) {
         const uint64_t ah = kstep(A, ah0, kk), bh = kstep(B, bh0, kk);
         mma_f16_ss(d, ah, bh, id, acc);
