@@ -745,10 +745,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     if (tid < 64) {
                         ut_diag_solve(s_at, T, Tdiag, out, tid);
                         __syncwarp();
-                        ut_level1(s_at, T, Tdiag, P, T, T32c, out, tid);
+                        ut_level1<TRowMajor, 4>(s_at, T, Tdiag, P, T, T32c, out, tid);
                     }
                     inverse_sync();
-                    ut_level2(s_at, T, Tdiag, T32c, P, out, tid);
+                    ut_level2<TRowMajor, 4>(s_at, T, Tdiag, T32c, P, out, tid);
                 }
                 __syncthreads();
                 // A_kk is consumed: q again into its area for the assembly

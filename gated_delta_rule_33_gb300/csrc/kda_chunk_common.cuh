@@ -201,10 +201,11 @@ struct Acc2x4 {
     }
 };
 
-template <int kN>
+// kU: unroll factor (a kernel short of instruction cache unrolls less)
+template <int kN, int kU = kN>
 __device__ __forceinline__ void gemm_2x4(Acc2x4 &acc, const float *Ac, int ac_stride,
                                          const float *B, int b_stride) {
-#pragma unroll
+#pragma unroll kU
     for (int s = 0; s < kN; ++s)
         acc.step(*reinterpret_cast<const float2 *>(Ac + s * ac_stride),
                  *reinterpret_cast<const float4 *>(B + s * b_stride));
@@ -274,7 +275,7 @@ __device__ __forceinline__ void ut_diag_solve(const float *At, float *T, float *
 // T_{t+1,t+1} itself): T_{t+1,t} = -T_{t+1,t+1} (A_{t+1,t} T_tt).  Lane l owns
 // rows r0 = 2 (l / 4), r0 + 1 and columns c0 = 4 (l % 4) .. + 3 of the block.
 // T_10 goes to T (row-major, part of T_top in level 2), T_32 to T32c.
-template <class Out>
+template <class Out, int kU = 32>
 __device__ __forceinline__ void ut_level1(const float *At, const float *T, const float *Tdiag,
                                           float *P, float *Tw, float *T32c, const Out &out,
                                           int tid) {
@@ -282,12 +283,12 @@ __device__ __forceinline__ void ut_level1(const float *At, const float *T, const
     float *Pt = P + (t >> 1) * 256;
     Acc2x4 a;
     // P_t = A_{t+1,t} T_tt (T_tt is zero above its diagonal)
-    gemm_2x4<16>(a, At + (16 * t) * 64 + 16 * (t + 1) + r0, 64, T + (16 * t) * 64 + 16 * t + c0, 64);
+    gemm_2x4<16, kU>(a, At + (16 * t) * 64 + 16 * (t + 1) + r0, 64, T + (16 * t) * 64 + 16 * t + c0, 64);
     *reinterpret_cast<float4 *>(Pt + r0 * 16 + c0) = a.row(0);
     *reinterpret_cast<float4 *>(Pt + (r0 + 1) * 16 + c0) = a.row(1);
     __syncwarp();
     Acc2x4 b;
-    gemm_2x4<16>(b, Tdiag + (t + 1) * 256 + r0, 16, Pt + c0, 16);
+    gemm_2x4<16, kU>(b, Tdiag + (t + 1) * 256 + r0, 16, Pt + c0, 16);
     const float4 x0 = b.neg_row(0), x1 = b.neg_row(1);
     if (t == 0) {
         *reinterpret_cast<float4 *>(Tw + (16 + r0) * 64 + c0) = x0;
@@ -308,7 +309,7 @@ __device__ __forceinline__ void ut_level1(const float *At, const float *T, const
 // owns rows 16 (w % 2) .. + 15 and columns 16 (w / 2) .. + 15 of Y and X, so
 // every triangular bound is warp-uniform; lane l owns rows r0 = 16 (w % 2) +
 // 2 (l / 4), r0 + 1 and columns c0 = 16 (w / 2) + 4 (l % 4) .. + 3.
-template <class Out>
+template <class Out, int kU = 32>
 __device__ __forceinline__ void ut_level2(const float *At, const float *T, const float *Tdiag,
                                           const float *T32c, float *Y, const Out &out, int tid) {
     const int w = tid >> 5, l = tid & 31, rh = w & 1, cb = w >> 1;
@@ -316,21 +317,21 @@ __device__ __forceinline__ void ut_level2(const float *At, const float *T, const
     Acc2x4 a;
     // Y = A_bl T_top: T_top[s][c] is zero for s < 16 * block(c)
     if (cb == 0)
-        gemm_2x4<32>(a, At + 32 + r0, 64, T + c0, 64);
+        gemm_2x4<32, kU>(a, At + 32 + r0, 64, T + c0, 64);
     else
-        gemm_2x4<16>(a, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
+        gemm_2x4<16, kU>(a, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
     *reinterpret_cast<float4 *>(Y + y_idx(r0, c0)) = a.row(0);
     *reinterpret_cast<float4 *>(Y + y_idx(r0 + 1, c0)) = a.row(1);
     inverse_sync();
     // X = -T_bot Y: T_bot[r][s] is zero for s >= 16 * (block(r) + 1)
     Acc2x4 b;
-#pragma unroll
+#pragma unroll kU
     for (int s = 0; s < 16; ++s)
         b.step(rh == 0 ? *reinterpret_cast<const float2 *>(Tdiag + 2 * 256 + s * 16 + r0)
                        : *reinterpret_cast<const float2 *>(T32c + s * 16 + r0 - 16),
                *reinterpret_cast<const float4 *>(Y + y_idx(s, c0)));
     if (rh == 1) {
-#pragma unroll
+#pragma unroll kU
         for (int s = 16; s < 32; ++s)
             b.step(*reinterpret_cast<const float2 *>(Tdiag + 3 * 256 + (s - 16) * 16 + r0 - 16),
                    *reinterpret_cast<const float4 *>(Y + y_idx(s, c0)));
