@@ -133,16 +133,16 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                     "bytes": 4 * 138.88e6,
+                     "bytes": 4 * 138.82e6,
                      "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
-                             "2c08ecee71ff165d965818832203d45381f1b8411cd06d8ba06d24bdfa04cb03",
+                             "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
                              "2e8c65c935ee4d7b3cfc9d2bca83976f27519751adc8c75f5083f6a2180b4b5b",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                   "bytes": 4 * 110.55e6,
+                   "bytes": 4 * 111.03e6,
                    "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
-                           "2c08ecee71ff165d965818832203d45381f1b8411cd06d8ba06d24bdfa04cb03",
+                           "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
                            "2e8c65c935ee4d7b3cfc9d2bca83976f27519751adc8c75f5083f6a2180b4b5b",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
