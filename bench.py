@@ -136,14 +136,14 @@ NCU_TRAFFIC = {
                      "bytes": 4 * 138.82e6,
                      "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
                              "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
-                             "2e8c65c935ee4d7b3cfc9d2bca83976f27519751adc8c75f5083f6a2180b4b5b",
+                             "aca04576a3e893bf9325136479cc45787af796290f2b3a34973bf1a4817b1fc9",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
                    "bytes": 4 * 111.03e6,
                    "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
                            "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
-                           "2e8c65c935ee4d7b3cfc9d2bca83976f27519751adc8c75f5083f6a2180b4b5b",
+                           "aca04576a3e893bf9325136479cc45787af796290f2b3a34973bf1a4817b1fc9",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
     "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,

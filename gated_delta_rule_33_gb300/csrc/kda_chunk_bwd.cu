@@ -36,11 +36,11 @@
 // every product is three kind::f16 MMAs per k-step (hi.hi + hi.lo + lo.hi, a
 // 16-bit mantissa; the raw bf16 inputs are exact and need no low part).
 // Images live in a per-CTA scratch area of the workspace (about 530 KB, L2
-// resident); a product copies its two operand images into two 64 KB shared
-// slots (16-byte cp.async by every thread) unless a slot already holds them,
-// runs its MMAs into tensor memory, and an epilogue writes the result's
-// image(s), mostly into a slot whose operand is dead, bulk-storing it from
-// there.  The chain's state gradient dS stays in
+// resident); a product copies the rows it reads of its two operand images into
+// two 64 KB shared slots (16-byte cp.async by every thread) unless a slot
+// already holds them, runs its MMAs into tensor memory, and an epilogue writes
+// the result's image(s), mostly into a slot whose operand is dead, and copies
+// it to the scratch from there.  The chain's state gradient dS stays in
 // tensor memory in fp32 for the whole sequence.
 //
 // The chunk-start states S come from the forward prefill kernel, which writes
@@ -282,8 +282,8 @@ __device__ __forceinline__ float lanes_sum16(float (&x)[16], int lane) {
 }
 
 // The product engine's state (identical in every thread): the image each of
-// the two operand slots holds (-1: none), the barrier phases, what is in
-// flight for the drain, and the bulk stores of images staged in a slot.
+// the two operand slots holds (-1: none) and which of its rows, the product
+// barrier's phase, and whether a product is in flight (for the drain).
 struct Sched {
     uint8_t *smem, *scr;
     uint64_t *bar_mma;
@@ -774,8 +774,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             set_slot(S, 1, I_TB, 0, 64);
 
             // Epilogues below write their image into a slot whose operand is
-            // dead (the image's own byte layout) and bulk-store it from there;
-            // a whole image stays in the slot for the products that follow.
+            // dead (the image's own byte layout) and copy it to the scratch from
+            // there; a whole image stays in the slot for the products that
+            // follow.
 
             // ---- W'^T = Kr^T (T beta)^T and Ut^T = V^T (T beta)^T; -W'^T image
             // in V's slot ----

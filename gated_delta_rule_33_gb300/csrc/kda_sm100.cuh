@@ -76,49 +76,6 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
-// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
-// aligned) from global to shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(smem_dst)),
-        "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// Untiled bulk copy of `bytes` from shared to global memory (bulk-group
-// completion); both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
-                 "r"(smem_addr(smem_src)), "r"(bytes)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until the committed bulk stores have read their shared-memory source.
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Waits until the committed bulk stores are complete.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Brings `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
-}
-// Brings the line holding `gmem` into L2.
-__device__ __forceinline__ void prefetch_l2(const void *gmem) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem) : "memory");
-}
-
-// Makes this thread's generic-proxy global writes visible to later
-// async-proxy reads (bulk copies) once the CTA has synchronised.
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
