@@ -143,3 +143,23 @@ def test_chunk_decay_beyond_range_is_reported(lib):
                                     dS_final=f64(dSf)[:, :1])
     for name, a, r in zip(NAMES, (dq, dk, dv, dg, dbeta, dS0), ref):
         assert rel_l2(f64(a)[:, :1], r) <= GRAD_TOL, name
+
+
+def test_product_wait_that_runs_out_is_reported_then_next_call_is_correct(lib):
+    """The backward's bounded waits on its tensor-core products (and those of
+    its checkpointing forward pass) give up at the first poll under the test
+    hook: KDA_ERR_DEVICE_TIMEOUT is recorded, every product still completes
+    before the kernel exits, and a normal call right after is correct."""
+    x, dO, dSf = make_case(lens=[130, 0, 60], H=2, seed=9)
+    g, beta = gpu_gate(lib, x)
+    assert lib.kda_get_last_device_error() == 0
+    try:
+        lib.kda_debug_set_wait_limit(-1, 0)
+        lib.backward_chunked(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g, beta, dO.to(DEV),
+                             cu_seqlens=x.cu_seqlens.to(DEV),
+                             initial_state=x.initial_state.to(DEV), dS_final=dSf.to(DEV))
+        st = lib.kda_get_last_device_error()
+    finally:
+        lib.kda_debug_set_wait_limit(-1, -1)
+    assert st == 7, lib.kda_status_string(st)   # KDA_ERR_DEVICE_TIMEOUT
+    run_case(lib, x, dO, dSf, 1.0)
