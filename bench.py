@@ -134,14 +134,14 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
                      "bytes": 4 * 138.82e6,
-                     "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
+                     "sha256": ["de302d8893db2371698075ad390eaa8c1ecdd57a5697ab39c26487c7c2281c65",
                              "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
                              "aca04576a3e893bf9325136479cc45787af796290f2b3a34973bf1a4817b1fc9",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
                    "bytes": 4 * 111.03e6,
-                   "sha256": ["a0416cd5e4f3b719287abd8be7613b224232cdce27edccd40f692a3c52a4ebfc",
+                   "sha256": ["de302d8893db2371698075ad390eaa8c1ecdd57a5697ab39c26487c7c2281c65",
                            "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
                            "aca04576a3e893bf9325136479cc45787af796290f2b3a34973bf1a4817b1fc9",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
@@ -591,7 +591,21 @@ def run_ours(args):
     proto["backward_chunked"] = protocol(
         lambda: kda.kda_chunk_backward(q, k, v, g, beta, None, 1.0, None, bdO, None, *bgrads,
                                        bdbeta, None, cws, stream), warmup=3, iters=10, repeats=3)
-    del bgrads, bws, bdO, cws
+    del cws
+    # the training pair: the prefill that keeps the chunk-start states, and the
+    # backward that reads them instead of running the forward again
+    ckpt = torch.empty(kda.kda_chunk_checkpoints_size(T_PREFILL, 1, H), dtype=torch.uint8,
+                       device=dev)
+    proto["prefill_checkpointed"] = protocol(
+        lambda: kda.kda_chunk_prefill_checkpointed(q, k, v, g, beta, None, 1.0, None, Sf, o, ckpt,
+                                                   ws, stream), warmup=3, iters=20, repeats=3)
+    kws = torch.empty(kda.kda_chunk_backward_checkpointed_workspace_size(T_PREFILL, 1, H),
+                      dtype=torch.uint8, device=dev)
+    proto["backward_checkpointed"] = protocol(
+        lambda: kda.kda_chunk_backward_checkpointed(q, k, v, g, beta, None, 1.0, ckpt, bdO, None,
+                                                    *bgrads, bdbeta, None, kws, stream),
+        warmup=3, iters=10, repeats=3)
+    del bgrads, bws, bdO, ckpt, kws
 
     prefill_leg_ms = max_over_ranks(fused_ms, world, dev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
@@ -758,6 +772,16 @@ def run_ours(args):
                "algorithmic_flops_per_launch": cb_flops, "ms": cb_ms,
                "tokens_per_s": T_PREFILL / (cb_ms * 1e-3),
                "protocol": proto["backward_chunked"]}
+    kb_ms = proto["backward_checkpointed"]["mean_ms"]
+    kb_flops = cb_flops - H * prefill_flops_per_head([T_PREFILL])
+    kb_tflops = kb_flops / (kb_ms * 1e-3) / 1e12
+    training = {"prefill_checkpointed_ms": proto["prefill_checkpointed"]["mean_ms"],
+                "backward_checkpointed_ms": kb_ms,
+                "backward_checkpointed_tflops": kb_tflops,
+                "backward_checkpointed_frac": kb_tflops / peaks["bf16_tflops"],
+                "checkpoint_bytes": kda.kda_chunk_checkpoints_size(T_PREFILL, 1, H),
+                "protocol": {"prefill_checkpointed": proto["prefill_checkpointed"],
+                             "backward_checkpointed": proto["backward_checkpointed"]}}
     for rl, kid in ((rl_prefill, "chunk_gated"), (rl_prefill_unfused, "chunk_unfused"),
                     (rl_decode, "decode"), (rl_pool, "decode_pool"), (rl_gate, "gate"),
                     (rl_conv, "short_conv"), (rl_bwd, "backward"), (rl_cbwd, "backward_chunked")):
@@ -783,6 +807,7 @@ def run_ours(args):
                       "prefill_unfused": rl_prefill_unfused, "decode": rl_decode,
                       "decode_bf16_pool": rl_pool, "short_conv": rl_conv, "backward": rl_bwd,
                       "backward_chunked": rl_cbwd},
+        "training": training,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "schedule": "steps pipelined over two buffer sets: H2D, prefill and D2H "

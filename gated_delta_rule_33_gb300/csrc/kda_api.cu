@@ -520,6 +520,86 @@ kda_status kda_chunk_backward(const void *q, const void *k, const void *v, const
         dev->error_word, dev->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+size_t kda_chunk_checkpoints_size(int64_t N, int B, int H, int K, int V) {
+    if (N < 0 || B < 1 || H < 1 || K != 128 || V != 128) return 0;
+    return kda::chunk_checkpoints_bytes(N, B, H);
+}
+
+kda_status kda_chunk_prefill_checkpointed(const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta,
+                                          const int32_t *cu_seqlens, int B, int64_t N, int H,
+                                          int K, int V, float scale, const float *initial_state,
+                                          float *final_state, void *o, kda_dtype o_dtype,
+                                          void *checkpoints, size_t checkpoints_bytes,
+                                          void *workspace, size_t workspace_bytes, void *stream) {
+    kda_status st = check_prefill_args(q, k, v, g, beta, cu_seqlens, B, N, H, K, V, initial_state,
+                                       final_state, o, o_dtype);
+    if (st != KDA_OK) return st;
+    if (!aligned16(workspace) || !aligned16(checkpoints)) return KDA_ERR_MISALIGNED;
+    const size_t need = kda::prefill_workspace_bytes(N, B, H);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr))
+        return KDA_ERR_WORKSPACE_TOO_SMALL;
+    if (checkpoints == nullptr || checkpoints_bytes < kda::chunk_checkpoints_bytes(N, B, H))
+        return KDA_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo *dev = nullptr;
+    st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    uint8_t *cp = static_cast<uint8_t *>(checkpoints);
+    return from_cuda(kda::launch_prefill_checkpointed(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), g, beta, cu_seqlens, B, N, H, scale, initial_state,
+        final_state, o, o_dtype == KDA_BF16,
+        reinterpret_cast<float *>(cp + kda::chunk_checkpoint_flags_bytes(B, H)),
+        reinterpret_cast<int *>(cp), workspace, dev->error_word, dev->num_sms,
+        static_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_chunk_backward_checkpointed_workspace_size(int64_t N, int B, int H, int K, int V) {
+    if (N < 0 || B < 1 || H < 1 || K != 128 || V != 128) return 0;
+    const int64_t chains = static_cast<int64_t>(B) * H;
+    const int ctas = static_cast<int>(chains < kda::kChunkBwdMaxCtas ? chains : kda::kChunkBwdMaxCtas);
+    return kda::chunk_bwd_from_checkpoints_workspace_bytes(ctas);
+}
+
+kda_status kda_chunk_backward_checkpointed(const void *q, const void *k, const void *v,
+                                           const float *g, const float *beta,
+                                           const int32_t *cu_seqlens, int B, int64_t N, int H,
+                                           int K, int V, float scale, const void *checkpoints,
+                                           size_t checkpoints_bytes, const void *dO,
+                                           kda_dtype dO_dtype, const float *dS_final, float *dq,
+                                           float *dk, float *dv, float *dg, float *dbeta,
+                                           float *dS0, void *workspace, size_t workspace_bytes,
+                                           void *stream) {
+    if (N < 0 || B < 1 || H < 1) return KDA_ERR_INVALID_ARG;
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+    if (!valid_dtype(dO_dtype)) return KDA_ERR_UNSUPPORTED_DTYPE;
+    if (cu_seqlens == nullptr && B != 1) return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (q == nullptr || k == nullptr || v == nullptr || g == nullptr ||
+                  beta == nullptr || dO == nullptr || dq == nullptr || dk == nullptr ||
+                  dv == nullptr || dg == nullptr || dbeta == nullptr))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(dO) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dg) ||
+        !aligned16(dbeta) || !aligned16(checkpoints) || !aligned16(dS_final) ||
+        !aligned16(dS0) || !aligned16(workspace) || !aligned16(cu_seqlens))
+        return KDA_ERR_MISALIGNED;
+    if (checkpoints == nullptr || checkpoints_bytes < kda::chunk_checkpoints_bytes(N, B, H))
+        return KDA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t need = kda_chunk_backward_checkpointed_workspace_size(N, B, H, K, V);
+    if (workspace_bytes < need || workspace == nullptr) return KDA_ERR_WORKSPACE_TOO_SMALL;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    const int64_t chains = static_cast<int64_t>(B) * H;
+    int ctas = dev->num_sms < kda::kChunkBwdMaxCtas ? dev->num_sms : kda::kChunkBwdMaxCtas;
+    if (chains < ctas) ctas = static_cast<int>(chains);
+    return from_cuda(kda::launch_chunk_backward_from_checkpoints(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+        static_cast<const __nv_bfloat16 *>(v), g, beta, cu_seqlens, B, N, H, scale, checkpoints,
+        dO, dO_dtype == KDA_BF16, dS_final, dq, dk, dv, dg, dbeta, dS0, workspace, ctas,
+        dev->error_word, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_debug_set_wait_limit(int64_t copy_polls, int64_t product_polls) {
     kda::set_prefill_wait_polls(copy_polls, product_polls);
     return KDA_OK;

@@ -878,6 +878,22 @@ cudaError_t launch_prefill_checkpoints(const __nv_bfloat16 *q, const __nv_bfloat
     return launch_chunk<false, true>(q, k, v, g, p, false, num_sms, s);
 }
 
+cudaError_t launch_prefill_checkpointed(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                        const __nv_bfloat16 *v, const float *g, const float *beta,
+                                        const int32_t *cu_seqlens, int B, int64_t N, int H,
+                                        float scale, const float *initial_state, float *final_state,
+                                        void *o, bool o_bf16, float *ckpt, int *split,
+                                        void *workspace, unsigned int *err, int num_sms,
+                                        cudaStream_t s) {
+    if (B == 0 || H == 0) return cudaSuccess;
+    cudaError_t e = cudaMemsetAsync(split, 0, static_cast<size_t>(B) * H * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    const Params p{g, beta, nullptr, nullptr, 0, nullptr, 0, nullptr, cu_seqlens, B, N, H, scale,
+                   initial_state, final_state, o, err, static_cast<unsigned int *>(workspace),
+                   kMaxPolls, kMaxPolls, ckpt, split};
+    return launch_chunk<false, true>(q, k, v, g, p, o_bf16, num_sms, s);
+}
+
 cudaError_t launch_prefill_gated(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                  const __nv_bfloat16 *v, const __nv_bfloat16 *f, const void *b,
                                  bool b_bf16, const float *A_log, int alog_mode,

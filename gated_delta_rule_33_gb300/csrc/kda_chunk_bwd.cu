@@ -123,14 +123,15 @@ constexpr uint32_t M_EM = 256;            // float[128] e^{m}
 constexpr uint32_t M_DEC = 768;           // float[128] e^{Gam_L}
 constexpr uint32_t M_PART = 1280;         // float[4][128] partial decay sums per row group
 constexpr uint32_t M_DGL = 3328;          // float[128] sum_v dS'[k][v] S[k][v]
-constexpr uint32_t M_DBETA = 3840;        // float[64]
-constexpr uint32_t M_SUF = 4096;          // float[4][128] dGam sums per row group
-constexpr uint32_t M_P = 6144;            // float[4][256] inverse partial products
+constexpr uint32_t M_SUF = 4096;          // float[4][128] dGam sums per row group; before
+                                          // the assembly the per-quarter parts of M_DGL
+constexpr uint32_t M_P = 6144;            // float[4][256] inverse partial products; after
+                                          // the inverse the parts of dbeta ([8][64]) and of
+                                          // colsum(dKh . Kh) ([4][128])
 constexpr uint32_t M_T32 = 10240;         // float[16][16]
 constexpr uint32_t M_TDIAG = 11264;       // float[4][16][16]
 constexpr uint32_t M_BAR = 15360;         // the product mbarrier
 constexpr uint32_t M_CTRL = 15376;        // int[8]: tmem base, chain, abort
-constexpr uint32_t M_KHS = 15424;         // float[128] colsum(dKh . Kh)
 constexpr uint32_t M_GL = 15936;          // float[128] Gam_L (log2 units)
 constexpr uint32_t OFF_STG = OFF_MISC + 16448;  // k, v bf16 [64][128] each, the whole chunk
 constexpr uint32_t kSmemBytes = OFF_STG + 32768;
@@ -441,9 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     float *s_dec = reinterpret_cast<float *>(misc + M_DEC);
     float *s_part = reinterpret_cast<float *>(misc + M_PART);
     float *s_dgl = reinterpret_cast<float *>(misc + M_DGL);
-    float *s_dbeta = reinterpret_cast<float *>(misc + M_DBETA);
     float *s_suf = reinterpret_cast<float *>(misc + M_SUF);
-    float *s_khs = reinterpret_cast<float *>(misc + M_KHS);
+    // Reductions across warps go through per-warp parts added in a fixed order
+    // (no shared-memory atomics), so the gradients do not depend on timing.
+    float *s_dglp = s_suf;                                     // [quarter][k]
+    float *s_dbp = reinterpret_cast<float *>(misc + M_P);      // [8][r]
+    float *s_khp = s_dbp + 512;                                // [grp][k]
     float *s_gl = reinterpret_cast<float *>(misc + M_GL);
     float *s_kk = reinterpret_cast<float *>(smem + OFF_KK);
     float *s_at = reinterpret_cast<float *>(smem + OFF_AT);
@@ -579,9 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 s_part[grp * kD + ch] = acc;
             }
             if (tid < kC) s_beta[tid] = tid < L ? p.beta[(tc + tid) * H + h] : 0.f;
-            if (tid < kC) s_dbeta[tid] = 0.f;
-            if (tid < kD) s_dgl[tid] = 0.f;
-            if (tid < kD) s_khs[tid] = 0.f;
             __syncthreads();
             float prefix = 0.f, gam_l = 0.f;
 #pragma unroll
@@ -724,9 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 #pragma unroll
                         for (int j = 0; j < 16; ++j) so[j] = ds[j] * sv[j];
                         const float t = lanes_sum16(so, lane);
-                        if ((lane & 1) == 0) atomicAdd(&s_dgl[k0 + (lane >> 1)], t);
+                        if ((lane & 1) == 0) s_dglp[quarter * kD + k0 + (lane >> 1)] = t;
                     }
-                    copy_out(I_SO);
+                    copy_out(I_SO);  // its barriers also order the parts above
+                    if (bt < kD)
+                        s_dgl[bt] = ((s_dglp[bt] + s_dglp[kD + bt]) + s_dglp[2 * kD + bt]) +
+                                    s_dglp[3 * kD + bt];
 #pragma unroll 1
                     for (int u = grp - 1; u < 8; u += 3) {
                         const int k0 = 16 * u;
@@ -918,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     sum[j] = vb[j] * vv[j] + rb[j] * kr[j] * fast_exp2(gam[j] - m);
                 }
                 const float t = lanes_sum16(sum, lane);
-                if ((lane & 1) == 0) atomicAdd(&s_dbeta[16 * grp + (lane >> 1)], t);
+                if ((lane & 1) == 0) s_dbp[quarter * kC + 16 * grp + (lane >> 1)] = t;
             }
 
             // ---- Y = dT T^T (lanes 0-63) ----
@@ -948,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     bd[j] = br * d16[j];
                     part += d16[j] * s_kk[s * 64 + r];
                 }
-                atomicAdd(&s_dbeta[r], part);
+                s_dbp[(4 + grp) * kC + r] = part;
                 uint8_t *sk = slot_ptr(S, S.sl0 == I_Y ? 0 : 1), *sb = slot_ptr(S, S.sl0 == I_Y ? 1 : 0);
                 put8(sk, img_half(I_DKK), 64, r, 16 * grp, d16);
                 put8(sk, img_half(I_DKK), 64, r, 16 * grp + 8, d16 + 8);
@@ -1014,20 +1018,27 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     dgam[j] = run;
                 }
                 s_suf[grp * kD + ch] = run;
-                atomicAdd(&s_khs[ch], khsum);
+                s_khp[grp * kD + ch] = khsum;
                 __syncthreads();
                 float later = 0.f;
 #pragma unroll
                 for (int g2 = 0; g2 < 4; ++g2)
                     if (g2 > grp) later += s_suf[g2 * kD + ch];
                 // dGam_L = colsum(dKh . Kh) + e^{Gam_L} sum_v dS' S, added to every row
-                const float dgl = s_khs[ch] + s_dec[ch] * s_dgl[ch];
+                const float khs = ((s_khp[ch] + s_khp[kD + ch]) + s_khp[2 * kD + ch]) +
+                                  s_khp[3 * kD + ch];
+                const float dgl = khs + s_dec[ch] * s_dgl[ch];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int r = 16 * grp + j;
                     if (r < L) p.dg[((tc + r) * H + h) * kD + ch] = dgam[j] + later + dgl;
                 }
-                if (tid < L) p.dbeta[(tc + tid) * H + h] = s_dbeta[tid];
+                if (tid < L) {
+                    float db = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) db += s_dbp[i * kC + tid];
+                    p.dbeta[(tc + tid) * H + h] = db;
+                }
             }
             // the gradients are not read back: a plain barrier before the next chunk
             tc_fence_before();
@@ -1072,10 +1083,58 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 
 }  // namespace
 
+namespace {
+size_t split_flags_bytes(int B, int H) {
+    return ((static_cast<size_t>(B) * H * sizeof(int) + 255) / 256) * 256;
+}
+size_t checkpoint_states_bytes(int64_t N, int B, int H) {
+    return (static_cast<size_t>(N / kC) + static_cast<size_t>(B)) * H * kD * kD * sizeof(float);
+}
+}  // namespace
+
+size_t chunk_checkpoint_flags_bytes(int B, int H) { return split_flags_bytes(B, H); }
+
+size_t chunk_checkpoints_bytes(int64_t N, int B, int H) {
+    return split_flags_bytes(B, H) + checkpoint_states_bytes(N, B, H);
+}
+
+size_t chunk_bwd_from_checkpoints_workspace_bytes(int ctas) {
+    return 512 + static_cast<size_t>(ctas) * kScratchPerCta;
+}
+
+// Workspace of the self-contained backward: the forward pass's counter (512
+// bytes), the checkpoint buffer (flags and states), then the workspace of the
+// backward from checkpoints (its counter and the per-CTA scratch).
 size_t chunk_bwd_workspace_bytes(int64_t N, int B, int H, int ctas) {
-    const size_t head = 512 + ((static_cast<size_t>(B) * H * sizeof(int) + 255) / 256) * 256;
-    const size_t ckpt = (static_cast<size_t>(N / kC) + static_cast<size_t>(B)) * H * kD * kD * sizeof(float);
-    return head + ckpt + static_cast<size_t>(ctas) * kScratchPerCta;
+    return 512 + chunk_checkpoints_bytes(N, B, H) + chunk_bwd_from_checkpoints_workspace_bytes(ctas);
+}
+
+cudaError_t launch_chunk_backward_from_checkpoints(
+    const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *g,
+    const float *beta, const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+    const void *checkpoints, const void *dO, bool dO_bf16, const float *dSf, float *dq, float *dk,
+    float *dv, float *dg, float *dbeta, float *dS0, void *workspace, int ctas, unsigned int *err,
+    cudaStream_t s) {
+    if (B == 0 || H == 0) return cudaSuccess;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaError_t e = cudaMemsetAsync(ws, 0, 512, s);  // the chain counter
+    if (e != cudaSuccess) return e;
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_bwd_kernel), static_cast<int>(kSmemAlloc));
+    if (e != cudaSuccess) return e;
+    const uint8_t *cp = static_cast<const uint8_t *>(checkpoints);
+    BwdParams p;
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    p.cu_seqlens = cu_seqlens; p.B = B; p.N = N; p.H = H; p.scale = scale;
+    p.dO = dO; p.dO_bf16 = dO_bf16 ? 1 : 0; p.dSf = dSf;
+    p.split = reinterpret_cast<const int *>(cp);
+    p.ckpt = reinterpret_cast<const float *>(cp + split_flags_bytes(B, H));
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dg; p.dbeta = dbeta; p.dS0 = dS0;
+    p.scratch = ws + 512;
+    p.counter = reinterpret_cast<unsigned int *>(ws);
+    p.err = err;
+    p.polls = prefill_wait_polls();
+    chunk_bwd_kernel<<<ctas, kThreads, kSmemAlloc, s>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
@@ -1087,34 +1146,18 @@ cudaError_t launch_chunk_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k
                                   int num_sms, cudaStream_t s) {
     if (B == 0 || H == 0) return cudaSuccess;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t flags_bytes = ((static_cast<size_t>(B) * H * sizeof(int) + 255) / 256) * 256;
-    unsigned int *counters = reinterpret_cast<unsigned int *>(ws);  // [0] forward, [64] backward
-    int *split = reinterpret_cast<int *>(ws + 512);
-    float *ckpt = reinterpret_cast<float *>(ws + 512 + flags_bytes);
-    const size_t ckpt_bytes = (static_cast<size_t>(N / kC) + static_cast<size_t>(B)) * H * kD * kD * sizeof(float);
-    uint8_t *scratch = ws + 512 + flags_bytes + ckpt_bytes;
-
-    cudaError_t e = cudaMemsetAsync(ws, 0, 512 + flags_bytes, s);
+    uint8_t *checkpoints = ws + 512;
+    int *split = reinterpret_cast<int *>(checkpoints);
+    float *ckpt = reinterpret_cast<float *>(checkpoints + split_flags_bytes(B, H));
+    cudaError_t e = cudaMemsetAsync(ws, 0, 512 + split_flags_bytes(B, H), s);
     if (e != cudaSuccess) return e;
     // forward pass: chunk-start states only
     e = launch_prefill_checkpoints(q, k, v, g, beta, cu_seqlens, B, N, H, scale, S0, ckpt, split,
-                                   counters, err, num_sms, s);
+                                   reinterpret_cast<unsigned int *>(ws), err, num_sms, s);
     if (e != cudaSuccess) return e;
-
-    e = ensure_dynamic_smem(reinterpret_cast<const void *>(chunk_bwd_kernel), static_cast<int>(kSmemAlloc));
-    if (e != cudaSuccess) return e;
-    BwdParams p;
-    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
-    p.cu_seqlens = cu_seqlens; p.B = B; p.N = N; p.H = H; p.scale = scale;
-    p.dO = dO; p.dO_bf16 = dO_bf16 ? 1 : 0; p.dSf = dSf;
-    p.ckpt = ckpt; p.split = split;
-    p.dq = dq; p.dk = dk; p.dv = dv; p.dg = dg; p.dbeta = dbeta; p.dS0 = dS0;
-    p.scratch = scratch;
-    p.counter = counters + 64;
-    p.err = err;
-    p.polls = prefill_wait_polls();
-    chunk_bwd_kernel<<<ctas, kThreads, kSmemAlloc, s>>>(p);
-    return cudaGetLastError();
+    return launch_chunk_backward_from_checkpoints(
+        q, k, v, g, beta, cu_seqlens, B, N, H, scale, checkpoints, dO, dO_bf16, dSf, dq, dk, dv, dg,
+        dbeta, dS0, ws + 512 + chunk_checkpoints_bytes(N, B, H), ctas, err, s);
 }
 
 }  // namespace kda

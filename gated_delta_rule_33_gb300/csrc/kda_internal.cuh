@@ -119,9 +119,31 @@ cudaError_t launch_prefill_checkpoints(const __nv_bfloat16 *q, const __nv_bfloat
                                        int *split, unsigned int *counter, unsigned int *err,
                                        int num_sms, cudaStream_t s);
 
+// The chunked prefill that also stores, for a later backward pass, the state
+// at every chunk start to ckpt and marks chains with a shortened chunk in split
+// (both laid out as for launch_prefill_checkpoints; split is zeroed here).
+cudaError_t launch_prefill_checkpointed(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                        const __nv_bfloat16 *v, const float *g, const float *beta,
+                                        const int32_t *cu_seqlens, int B, int64_t N, int H,
+                                        float scale, const float *initial_state, float *final_state,
+                                        void *o, bool o_bf16, float *ckpt, int *split,
+                                        void *workspace, unsigned int *err, int num_sms,
+                                        cudaStream_t s);
+
 // Chunked backward (kda_chunk_bwd.cu).
 constexpr int kChunkBwdMaxCtas = 160;
 size_t chunk_bwd_workspace_bytes(int64_t N, int B, int H, int ctas);
+// Checkpoint buffer (split flags, then the chunk-start states) and the
+// workspace of the backward that reads one.
+size_t chunk_checkpoints_bytes(int64_t N, int B, int H);
+size_t chunk_checkpoint_flags_bytes(int B, int H);  // the flags' part, at its start
+size_t chunk_bwd_from_checkpoints_workspace_bytes(int ctas);
+cudaError_t launch_chunk_backward_from_checkpoints(
+    const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v, const float *g,
+    const float *beta, const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,
+    const void *checkpoints, const void *dO, bool dO_bf16, const float *dSf, float *dq, float *dk,
+    float *dv, float *dg, float *dbeta, float *dS0, void *workspace, int ctas, unsigned int *err,
+    cudaStream_t s);
 cudaError_t launch_chunk_backward(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                   const __nv_bfloat16 *v, const float *g, const float *beta,
                                   const int32_t *cu_seqlens, int B, int64_t N, int H, float scale,

@@ -98,6 +98,18 @@ def load():
         lib.kda_chunk_backward.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P, I, P,
                                            P, P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.kda_chunk_backward.restype = I
+        lib.kda_chunk_checkpoints_size.argtypes = [I64, I, I, I, I]
+        lib.kda_chunk_checkpoints_size.restype = ctypes.c_size_t
+        lib.kda_chunk_prefill_checkpointed.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P, P,
+                                                       P, I, P, ctypes.c_size_t, P,
+                                                       ctypes.c_size_t, P]
+        lib.kda_chunk_prefill_checkpointed.restype = I
+        lib.kda_chunk_backward_checkpointed_workspace_size.argtypes = [I64, I, I, I, I]
+        lib.kda_chunk_backward_checkpointed_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_backward_checkpointed.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, F, P,
+                                                        ctypes.c_size_t, P, I, P, P, P, P, P, P,
+                                                        P, P, ctypes.c_size_t, P]
+        lib.kda_chunk_backward_checkpointed.restype = I
         lib.kda_recurrent_decode_gated.argtypes = [P, P, P, P, I, P, I, P, I, P, P, I, P, I, I, I,
                                                    I, I, F, P, I, P]
         lib.kda_recurrent_decode_gated.restype = I
@@ -283,6 +295,42 @@ def kda_chunk_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, d
     _check(st, "kda_chunk_backward")
 
 
+def kda_chunk_checkpoints_size(N, B, H, K=128, V=128) -> int:
+    return int(load().kda_chunk_checkpoints_size(N, B, H, K, V))
+
+
+def kda_chunk_prefill_checkpointed(q, k, v, g, beta, cu_seqlens, scale, initial_state,
+                                   final_state, o, checkpoints, workspace, stream=None):
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().kda_chunk_prefill_checkpointed(
+        _p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), B, N, H, K, V, float(scale),
+        _p(initial_state), _p(final_state), _p(o), _dtype_code(o), _p(checkpoints),
+        checkpoints.numel() * checkpoints.element_size(), _p(workspace), ws_bytes,
+        _stream(stream, q.device))
+    _check(st, "kda_chunk_prefill_checkpointed")
+
+
+def kda_chunk_backward_checkpointed_workspace_size(N, B, H, K=128, V=128) -> int:
+    return int(load().kda_chunk_backward_checkpointed_workspace_size(N, B, H, K, V))
+
+
+def kda_chunk_backward_checkpointed(q, k, v, g, beta, cu_seqlens, scale, checkpoints, dO,
+                                    dS_final, dq, dk, dv, dg, dbeta, dS0, workspace,
+                                    stream=None):
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_chunk_backward_checkpointed(
+        _p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), B, N, H, K, V, float(scale),
+        _p(checkpoints), checkpoints.numel() * checkpoints.element_size(), _p(dO),
+        _dtype_code(dO), _p(dS_final), _p(dq), _p(dk), _p(dv), _p(dg), _p(dbeta), _p(dS0),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    _check(st, "kda_chunk_backward_checkpointed")
+
+
 def kda_recurrent_decode_gated(q, k, v, f, b, A_log, alog_mode, dt_bias, state_pool,
                                state_indices, scale, o, stream=None):
     """state_indices None: slot b for sequence b."""
@@ -425,6 +473,43 @@ def backward_chunked(q, k, v, g, beta, dO, cu_seqlens=None, scale=1.0, initial_s
                      device=dev)
     kda_chunk_backward(q, k, v, g, beta, cu_seqlens, scale, initial_state, dO, dS_final, dq, dk,
                        dv, dg, dbeta, dS0, ws, stream)
+    return dq, dk, dv, dg, dbeta, dS0
+
+
+def prefill_checkpointed(q, k, v, g, beta, cu_seqlens=None, scale=1.0, initial_state=None,
+                         o_dtype=torch.bfloat16, stream=None):
+    """The chunked prefill that also keeps the chunk-start states for the backward;
+    returns (o, final_state, checkpoints)."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.device
+    o = torch.empty(N, H, V, dtype=o_dtype, device=dev)
+    final = torch.empty(B, H, K, V, dtype=torch.float32, device=dev)
+    ckpt = torch.empty(kda_chunk_checkpoints_size(N, B, H, K, V), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(kda_chunk_prefill_workspace_size(N, B, H, K, V), 16), dtype=torch.uint8,
+                     device=dev)
+    kda_chunk_prefill_checkpointed(q, k, v, g, beta, cu_seqlens, scale, initial_state, final, o,
+                                   ckpt, ws, stream)
+    return o, final, ckpt
+
+
+def backward_from_checkpoints(q, k, v, g, beta, dO, checkpoints, cu_seqlens=None, scale=1.0,
+                              dS_final=None, want_dS0=True, stream=None):
+    """Gradients by the chunked backward from the checkpoints of prefill_checkpointed;
+    returns (dq, dk, dv, dg, dbeta, dS0 or None)."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    B = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = q.device
+    dq, dk, dg = (torch.empty(N, H, K, device=dev) for _ in range(3))
+    dv = torch.empty(N, H, V, device=dev)
+    dbeta = torch.empty(N, H, device=dev)
+    dS0 = torch.empty(B, H, K, V, device=dev) if want_dS0 else None
+    ws = torch.empty(kda_chunk_backward_checkpointed_workspace_size(N, B, H, K, V),
+                     dtype=torch.uint8, device=dev)
+    kda_chunk_backward_checkpointed(q, k, v, g, beta, cu_seqlens, scale, checkpoints, dO,
+                                    dS_final, dq, dk, dv, dg, dbeta, dS0, ws, stream)
     return dq, dk, dv, dg, dbeta, dS0
 
 

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define KDA_VERSION 10100 /* 1.1.0 */
+#define KDA_VERSION 10200 /* 1.2.0 */
 
 typedef enum kda_status {
     KDA_OK = 0,
@@ -346,7 +346,8 @@ kda_status kda_recurrent_backward(const void *q, const void *k, const void *v,
  * a 16-bit significand) with fp32 accumulation; the chunk-start states come
  * from the tf32 forward, so the gradients agree with the exact reverse mode
  * to about 1e-3 relative L2 (the forward's state precision), not to fp32
- * rounding as kda_recurrent_backward does.
+ * rounding as kda_recurrent_backward does.  Every sum is added in a fixed
+ * order, so two calls on the same inputs write the same bits.
  *
  * A (sequence, head) whose forward pass had to shorten a chunk (a chunk's
  * decay -sum(g) in some channel above 160) has no 64-token-aligned states:
@@ -370,6 +371,67 @@ kda_status kda_chunk_backward(const void *q, const void *k, const void *v,
                               float *dq, float *dk, float *dv, float *dg, float *dbeta,
                               float *dS0, void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/*
+ * kda_chunk_prefill_checkpointed / kda_chunk_backward_checkpointed -- the
+ * training pair of the chunked form: the forward pass that a training step
+ * runs anyway also keeps the chunk-start states, and the backward reads them
+ * instead of running the forward a second time (kda_chunk_backward does both
+ * in one call, about 0.5 ms of its time for N = 4096, H = 96).
+ *
+ * kda_chunk_prefill_checkpointed takes the arguments of kda_chunk_prefill and
+ * writes the same o and final_state (the same kernel, bit for bit), and in
+ * addition:
+ *   checkpoints  device, >= kda_chunk_checkpoints_size() bytes, 16-byte
+ *                aligned, written (caller-owned; nothing else is kept): first
+ *                one int32 per (sequence, head), b H + h, set to 1 where a
+ *                chunk had to be shortened (decay -sum(g) in some channel
+ *                above 160 within 64 tokens), padded to 256 bytes; then the
+ *                fp32 state S [K, V] at the start of every 64-token chunk,
+ *                chunk c of sequence b (c = 0, 1, ..) in slot
+ *                cu_seqlens[b] / 64 + b + c, [slot, H, K, V] row-major
+ *                ((N / 64 + B) H 64 KB: 400 MB for N = 4096, H = 96).
+ *   workspace    >= kda_chunk_prefill_workspace_size() bytes, as for
+ *                kda_chunk_prefill.
+ *
+ * kda_chunk_backward_checkpointed takes the arguments of kda_chunk_backward
+ * with the checkpoints of a kda_chunk_prefill_checkpointed call on the same
+ * q, k, v, g, beta, cu_seqlens, scale and initial state in place of
+ * initial_state, and writes the same gradients, bit for bit, with the same
+ * KDA_ERR_DECAY_RANGE rule for a marked (sequence, head).  It only reads the
+ * checkpoints (they may serve several backward calls).
+ *   workspace    device, >= kda_chunk_backward_checkpointed_workspace_size()
+ *                bytes (512 bytes plus 528 KB for each of up to
+ *                min(B H, 160) CTAs), 16-byte aligned; scratch.
+ * Both return KDA_ERR_WORKSPACE_TOO_SMALL when checkpoints_bytes is below the
+ * size above, and otherwise fail as the calls they extend.  The sizes return
+ * 0 for arguments those calls reject.
+ */
+size_t kda_chunk_checkpoints_size(int64_t N, int B, int H, int K, int V);
+
+kda_status kda_chunk_prefill_checkpointed(const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta,
+                                          const int32_t *cu_seqlens, int B,
+                                          int64_t N, int H, int K, int V, float scale,
+                                          const float *initial_state, float *final_state,
+                                          void *o, kda_dtype o_dtype,
+                                          void *checkpoints, size_t checkpoints_bytes,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream);
+
+size_t kda_chunk_backward_checkpointed_workspace_size(int64_t N, int B, int H, int K, int V);
+
+kda_status kda_chunk_backward_checkpointed(const void *q, const void *k, const void *v,
+                                           const float *g, const float *beta,
+                                           const int32_t *cu_seqlens, int B,
+                                           int64_t N, int H, int K, int V, float scale,
+                                           const void *checkpoints, size_t checkpoints_bytes,
+                                           const void *dO, kda_dtype dO_dtype,
+                                           const float *dS_final,
+                                           float *dq, float *dk, float *dv, float *dg,
+                                           float *dbeta, float *dS0,
+                                           void *workspace, size_t workspace_bytes,
+                                           void *stream);
 
 /*
  * kda_gate_backward -- gradients of the gate (the training regime, after

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(clib):
 
 def test_version_and_status_strings(clib):
     import gated_delta_rule_33_gb300 as kda
-    assert kda.kda_version() == 10100
+    assert kda.kda_version() == 10200
     assert kda.kda_status_string(0) == "KDA_OK"
     assert kda.kda_status_string(5) == "KDA_ERR_WORKSPACE_TOO_SMALL"
     assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
@@ -55,6 +55,52 @@ def test_workspace_size_rules(clib):
     assert kda.kda_chunk_prefill_workspace_size(4096, 1, 96) < 64 * 1024
     assert kda.kda_chunk_prefill_workspace_size(4096, 1, 96, 64, 128) == 0
     assert kda.kda_chunk_prefill_workspace_size(-1, 1, 96) == 0
+
+
+def test_checkpoint_sizes(clib):
+    import gated_delta_rule_33_gb300 as kda
+    # split flags (one int32 per sequence and head, padded to 256 bytes), then one fp32
+    # 128 x 128 state per chunk start: N / 64 + B slots per head
+    assert kda.kda_chunk_checkpoints_size(4096, 1, 96) == 512 + (64 + 1) * 96 * 65536
+    assert kda.kda_chunk_checkpoints_size(100, 3, 2) == 256 + (1 + 3) * 2 * 65536
+    assert kda.kda_chunk_checkpoints_size(0, 1, 1) == 256 + 65536
+    assert kda.kda_chunk_checkpoints_size(64, 1, 1, 64, 128) == 0
+    assert kda.kda_chunk_checkpoints_size(-1, 1, 1) == 0
+    # the backward from checkpoints: a 512-byte counter and 528 KB per CTA (up to 160)
+    per_cta = 528 * 1024
+    assert kda.kda_chunk_backward_checkpointed_workspace_size(4096, 1, 96) == 512 + 96 * per_cta
+    assert kda.kda_chunk_backward_checkpointed_workspace_size(64, 4, 96) == 512 + 160 * per_cta
+    # the self-contained backward holds a counter, the checkpoints and that workspace
+    assert kda.kda_chunk_backward_workspace_size(4096, 1, 96) == (
+        512 + kda.kda_chunk_checkpoints_size(4096, 1, 96)
+        + kda.kda_chunk_backward_checkpointed_workspace_size(4096, 1, 96))
+
+
+def test_checkpointed_argument_checks(clib):
+    P = _fake()
+    need = clib.kda_chunk_checkpoints_size(128, 1, 2, 128, 128)
+
+    def fwd(ck=P, ckb=need, K=128, ws=_fake(), wsb=4096):
+        return clib.kda_chunk_prefill_checkpointed(P, P, P, P, P, None, 1, 128, 2, K, 128, 1.0,
+                                                   None, None, P, 0, ck, ckb, ws, wsb, None)
+
+    assert fwd(K=64) == 2                        # KDA_ERR_UNSUPPORTED_SHAPE
+    assert fwd(ckb=need - 1) == 5                # KDA_ERR_WORKSPACE_TOO_SMALL
+    assert fwd(ck=None) == 5
+    assert fwd(ck=_fake(0x10008)) == 4           # KDA_ERR_MISALIGNED
+    assert fwd(wsb=0) == 5
+    wneed = clib.kda_chunk_backward_checkpointed_workspace_size(128, 1, 2, 128, 128)
+
+    def bwd(ck=P, ckb=need, dodt=0, ws=_fake(), wsb=wneed, dq=P):
+        return clib.kda_chunk_backward_checkpointed(P, P, P, P, P, None, 1, 128, 2, 128, 128,
+                                                    1.0, ck, ckb, P, dodt, None, dq, P, P, P, P,
+                                                    None, ws, wsb, None)
+
+    assert bwd(dodt=7) == 3                      # KDA_ERR_UNSUPPORTED_DTYPE
+    assert bwd(dq=None) == 1                     # KDA_ERR_INVALID_ARG
+    assert bwd(ckb=need - 1) == 5
+    assert bwd(wsb=wneed - 1) == 5
+    assert bwd(ws=_fake(0x10004)) == 4
 
 
 def _fake(addr=0x10000):
