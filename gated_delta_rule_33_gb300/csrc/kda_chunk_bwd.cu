@@ -213,7 +213,9 @@ struct TRowMajor {
 // K-major: rows are M / N, `blk` the bytes between 64-column K blocks.
 // MN-major: rows are K, `blk` the bytes between 64-column M / N blocks (LBO).
 struct Opd {
-    uint32_t hi, lo;   // shared addresses of the hi and lo tiles (lo = 0: exact)
+    uint32_t hi;       // shared address of the hi tile
+    uint32_t hi_lo;    // bytes from the hi tile to the lo tile
+    bool has_lo;       // false: an exact bf16 image (no lo tile)
     uint32_t blk;
     uint32_t mn;
 };
@@ -221,41 +223,49 @@ struct Opd {
 __device__ __forceinline__ Opd opd(uint32_t slot, int img, uint32_t row0, bool mn) {
     Opd o;
     o.hi = slot + row0 * 128;
-    o.lo = img_exact(img) ? 0u : o.hi + img_half(img);
+    o.hi_lo = img_half(img);
+    o.has_lo = !img_exact(img);
     o.blk = img_rows(img) * 128;
     o.mn = mn ? 1u : 0u;
     return o;
 }
 
-// Descriptor of k-step kk (16 elements) of an operand, from its descriptor at
-// k-step 0 (`d0`, built for the hi or lo tile): the start address advances by
-// whole 8-row groups (MN-major) or by 32 bytes inside the 128-byte rows and a
-// block per four steps (K-major).
-__device__ __forceinline__ uint64_t kstep(const Opd &o, uint64_t d0, int kk) {
-    const uint32_t off = o.mn ? kk * 2048u : (kk >> 2) * o.blk + (kk & 3) * 32u;
-    return d0 + static_cast<uint64_t>(off >> 4);
-}
 __device__ __forceinline__ uint64_t desc0(const Opd &o, uint32_t base) {
     return smem_desc(base, o.mn ? o.blk : 16u, 1024, kSwizzle128B);
 }
 
-// D[tmem d] (+)= A B over `ksteps` k-steps of 16 (M = 128, N columns), as
-// hi.hi + hi.lo + lo.hi per k-step.  Issued by one thread.
+// D[tmem d] (+)= A B over `ksteps` k-steps of 16 (a multiple of 4; M = 128, N
+// columns), as hi.hi + hi.lo + lo.hi per k-step, issued by one elected lane of
+// the converged warp 0.  Each descriptor's low word (the start address) steps
+// by a constant: 32 bytes per k-step for a K-major operand, with a jump to the
+// next 64-column block after every fourth step, and eight 256-byte rows per
+// k-step for an MN-major one.  The loop holds little besides the MMAs: every
+// instruction of the issuing warp delays the next MMA, and an N = 64 or 128
+// MMA completes in about 50 cycles, less than a longer issue path takes to
+// produce it.  The loop stays rolled: the kernel is bound by its instruction
+// cache, and every unrolled copy of this loop costs more than it saves.
 __device__ __forceinline__ void issue(uint32_t d, const Opd &A, const Opd &B, uint32_t N, int ksteps,
-                                  bool accumulate) {
+                                      bool accumulate) {
     const uint32_t id = instr_desc(128, N, kFmtBF16, A.mn, B.mn);
-    const uint64_t ah0 = desc0(A, A.hi), bh0 = desc0(B, B.hi);
-    const uint64_t al0 = A.lo ? desc0(A, A.lo) : 0, bl0 = B.lo ? desc0(B, B.lo) : 0;
+    const uint64_t a0 = desc0(A, A.hi), b0 = desc0(B, B.hi);
+    const uint32_t dh_a = static_cast<uint32_t>(a0 >> 32), dh_b = static_cast<uint32_t>(b0 >> 32);
+    uint32_t ah = static_cast<uint32_t>(a0), bh = static_cast<uint32_t>(b0);
+    uint32_t al = ah + (A.hi_lo >> 4), bl = bh + (B.hi_lo >> 4);
+    const uint32_t sa = A.mn ? 128u : 2u, sb = B.mn ? 128u : 2u;
+    const uint32_t ja = A.mn ? 512u : (A.blk >> 4), jb = B.mn ? 512u : (B.blk >> 4);
+    auto dsc = [](uint32_t hi, uint32_t lo) { return (static_cast<uint64_t>(hi) << 32) | lo; };
     uint32_t acc = accumulate ? 1u : 0u;
-    // (kept rolled: the kernel's code size, not the issuing loop, is what
-    // costs; every copy of it fills the instruction cache)
+    // after the fourth step of a block: to the next block
+    const uint32_t ea = ja - 3 * sa, eb = jb - 3 * sb;
 #pragma unroll 1
     for (int kk = 0; kk < ksteps; ++kk) {
-        const uint64_t ah = kstep(A, ah0, kk), bh = kstep(B, bh0, kk);
-        mma_f16_ss(d, ah, bh, id, acc);
+        mma_f16_ss_w(d, dsc(dh_a, ah), dsc(dh_b, bh), id, acc);
         acc = 1u;
-        if (B.lo != 0) mma_f16_ss(d, ah, kstep(B, bl0, kk), id, 1u);
-        if (A.lo != 0) mma_f16_ss(d, kstep(A, al0, kk), bh, id, 1u);
+        if (B.has_lo) mma_f16_ss_w(d, dsc(dh_a, ah), dsc(dh_b, bl), id, 1u);
+        if (A.has_lo) mma_f16_ss_w(d, dsc(dh_a, al), dsc(dh_b, bh), id, 1u);
+        const bool last = (kk & 3) == 3;
+        const uint32_t da = last ? ea : sa, db = last ? eb : sb;
+        ah += da; al += da; bh += db; bl += db;
     }
 }
 
@@ -342,15 +352,18 @@ __device__ __forceinline__ void copy_rows(const Sched &S, int sl, int i, uint32_
         }
         return;
     }
-    const uint32_t nblk = img_cols(i) / 64, per = (r1 - r0) * 8;  // pieces per (tile, block) range
-    const uint32_t n = (img_exact(i) ? 1u : 2u) * nblk * per;
-    for (uint32_t u = S.tid; u < n; u += kThreads) {
-        const uint32_t q = u / per, w = u - q * per;  // q = tile * nblk + block
-        const uint32_t o = (q / nblk) * img_half(i) + (q % nblk) * rows * 128 + r0 * 128 + w * 16;
-        if (kLoad)
-            cp_async_16(slot + o, glob + o, true);
-        else
-            *reinterpret_cast<uint4 *>(glob + o) = *reinterpret_cast<const uint4 *>(slot + o);
+    // in each (tile, 64-column block) the rows are one contiguous range
+    const uint32_t pieces = (r1 - r0) * 8;
+#pragma unroll 1
+    for (uint32_t q = 0; q < (img_exact(i) ? 1u : 2u) * (img_cols(i) / 64); ++q) {
+        const uint32_t base = q * rows * 128 + r0 * 128;  // the lo tile follows the hi tile's blocks
+        for (uint32_t u = S.tid; u < pieces; u += kThreads) {
+            if (kLoad)
+                cp_async_16(slot + base + u * 16, glob + base + u * 16, true);
+            else
+                *reinterpret_cast<uint4 *>(glob + base + u * 16) =
+                    *reinterpret_cast<const uint4 *>(slot + base + u * 16);
+        }
     }
 }
 
@@ -422,10 +435,11 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         if (la >= 0) set_slot(S, la, ia, alo, ahi);
         if (lb >= 0) set_slot(S, lb, ib, blo, bhi);
     }
-    if (S.tid == 0) {
+    if (S.tid < 32) {
+        __syncwarp();
         issue(d, opd(pa ? S.sb : S.sa, ia, A.row0, A.mn != 0), opd(pb ? S.sb : S.sa, ib, B.row0, B.mn != 0),
               N, ksteps, accumulate);
-        mma_commit(S.bar_mma);
+        mma_commit_w(S.bar_mma);
     }
     S.pend_mma = true;
     if (!cta_wait(S.bar_mma, S.ph_mma & 1, S.abort_flag, S.err, S.tid, S.polls)) return false;
