@@ -704,16 +704,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             {
                 float *T = reinterpret_cast<float *>(smem + OFF_TT);
                 if (warp >= 4) {
-                    // the checkpoint S into slot A (its Ks is dead since D_A);
-                    // each image is staged in slot B (QK's copy there is given
-                    // up: the W' product copies its rows back) and then copied
-                    // to the scratch with coalesced stores
+                    // the checkpoint S into slot A (its Ks is dead since D_A),
+                    // in flight while the dS' image is formed; each image is
+                    // staged in slot B (QK's copy there is given up: the W'
+                    // product copies its rows back) and then copied to the
+                    // scratch with coalesced stores
                     const int bt = tid - 128;  // 0 .. 383
                     for (int u = bt; u < 4096; u += kThreads - 128)
                         cp_async_16(smem + SLOT_A + u * 16, Sc + u * 4, true);
-                    cp_async_wait_all();
-                    named_sync(2, kThreads - 128);
-                    const float *Ss = reinterpret_cast<const float *>(smem + SLOT_A);
                     uint8_t *stage = smem + SLOT_B;
                     auto copy_out = [&](int i) {
                         named_sync(2, kThreads - 128);
@@ -724,6 +722,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     };
                     // 16-column units of k: warps 4-7 take units 0, 3, 6, warps
                     // 8-11 units 1, 4, 7 and warps 12-15 units 2, 5
+#pragma unroll 1
+                    for (int u = grp - 1; u < 8; u += 3) {
+                        const int k0 = 16 * u;
+                        float ds[16];
+                        tmem_ld16(tl + C_DS + k0, ds);
+                        tmem_wait_ld();
+                        put8(stage, img_half(I_DS), 128, ch, k0, ds);
+                        put8(stage, img_half(I_DS), 128, ch, k0 + 8, ds + 8);
+                    }
+                    copy_out(I_DS);
+                    cp_async_wait_all();
+                    named_sync(2, kThreads - 128);
+                    const float *Ss = reinterpret_cast<const float *>(smem + SLOT_A);
 #pragma unroll 1
                     for (int u = grp - 1; u < 8; u += 3) {
                         const int k0 = 16 * u;
@@ -745,16 +756,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     if (bt < kD)
                         s_dgl[bt] = ((s_dglp[bt] + s_dglp[kD + bt]) + s_dglp[2 * kD + bt]) +
                                     s_dglp[3 * kD + bt];
-#pragma unroll 1
-                    for (int u = grp - 1; u < 8; u += 3) {
-                        const int k0 = 16 * u;
-                        float ds[16];
-                        tmem_ld16(tl + C_DS + k0, ds);
-                        tmem_wait_ld();
-                        put8(stage, img_half(I_DS), 128, ch, k0, ds);
-                        put8(stage, img_half(I_DS), 128, ch, k0 + 8, ds + 8);
-                    }
-                    copy_out(I_DS);
                 } else {
                     float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
                     float *T32c = reinterpret_cast<float *>(misc + M_T32);
