@@ -306,6 +306,7 @@ struct Sched {
     int lo0, hi0, lo1, hi1;  // the rows of its image each slot holds
     uint32_t ph_mma;
     bool pend_mma;
+    bool pend_copy;  // a preloaded operand's copies may still be in flight
 };
 
 // An operand: image, first row used, MN-major.
@@ -424,9 +425,10 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         pb = (pa == 0) ? 1 : 0;
         lb = pb;
     }
-    if (la >= 0 || lb >= 0) {
+    if (la >= 0 || lb >= 0 || S.pend_copy) {
         // the rows it reads of each image not in a slot, by cp.async (the
-        // images were written by this CTA's threads before a barrier)
+        // images were written by this CTA's threads before a barrier), and
+        // any preloaded rows
         if (la >= 0) copy_rows<true>(S, la, ia, alo, ahi);
         if (lb >= 0) copy_rows<true>(S, lb, ib, blo, bhi);
         cp_async_wait_all();
@@ -434,6 +436,7 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         __syncthreads();
         if (la >= 0) set_slot(S, la, ia, alo, ahi);
         if (lb >= 0) set_slot(S, lb, ib, blo, bhi);
+        S.pend_copy = false;
     }
     if (S.tid < 32) {
         __syncwarp();
@@ -446,6 +449,17 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
     S.ph_mma++;
     S.pend_mma = false;
     return true;
+}
+
+// Starts copying rows [r0, r1) of image i into slot sl for the next product,
+// under the epilogue in between: the slot's operand is dead and nothing else
+// writes the slot before that product, which waits for the copies.  Called
+// by every thread after a product's completion (its barrier orders the copy
+// after every read of the slot).
+__device__ __forceinline__ void preload(Sched &S, int sl, int i, int r0, int r1) {
+    copy_rows<true>(S, sl, i, static_cast<uint32_t>(r0), static_cast<uint32_t>(r1));
+    set_slot(S, sl, i, r0, r1);
+    S.pend_copy = true;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams p) {
@@ -507,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.lo0 = S.hi0 = S.lo1 = S.hi1 = 0;
     S.ph_mma = 0;
     S.pend_mma = false;
+    S.pend_copy = false;
     const float kLog2e = 1.4426950408889634f;
     const float kMaxChunkLog2 = kMaxChunkDecay * kLog2e;
 
@@ -770,6 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     ut_level2<TRowMajor, 4>(s_at, T, Tdiag, T32c, P, out, tid);
                 }
                 __syncthreads();
+                // the checkpoint in slot A is dead: the W' product's Kr rows
+                // meanwhile
+                preload(S, 0, I_QK, 64, 128);
                 // A_kk is consumed: q again into its area for the assembly
                 for (int u = tid; u < kC * 16; u += kThreads) {
                     const int r = u >> 4, pc = u & 15;
@@ -789,7 +807,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             }
             fence_proxy_async_smem();
             publish();
-            S.sl0 = -1;  // slot A holds the checkpoint
             set_slot(S, 1, I_TB, 0, 64);
 
             // Epilogues below write their image into a slot whose operand is
@@ -801,6 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // in V's slot ----
             if (!product(S, {I_QK, 64, 1}, {I_TB, 0, 0}, tmem + C_TA, 64, 4, false)) break;
             if (!product(S, {I_V, 0, 1}, {I_TB, 0, 0}, tmem + C_TB, 64, 4, false)) break;
+            preload(S, S.sl0 == I_TB ? 0 : 1, I_SO, 0, 128);
             {
                 const int sl = (S.sl0 == I_V) ? 0 : 1;
                 float w16[16];
@@ -815,6 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 
             // ---- U^T = Ut^T + S_op^T (-W'^T); U^T image in S_op's slot ----
             if (!product(S, {I_SO, 0, 0}, {I_WT, 0, 1}, tmem + C_TB, 64, 8, true)) break;
+            preload(S, S.sl0 == I_WT ? 0 : 1, I_DS, 0, 128);
             {
                 const int sl = (S.sl0 == I_SO) ? 0 : 1;
                 float u16[16];
@@ -829,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // stays in its slot ----
             if (!product(S, {I_DS, 0, 0}, {I_KH, 0, 0}, tmem + C_TA, 64, 8, false)) break;
             if (!product(S, {I_DU2, 64, 1}, {I_AQ, 0, 1}, tmem + C_TA, 64, 4, true)) break;
+            preload(S, S.sl0 == I_AQ ? 0 : 1, I_QK, 0, 64);
             {
                 const int sl = (S.sl0 == I_DU2) ? 0 : 1;
                 float d16[16];
@@ -843,6 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // ---- P^T = dO^T Qt - dU^T W'^T... ; dS <- e^{Gam_L} dS' + e^m P ----
             if (!product(S, {I_DU2, 64, 1}, {I_QK, 0, 1}, tmem + C_TA, 128, 4, false)) break;
             if (!product(S, {I_DU2, 0, 1}, {I_WT, 0, 0}, tmem + C_TA, 128, 4, true)) break;
+            preload(S, S.sl0 == I_WT ? 0 : 1, I_UT, 0, 128);
             {
                 float pv[32], ds[32];
                 tmem_ld32(tl + C_TA + 32 * grp, pv);
@@ -882,6 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             if (!product(S, {I_SO, 0, 1}, {I_DU2, 0, 0}, tmem + C_TA, 128, 8, false)) break;
             if (!product(S, {I_QK, 0, 1}, {I_DAQ, 0, 1}, tmem + C_S, 64, 4, false)) break;
             if (!product(S, {I_KS, 0, 1}, {I_DAQ, 0, 0}, tmem + C_TB, 64, 4, true)) break;
+            preload(S, S.sl0 == I_KS ? 0 : 1, I_DS, 0, 128);
             {
                 // -dW'^T[k = ch][r]: dW'[r][k] into rows 0-63 of the QK image (Qt is
                 // dead), staged in the slot dA_qk used
@@ -901,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // ---- dT = (dW' Kr^T + dU V^T) diag(beta) (lanes 0-63) ----
             if (!product(S, {I_QK, 0, 0}, {I_QK, 64, 0}, tmem + C_TA, 64, 8, false, 0, 64)) break;  // lanes 0-63
             if (!product(S, {I_DU2, 0, 0}, {I_V, 0, 0}, tmem + C_TA, 64, 8, true, 0, 64)) break;  // lanes 0-63
+            preload(S, S.sl0 == I_DU2 ? 0 : 1, I_QK, 0, 64);
             if (quarter < 2) {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
@@ -915,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // ---- d(beta Kr)^T = dW'^T T and d(beta V)^T = dU^T T ----
             if (!product(S, {I_QK, 0, 1}, {I_T, 0, 1}, tmem + C_R, 64, 4, false)) break;
             if (!product(S, {I_DU2, 0, 1}, {I_T, 0, 1}, tmem + C_VB, 64, 4, false)) break;
+            preload(S, S.sl0 == I_DU2 ? 0 : 1, I_DT, 0, 64);
             {
                 // d(beta V)^T[v = ch][r]: dv = beta_r d(beta V); dbeta += sum_v d(beta V) v.
                 // d(beta Kr)^T[k = ch][r]: dbeta += sum_k d(beta Kr) Kr.
