@@ -396,6 +396,17 @@ __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0
     }
 }
 
+// As stage_store for an image that only the next products read, from the
+// slot: no copy to the scratch (the scratch's copy stays stale, so no later
+// product may miss it in the slot).
+__device__ __forceinline__ void stage_only(Sched &S, int sl, int i, int r0, int r1) {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    set_slot(S, sl, i, r0, r1);
+}
+
 // One product term, D[tmem d] (+)= A B: copies the operand images that are not
 // already in a slot (a slot keeps its image until it is reused or the image is
 // rewritten), issues the MMAs from thread 0 and waits for them.  Returns
@@ -496,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
         fence_mbar_init();
         ctrl[2] = 0;
     }
-    // the inverse's T: the blocks above the diagonal stay zero for every chunk
+    // the inverse's T: the blocks above the diagonal are zero (restored after
+    // D_A in every chunk, whose Ks copy overwrites them)
     for (int e = tid; e < 4096 / 4; e += kThreads)
         reinterpret_cast<float4 *>(smem + OFF_TT)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     tc_fence_before();
@@ -678,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(smem + SLOT_B, img_half(I_QK), 128, r, c0, qt);  // staged (slot B is free)
                 put8(smem + SLOT_B, img_half(I_QK), 128, 64 + r, c0, kr);
                 put8(img(I_KS), img_half(I_KS), 64, r, c0, ks);
+                put8(smem + OFF_TT, img_half(I_KS), 64, r, c0, ks);  // for D_A, below
                 put8(img(I_KH), img_half(I_KH), 64, r, c0, kh);
                 put8(img(I_V), 0, 64, r, c0, vv);
                 put8(img(I_DU2), img_half(I_DU2), 128, 64 + r, c0, dov);
@@ -685,7 +698,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             stage_store(S, 1, I_QK, 0, 128);
 
             // ---- D_A = [Qt; Kr] Ks^T ----
-            if (!product(S, {I_QK, 0, 0}, {I_KS, 0, 0}, tmem + C_TA, 64, 8, false)) break;
+            // Ks from its copy in the inverse's work areas (T and kk, both
+            // free until D_A completes), standing in for slot A
+            S.sa = smem_addr(smem + OFF_TT);
+            set_slot(S, 0, I_KS, 0, 64);
+            const bool da_ok = product(S, {I_QK, 0, 0}, {I_KS, 0, 0}, tmem + C_TA, 64, 8, false);
+            S.sa = smem_addr(smem + SLOT_A);
+            S.sl0 = -1;
+            if (!da_ok) break;
             {
                 float d16[16];
                 tmem_ld16(tl + C_TA + 16 * grp, d16);
@@ -706,6 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                         s_at[s * 64 + r] = (s < r) ? br * d16[j] : 0.f;
                     }
                 }
+            }
+            {
+                // Ks's copy is consumed: the blocks of T above its diagonal
+                // back to zero (the inverse leaves them alone and reads them)
+                float *T = reinterpret_cast<float *>(smem + OFF_TT);
+                for (int e = tid; e < kC * kC; e += kThreads)
+                    if (((e & 63) >> 4) > (e >> 10)) T[e] = 0.f;
             }
             dirty(S, I_AQ);
             __syncthreads();
@@ -973,10 +1000,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 put8(slot_ptr(S, S.sl0 == I_DT ? 0 : 1), img_half(I_Y), 64, ch, 16 * grp, d16);
                 put8(slot_ptr(S, S.sl0 == I_DT ? 0 : 1), img_half(I_Y), 64, ch, 16 * grp + 8, d16 + 8);
             }
-            stage_store(S, S.sl0 == I_DT ? 0 : 1, I_Y, 0, 64);
+            stage_only(S, S.sl0 == I_DT ? 0 : 1, I_Y, 0, 64);  // read from the slot only
 
             // ---- dA_kk = -strict_tril(T^T Y) (lanes 0-63); dbeta += rowsum(dA_kk kk) ----
             if (!product(S, {I_T, 0, 1}, {I_Y, 0, 1}, tmem + C_TA, 64, 4, false)) break;
+            // Kr's rows for the dKs product into Y's slot meanwhile; beta dA_kk
+            // staged in T's slot (read from there only), dA_kk to the scratch
+            const int sy = S.sl0 == I_Y ? 0 : 1;
+            preload(S, sy, I_QK, 64, 128);
             if (quarter < 2) {
                 const int r = ch;
                 float d16[16], bd[16];
@@ -992,17 +1023,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     part += d16[j] * s_kk[s * 64 + r];
                 }
                 s_dbp[(4 + grp) * kC + r] = part;
-                uint8_t *sk = slot_ptr(S, S.sl0 == I_Y ? 0 : 1), *sb = slot_ptr(S, S.sl0 == I_Y ? 1 : 0);
-                put8(sk, img_half(I_DKK), 64, r, 16 * grp, d16);
-                put8(sk, img_half(I_DKK), 64, r, 16 * grp + 8, d16 + 8);
+                put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp, d16);
+                put8(img(I_DKK), img_half(I_DKK), 64, r, 16 * grp + 8, d16 + 8);
+                uint8_t *sb = slot_ptr(S, 1 - sy);
                 put8(sb, img_half(I_BDKK), 64, r, 16 * grp, bd);
                 put8(sb, img_half(I_BDKK), 64, r, 16 * grp + 8, bd + 8);
             }
-            {
-                const int sk = S.sl0 == I_Y ? 0 : 1;
-                stage_store(S, sk, I_DKK, 0, 64);
-                stage_store(S, 1 - sk, I_BDKK, 0, 64);
-            }
+            dirty(S, I_DKK);
+            stage_only(S, 1 - sy, I_BDKK, 0, 64);
 
             // ---- dKs^T += Kr^T (beta dA_kk) ; (dA_kk Ks)^T into C_R ----
             if (!product(S, {I_QK, 64, 1}, {I_BDKK, 0, 1}, tmem + C_S, 64, 4, true)) break;
