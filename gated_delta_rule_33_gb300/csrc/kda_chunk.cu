@@ -562,16 +562,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             const int Ln = static_cast<int>(tn >= t1 ? 0 : ((t1 - tn) < kC ? (t1 - tn) : kC));
 
             // ---- S2: D_A = [Qt; Kr] Ks^T ; next q/k loads ; previous chunk's output ----
-            if (tid == 0) {
+            if (warp == 0) {
+                // a converged warp issues faster than one lane of a divergent one
+                __syncwarp();
                 const uint32_t id = instr_desc(128, 64, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
                     const uint64_t ad = (d_qk + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
                     const uint64_t bd = (d_ks + static_cast<uint64_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ss(tmem + T_A, ad, bd, id, kk > 0);
+                    mma_tf32_ss_w(tmem + T_A, ad, bd, id, kk > 0);
                 }
-                mma_commit(bar_mma);
-                if (Ln > 0) issue_qk(tn);
+                mma_commit_w(bar_mma);
+                if (tid == 0 && Ln > 0) issue_qk(tn);
             }
             pend_mma = true;
             // warp 0 issues the products; warp 4 (same lane quarter) takes its rows
@@ -697,14 +699,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_after();
 
             // ---- S7: [O^T | U^T] += S_op [Qt ; -W']^T (O columns start at zero) ----
-            if (tid == 0) {
+            if (warp == 0) {
+                __syncwarp();
                 const uint32_t id = instr_desc(128, 128, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
                     const uint64_t bq = (d_qk + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_O, tmem + T_SOP + kk * 8, bq, id, 1);
+                    mma_tf32_ts_w(tmem + T_O, tmem + T_SOP + kk * 8, bq, id, 1);
                 }
-                mma_commit(bar_mma);
+                mma_commit_w(bar_mma);
             }
             pend_mma = true;
             // A_qk (K-major [r][s], zero above the diagonal) while MMA1/MMA2 run;
@@ -746,14 +749,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             tc_fence_after();
 
             // ---- S9: [S_acc^T | O^T] += U^T [Khat^T ; A_qk]^T ----
-            if (tid == 0) {
+            if (warp == 0) {
+                __syncwarp();
                 const uint32_t id = instr_desc(128, 192, kFmtTF32, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t bk = (d_kh + static_cast<uint64_t>(((kk >> 2) * 24576 + (kk & 3) * 32) >> 4));
-                    mma_tf32_ts(tmem + T_SACC, tmem + T_U + kk * 8, bk, id, 1);
+                    mma_tf32_ts_w(tmem + T_SACC, tmem + T_U + kk * 8, bk, id, 1);
                 }
-                mma_commit(bar_mma);
+                mma_commit_w(bar_mma);
             }
             // ---- S10: the product completes under the next chunk's operand
             // build, and this chunk's output is read out under the next MMA ----
