@@ -10,7 +10,8 @@ instead of running the forward again.
   the tokens before it, within the prefill's state bound (1e-3 relative L2).
 - The checkpointed backward writes the same gradients as the self-contained
   kda_chunk_backward, bit for bit, and so stays within that test's bound of
-  the oracle's reverse mode (checked here too on one varlen case).
+  the oracle's reverse mode (checked here too on two varlen cases: bf16 dO
+  with empty sequences, and fp32 dO with a query scale and ragged tails).
 - A (sequence, head) whose chunk had to be shortened is marked in the flags
   and the backward reports KDA_ERR_DECAY_RANGE with zero gradients for it."""
 import numpy as np
@@ -84,11 +85,15 @@ def test_prefill_checkpointed_matches_prefill_and_the_oracle_states(lib, lens, H
                                     scale=0.7, initial_state=S, nthreads=4)
 
 
-def test_backward_checkpointed_matches_backward_and_the_oracle(lib):
-    x, dO, dSf = make_case(lens=[0, 1, 17, 130, 64, 33, 0, 5], H=2, seed=3)
+@pytest.mark.parametrize("lens,do_dtype,scale", [
+    ([0, 1, 17, 130, 64, 33, 0, 5], torch.bfloat16, 128 ** -0.5),
+    ([300, 1, 64, 127], torch.float32, 0.8),
+])
+def test_backward_checkpointed_matches_backward_and_the_oracle(lib, lens, do_dtype, scale):
+    x, dO, dSf = make_case(lens=lens, H=2, seed=3)
+    dO = dO.to(do_dtype)
     q, k, v, cu, S0 = device_args(x)
     g, beta = gpu_gate(lib, x)
-    scale = 128 ** -0.5
     _, _, ckpt = lib.prefill_checkpointed(q, k, v, g, beta, cu_seqlens=cu, scale=scale,
                                           initial_state=S0)
     a = lib.backward_from_checkpoints(q, k, v, g, beta, dO.to(DEV), ckpt, cu_seqlens=cu,
