@@ -16,8 +16,12 @@
 // w, w+8, ..., w+120 and lane l owns columns 4l..4l+3, so each warp-wide 16-byte
 // load or store moves one contiguous 512-byte state row.  The 64 KB state stays
 // in registers (16 float4 per thread) between the column reductions and the
-// write, so HBM sees exactly one read and one write of it.
+// write, so HBM sees exactly one read and one write of it.  A bf16 state (32 KB)
+// is staged in shared memory instead, by 16-byte cp.async: it holds no
+// registers, so six CTAs share an SM and their loads keep more bytes in flight
+// than register-held states could.
 #include "kda_gate_spec.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
@@ -27,9 +31,8 @@ constexpr int kThreads = 256;
 constexpr int kRowsPerThread = kD / (kThreads / 32);  // 16
 
 // The thread's 16 x 4 state elements between the two passes of a step: fp32
-// values, or the raw bf16 pairs as loaded (half the registers, so twice the
-// CTAs per SM and twice the state bytes in flight; the values are widened
-// again where used).
+// values in registers, or a bf16 state read from its copy in shared memory
+// (widened where used).
 template <bool kStateBf16>
 struct StateRegs;
 
@@ -47,13 +50,11 @@ struct StateRegs<false> {
 
 template <>
 struct StateRegs<true> {
-    uint2 v[kRowsPerThread];
-    __device__ __forceinline__ void load(int i, const void *S, int64_t idx) {
-        v[i] = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(S) + idx));
-    }
+    const uint2 *sp;  // this thread's columns of row `warp` of the staged state
     __device__ __forceinline__ float4 get(int i) const {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i].x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i].y));
+        const uint2 raw = sp[i * 8 * (kD / 4)];  // row warp + 8 i
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
         return make_float4(a.x, a.y, b.x, b.y);
     }
     __device__ __forceinline__ void store(void *S, int64_t idx, float4 x) const {
@@ -82,7 +83,7 @@ struct DecodeGate {
 // pool slot slots[b] (negative: inactive sequence, nothing read or written,
 // o = 0; >= num_slots: a device error, skipped); without it, slot b.
 template <bool kOutBf16, bool kStateBf16, bool kGate>
-__global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
+__global__ void __launch_bounds__(kThreads, kStateBf16 ? 6 : 2) decode_kernel(
     const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
     const float *__restrict__ beta, const DecodeGate gt, void *__restrict__ state,
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
     __shared__ __align__(16) float s_u[kD];                   // read as float4
     __shared__ __align__(16) float s_red[2][kThreads / 32][kD];   // written as float4
     __shared__ float s_kq, s_beta;
+    __shared__ __align__(16) uint8_t s_state[kStateBf16 ? kD * kD * 2 : 16];
 
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -114,8 +116,16 @@ __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
 
     // Issue the whole state read first: the full state in flight per CTA.
     StateRegs<kStateBf16> s;
+    if constexpr (kStateBf16) {
+        const uint8_t *src = static_cast<const uint8_t *>(state) + sbase * 2;
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) s.load(i, state, sbase + (warp + 8 * i) * kD + 4 * lane);
+        for (int j = 0; j < kD * kD * 2 / 16 / kThreads; ++j)
+            sm100::cp_async_16(s_state + (tid + kThreads * j) * 16, src + (tid + kThreads * j) * 16, true);
+        s.sp = reinterpret_cast<const uint2 *>(s_state) + warp * (kD / 4) + lane;
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) s.load(i, state, sbase + (warp + 8 * i) * kD + 4 * lane);
+    }
 
     if (tid < kD) {
         const int64_t idx = bh * kD + tid;
@@ -141,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, kStateBf16 ? 3 : 2) decode_kernel(
             s_beta = gate_sigmoid(bl);
         }
     }
+    if constexpr (kStateBf16) sm100::cp_async_wait_all();
     __syncthreads();
 
     if (warp == 0) {  // scale * k.q
