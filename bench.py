@@ -146,12 +146,12 @@ NCU_TRAFFIC = {
                            "8881aa469733f65a4c014ed9f4f0aa68c6f6518704b09fe54617047b32840e72",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
-    "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.26e6,
-               "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
+    "decode": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 754.03e6,
+               "sha256": ["68f5f05ba5aab124309cb1ad3f458a194b6ceada7c9f575cd296d72aa540af8c",
                           "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                "note": "B=64 capture x 4 (profiles/decode_B64_H96.md)"},
-    "decode_pool": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 354.09e6,
-                    "sha256": ["5d57b93248a30cb3864f4d6e2455b7d3c79335368e47cd7d226c8da58479cc9d",
+    "decode_pool": {"src": ["kda_decode.cu", "kda_gate_spec.cuh"], "bytes": 4 * 350.96e6,
+                    "sha256": ["68f5f05ba5aab124309cb1ad3f458a194b6ceada7c9f575cd296d72aa540af8c",
                                "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
     "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh", "kda_gate_spec_x2.cuh", "kda_f32x2.cuh"],
