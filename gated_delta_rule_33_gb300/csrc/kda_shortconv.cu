@@ -21,7 +21,9 @@
 // inside one sequence, requesting 4 rows at a time; the rows two batches
 // ahead are brought into L2 by bulk prefetches, so each load waits on L2
 // rather than HBM (the taps and the three-token halo before the first row are
-// loaded once per segment).
+// loaded once per segment).  The arithmetic runs on packed pairs of channels
+// (f32x2 instructions, each the IEEE operation on both halves).
+#include "kda_f32x2.cuh"
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -52,73 +54,98 @@ __device__ __forceinline__ T pick(const T (&a)[3], int z) {
     return z == 0 ? a[0] : (z == 1 ? a[1] : a[2]);
 }
 
-__device__ __forceinline__ void unpack_row(uint4 raw, float (&r)[kLaneCh]) {
+constexpr int kLanePairs = kLaneCh / 2;   // channel pairs per lane
+using Pair = uint64_t;                     // two fp32 values: channels 2i, 2i + 1
+
+// The 8 bf16 channels of a 16-byte row piece as 4 packed pairs.
+__device__ __forceinline__ void unpack_row(uint4 raw, Pair (&r)[kLanePairs]) {
     const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[i]));
-        r[2 * i] = f.x;
-        r[2 * i + 1] = f.y;
-    }
+    for (int i = 0; i < kLanePairs; ++i)
+        r[i] = f2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xffff0000u));
 }
 
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&r)[kLaneCh]) {
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, Pair (&r)[kLanePairs]) {
     unpack_row(__ldcs(reinterpret_cast<const uint4 *>(p)), r);
 }
 
-__device__ __forceinline__ void store_row(__nv_bfloat16 *p, const float (&r)[kLaneCh]) {
+__device__ __forceinline__ void store_row(__nv_bfloat16 *p, const Pair (&r)[kLanePairs]) {
     uint32_t u[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(r[2 * i], r[2 * i + 1]);
+    for (int i = 0; i < kLanePairs; ++i) {
+        const float2 v = f2_split(r[i]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
         u[i] = *reinterpret_cast<const uint32_t *>(&b);
     }
     __stcs(reinterpret_cast<uint4 *>(p), make_uint4(u[0], u[1], u[2], u[3]));
 }
 
-__device__ __forceinline__ void zero_row(float (&r)[kLaneCh]) {
+__device__ __forceinline__ void zero_row(Pair (&r)[kLanePairs]) {
 #pragma unroll
-    for (int i = 0; i < kLaneCh; ++i) r[i] = 0.f;
+    for (int i = 0; i < kLanePairs; ++i) r[i] = 0ull;
 }
 
+// w[i][j]: tap j of channels 2i and 2i + 1.
 __device__ __forceinline__ void load_taps(const float *wz, int c, bool active,
-                                          float (&w)[kLaneCh][kTaps]) {
+                                          Pair (&w)[kLanePairs][kTaps]) {
     if (active) {
         const float4 *w4 = reinterpret_cast<const float4 *>(wz + static_cast<int64_t>(c) * kTaps);
 #pragma unroll
-        for (int i = 0; i < kLaneCh; ++i) {
-            const float4 t = __ldg(w4 + i);
-            w[i][0] = t.x; w[i][1] = t.y; w[i][2] = t.z; w[i][3] = t.w;
+        for (int i = 0; i < kLanePairs; ++i) {
+            const float4 a = __ldg(w4 + 2 * i), b = __ldg(w4 + 2 * i + 1);
+            w[i][0] = f2(a.x, b.x);
+            w[i][1] = f2(a.y, b.y);
+            w[i][2] = f2(a.z, b.z);
+            w[i][3] = f2(a.w, b.w);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kLaneCh; ++i) w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0.f;
+        for (int i = 0; i < kLanePairs; ++i) w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0ull;
     }
 }
 
-// One output row: the 4-tap convolution, SiLU and, for q and k, the head norm.
-// All 32 lanes must call it together (the norm shuffles within 16-lane halves).
-__device__ __forceinline__ void conv_row(const float (&w)[kLaneCh][kTaps],
-                                         const float (&win)[kHalo][kLaneCh],
-                                         const float (&xt)[kLaneCh], bool norm,
-                                         float (&out)[kLaneCh]) {
-    float ss = 0.f;
+// 2^x and 1/x on the special-function unit.
+__device__ __forceinline__ float sfu_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sfu_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One output row: the 4-tap convolution, SiLU (a / (1 + e^-a), with e^-a as
+// 2^(-a log2 e)) and, for q and k, the head norm.  All 32 lanes must call it
+// together (the norm shuffles within 16-lane halves).
+__device__ __forceinline__ void conv_row(const Pair (&w)[kLanePairs][kTaps],
+                                         const Pair (&win)[kHalo][kLanePairs],
+                                         const Pair (&xt)[kLanePairs], bool norm,
+                                         Pair (&out)[kLanePairs]) {
+    const Pair nl2e = f2(-1.4426950408889634f, -1.4426950408889634f), one = f2(1.f, 1.f);
+    Pair ss2 = 0ull;
 #pragma unroll
-    for (int i = 0; i < kLaneCh; ++i) {
-        float a = w[i][0] * win[0][i];
-        a = fmaf(w[i][1], win[1][i], a);
-        a = fmaf(w[i][2], win[2][i], a);
-        a = fmaf(w[i][3], xt[i], a);
-        const float y = __fdividef(a, 1.f + __expf(-a));
+    for (int i = 0; i < kLanePairs; ++i) {
+        Pair a = f2_mul(w[i][0], win[0][i]);
+        a = f2_fma(w[i][1], win[1][i], a);
+        a = f2_fma(w[i][2], win[2][i], a);
+        a = f2_fma(w[i][3], xt[i], a);
+        const float2 t = f2_split(f2_mul(a, nl2e));
+        const float2 d = f2_split(f2_add(one, f2(sfu_exp2(t.x), sfu_exp2(t.y))));
+        const Pair y = f2_mul(a, f2(sfu_rcp(d.x), sfu_rcp(d.y)));
         out[i] = y;
-        ss = fmaf(y, y, ss);
+        ss2 = f2_fma(y, y, ss2);
     }
     if (norm) {
+        const float2 sp = f2_split(ss2);
+        float ss = sp.x + sp.y;
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float inv = rsqrtf(ss + kNormEps);
+        const Pair inv2 = f2(inv, inv);
 #pragma unroll
-        for (int i = 0; i < kLaneCh; ++i) out[i] *= inv;
+        for (int i = 0; i < kLanePairs; ++i) out[i] = f2_mul(out[i], inv2);
     }
 }
 
@@ -169,7 +196,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) short_conv_kernel(
         for (int s = 0; s < B && seq_end(s) <= 0; ++s) pass_state(s);
     if (t_begin >= t_end) return;
 
-    float w[kLaneCh][kTaps];
+    Pair w[kLanePairs][kTaps];
     load_taps(pick(io.w, z), c, active, w);
 
     // The sequence holding t_begin: the first s with cu[s + 1] > t_begin.
@@ -184,7 +211,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) short_conv_kernel(
     }
 
     // Window rows 0..2 hold positions t-3, t-2, t-1 of the current sequence.
-    float win[kHalo][kLaneCh];
+    Pair win[kHalo][kLanePairs];
     auto load_window = [&](int64_t t, int seq) {
         const int64_t start = seq_start(seq);
 #pragma unroll
@@ -232,14 +259,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) short_conv_kernel(
                              : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
-                float xt[kLaneCh], out[kLaneCh];
+                Pair xt[kLanePairs], out[kLanePairs];
                 unpack_row(raw[j], xt);
                 conv_row(w, win, xt, norm, out);
                 if (active && tb + j < b) store_row(y + (tb + j) * C + c, out);
                 // (rows past the segment only shift the window, which the
                 // next segment reloads)
 #pragma unroll
-                for (int i = 0; i < kLaneCh; ++i) {
+                for (int i = 0; i < kLanePairs; ++i) {
                     win[0][i] = win[1][i];
                     win[1][i] = win[2][i];
                     win[2][i] = xt[i];
@@ -273,12 +300,12 @@ __global__ void __launch_bounds__(kWarps * 32) short_conv_step_kernel(
     if (sl < 0 || sl >= num_slots) {
         if (sl >= num_slots && threadIdx.x == 0 && blockIdx.x == 0 && z == 0)
             record_device_error(err, kDevInvalidArg);
-        float zero[kLaneCh];
+        Pair zero[kLanePairs];
         zero_row(zero);
         if (active) store_row(y, zero);
         return;
     }
-    float w[kLaneCh][kTaps], win[kHalo][kLaneCh], xt[kLaneCh], out[kLaneCh];
+    Pair w[kLanePairs][kTaps], win[kHalo][kLanePairs], xt[kLanePairs], out[kLanePairs];
     load_taps(pick(io.w, z), c, active, w);
     if (active) {
 #pragma unroll
