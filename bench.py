@@ -161,8 +161,8 @@ NCU_TRAFFIC = {
                         "3d6b65a9dfcc8c2e0ff562dd93aa28c5dad21e08b1edd9f0bffbe9f00f47dcfd",
                         "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
              "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
-    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 552.06e6,
-                   "sha256": ["094b0cd14e6dc076b32a65ea2c43e303f58b69df86299636d303604ef5ecdea3"],
+    "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 552.45e6,
+                   "sha256": ["d69ef349b594f9f5be7de9855c96ce080dc0c0fb1d58e2a9aa31d2fd7cc2d4a6"],
                    "note": "T=4096 capture (profiles/short_conv_T4096_H96.md)"},
     "backward": {"src": ["kda_backward.cu"], "bytes": 16 * 2.067e9,
                  "sha256": ["58f242b881fc2d1b1acb1532ced68f7c8a83e5dd92b3b19f71833997525eacc1"],
