@@ -607,6 +607,58 @@ def run_ours(args):
         warmup=3, iters=10, repeats=3)
     del bgrads, bws, bdO, ckpt, kws
 
+    # the other prefill configurations of the hot path: a varlen batch of 8
+    # sequences (lengths uniform in [512, 8192], partial tail chunks) and one
+    # long sequence (T = 65536, nonzero initial state) followed by 128
+    # one-token decode steps from its final state
+    vx = synth.make_inputs(lengths=synth.varlen_lengths(8, 512, 8192, seed=3), H=H, D=D,
+                           seed=rank + 5, device=dev)
+    vo = torch.empty(vx.N, H, D, dtype=torch.bfloat16, device=dev)
+    vS = torch.empty(vx.B, H, D, D, device=dev)
+    vws = torch.empty(max(kda.kda_chunk_prefill_workspace_size(vx.N, vx.B, H), 16),
+                      dtype=torch.uint8, device=dev)
+    proto["prefill_varlen"] = protocol(
+        lambda: kda.kda_chunk_prefill_gated(vx.q, vx.k, vx.v, vx.f, vx.b, vx.A_log, vx.alog_mode,
+                                            vx.dt_bias, vx.cu_seqlens, 1.0, None, vS, vo, vws,
+                                            stream), warmup=3, iters=10, repeats=3)
+    varlen = {"sequences": vx.B, "tokens": vx.N,
+              "lengths": [int(a) for a in (vx.cu_seqlens[1:] - vx.cu_seqlens[:-1]).tolist()],
+              "ms": proto["prefill_varlen"]["mean_ms"],
+              "tokens_per_s": world * vx.N / (proto["prefill_varlen"]["mean_ms"] * 1e-3),
+              "protocol": proto["prefill_varlen"]}
+    del vx, vo, vS, vws
+    T_LONG = 65536
+    lx = synth.make_inputs(T_LONG, H=H, D=D, seed=rank + 6, s0_std=0.05, device=dev)
+    lo_ = torch.empty(T_LONG, H, D, dtype=torch.bfloat16, device=dev)
+    lS = torch.empty(1, H, D, D, device=dev)
+    lws = torch.empty(max(kda.kda_chunk_prefill_workspace_size(T_LONG, 1, H), 16),
+                      dtype=torch.uint8, device=dev)
+    proto["prefill_long"] = protocol(
+        lambda: kda.kda_chunk_prefill_gated(lx.q, lx.k, lx.v, lx.f, lx.b, lx.A_log, lx.alog_mode,
+                                            lx.dt_bias, None, 1.0, lx.initial_state, lS, lo_,
+                                            lws, stream), warmup=2, iters=5, repeats=3)
+    ld = synth.make_inputs(128, H=H, D=D, seed=rank + 7, device=dev)
+    lg = torch.empty(128, H, D, device=dev)
+    lbeta = torch.empty(128, H, device=dev)
+    kda.kda_gate_fused(ld.f, ld.b, ld.A_log, ld.alog_mode, ld.dt_bias, lg, lbeta, stream)
+    ldo = torch.empty(1, H, D, dtype=torch.bfloat16, device=dev)
+
+    def decode_128():
+        for t in range(128):
+            kda.kda_recurrent_decode(ld.q[t:t + 1], ld.k[t:t + 1], ld.v[t:t + 1], lg[t:t + 1],
+                                     lbeta[t:t + 1], lS, 1.0, ldo, stream)
+
+    proto["decode_after_long"] = protocol(decode_128, warmup=2, iters=3, repeats=3)
+    long_context = {"tokens": T_LONG, "ms": proto["prefill_long"]["mean_ms"],
+                    "tokens_per_s": world * T_LONG / (proto["prefill_long"]["mean_ms"] * 1e-3),
+                    "decode_steps": 128,
+                    "decode_ms_per_step": proto["decode_after_long"]["mean_ms"] / 128,
+                    "decode_note": "B=1: the 6.3 MB state stays in L2, so this is latency, "
+                                   "not an HBM figure",
+                    "protocol": {"prefill": proto["prefill_long"],
+                                 "decode_128_steps": proto["decode_after_long"]}}
+    del lx, lo_, lS, lws, ld, lg, lbeta, ldo
+
     prefill_leg_ms = max_over_ranks(fused_ms, world, dev)
     step_ms_max = max_over_ranks(step_ms, world, dev)
     decode_ms_max = max_over_ranks(decode_ms, world, dev)
@@ -808,6 +860,8 @@ def run_ours(args):
                       "decode_bf16_pool": rl_pool, "short_conv": rl_conv, "backward": rl_bwd,
                       "backward_chunked": rl_cbwd},
         "training": training,
+        "prefill_varlen": varlen,
+        "prefill_long_context": long_context,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "schedule": "steps pipelined over two buffer sets: H2D, prefill and D2H "
