@@ -304,6 +304,10 @@ struct Sched {
     int tid;
     int sl0, sl1;
     int lo0, hi0, lo1, hi1;  // the rows of its image each slot holds
+    // one more image per slot, in its own byte layout from an offset past the
+    // first image's (loaded under a product for the next one)
+    int xi0, xlo0, xhi0, xi1, xlo1, xhi1;
+    uint32_t xoff0, xoff1;
     uint32_t ph_mma;
     bool pend_mma;
     bool pend_copy;  // a preloaded operand's copies may still be in flight
@@ -314,21 +318,74 @@ struct OpSpec {
     int img, row0, mn;
 };
 
+__device__ __forceinline__ void clear_extra(Sched &S) {
+    S.xi0 = S.xi1 = -1;
+    S.xoff0 = S.xoff1 = 0;
+}
+
 __device__ __forceinline__ void dirty(Sched &S, int i) {
     if (S.sl0 == i) S.sl0 = -1;
     if (S.sl1 == i) S.sl1 = -1;
+    if (S.xi0 == i) S.xi0 = -1;
+    if (S.xi1 == i) S.xi1 = -1;
 }
 
 __device__ __forceinline__ uint8_t *slot_ptr(const Sched &S, int sl) {
     return S.smem + (sl ? SLOT_B : SLOT_A);
 }
 
-// Slot `sl` holds rows [lo, hi) of image i.
+// Slot `sl` holds rows [lo, hi) of image i (from its start); the images
+// placed further on that it overlaps are gone.
 __device__ __forceinline__ void set_slot(Sched &S, int sl, int i, int lo, int hi) {
     if (sl) {
         S.sl1 = i; S.lo1 = lo; S.hi1 = hi;
     } else {
         S.sl0 = i; S.lo0 = lo; S.hi0 = hi;
+    }
+    if (sl) {
+        if (S.xoff1 < img_bytes(i)) S.xi1 = -1;
+    } else {
+        if (S.xoff0 < img_bytes(i)) S.xi0 = -1;
+    }
+}
+
+// The slot holding rows [lo, hi) of image i and the byte offset of its
+// layout there (kExtra: the second images too), or -1.
+template <bool kExtra>
+__device__ __forceinline__ int find_img(const Sched &S, int i, int lo, int hi, uint32_t &off) {
+    off = 0;
+    if (S.sl0 == i && S.lo0 <= lo && hi <= S.hi0) return 0;
+    if (S.sl1 == i && S.lo1 <= lo && hi <= S.hi1) return 1;
+    if (kExtra) {
+        if (S.xi0 == i && S.xlo0 <= lo && hi <= S.xhi0) {
+            off = S.xoff0;
+            return 0;
+        }
+        if (S.xi1 == i && S.xlo1 <= lo && hi <= S.xhi1) {
+            off = S.xoff1;
+            return 1;
+        }
+    }
+    return -1;
+}
+
+// The slot holding image i (any of its rows, any placement), or -1.
+__device__ __forceinline__ int slot_of(const Sched &S, int i) {
+    uint32_t off;
+    return find_img<true>(S, i, 0x7fff, 0, off);
+}
+
+// Slot `sl` holds rows [lo, hi) of image i in the image's layout from byte
+// `off`; whatever it overlaps in the slot is gone.
+__device__ __forceinline__ void place_extra(Sched &S, int sl, int i, int lo, int hi, uint32_t off) {
+    const int p = sl ? S.sl1 : S.sl0;
+    if (p >= 0 && off < img_bytes(p)) {
+        if (sl) S.sl1 = -1; else S.sl0 = -1;
+    }
+    if (sl) {
+        S.xi1 = i; S.xlo1 = lo; S.xhi1 = hi; S.xoff1 = off;
+    } else {
+        S.xi0 = i; S.xlo0 = lo; S.xhi0 = hi; S.xoff0 = off;
     }
 }
 __device__ __forceinline__ bool slot_has(const Sched &S, int sl, int i, int lo, int hi) {
@@ -340,8 +397,9 @@ __device__ __forceinline__ bool slot_has(const Sched &S, int sl, int i, int lo, 
 // the image's byte layout; cp.async into the slot (load) or plain 16-byte
 // stores to the scratch (store).
 template <bool kLoad>
-__device__ __forceinline__ void copy_rows(const Sched &S, int sl, int i, uint32_t r0, uint32_t r1) {
-    uint8_t *slot = slot_ptr(S, sl);
+__device__ __forceinline__ void copy_rows(const Sched &S, int sl, int i, uint32_t r0, uint32_t r1,
+                                          uint32_t off = 0) {
+    uint8_t *slot = slot_ptr(S, sl) + off;
     uint8_t *glob = S.scr + img_off(i);
     const uint32_t rows = img_rows(i);
     if (r0 == 0 && r1 == rows) {
@@ -394,6 +452,8 @@ __device__ __forceinline__ void stage_store(Sched &S, int sl, int i, uint32_t r0
         if (sl && S.sl0 == i) S.sl0 = -1;
         if (!sl && S.sl1 == i) S.sl1 = -1;
     }
+    if (S.xi0 == i) S.xi0 = -1;
+    if (S.xi1 == i) S.xi1 = -1;
 }
 
 // As stage_store for an image that only the next products read, from the
@@ -407,12 +467,24 @@ __device__ __forceinline__ void stage_only(Sched &S, int sl, int i, int r0, int 
     set_slot(S, sl, i, r0, r1);
 }
 
+// An operand image to bring in while a product runs, for the products after
+// it: rows [lo, hi) of image img, in its own layout from byte `off` of the
+// slot that holds the product's A (rel 0) or B (rel 1) operand, or of the slot
+// the product does not read (rel 2, for a product whose operands share one).
+struct Pre {
+    int img, lo, hi, rel;
+    uint32_t off;
+};
+
 // One product term, D[tmem d] (+)= A B: copies the operand images that are not
-// already in a slot (a slot keeps its image until it is reused or the image is
-// rewritten), issues the MMAs from thread 0 and waits for them.  Returns
-// false when a wait ran out (the CTA is aborting).
+// already in a slot (a slot keeps its images until they are overwritten or
+// rewritten), issues the MMAs from warp 0, starts the copies of `pre` while
+// they run, and waits for the MMAs.  Returns false when a wait ran out (the
+// CTA is aborting).
+template <bool kExtra = false>
 __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d, uint32_t N,
-                                     int ksteps, bool accumulate, int a_lo = 0, int a_hi = 128) {
+                                     int ksteps, bool accumulate, int a_lo = 0, int a_hi = 128,
+                                     const Pre *pre = nullptr) {
     const int ia = A.img, ib = B.img;
     // the rows each operand reads: K rows for an MN-major operand, the M rows
     // whose results are used (a_lo .. a_hi) for A, N rows for B
@@ -424,17 +496,23 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
         alo = blo = min(alo, blo);
         ahi = bhi = max(ahi, bhi);
     }
-    int pa = slot_has(S, 0, ia, alo, ahi) ? 0 : slot_has(S, 1, ia, alo, ahi) ? 1 : -1;
-    int pb = slot_has(S, 0, ib, blo, bhi) ? 0 : slot_has(S, 1, ib, blo, bhi) ? 1 : -1;
+    uint32_t fa, fb;  // byte offsets of the operands' layouts in their slots
+    int pa = find_img<kExtra>(S, ia, alo, ahi, fa);
+    int pb = find_img<kExtra>(S, ib, blo, bhi, fb);
     int la = -1, lb = -1;
-    if (pa < 0) {
+    if (pa < 0) {  // loaded at the start of the slot the other operand is not in
         pa = (pb == 0) ? 1 : 0;
         la = pa;
+        fa = 0;
     }
-    if (ib == ia) pb = pa;
+    if (ib == ia) {
+        pb = pa;
+        fb = fa;
+    }
     if (pb < 0) {
         pb = (pa == 0) ? 1 : 0;
         lb = pb;
+        fb = 0;
     }
     if (la >= 0 || lb >= 0 || S.pend_copy) {
         // the rows it reads of each image not in a slot, by cp.async (the
@@ -451,9 +529,16 @@ __device__ __forceinline__ bool product(Sched &S, OpSpec A, OpSpec B, uint32_t d
     }
     if (S.tid < 32) {
         __syncwarp();
-        issue(d, opd(pa ? S.sb : S.sa, ia, A.row0, A.mn != 0), opd(pb ? S.sb : S.sa, ib, B.row0, B.mn != 0),
-              N, ksteps, accumulate);
+        issue(d, opd((pa ? S.sb : S.sa) + fa, ia, A.row0, A.mn != 0),
+              opd((pb ? S.sb : S.sa) + fb, ib, B.row0, B.mn != 0), N, ksteps, accumulate);
         mma_commit_w(S.bar_mma);
+    }
+    if (pre != nullptr) {  // into bytes of the slots this product does not read
+        const int sl = pre->rel == 0 ? pa : pre->rel == 1 ? pb : 1 - pa;
+        copy_rows<true>(S, sl, pre->img, static_cast<uint32_t>(pre->lo), static_cast<uint32_t>(pre->hi),
+                        pre->off);
+        place_extra(S, sl, pre->img, pre->lo, pre->hi, pre->off);
+        S.pend_copy = true;
     }
     S.pend_mma = true;
     if (!cta_wait(S.bar_mma, S.ph_mma & 1, S.abort_flag, S.err, S.tid, S.polls)) return false;
@@ -530,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
     S.sb = sb;
     S.tid = tid;
     S.sl0 = S.sl1 = -1;
+    clear_extra(S);
     S.lo0 = S.hi0 = S.lo1 = S.hi1 = 0;
     S.ph_mma = 0;
     S.pend_mma = false;
@@ -582,6 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             const int L = static_cast<int>((t1 - tc) < kC ? (t1 - tc) : kC);
             const float *Sc = p.ckpt + ((slot0 + c) * H + h) * (kD * kD);
             S.sl0 = S.sl1 = -1;  // every image is rewritten for this chunk
+            clear_extra(S);
             // ---- B0: the chunk's rows into shared memory by 16-byte cp.async
             // (rows past the sequence zero-filled): g and dO to slot A, q to the
             // A_kk area (free until the D_A epilogue), k and v to the staging
@@ -873,9 +960,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
 
             // ---- dU^T = dS'^T Kh + dO^T A_qk ; dU into rows 0-63 of DU2, which
             // stays in its slot ----
-            if (!product(S, {I_DS, 0, 0}, {I_KH, 0, 0}, tmem + C_TA, 64, 8, false)) break;
-            if (!product(S, {I_DU2, 64, 1}, {I_AQ, 0, 1}, tmem + C_TA, 64, 4, true)) break;
-            preload(S, S.sl0 == I_AQ ? 0 : 1, I_QK, 0, 64);
+            {
+                // A_qk for the next product into Kh's slot, past Kh (32 KB)
+                const Pre pre_aq{I_AQ, 0, 64, 1, 32768};
+                if (!product(S, {I_DS, 0, 0}, {I_KH, 0, 0}, tmem + C_TA, 64, 8, false, 0, 128, &pre_aq))
+                    break;
+            }
+            if (!product<true>(S, {I_DU2, 64, 1}, {I_AQ, 0, 1}, tmem + C_TA, 64, 4, true)) break;
+            preload(S, slot_of(S, I_AQ), I_QK, 0, 64);
             {
                 const int sl = (S.sl0 == I_DU2) ? 0 : 1;
                 float d16[16];
@@ -928,9 +1020,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             // ---- [-dW'^T | dQt^T] = S_op [dU; dO]^T (DU2 still in its slot) ;
             // dKs^T = Qt^T dA_qk ; dQt^T += Ks^T dA_qk^T ----
             if (!product(S, {I_SO, 0, 1}, {I_DU2, 0, 0}, tmem + C_TA, 128, 8, false)) break;
-            if (!product(S, {I_QK, 0, 1}, {I_DAQ, 0, 1}, tmem + C_S, 64, 4, false)) break;
-            if (!product(S, {I_KS, 0, 1}, {I_DAQ, 0, 0}, tmem + C_TB, 64, 4, true)) break;
-            preload(S, S.sl0 == I_KS ? 0 : 1, I_DS, 0, 128);
+            {
+                // Ks for the next product into dA_qk's slot, past dA_qk (16 KB)
+                const Pre pre_ks{I_KS, 0, 64, 1, 16384};
+                if (!product(S, {I_QK, 0, 1}, {I_DAQ, 0, 1}, tmem + C_S, 64, 4, false, 0, 128, &pre_ks))
+                    break;
+            }
+            if (!product<true>(S, {I_KS, 0, 1}, {I_DAQ, 0, 0}, tmem + C_TB, 64, 4, true)) break;
+            preload(S, 1 - slot_of(S, I_DAQ), I_DS, 0, 128);
             {
                 // -dW'^T[k = ch][r]: dW'[r][k] into rows 0-63 of the QK image (Qt is
                 // dead), staged in the slot dA_qk used
@@ -948,8 +1045,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             if (!product(S, {I_DS, 0, 1}, {I_UT, 0, 1}, tmem + C_H, 64, 8, false)) break;
 
             // ---- dT = (dW' Kr^T + dU V^T) diag(beta) (lanes 0-63) ----
-            if (!product(S, {I_QK, 0, 0}, {I_QK, 64, 0}, tmem + C_TA, 64, 8, false, 0, 64)) break;  // lanes 0-63
-            if (!product(S, {I_DU2, 0, 0}, {I_V, 0, 0}, tmem + C_TA, 64, 8, true, 0, 64)) break;  // lanes 0-63
+            {
+                // v for the next product into the other slot, at 48 KB (its
+                // images are dead)
+                const Pre pre_v{I_V, 0, 64, 2, 49152};
+                if (!product(S, {I_QK, 0, 0}, {I_QK, 64, 0}, tmem + C_TA, 64, 8, false, 0, 64, &pre_v))
+                    break;  // lanes 0-63
+            }
+            if (!product<true>(S, {I_DU2, 0, 0}, {I_V, 0, 0}, tmem + C_TA, 64, 8, true, 0, 64)) break;  // lanes 0-63
             preload(S, S.sl0 == I_DU2 ? 0 : 1, I_QK, 0, 64);
             if (quarter < 2) {
                 float d16[16];
@@ -957,10 +1060,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) d16[j] *= s_beta[16 * grp + j];
-                put8(slot_ptr(S, S.sl0 == I_V ? 0 : 1), img_half(I_DT), 64, ch, 16 * grp, d16);
-                put8(slot_ptr(S, S.sl0 == I_V ? 0 : 1), img_half(I_DT), 64, ch, 16 * grp + 8, d16 + 8);
+                put8(slot_ptr(S, slot_of(S, I_V)), img_half(I_DT), 64, ch, 16 * grp, d16);
+                put8(slot_ptr(S, slot_of(S, I_V)), img_half(I_DT), 64, ch, 16 * grp + 8, d16 + 8);
             }
-            stage_store(S, S.sl0 == I_V ? 0 : 1, I_DT, 0, 64);
+            stage_store(S, slot_of(S, I_V), I_DT, 0, 64);
 
             // ---- d(beta Kr)^T = dW'^T T and d(beta V)^T = dU^T T ----
             if (!product(S, {I_QK, 0, 1}, {I_T, 0, 1}, tmem + C_R, 64, 4, false)) break;
@@ -1033,8 +1136,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
             stage_only(S, 1 - sy, I_BDKK, 0, 64);
 
             // ---- dKs^T += Kr^T (beta dA_kk) ; (dA_kk Ks)^T into C_R ----
-            if (!product(S, {I_QK, 64, 1}, {I_BDKK, 0, 1}, tmem + C_S, 64, 4, true)) break;
-            if (!product(S, {I_KS, 0, 1}, {I_DKK, 0, 0}, tmem + C_R, 64, 4, true)) break;
+            {
+                // Ks for the next product into beta dA_kk's slot, past it (16 KB)
+                const Pre pre_ks2{I_KS, 0, 64, 1, 16384};
+                if (!product(S, {I_QK, 64, 1}, {I_BDKK, 0, 1}, tmem + C_S, 64, 4, true, 0, 128, &pre_ks2))
+                    break;
+            }
+            if (!product<true>(S, {I_KS, 0, 1}, {I_DKK, 0, 0}, tmem + C_R, 64, 4, true)) break;
 
             // ---- assembly: dq, dk, dg, dbeta (lane k = ch, rows r = 16 grp + j) ----
             cp_async_wait_all();  // q staged after the inverse
