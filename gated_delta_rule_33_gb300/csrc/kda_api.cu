@@ -600,6 +600,18 @@ kda_status kda_chunk_backward_checkpointed(const void *q, const void *k, const v
         dev->error_word, static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_debug_check_gate_division(uint64_t *mismatches, void *stream) {
+    if (mismatches == nullptr) return KDA_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    kda_status st = current_device(&dev);
+    if (st != KDA_OK) return st;
+    unsigned long long n = 0;
+    st = from_cuda(kda::check_gate_division(&n, dev->num_sms, static_cast<cudaStream_t>(stream)));
+    if (st != KDA_OK) return st;
+    *mismatches = static_cast<uint64_t>(n);
+    return KDA_OK;
+}
+
 kda_status kda_debug_set_wait_limit(int64_t copy_polls, int64_t product_polls) {
     kda::set_prefill_wait_polls(copy_polls, product_polls);
     return KDA_OK;

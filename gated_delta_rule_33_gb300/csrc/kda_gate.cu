@@ -138,4 +138,63 @@ cudaError_t launch_gate(const void *f, bool f_bf16, const void *b, bool b_bf16,
     return cudaGetLastError();
 }
 
+namespace {
+
+__device__ unsigned long long g_division_mismatches;
+
+// Every operand pair of the two divisions in the gate's common path, through
+// div2_common, against IEEE division: index i < kY runs y over every normal
+// binary32 value in [2^-126, 1] (a = y - (u - 1), b = u = 1 + y, as formed
+// there); the rest runs u over every binary32 value in [1, 2] (a = f, b = 2 + f
+// with f = u - 1, or u / 2 - 1 above sqrt 2).  Consecutive indices make the
+// pairs of the packed division.
+constexpr uint32_t kYLo = 0x00800000u, kYHi = 0x3f800000u;   // 2^-126 .. 1
+constexpr uint32_t kULo = 0x3f800000u, kUHi = 0x40000000u;   // [1, 2]
+constexpr int64_t kY = kYHi - kYLo + 1, kU = kUHi - kULo + 1;
+
+__device__ __forceinline__ void division_operands(int64_t i, float &a, float &b) {
+    if (i < kY) {
+        const float y = __uint_as_float(kYLo + static_cast<uint32_t>(i));
+        const float u = __fadd_rn(1.0f, y);
+        a = __fsub_rn(y, __fsub_rn(u, 1.0f));
+        b = u;
+    } else {
+        const float u = __uint_as_float(kULo + static_cast<uint32_t>(i - kY));
+        const float f = __fsub_rn(__fmul_rn(u, u > 0x1.6a09e6p+0f ? 0.5f : 1.0f), 1.0f);
+        a = f;
+        b = __fadd_rn(2.0f, f);
+    }
+}
+
+__global__ void __launch_bounds__(256) gate_division_check_kernel() {
+    unsigned long long bad = 0;
+    const int64_t n = kY + kU;
+    for (int64_t i = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x); i < n;
+         i += 2 * static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float a0, b0, a1 = 1.0f, b1 = 1.0f;
+        division_operands(i, a0, b0);
+        if (i + 1 < n) division_operands(i + 1, a1, b1);
+        const float2 q = f2_split(div2_common(f2(a0, a1), f2(b0, b1)));
+        if (__float_as_uint(q.x) != __float_as_uint(__fdiv_rn(a0, b0))) ++bad;
+        if (i + 1 < n && __float_as_uint(q.y) != __float_as_uint(__fdiv_rn(a1, b1))) ++bad;
+    }
+    if (bad != 0) atomicAdd(&g_division_mismatches, bad);
+}
+
+}  // namespace
+
+cudaError_t check_gate_division(unsigned long long *mismatches, int num_sms, cudaStream_t s) {
+    const unsigned long long zero = 0;
+    cudaError_t e = cudaMemcpyToSymbolAsync(g_division_mismatches, &zero, sizeof(zero), 0,
+                                            cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    gate_division_check_kernel<<<static_cast<unsigned>(num_sms) * 8, 256, 0, s>>>();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbolAsync(mismatches, g_division_mismatches, sizeof(*mismatches), 0,
+                                  cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(s);
+}
+
 }  // namespace kda

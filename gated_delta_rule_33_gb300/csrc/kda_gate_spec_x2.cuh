@@ -12,6 +12,28 @@ namespace gate_spec {
 // Two elements per instruction where the operation is +, -, x or fma;
 // divisions, conversions and the special cases per element.
 
+// a / b rounded to nearest even, for the divisions of the common path below
+// (a normal or +0, b in [1, 2.5], the quotient normal or +0), two at a time,
+// by Markstein's method (P. W. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): the
+// special-function unit's reciprocal refined by one Newton step, the quotient,
+// its remainder (exact in an fma) and one correction.  Over every operand pair
+// the common path can form, the result equals IEEE division bit for bit
+// (checked exhaustively on the device: kda_debug_check_gate_division).
+__device__ __forceinline__ float rcp_sfu(float b) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(b));
+    return y;
+}
+__device__ __forceinline__ uint64_t div2_common(uint64_t a, uint64_t b) {
+    const float2 bb = f2_split(b);
+    const uint64_t nb = f2(-bb.x, -bb.y);
+    const uint64_t y0 = f2(rcp_sfu(bb.x), rcp_sfu(bb.y));
+    const uint64_t y1 = f2_fma(y0, f2_fma(nb, y0, f2(1.0f, 1.0f)), y0);
+    const uint64_t q0 = f2_mul(a, y1);
+    return f2_fma(f2_fma(nb, q0, a), y1, q0);
+}
+
 __device__ __forceinline__ uint64_t gate_exp_x2(float x0, float x1) {
     const uint64_t x = f2(x0, x1);
     const uint64_t n_f = f2_sub(f2_fma(x, f2(0x1.715476p+0f, 0x1.715476p+0f), f2(0x1.8p23f, 0x1.8p23f)),
@@ -115,10 +137,9 @@ __device__ __forceinline__ uint64_t softplus_x2_common(float x0, float x1) {
     const bool h0 = u2.x > 0x1.6a09e6p+0f, h1 = u2.y > 0x1.6a09e6p+0f;
     const float e0 = h0 ? 1.0f : 0.0f, e1 = h1 ? 1.0f : 0.0f;
     const uint64_t f = f2_sub(f2_mul(u, f2(h0 ? 0.5f : 1.0f, h1 ? 0.5f : 1.0f)), one);
-    const float2 num = f2_split(f2_sub(y, f2_sub(u, one)));
-    const float2 fs = f2_split(f), den = f2_split(f2_add(f2(2.0f, 2.0f), f));
-    const float2 cp = make_float2(__fdiv_rn(num.x, u2.x), __fdiv_rn(num.y, u2.y));
-    const uint64_t s = f2(__fdiv_rn(fs.x, den.x), __fdiv_rn(fs.y, den.y));
+    const float2 fs = f2_split(f);
+    const float2 cp = f2_split(div2_common(f2_sub(y, f2_sub(u, one)), u));
+    const uint64_t s = div2_common(f, f2_add(f2(2.0f, 2.0f), f));
     const uint64_t z = f2_mul(s, s);
     uint64_t R = f2(0x1.745d18p-3f, 0x1.745d18p-3f);
     R = f2_fma(R, z, f2(0x1.c71c72p-3f, 0x1.c71c72p-3f));

@@ -34,6 +34,11 @@ cudaError_t launch_gate(const void *f, bool f_bf16, const void *b, bool b_bf16,
                         const float *A_log, int alog_mode, const float *dt_bias, float *g,
                         float *beta, int64_t N, int H, int K, int num_sms, cudaStream_t s);
 
+// Test hook: the gate's fast division against IEEE division over every operand
+// pair its common path forms; the count of differing results to *mismatches
+// (host), the stream synchronised.
+cudaError_t check_gate_division(unsigned long long *mismatches, int num_sms, cudaStream_t s);
+
 cudaError_t launch_decode(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, const float *g, const float *beta,
                           float *state, int B, int H, float scale, void *o, bool o_bf16,

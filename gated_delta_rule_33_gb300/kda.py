@@ -118,6 +118,8 @@ def load():
         lib.kda_gate_backward.argtypes = [P, I, P, I, P, I, P, P, P, P, P, P, P, I64, I, I, P,
                                           ctypes.c_size_t, P]
         lib.kda_gate_backward.restype = I
+        lib.kda_debug_check_gate_division.argtypes = [P, P]
+        lib.kda_debug_check_gate_division.restype = I
         lib.kda_debug_set_wait_limit.argtypes = [I64, I64]
         lib.kda_debug_set_wait_limit.restype = I
         lib.kda_get_last_device_error.argtypes = [P]
@@ -357,6 +359,15 @@ def kda_gate_backward(f, b, A_log, alog_mode, dt_bias, dg, dbeta, df, db, dA_log
         N, H, K, _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream, f.device))
     _check(st, "kda_gate_backward")
+
+
+def kda_debug_check_gate_division(stream=None) -> int:
+    """Differing results of the gate's fast division against IEEE division
+    over every operand pair of its common path (0: bit-exact)."""
+    n = ctypes.c_uint64(0)
+    _check(load().kda_debug_check_gate_division(ctypes.byref(n), _stream(stream)),
+           "kda_debug_check_gate_division")
+    return int(n.value)
 
 
 def kda_debug_set_wait_limit(copy_polls: int = -1, product_polls: int = -1):

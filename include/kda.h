@@ -524,6 +524,16 @@ kda_status kda_short_conv_qkv_step(const void *x_q, const void *x_k, const void 
                                    void *q, void *k, void *v, void *stream);
 
 /*
+ * kda_debug_check_gate_division -- test hook: the gate kernel's common path
+ * (|f + dt_bias| < 87) divides with an fma-based correctly rounded division
+ * (Markstein's method) instead of IEEE division; this call runs it against
+ * IEEE division on the device for every operand pair that path can form
+ * (about 1.07e9) and writes the number of differing results to *mismatches
+ * (host pointer; 0 is the gate's bit-exactness).  Synchronises `stream`.
+ */
+kda_status kda_debug_check_gate_division(uint64_t *mismatches, void *stream);
+
+/*
  * kda_debug_set_wait_limit -- test hook for the bounded device waits.  Every
  * wait of the chunked prefill kernels on a copy (TMA) or a tensor-core product
  * gives up after a bounded number of polls and records KDA_ERR_DEVICE_TIMEOUT

@@ -17,6 +17,14 @@ pytestmark = pytest.mark.gpu
 
 # --- gate -----------------------------------------------------------------------------------
 
+def test_gate_fast_division_is_ieee_division(lib):
+    """The gate kernel's common path divides by Markstein's method (an fma
+    correction of a refined reciprocal) instead of IEEE division; over every
+    operand pair that path can form (about 1.07e9) the quotients are the same
+    bits, so the gate stays bit-exact to its specification."""
+    assert lib.kda_debug_check_gate_division() == 0
+
+
 @pytest.mark.parametrize("mode", [synth.ALOG_PER_HEAD, synth.ALOG_PER_CHANNEL,
                                   synth.ALOG_PER_HEAD_CHANNEL])
 def test_gate_bit_exact_k3_shape(lib, mode):
