@@ -155,10 +155,10 @@ NCU_TRAFFIC = {
                                "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816"],
                     "note": "B=64 capture x 4 (profiles/decode_bf16_pool_B64_H96.md)"},
     "gate": {"src": ["kda_gate.cu", "kda_gate_spec.cuh", "kda_gate_spec_x2.cuh", "kda_f32x2.cuh"],
-             "bytes": 246.82e6,
-             "sha256": ["eb300c819670ac1a050c42847653314c1bb80e16d967403f83c881ac23a979d1",
+             "bytes": 246.59e6,
+             "sha256": ["b2531cbc98d87995bf0d28e746d0b8e2bc9fe32797688b40f6fbf14c0f35f229",
                         "8aed1e00efe29355e1843f1ca8a41b9485b9cc3ac211f3cdca9a9c6f7ba36816",
-                        "3d6b65a9dfcc8c2e0ff562dd93aa28c5dad21e08b1edd9f0bffbe9f00f47dcfd",
+                        "778d78a20aa1906029a458cd4637581380c9c9720ad6861eb5dfc943faf9199d",
                         "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
              "note": "T=4096 capture (profiles/gate_T4096_H96.md)"},
     "short_conv": {"src": ["kda_shortconv.cu"], "bytes": 552.45e6,
