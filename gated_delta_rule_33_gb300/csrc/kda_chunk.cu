@@ -839,10 +839,14 @@ cudaError_t launch_chunk(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const _
                                                   static_cast<int>(kSmemAlloc));
     if (ea != cudaSuccess) return ea;
     CUtensorMap mq, mk, mv, mg;
+    // With no tokens no tile is ever loaded (every chain is empty), but a map
+    // needs a valid aligned address: the chain counter's stands in for the
+    // token tensors, which may then be absent.
     const int64_t Nmap = p.N > 0 ? p.N : 1;
-    if (!make_map(&mq, q, Nmap, p.H, 128, false) || !make_map(&mk, k, Nmap, p.H, 128, false) ||
-        !make_map(&mv, v, Nmap, p.H, 64, true) ||
-        !make_map(&mg, g_or_f, Nmap, p.H, 128, false, !kGate))
+    auto at = [&](const void *t) -> const void * { return p.N > 0 ? t : p.counter; };
+    if (!make_map(&mq, at(q), Nmap, p.H, 128, false) || !make_map(&mk, at(k), Nmap, p.H, 128, false) ||
+        !make_map(&mv, at(v), Nmap, p.H, 64, true) ||
+        !make_map(&mg, at(g_or_f), Nmap, p.H, 128, false, !kGate))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;

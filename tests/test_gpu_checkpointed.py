@@ -152,3 +152,27 @@ def test_shortened_chunk_is_flagged_and_reported(lib):
     for name, ga, gr in zip(NAMES, a, ref):
         assert float(ga[:, 1].abs().max()) == 0.0, name
         assert torch.equal(ga[:, 0], gr[:, 0]), name
+
+
+def test_all_sequences_empty(lib):
+    """A batch whose sequences are all empty (N = 0): the prefills pass the
+    initial states through, and the backward passes dS_final through to dS0."""
+    x, dO, dSf = make_case(lens=[0, 0], H=2, seed=13)
+    q, k, v, cu, S0 = device_args(x)
+    g, beta = gpu_gate(lib, x)
+    o, Sf = lib.prefill(q, k, v, g, beta, cu_seqlens=cu, initial_state=S0)
+    o2, Sf2, ckpt = lib.prefill_checkpointed(q, k, v, g, beta, cu_seqlens=cu, initial_state=S0)
+    og, Sfg = lib.prefill_gated(q, k, v, x.f.to(DEV), x.b.to(DEV), x.A_log.to(DEV),
+                                x.dt_bias.to(DEV), x.alog_mode, cu, 1.0, S0)
+    assert lib.kda_get_last_device_error() == 0
+    assert o.numel() == o2.numel() == og.numel() == 0
+    for S in (Sf, Sf2, Sfg):
+        assert torch.equal(S, S0)
+    a = lib.backward_from_checkpoints(q, k, v, g, beta, dO.to(DEV), ckpt, cu_seqlens=cu,
+                                      dS_final=dSf.to(DEV))
+    b = lib.backward_chunked(q, k, v, g, beta, dO.to(DEV), cu_seqlens=cu, initial_state=S0,
+                             dS_final=dSf.to(DEV))
+    assert lib.kda_get_last_device_error() == 0
+    for grads in (a, b):
+        assert all(t.numel() == 0 for t in grads[:5])
+        assert torch.equal(grads[5], dSf.to(DEV))
