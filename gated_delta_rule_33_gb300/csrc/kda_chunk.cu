@@ -110,19 +110,32 @@ struct Params {
     int *split;                  // per chain: set when a chunk was shortened (with ckpt)
 };
 
+// Where the first two levels of the inverse leave their blocks: T row-major
+// only (T_32 too, beside its column-major copy); the T beta tiles of those
+// blocks are written by two other warps (tbeta_writer).
+struct TOnly {
+    float *t;
+    __device__ __forceinline__ void col(int, int, const float (&)[16]) const {}  // already in T
+    __device__ __forceinline__ void four(int r, int s4, float4 x) const {
+        *reinterpret_cast<float4 *>(t + r * 64 + s4) = x;
+    }
+};
+
 // T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk (column-major
 // in the OFF_KS region), by 16 x 16 blocks, on warps 0-3: the diagonal blocks by
 // forward substitution (warps 0-1), then the off-diagonal blocks in two levels,
 // T_10 and T_32 (ut_level1, each warp on the blocks it solved), then the whole
 // lower-left 32 x 32 block (ut_level2) -- the 2 x 2-block inverse
 // [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]] applied at 16 and
-// then at 32 rows.  Every lower block of T beta is written as soon as its block
-// of T is final (the strictly upper blocks of the T beta tiles hold zeros
-// written once), and the warp that issues the W' and U-tilde products is told
-// when each column block of T beta is complete: block 3 after the diagonal
-// solve, block 2 after level 1, blocks 0-1 after level 2.  The operands are
-// found from the shared-memory base inside the function (a pointer argument
-// would reach it as a generic address).
+// then at 32 rows.  The first two levels write T only; warps 6-7
+// (tbeta_writer) turn their blocks into T beta as each level completes, so the
+// conversion and its stores stay off the inverse's path, and level 2 writes
+// its T beta block itself.  (The strictly upper blocks of the T beta tiles hold
+// zeros.)  The warp that issues the W' and U-tilde products is told when each
+// column block of T beta is complete: block 3 after the diagonal solve, block 2
+// after level 1, blocks 0-1 after level 2.  The operands are found from the
+// shared-memory base inside the function (a pointer argument would reach it as
+// a generic address).
 __device__ __forceinline__ void ut_inverse(int tid) {
     uint8_t *smem = smem_base();
     uint8_t *misc = smem + OFF_MISC;
@@ -132,20 +145,48 @@ __device__ __forceinline__ void ut_inverse(int tid) {
     float *T32c = reinterpret_cast<float *>(misc + MISC_T32);
     float *P = reinterpret_cast<float *>(misc + MISC_P);
     const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
-    const TbetaTiles out{smem + OFF_KH, smem + OFF_TB16, beta};
     if (tid < 64) {
-        ut_diag_solve(At, T, Tdiag, out, tid);
-        fence_proxy_async_smem();
-        named_arrive(kBarDiag, 96);
+        const TOnly t_only{T};
+        ut_diag_solve(At, T, Tdiag, t_only, tid);
+        named_arrive(kBarDiagT, 128);
         __syncwarp();
-        ut_level1(At, T, Tdiag, P, T, T32c, out, tid);
-        fence_proxy_async_smem();
-        named_arrive(kBarLevel1, 96);
+        ut_level1(At, T, Tdiag, P, T, T32c, t_only, tid);
+        named_arrive(kBarLevel1T, 128);
     }
     inverse_sync();
+    const TbetaTiles out{smem + OFF_KH, smem + OFF_TB16, beta};
     ut_level2(At, T, Tdiag, T32c, P, out, tid);
     fence_proxy_async_smem();
     named_arrive(kBarLevel2, 160);
+}
+
+// Warps 6-7 (w = 0..63) during the inverse: T beta of the diagonal blocks once
+// the diagonal solve is done (block 3 first, for the first W' / U-tilde k-steps),
+// then of T_10 and T_32 once level 1 is done; one row quad T[r][s4 .. s4 + 3]
+// read from T per store.
+__device__ __forceinline__ void tbeta_writer(int w) {
+    uint8_t *smem = smem_base();
+    uint8_t *misc = smem + OFF_MISC;
+    const float *T = reinterpret_cast<const float *>(smem + OFF_KS) + 64 * 64;
+    const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
+    uint8_t *tb = smem + OFF_KH, *tb16 = smem + OFF_TB16;
+    const int r = w >> 2, s4 = 4 * (w & 3);  // row and column quad within a 16 x 16 block
+    auto quad = [&](int r0, int c0) {
+        store_tbeta4(tb, tb16, r0 + r, c0 + s4,
+                     *reinterpret_cast<const float4 *>(T + (r0 + r) * 64 + c0 + s4), beta);
+    };
+    named_sync(kBarDiagT, 128);
+    quad(48, 48);
+    fence_proxy_async_smem();
+    named_arrive(kBarDiag, 96);
+    quad(32, 32);
+    quad(16, 16);
+    quad(0, 0);
+    named_sync(kBarLevel1T, 128);
+    quad(48, 32);
+    quad(16, 0);
+    fence_proxy_async_smem();
+    named_arrive(kBarLevel1, 96);
 }
 
 // The state pass of a chunk, S_op = tf32(e^{m_k} S[k][v]) and
@@ -655,6 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
                     issue_u(1, false);
                 }
                 mma_commit_w(bar_mma);
+            } else if (warp == 6 || warp == 7) {
+                tbeta_writer(tid - 192);
             } else if (warp >= 8) {
                 float *ck = nullptr;
                 if (kCkpt && ckpt_ok && ((tc - t0) % kC) == 0)

@@ -80,6 +80,9 @@ __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 constexpr int kBarDiag = 2, kBarLevel1 = 3, kBarLevel2 = 4;
+// Between the inverse warps (which arrive) and the forward's T beta writers
+// (which wait): T of the diagonal blocks, then of level 1, is in place.
+constexpr int kBarDiagT = 5, kBarLevel1T = 6;
 
 // 2^x with the special-function unit (inputs here lie within +-116).
 __device__ __forceinline__ float fast_exp2(float x) {
