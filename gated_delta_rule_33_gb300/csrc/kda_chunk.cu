@@ -121,21 +121,49 @@ struct TOnly {
     }
 };
 
+// Y[r][c] of level 2 (32 x 32, fp32) in the unused upper-right quarter of T
+// (rows 0-31, columns 32-63), the float4 group index XOR-ed by row % 8
+__device__ __forceinline__ int ty_idx(int r, int c) { return r * 64 + 32 + (((c >> 2) ^ (r & 7)) << 2); }
+
+// Accumulators of rows r0, r0 + 1 and columns c .. c + 3 of Y as stored.
+__device__ __forceinline__ Acc2x4 load_y(const float *T, int r0, int c) {
+    Acc2x4 a;
+    const float4 y0 = *reinterpret_cast<const float4 *>(T + ty_idx(r0, c));
+    const float4 y1 = *reinterpret_cast<const float4 *>(T + ty_idx(r0 + 1, c));
+    a.v[0] = f2(y0.x, y0.y);
+    a.v[1] = f2(y0.z, y0.w);
+    a.v[2] = f2(y1.x, y1.y);
+    a.v[3] = f2(y1.z, y1.w);
+    return a;
+}
+__device__ __forceinline__ void store_y(float *T, int r0, int c, const Acc2x4 &a) {
+    *reinterpret_cast<float4 *>(T + ty_idx(r0, c)) = a.row(0);
+    *reinterpret_cast<float4 *>(T + ty_idx(r0 + 1, c)) = a.row(1);
+}
+
 // T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk (column-major
-// in the OFF_KS region), by 16 x 16 blocks, on warps 0-3: the diagonal blocks by
-// forward substitution (warps 0-1), then the off-diagonal blocks in two levels,
-// T_10 and T_32 (ut_level1, each warp on the blocks it solved), then the whole
-// lower-left 32 x 32 block (ut_level2) -- the 2 x 2-block inverse
-// [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]] applied at 16 and
-// then at 32 rows.  The first two levels write T only; warps 6-7
-// (tbeta_writer) turn their blocks into T beta as each level completes, so the
-// conversion and its stores stay off the inverse's path, and level 2 writes
-// its T beta block itself.  (The strictly upper blocks of the T beta tiles hold
-// zeros.)  The warp that issues the W' and U-tilde products is told when each
-// column block of T beta is complete: block 3 after the diagonal solve, block 2
-// after level 1, blocks 0-1 after level 2.  The operands are found from the
-// shared-memory base inside the function (a pointer argument would reach it as
-// a generic address).
+// in the OFF_KS region), by 16 x 16 blocks, on warps 0-3 -- the 2 x 2-block
+// inverse [[A, 0], [C, B]]^-1 = [[A^-1, 0], [-B^-1 C A^-1, B^-1]] applied at 16
+// and then at 32 rows:
+//   diagonal blocks T_bb by forward substitution (warps 0-1);
+//   level 1, T_10 and T_32 (warps 0-1, each on the blocks it solved);
+//   level 2, the lower-left 32 x 32 block X = -T_bot Y, Y = A_bl T_top
+//   (T_top = T[0:32, 0:32], T_bot = T[32:64, 32:64], A_bl = A[32:64, 0:32]).
+// Warp w owns rows 16 (w % 2) .. + 15 and columns 16 (w / 2) .. + 15 of Y and
+// X.  What level 2 needs of the diagonal blocks alone is done by warps 2-3
+// while warps 0-1 run level 1: their own Y blocks (T_11 only) and the first
+// half (T_00) of the K range of warps 0-1's Y blocks.  After level 1, warps 0-1
+// finish their Y blocks over the T_10 half, and every warp forms its X block.
+// Every sum runs over k in the same order as in one pass.
+// The first two levels write T only; warps 6-7 (tbeta_writer) turn their
+// blocks into T beta as each level completes, so the conversion and its stores
+// stay off the inverse's path; level 2 writes its T beta blocks itself.  (The
+// strictly upper blocks of the T beta tiles hold zeros.)  The warp that issues
+// the W' and U-tilde products is told when each column block of T beta is
+// complete: block 3 after the diagonal solve, block 2 after level 1, blocks
+// 0-1 after level 2.  The operands are found from the shared-memory base
+// inside the function (a pointer argument would reach it as a generic
+// address).
 __device__ __forceinline__ void ut_inverse(int tid) {
     uint8_t *smem = smem_base();
     uint8_t *misc = smem + OFF_MISC;
@@ -145,17 +173,54 @@ __device__ __forceinline__ void ut_inverse(int tid) {
     float *T32c = reinterpret_cast<float *>(misc + MISC_T32);
     float *P = reinterpret_cast<float *>(misc + MISC_P);
     const float *beta = reinterpret_cast<const float *>(misc + MISC_BETA);
+    const TbetaTiles out{smem + OFF_KH, smem + OFF_TB16, beta};
+    const int w = tid >> 5, l = tid & 31, rh = w & 1, cb = w >> 1;
+    const int r0 = 16 * rh + 2 * (l >> 2), c0 = 16 * cb + 4 * (l & 3);
     if (tid < 64) {
         const TOnly t_only{T};
         ut_diag_solve(At, T, Tdiag, t_only, tid);
-        named_arrive(kBarDiagT, 128);
+        named_arrive(kBarDiagT, 192);
         __syncwarp();
         ut_level1(At, T, Tdiag, P, T, T32c, t_only, tid);
         named_arrive(kBarLevel1T, 128);
+    } else {
+        named_sync(kBarDiagT, 192);
+        // Y over T_11 (final) and Y over T_00 (the first half of column block 0)
+        Acc2x4 y1, y0;
+        gemm_2x4<16>(y1, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
+        gemm_2x4<16>(y0, At + 32 + r0, 64, T + c0 - 16, 64);
+        store_y(T, r0, c0, y1);
+        store_y(T, r0, c0 - 16, y0);
     }
     inverse_sync();
-    const TbetaTiles out{smem + OFF_KH, smem + OFF_TB16, beta};
-    ut_level2(At, T, Tdiag, T32c, P, out, tid);
+    if (w < 2) {
+        // the T_10 half of column block 0 of Y
+        Acc2x4 y = load_y(T, r0, c0);
+        gemm_2x4<16>(y, At + 16 * 64 + 32 + r0, 64, T + 16 * 64 + c0, 64);
+        store_y(T, r0, c0, y);
+        if (w == 0) {
+            __syncwarp();
+            named_arrive(kBarLevel2Y, 64);
+        } else {
+            named_sync(kBarLevel2Y, 64);
+        }
+    }
+    // X block of this warp: -T_bot[rows][k] Y[k][c0 .. + 3], k over the nonzero
+    // blocks of T_bot (T_32 first, then T_33, for rows 16-31)
+    Acc2x4 x;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+        x.step(rh == 0 ? *reinterpret_cast<const float2 *>(Tdiag + 2 * 256 + s * 16 + r0)
+                       : *reinterpret_cast<const float2 *>(T32c + s * 16 + r0 - 16),
+               *reinterpret_cast<const float4 *>(T + ty_idx(s, c0)));
+    if (rh == 1) {
+#pragma unroll
+        for (int s = 16; s < 32; ++s)
+            x.step(*reinterpret_cast<const float2 *>(Tdiag + 3 * 256 + (s - 16) * 16 + r0 - 16),
+                   *reinterpret_cast<const float4 *>(T + ty_idx(s, c0)));
+    }
+    out.four(32 + r0, c0, x.neg_row(0));
+    out.four(33 + r0, c0, x.neg_row(1));
     fence_proxy_async_smem();
     named_arrive(kBarLevel2, 160);
 }
@@ -175,7 +240,7 @@ __device__ __forceinline__ void tbeta_writer(int w) {
         store_tbeta4(tb, tb16, r0 + r, c0 + s4,
                      *reinterpret_cast<const float4 *>(T + (r0 + r) * 64 + c0 + s4), beta);
     };
-    named_sync(kBarDiagT, 128);
+    named_sync(kBarDiagT, 192);
     quad(48, 48);
     fence_proxy_async_smem();
     named_arrive(kBarDiag, 96);

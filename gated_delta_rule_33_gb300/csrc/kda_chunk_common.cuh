@@ -83,6 +83,8 @@ constexpr int kBarDiag = 2, kBarLevel1 = 3, kBarLevel2 = 4;
 // Between the inverse warps (which arrive) and the forward's T beta writers
 // (which wait): T of the diagonal blocks, then of level 1, is in place.
 constexpr int kBarDiagT = 5, kBarLevel1T = 6;
+// Between the forward's level-2 warps 0 (arrives) and 1 (waits): Y rows 0-15.
+constexpr int kBarLevel2Y = 7;
 
 // 2^x with the special-function unit (inputs here lie within +-116).
 __device__ __forceinline__ float fast_exp2(float x) {
