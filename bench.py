@@ -133,16 +133,16 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 # of the kernel source they were taken on: a changed source reports null.
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                     "bytes": 4 * 138.64e6,
-                     "sha256": ["4f4b8169bcf2c60666e553fcd2c3fb6b4e174bcc2cf174b70a636b202776d5cf",
-                             "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
+                     "bytes": 4 * 138.82e6,
+                     "sha256": ["429c3670782a0e1c1bc49607db403836c96fb0aeb1697417fe8fb831b8f93169",
+                             "c2047f293a3d9efd31ff042d0a436ddc1b5f5c700cf1a9c905081414caf2cd53",
                              "8881aa469733f65a4c014ed9f4f0aa68c6f6518704b09fe54617047b32840e72",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
-                   "bytes": 4 * 110.39e6,
-                   "sha256": ["4f4b8169bcf2c60666e553fcd2c3fb6b4e174bcc2cf174b70a636b202776d5cf",
-                           "529388b8c9579dedc24951035c8195c9b7713d0eb19e279bd75a7c3bf3c6c6b6",
+                   "bytes": 4 * 110.78e6,
+                   "sha256": ["429c3670782a0e1c1bc49607db403836c96fb0aeb1697417fe8fb831b8f93169",
+                           "c2047f293a3d9efd31ff042d0a436ddc1b5f5c700cf1a9c905081414caf2cd53",
                            "8881aa469733f65a4c014ed9f4f0aa68c6f6518704b09fe54617047b32840e72",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},
