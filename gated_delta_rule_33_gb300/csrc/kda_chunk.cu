@@ -711,7 +711,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_kernel(const __grid_constan
             }
             __syncthreads();
 
-            // ---- S4: UT inverse (warps 0-3); W'^T = Kr^T (T beta)^T and
+            // ---- S4: UT inverse (warps 0-3) with its T beta tiles (warps 6-7
+            // for the first two levels); W'^T = Kr^T (T beta)^T and
             // Ut^T = V^T (T beta)^T issued by warp 4 one column block of T beta
             // (one K range of the products) at a time as the inverse completes
             // it; the state pass (warps 8-15) ----
