@@ -134,15 +134,15 @@ def decode_bytes(B=B_DECODE, Hh=H, K=D, V=D, state_bytes=4, gated=False):
 NCU_TRAFFIC = {
     "chunk_unfused": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
                      "bytes": 4 * 138.82e6,
-                     "sha256": ["6efede901ecec02629aa2af58fd6c9333e2ec87ba8d4b1198c209e924291e24f",
-                             "c2047f293a3d9efd31ff042d0a436ddc1b5f5c700cf1a9c905081414caf2cd53",
+                     "sha256": ["1dc515dc5e3ccbdf95b753842424885a65626cc9722c56b2c2bb356b6a3c1a47",
+                             "17d6fd9cfa56e1c3a45045394b09808f9856c13fe0200ad23e45cd6bc4b02399",
                              "8881aa469733f65a4c014ed9f4f0aa68c6f6518704b09fe54617047b32840e72",
                              "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                      "note": "T=1024 capture x 4 (profiles/chunk_prefill_T1024_H96.md)"},
     "chunk_gated": {"src": ["kda_chunk.cu", "kda_chunk_common.cuh", "kda_sm100.cuh", "kda_f32x2.cuh"],
                    "bytes": 4 * 110.78e6,
-                   "sha256": ["6efede901ecec02629aa2af58fd6c9333e2ec87ba8d4b1198c209e924291e24f",
-                           "c2047f293a3d9efd31ff042d0a436ddc1b5f5c700cf1a9c905081414caf2cd53",
+                   "sha256": ["1dc515dc5e3ccbdf95b753842424885a65626cc9722c56b2c2bb356b6a3c1a47",
+                           "17d6fd9cfa56e1c3a45045394b09808f9856c13fe0200ad23e45cd6bc4b02399",
                            "8881aa469733f65a4c014ed9f4f0aa68c6f6518704b09fe54617047b32840e72",
                            "c5455d461a5735fe8529d24adc80e51f03cd6f12a6b4cb7c406826b40c47bd2d"],
                    "note": "T=1024 capture x 4 (profiles/chunk_prefill_gated_T1024_H96.md)"},

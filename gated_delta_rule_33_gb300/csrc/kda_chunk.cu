@@ -110,17 +110,6 @@ struct Params {
     int *split;                  // per chain: set when a chunk was shortened (with ckpt)
 };
 
-// Where the first two levels of the inverse leave their blocks: T row-major
-// only (T_32 too, beside its column-major copy); the T beta tiles of those
-// blocks are written by two other warps (tbeta_writer).
-struct TOnly {
-    float *t;
-    __device__ __forceinline__ void col(int, int, const float (&)[16]) const {}  // already in T
-    __device__ __forceinline__ void four(int r, int s4, float4 x) const {
-        *reinterpret_cast<float4 *>(t + r * 64 + s4) = x;
-    }
-};
-
 // Y[r][c] of level 2 (32 x 32, fp32) in the unused upper-right quarter of T
 // (rows 0-31, columns 32-63), the float4 group index XOR-ed by row % 8
 __device__ __forceinline__ int ty_idx(int r, int c) { return r * 64 + 32 + (((c >> 2) ^ (r & 7)) << 2); }
@@ -177,7 +166,9 @@ __device__ __forceinline__ void ut_inverse(int tid) {
     const int w = tid >> 5, l = tid & 31, rh = w & 1, cb = w >> 1;
     const int r0 = 16 * rh + 2 * (l >> 2), c0 = 16 * cb + 4 * (l & 3);
     if (tid < 64) {
-        const TOnly t_only{T};
+        // the first two levels into T only (T_32 too, beside its column-major
+        // copy); their T beta tiles are written by warps 6-7
+        const TRowMajor t_only{T};
         ut_diag_solve(At, T, Tdiag, t_only, tid);
         named_arrive(kBarDiagT, 192);
         __syncwarp();

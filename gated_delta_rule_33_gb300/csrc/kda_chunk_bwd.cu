@@ -195,18 +195,6 @@ __device__ __forceinline__ void put8(uint8_t *img, uint32_t half, uint32_t rows,
     if (half != 0) *reinterpret_cast<uint4 *>(img + half + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-// The UT inverse's output policy here: the blocks it does not keep in its
-// row-major T itself (T_32 and the lower-left 32 x 32 block) are written there,
-// so that T is complete (fp32, row-major, zero above the diagonal) when the
-// inverse returns; the split images are formed from it by the whole CTA.
-struct TRowMajor {
-    float *t;
-    __device__ __forceinline__ void col(int, int, const float (&)[16]) const {}  // already in T
-    __device__ __forceinline__ void four(int r, int s4, float4 x) const {
-        *reinterpret_cast<float4 *>(t + r * 64 + s4) = x;
-    }
-};
-
 // ---- product issue ---------------------------------------------------------------------
 
 // One operand of a product: an image (or a row range of it) in a shared slot.
@@ -388,10 +376,6 @@ __device__ __forceinline__ void place_extra(Sched &S, int sl, int i, int lo, int
         S.xi0 = i; S.xlo0 = lo; S.xhi0 = hi; S.xoff0 = off;
     }
 }
-__device__ __forceinline__ bool slot_has(const Sched &S, int sl, int i, int lo, int hi) {
-    return sl ? (S.sl1 == i && S.lo1 <= lo && hi <= S.hi1) : (S.sl0 == i && S.lo0 <= lo && hi <= S.hi0);
-}
-
 // Every thread copies 16-byte pieces between a slot and the image in the
 // scratch: rows [r0, r1) of each 64-column block of the hi (and lo) tile, in
 // the image's byte layout; cp.async into the slot (load) or plain 16-byte
@@ -889,6 +873,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_bwd_kernel(const BwdParams 
                     float *Tdiag = reinterpret_cast<float *>(misc + M_TDIAG);
                     float *T32c = reinterpret_cast<float *>(misc + M_T32);
                     float *P = reinterpret_cast<float *>(misc + M_P);
+                    // T complete in its row-major form; the split images are formed
+                    // from it by the whole CTA
                     const TRowMajor out{T};
                     if (tid < 64) {
                         ut_diag_solve(s_at, T, Tdiag, out, tid);

@@ -164,6 +164,19 @@ struct TbetaTiles {
     }
 };
 
+// An output policy that keeps every block of T in the row-major T itself: the
+// diagonal solve already writes its columns there, and four() stores the
+// blocks of the two levels (T_32 and the lower-left 32 x 32 block too), so
+// that T is complete (fp32, row-major, zero above the diagonal) wherever a
+// level ends.
+struct TRowMajor {
+    float *t;
+    __device__ __forceinline__ void col(int, int, const float (&)[16]) const {}  // already in T
+    __device__ __forceinline__ void four(int r, int s4, float4 x) const {
+        *reinterpret_cast<float4 *>(t + r * 64 + s4) = x;
+    }
+};
+
 // ---- T = (I + A)^{-1} for the strictly lower-triangular 64 x 64 A_kk ----
 // Layouts (fp32, shared memory):
 //   At     A column-major, At[s * 64 + r] = A[r][s] (zero for s >= r)
